@@ -1,0 +1,342 @@
+"""CPU oracle for the diffusion-LLM denoising-step hot path (test infrastructure).
+
+ONLY the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package. It shares no code with the CUDA library: the
+arithmetic lives in ``orc.c`` (plain C, f64, OpenMP over output rows) and the
+compositions below chain those primitives in the order the pages give:
+
+* mojo-dllm "Technical Specification", section 11 (one LLaDA layer: RMSNorm,
+  QKV projection, RoPE, bidirectional attention, output projection, residual,
+  RMSNorm, MLP, residual) and "Development plan", "Model facts" (eps 1e-5,
+  NORM RoPE with theta 500000, SwiGLU 12288, untied output);
+* "Development plan", "Compute design": every projection consumes Q8_K
+  activations (quantized per token, decisions in f32) and decoded Q4_K/Q6_K
+  weights; the LM head runs only on the masked rows of the current block;
+* "Technical Specification", section 12: confidence, top-k select, scatter.
+
+Readings where the pages are silent:
+* the final RMSNorm (``out_norm``) is applied to the masked rows before the
+  LM head;
+* the "linear stream" workload has no attention: the O projection consumes
+  the V projection's output;
+* confidence = softmax probability of the argmax token; ties in the argmax go
+  to the lowest token id, ties in top-k to the lowest position.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "orc.c")
+_LIB = os.path.join(_HERE, "liborc.so")
+_lock = threading.Lock()
+_lib = None
+
+TYPE_Q4_K = 12
+TYPE_Q6_K = 14
+QK = 256
+BLOCK_BYTES = {TYPE_Q4_K: 144, TYPE_Q6_K: 210}
+
+
+def build(force: bool = False) -> str:
+    """Compile orc.c into liborc.so (plain gcc, OpenMP, no FP contraction)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+               "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = C.CDLL(_LIB)
+            P, I64, I32, D = C.c_void_p, C.c_int64, C.c_int32, C.c_double
+            sig = {
+                "orc_num_threads": ([], C.c_int),
+                "orc_dequant": ([C.c_int, P, I64, P], C.c_int),
+                "orc_quantize_q8k": ([P, I64, I64, I64, P, P, P], None),
+                "orc_rmsnorm": ([P, I64, I64, P, D, P], None),
+                "orc_qgemm_rows": ([C.c_int, P, I64, I64, P, P, I64, P, I64, P], C.c_int),
+                "orc_qgemm_intsums": ([C.c_int, P, I64, I64, P, I64, P, P], C.c_int),
+                "orc_block_scales": ([C.c_int, P, I64, P, P], C.c_int),
+                "orc_q4k_fields": ([P, P, P, P], None),
+                "orc_q6k_fields": ([P, P, P], None),
+                "orc_rope": ([P, I64, I64, I64, D], None),
+                "orc_attention": ([P, P, P, I64, I64, I64, P], None),
+                "orc_swiglu": ([P, P, I64, P], None),
+                "orc_embed_q4k": ([P, I64, I64, P, I64, P], C.c_int),
+                "orc_row_confidence": ([P, I64, I64, P, P, P, P], None),
+                "orc_commit_topk": ([P, I64, I32, I64, I64, P, P, I64, P, P], C.c_int),
+                "orc_transfer_counts": ([I64, I64, P], None),
+            }
+            for name, (args, res) in sig.items():
+                f = getattr(lib, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    return int(_load().orc_num_threads())
+
+
+# --- formats ---------------------------------------------------------------------------------
+
+def dequant(type_id: int, blocks: np.ndarray) -> np.ndarray:
+    """Exact decoded weights (f64). blocks [..., nb, bytes] -> [..., nb*256]."""
+    b = _c(blocks, np.uint8)
+    bb = BLOCK_BYTES[type_id]
+    nb = b.size // bb
+    out = np.empty(nb * QK, dtype=np.float64)
+    rc = _load().orc_dequant(type_id, _p(b), nb, _p(out))
+    if rc:
+        raise ValueError(f"orc_dequant failed ({rc})")
+    return out.reshape(*b.shape[:-2], b.shape[-2] * QK) if b.ndim >= 2 else out
+
+
+def q4k_fields(block: np.ndarray):
+    """(scales[8], mins[8], quants[256]) of one Q4_K block."""
+    b = _c(block, np.uint8)
+    sc = np.zeros(8, np.int32)
+    mn = np.zeros(8, np.int32)
+    q = np.zeros(256, np.uint8)
+    _load().orc_q4k_fields(_p(b), _p(sc), _p(mn), _p(q))
+    return sc, mn, q
+
+
+def q6k_fields(block: np.ndarray):
+    """(scales[16], quants[256] in [0,63]) of one Q6_K block."""
+    b = _c(block, np.uint8)
+    sc = np.zeros(16, np.int32)
+    q = np.zeros(256, np.uint8)
+    _load().orc_q6k_fields(_p(b), _p(sc), _p(q))
+    return sc, q
+
+
+def quantize_q8k(x: np.ndarray):
+    """Q8_K codes of f32 rows: (q int8 [r,k], d f32 [r,k/256], bsum int16 [r,k/16])."""
+    x = _c(x, np.float32)
+    rows, k = x.shape
+    if k % QK:
+        raise ValueError("k must be a multiple of 256")
+    q = np.empty((rows, k), np.int8)
+    d = np.empty((rows, k // QK), np.float32)
+    bs = np.empty((rows, k // 16), np.int16)
+    _load().orc_quantize_q8k(_p(x), rows, k, k, _p(q), _p(d), _p(bs))
+    return q, d, bs
+
+
+def rmsnorm(x: np.ndarray, w=None, eps: float = 1e-5) -> np.ndarray:
+    x = _c(x, np.float64)
+    rows, k = x.shape
+    out = np.empty_like(x)
+    wp = None if w is None else _c(w, np.float32)
+    _load().orc_rmsnorm(_p(x), rows, k, None if wp is None else _p(wp), float(eps), _p(out))
+    return out
+
+
+def quantize_act(x: np.ndarray, norm_w=None, eps: float = 1e-5):
+    """Activation quantization as the path does it: optional RMSNorm (f64), then the
+    normalized values rounded to f32 and quantized to Q8_K with f32 decisions."""
+    if norm_w is not None:
+        x = rmsnorm(np.asarray(x, np.float64), norm_w, eps)
+    return quantize_q8k(np.asarray(x, np.float32))
+
+
+def qgemm(type_id: int, wblocks: np.ndarray, q: np.ndarray, d: np.ndarray, rows=None) -> np.ndarray:
+    """y[m][n] = sum_k W[n][k] * d[m][k/256] * q[m][k] in f64 (rows: subset of n)."""
+    w = _c(wblocks, np.uint8)
+    n, nsb = w.shape[0], w.shape[1]
+    k = nsb * QK
+    q = _c(q, np.int8)
+    d = _c(d, np.float32)
+    m = q.shape[0]
+    if rows is None:
+        sel, nsel = None, n
+    else:
+        sel = _c(rows, np.int64)
+        nsel = sel.size
+    y = np.empty((m, nsel), np.float64)
+    rc = _load().orc_qgemm_rows(type_id, _p(w), n, k, _p(q), _p(d), m,
+                                None if sel is None else _p(sel), nsel, _p(y))
+    if rc:
+        raise RuntimeError(f"orc_qgemm_rows failed ({rc})")
+    return y
+
+
+def intsums(type_id: int, wblocks: np.ndarray, q: np.ndarray):
+    """Integer sums U, J [m][n][nsb] (int64) of the unified decoded form."""
+    w = _c(wblocks, np.uint8)
+    n, nsb = w.shape[0], w.shape[1]
+    q = _c(q, np.int8)
+    m = q.shape[0]
+    U = np.empty((m, n, nsb), np.int64)
+    J = np.empty((m, n, nsb), np.int64)
+    rc = _load().orc_qgemm_intsums(type_id, _p(w), n, nsb * QK, _p(q), m, _p(U), _p(J))
+    if rc:
+        raise RuntimeError("orc_qgemm_intsums failed")
+    return U, J
+
+
+def block_scales(type_id: int, wblocks: np.ndarray):
+    """Per-block (c0, c1) with block value = c0*U - c1*J (shape [n, nsb])."""
+    w = _c(wblocks, np.uint8)
+    nb = w.size // BLOCK_BYTES[type_id]
+    c0 = np.empty(nb, np.float64)
+    c1 = np.empty(nb, np.float64)
+    _load().orc_block_scales(type_id, _p(w), nb, _p(c0), _p(c1))
+    return c0.reshape(w.shape[:-1]), c1.reshape(w.shape[:-1])
+
+
+# --- layer maths -----------------------------------------------------------------------------
+
+def rope(x: np.ndarray, n_heads: int, head_dim: int, theta: float) -> np.ndarray:
+    out = _c(x, np.float64).copy()
+    _load().orc_rope(_p(out), out.shape[0], n_heads, head_dim, float(theta))
+    return out
+
+
+def attention(q, k, v, n_heads: int, head_dim: int) -> np.ndarray:
+    q, k, v = (_c(a, np.float64) for a in (q, k, v))
+    o = np.empty_like(q)
+    _load().orc_attention(_p(q), _p(k), _p(v), q.shape[0], n_heads, head_dim, _p(o))
+    return o
+
+
+def swiglu(g, u) -> np.ndarray:
+    g = _c(g, np.float64)
+    u = _c(u, np.float64)
+    h = np.empty_like(g)
+    _load().orc_swiglu(_p(g), _p(u), g.size, _p(h))
+    return h
+
+
+def embed(table_blocks: np.ndarray, ids: np.ndarray) -> np.ndarray:
+    t = _c(table_blocks, np.uint8)
+    vocab, nsb = t.shape[0], t.shape[1]
+    ids = _c(ids, np.int32)
+    x = np.empty((ids.size, nsb * QK), np.float64)
+    if _load().orc_embed_q4k(_p(t), vocab, nsb * QK, _p(ids), ids.size, _p(x)):
+        raise ValueError("token id out of range")
+    return x
+
+
+def row_confidence(logits: np.ndarray):
+    """(argmax id int32, softmax confidence f64, top1 logit, top2 logit) per row."""
+    l = _c(logits, np.float64)
+    r, v = l.shape
+    ids = np.empty(r, np.int32)
+    conf = np.empty(r, np.float64)
+    t1 = np.empty(r, np.float64)
+    t2 = np.empty(r, np.float64)
+    _load().orc_row_confidence(_p(l), r, v, _p(ids), _p(conf), _p(t1), _p(t2))
+    return ids, conf, t1, t2
+
+
+def commit_topk(canvas: np.ndarray, mask_id: int, b0: int, b1: int, conf_by_pos, ids_by_pos, k: int):
+    """Commit in place; returns (positions, ids) in selection order."""
+    cv = np.ascontiguousarray(canvas, np.int32)
+    conf = _c(conf_by_pos, np.float64)
+    ids = _c(ids_by_pos, np.int32)
+    pos = np.zeros(max(k, 1), np.int32)
+    tid = np.zeros(max(k, 1), np.int32)
+    n = _load().orc_commit_topk(_p(cv), cv.size, int(mask_id), int(b0), int(b1), _p(conf), _p(ids),
+                                int(k), _p(pos), _p(tid))
+    if n < 0:
+        raise ValueError("bad block range")
+    canvas[...] = cv
+    return pos[:n].copy(), tid[:n].copy()
+
+
+def transfer_counts(masked: int, steps: int) -> np.ndarray:
+    out = np.empty(steps, np.int64)
+    _load().orc_transfer_counts(int(masked), int(steps), _p(out))
+    return out
+
+
+# --- compositions ----------------------------------------------------------------------------
+
+def linear(type_id, wblocks, x, norm_w=None, eps=1e-5, rows=None):
+    """One quantized projection of activation rows x (optionally RMSNorm-ed first)."""
+    q, d, _ = quantize_act(x, norm_w, eps)
+    return qgemm(type_id, wblocks, q, d, rows)
+
+
+def layer(lw: dict, x, dims: dict, attention_on: bool, with_qk: bool = True):
+    """One LLaDA layer on residual rows x (f64 out).
+
+    attention_on=False is the "linear stream" workload: Q and K are projected
+    (and returned) but unused, and the O projection consumes V's output.
+    Returns (x_out, extras) where extras holds the intermediate f64 tensors.
+    """
+    eps, nh, hd = dims["eps"], dims["n_heads"], dims["head_dim"]
+    x = np.asarray(x, np.float64)
+    q1, d1, _ = quantize_act(x, lw["attn_norm"], eps)
+    ex = {}
+    if with_qk or attention_on:
+        ex["q"] = qgemm(TYPE_Q4_K, lw["wq"], q1, d1)
+        ex["k"] = qgemm(TYPE_Q4_K, lw["wk"], q1, d1)
+    ex["v"] = qgemm(TYPE_Q6_K, lw["wv"], q1, d1)
+    if attention_on:
+        ex["q_rope"] = rope(ex["q"], nh, hd, dims["rope_theta"])
+        ex["k_rope"] = rope(ex["k"], nh, hd, dims["rope_theta"])
+        o = attention(ex["q_rope"], ex["k_rope"], ex["v"], nh, hd)
+    else:
+        o = ex["v"]
+    ex["attn_out"] = o
+    q2, d2, _ = quantize_act(o)
+    x = x + qgemm(TYPE_Q4_K, lw["wo"], q2, d2)
+    ex["x_mid"] = x
+    q3, d3, _ = quantize_act(x, lw["ffn_norm"], eps)
+    g = qgemm(TYPE_Q4_K, lw["wgate"], q3, d3)
+    u = qgemm(TYPE_Q4_K, lw["wup"], q3, d3)
+    h = swiglu(g, u)
+    ex["h"] = h
+    q4, d4, _ = quantize_act(h)
+    x = x + qgemm(TYPE_Q6_K, lw["wdown"], q4, d4)
+    return x, ex
+
+
+def lmhead_logits(hidden_rows, out_norm, w_out, eps=1e-5):
+    """Logits (f64) of the given hidden rows: RMSNorm -> Q8_K -> Q6_K head."""
+    q, d, _ = quantize_act(hidden_rows, out_norm, eps)
+    return qgemm(TYPE_Q6_K, w_out, q, d)
+
+
+def lmhead_commit(hidden, canvas, mask_id, b0, b1, k, out_norm, w_out, eps=1e-5):
+    """Masked-rows-only LM head + softmax confidence + top-k commit (canvas updated in place).
+
+    Returns dict(pos, id, conf, rows, ids_rows, conf_rows, top1, top2)."""
+    rows = np.array([p for p in range(b0, b1) if canvas[p] == mask_id], dtype=np.int64)
+    res = dict(rows=rows)
+    L = canvas.size
+    conf_pos = np.full(L, -np.inf)
+    ids_pos = np.zeros(L, np.int32)
+    if rows.size:
+        logits = lmhead_logits(np.asarray(hidden, np.float64)[rows], out_norm, w_out, eps)
+        ids, conf, t1, t2 = row_confidence(logits)
+        conf_pos[rows] = conf
+        ids_pos[rows] = ids
+        res.update(ids_rows=ids, conf_rows=conf, top1=t1, top2=t2)
+    pos, tid = commit_topk(canvas, mask_id, b0, b1, conf_pos, ids_pos, k)
+    res.update(pos=pos, id=tid, conf=conf_pos[pos] if pos.size else np.zeros(0))
+    return res

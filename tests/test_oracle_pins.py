@@ -1,0 +1,446 @@
+"""Pins of the CPU oracle against facts fixed outside it (no GPU).
+
+Each check ties the oracle to something other than itself: hand-worked block
+bytes (tests/golden), an independent encoder that packs known fields into
+the GGUF bytes, numpy's own f16 decoding, exact rational arithmetic,
+closed forms and invariants of the method.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as orc
+from quantized_gemm_q8_gb300 import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    out = {}
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(":", 1)
+            out[k.strip()] = v.split()
+    return out
+
+
+def f16_bits(x: float) -> int:
+    return int(np.array([x], np.float16).view(np.uint16)[0])
+
+
+def f16_val(bits: int) -> float:
+    return float(np.array([bits], np.uint16).view(np.float16)[0])
+
+
+# ---- independent encoders: known fields -> GGUF bytes (inverse of the layout) ----------------
+
+def encode_q4k(d_bits, dmin_bits, sc, mn, q):
+    blk = np.zeros(144, np.uint8)
+    blk[0:2] = np.array([d_bits], np.uint16).view(np.uint8)
+    blk[2:4] = np.array([dmin_bits], np.uint16).view(np.uint8)
+    s = np.zeros(12, np.int64)
+    for j in range(8):
+        if j < 4:
+            s[j] |= sc[j] & 63
+            s[j + 4] |= mn[j] & 63
+        else:
+            s[j + 4] |= (sc[j] & 15) | ((mn[j] & 15) << 4)
+            s[j - 4] |= (sc[j] >> 4) << 6
+            s[j] |= (mn[j] >> 4) << 6
+    blk[4:16] = s.astype(np.uint8)
+    for c in range(4):
+        for l in range(32):
+            blk[16 + 32 * c + l] = (q[64 * c + l] & 15) | ((q[64 * c + 32 + l] & 15) << 4)
+    return blk
+
+
+def encode_q6k(d_bits, sc, q):
+    blk = np.zeros(210, np.uint8)
+    for i in range(256):
+        h, t, l = i // 128, (i % 128) // 32, i % 32
+        lo, hi = q[i] & 15, (q[i] >> 4) & 3
+        idx = 64 * h + l + 32 * (t & 1)
+        blk[idx] |= lo if t < 2 else (lo << 4)
+        blk[128 + 32 * h + l] |= hi << (2 * t)
+    blk[192:208] = np.array(sc, np.int8).view(np.uint8)
+    blk[208:210] = np.array([d_bits], np.uint16).view(np.uint8)
+    return blk
+
+
+def q4k_expected(d_bits, dmin_bits, sc, mn, q):
+    d, dmin = f16_val(d_bits), f16_val(dmin_bits)
+    return np.array([d * sc[i // 32] * q[i] - dmin * mn[i // 32] for i in range(256)])
+
+
+def q6k_expected(d_bits, sc, q):
+    d = f16_val(d_bits)
+    return np.array([d * sc[8 * (i // 128) + (i % 128) // 16] * (int(q[i]) - 32) for i in range(256)])
+
+
+# ---- Q4_K -------------------------------------------------------------------------------------
+
+def test_q4k_scales_handworked():
+    g = _golden("q4k_scales_handworked.txt")
+    blk = np.zeros(144, np.uint8)
+    blk[4:16] = [int(b, 16) for b in g["scales_bytes"]]
+    sc, mn, _ = orc.q4k_fields(blk)
+    assert sc.tolist() == [int(v) for v in g["scale"]]
+    assert mn.tolist() == [int(v) for v in g["min"]]
+
+
+def test_q4k_closed_form_block():
+    # d = 1, dmin = 0.5, scale_j = j+1, min_j = 2j, q_i = i mod 16  ->  w_i = (j+1)(i%16) - j
+    sc = [j + 1 for j in range(8)]
+    mn = [2 * j for j in range(8)]
+    q = [i % 16 for i in range(256)]
+    blk = encode_q4k(0x3C00, 0x3800, sc, mn, q)
+    w = orc.dequant(orc.TYPE_Q4_K, blk[None, None, :])[0]
+    want = np.array([(i // 32 + 1) * (i % 16) - (i // 32) for i in range(256)], np.float64)
+    np.testing.assert_array_equal(w, want)
+
+
+@pytest.mark.parametrize("j", range(8))
+def test_q4k_single_subblock_high_bits(j):
+    # scale = min = 63 in sub-block j only: exercises the 2 high bits packed for j >= 4
+    sc = [0] * 8
+    mn = [0] * 8
+    sc[j], mn[j] = 63, 63
+    q = [15] * 256
+    blk = encode_q4k(0x3C00, 0x3C00, sc, mn, q)
+    w = orc.dequant(orc.TYPE_Q4_K, blk[None, None, :])[0]
+    want = np.zeros(256)
+    want[32 * j:32 * j + 32] = 63 * 15 - 63
+    np.testing.assert_array_equal(w, want)
+
+
+def test_q4k_random_fields_roundtrip():
+    rng = np.random.default_rng(7)
+    for _ in range(20):
+        sc = rng.integers(0, 64, 8).tolist()
+        mn = rng.integers(0, 64, 8).tolist()
+        q = rng.integers(0, 16, 256).tolist()
+        db, mb = int(rng.integers(0x0400, 0x7800)), int(rng.integers(0x0001, 0x7800))
+        blk = encode_q4k(db, mb, sc, mn, q)
+        s2, m2, q2 = orc.q4k_fields(blk)
+        assert s2.tolist() == sc and m2.tolist() == mn and q2.tolist() == q
+        w = orc.dequant(orc.TYPE_Q4_K, blk[None, None, :])[0]
+        np.testing.assert_array_equal(w, q4k_expected(db, mb, sc, mn, q))
+
+
+def test_f16_subnormal_and_sign():
+    # d = smallest subnormal 2^-24, dmin = -2.0 (sign bit)
+    sc = [1] * 8
+    mn = [1] * 8
+    q = [1] * 256
+    blk = encode_q4k(0x0001, f16_bits(-2.0), sc, mn, q)
+    w = orc.dequant(orc.TYPE_Q4_K, blk[None, None, :])[0]
+    np.testing.assert_array_equal(w, np.full(256, 2.0 ** -24 + 2.0))
+
+
+# ---- Q6_K -------------------------------------------------------------------------------------
+
+def test_q6k_handworked():
+    g = _golden("q6k_handworked.txt")
+    blk = np.zeros(210, np.uint8)
+    for item in g["bytes"]:
+        name, val = item.split("=")
+        off = int(name[2:]) + (128 if name.startswith("qh") else 0)
+        blk[off] = int(val, 16)
+    blk[192:208] = np.array([int(v) for v in g["scales"]], np.int8).view(np.uint8)
+    blk[208:210] = np.array([0x3C00], np.uint16).view(np.uint8)
+    w = orc.dequant(orc.TYPE_Q6_K, blk[None, None, :])[0]
+    for item in g["expect"]:
+        i, v = item.split(":")
+        assert w[int(i)] == float(v), (i, w[int(i)], v)
+
+
+def test_q6k_random_fields_roundtrip():
+    rng = np.random.default_rng(11)
+    for it in range(20):
+        sc = rng.integers(-128, 128, 16).tolist()
+        if it == 0:
+            sc[3] = -128
+        q = rng.integers(0, 64, 256).tolist()
+        db = int(rng.integers(0x0400, 0x7800))
+        blk = encode_q6k(db, sc, q)
+        s2, q2 = orc.q6k_fields(blk)
+        assert s2.tolist() == sc and q2.tolist() == q
+        w = orc.dequant(orc.TYPE_Q6_K, blk[None, None, :])[0]
+        np.testing.assert_array_equal(w, q6k_expected(db, sc, q))
+
+
+def test_q6k_t_patterns():
+    # q values that set each t slot's nibble choice and high bits distinctly
+    q = [(i * 37 + (i // 32)) % 64 for i in range(256)]
+    sc = [1] * 16
+    blk = encode_q6k(0x3C00, sc, q)
+    w = orc.dequant(orc.TYPE_Q6_K, blk[None, None, :])[0]
+    np.testing.assert_array_equal(w, np.array(q, np.float64) - 32)
+
+
+# ---- Q8_K -------------------------------------------------------------------------------------
+
+def test_q8k_zero_block():
+    q, d, bs = orc.quantize_q8k(np.zeros((1, 256), np.float32))
+    assert not q.any() and d[0, 0] == 0.0 and not bs.any()
+
+
+def test_q8k_spike_and_extremes():
+    x = np.zeros((2, 256), np.float32)
+    x[0, 7] = 5.0
+    x[1, 0], x[1, 1] = 3.0, -3.0
+    q, d, bs = orc.quantize_q8k(x)
+    assert q[0, 7] == 127 and np.count_nonzero(q[0]) == 1
+    assert d[0, 0] == np.float32(5.0) / np.float32(127.0)
+    assert q[1, 0] == 127 and q[1, 1] == -127
+    assert bs[0, 0] == 127 and bs[1, 0] == 0
+
+
+def test_q8k_round_half_even():
+    # amax = 127 -> iscale = 1 exactly, so the codes are rint(x) with ties to even
+    x = np.zeros((1, 256), np.float32)
+    vals = [127.0, 2.5, 3.5, -2.5, -0.5, 126.5, -126.5, 0.49999997]
+    x[0, :len(vals)] = vals
+    q, d, _ = orc.quantize_q8k(x)
+    assert q[0, :len(vals)].tolist() == [127, 2, 4, -2, 0, 126, -126, 0]
+    assert d[0, 0] == np.float32(1.0)
+
+
+def test_q8k_error_bound_and_bsums():
+    x = synth.activations(3, 8, 1024)
+    q, d, bs = orc.quantize_q8k(x)
+    recon = q.reshape(8, 4, 256).astype(np.float64) * d[:, :, None].astype(np.float64)
+    err = np.abs(recon - x.reshape(8, 4, 256))
+    assert np.all(err <= d[:, :, None] * (0.5 + 1e-6) + 1e-12)
+    np.testing.assert_array_equal(bs, q.reshape(8, 64, 16).astype(np.int64).sum(-1))
+    amax = np.abs(x.reshape(8, 4, 256)).max(-1)
+    assert np.all(np.abs(q.reshape(8, 4, 256)).max(-1) == 127)
+    np.testing.assert_array_equal(d, (amax / np.float32(127.0)).astype(np.float32))
+
+
+# ---- GEMM -------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("t", [orc.TYPE_Q4_K, orc.TYPE_Q6_K])
+def test_qgemm_equals_dequant_then_dot(t):
+    n, k, m = 37, 768, 5
+    w = synth.blocks(t, 101 + t, n, k)
+    x = synth.activations(202 + t, m, k)
+    q, d, _ = orc.quantize_q8k(x)
+    y = orc.qgemm(t, w, q, d)
+    W = orc.dequant(t, w).reshape(n, k)
+    A = q.astype(np.float64) * np.repeat(d.astype(np.float64), 256, axis=1)
+    ref = A @ W.T
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12 * (np.abs(A) @ np.abs(W).T).max())
+    rows = np.array([36, 0, 5])
+    np.testing.assert_array_equal(orc.qgemm(t, w, q, d, rows=rows), y[:, rows])
+
+
+@pytest.mark.parametrize("t", [orc.TYPE_Q4_K, orc.TYPE_Q6_K])
+def test_intsums_compose_to_gemm(t):
+    n, k, m = 19, 1024, 4
+    w = synth.blocks(t, 303 + t, n, k)
+    x = synth.activations(404 + t, m, k)
+    q, d, _ = orc.quantize_q8k(x)
+    U, J = orc.intsums(t, w, q)
+    c0, c1 = orc.block_scales(t, w)
+    y_int = (d.astype(np.float64)[:, None, :] * (c0[None] * U - c1[None] * J)).sum(-1)
+    y = orc.qgemm(t, w, q, d)
+    np.testing.assert_allclose(y_int, y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
+
+
+def test_q4k_intsums_brute_force():
+    rng = np.random.default_rng(5)
+    for m, n, k in [(1, 1, 256), (2, 3, 512), (3, 2, 256)]:
+        fields, wb = [], []
+        for _ in range(n):
+            row = []
+            for _ in range(k // 256):
+                sc = rng.integers(0, 64, 8).tolist()
+                mn = rng.integers(0, 64, 8).tolist()
+                q = rng.integers(0, 16, 256).tolist()
+                db, mb = int(rng.integers(0x0400, 0x3C00)), int(rng.integers(0x0400, 0x3C00))
+                row.append(encode_q4k(db, mb, sc, mn, q))
+                fields.append((db, mb, sc, mn, q))
+            wb.append(np.stack(row))
+        wb = np.stack(wb)
+        a = rng.integers(-127, 128, (m, k)).astype(np.int8)
+        da = rng.uniform(0.001, 0.1, (m, k // 256)).astype(np.float32)
+        U, J = orc.intsums(orc.TYPE_Q4_K, wb, a)
+        y = orc.qgemm(orc.TYPE_Q4_K, wb, a, da)
+        for mm in range(m):
+            for nn in range(n):
+                tot = Fraction(0)
+                for b in range(k // 256):
+                    db, mb, sc, mn, q = fields[nn * (k // 256) + b]
+                    u = sum(sc[i // 32] * q[i] * int(a[mm, 256 * b + i]) for i in range(256))
+                    jj = sum(mn[i // 32] * int(a[mm, 256 * b + i]) for i in range(256))
+                    assert U[mm, nn, b] == u and J[mm, nn, b] == jj
+                    tot += Fraction(float(da[mm, b])) * (Fraction(f16_val(db)) * u - Fraction(f16_val(mb)) * jj)
+                assert abs(Fraction(y[mm, nn]) - tot) <= abs(tot) * Fraction(1, 10 ** 13) + Fraction(1, 10 ** 18)
+
+
+def test_q6k_intsums_brute_force():
+    rng = np.random.default_rng(6)
+    m, n, k = 2, 2, 512
+    fields, wb = [], []
+    for _ in range(n):
+        row = []
+        for _ in range(k // 256):
+            sc = rng.integers(-128, 128, 16).tolist()
+            q = rng.integers(0, 64, 256).tolist()
+            db = int(rng.integers(0x0400, 0x3C00))
+            row.append(encode_q6k(db, sc, q))
+            fields.append((db, sc, q))
+        wb.append(np.stack(row))
+    wb = np.stack(wb)
+    a = rng.integers(-127, 128, (m, k)).astype(np.int8)
+    da = rng.uniform(0.001, 0.1, (m, k // 256)).astype(np.float32)
+    U, J = orc.intsums(orc.TYPE_Q6_K, wb, a)
+    y = orc.qgemm(orc.TYPE_Q6_K, wb, a, da)
+    for mm in range(m):
+        for nn in range(n):
+            tot = Fraction(0)
+            for b in range(k // 256):
+                db, sc, q = fields[nn * (k // 256) + b]
+                g = lambda i: 8 * (i // 128) + (i % 128) // 16
+                u = sum(sc[g(i)] * q[i] * int(a[mm, 256 * b + i]) for i in range(256))
+                jj = sum(sc[g(i)] * int(a[mm, 256 * b + i]) for i in range(256))
+                assert U[mm, nn, b] == u and J[mm, nn, b] == jj
+                tot += Fraction(float(da[mm, b])) * Fraction(f16_val(db)) * (u - 32 * jj)
+            assert abs(Fraction(y[mm, nn]) - tot) <= abs(tot) * Fraction(1, 10 ** 13) + Fraction(1, 10 ** 18)
+
+
+# ---- layer maths ------------------------------------------------------------------------------
+
+def test_rmsnorm_constant_vector():
+    x = np.full((2, 512), -3.0)
+    w = np.linspace(0.5, 1.5, 512).astype(np.float32)
+    out = orc.rmsnorm(x, w, 1e-5)
+    np.testing.assert_allclose(out, np.tile(-3.0 / math.sqrt(9.0 + 1e-5) * w.astype(np.float64), (2, 1)), rtol=1e-14)
+
+
+def test_rope_identities():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((6, 2 * 8))
+    # theta -> infinity: only pair 0 rotates (angle = position)
+    r = orc.rope(x, 2, 8, 1e300)
+    for p in range(6):
+        for h in range(2):
+            v, o = x[p, 8 * h:8 * h + 8], r[p, 8 * h:8 * h + 8]
+            c, s = math.cos(p), math.sin(p)
+            assert abs(o[0] - (v[0] * c - v[1] * s)) < 1e-14 and abs(o[1] - (v[0] * s + v[1] * c)) < 1e-14
+            np.testing.assert_allclose(o[2:], v[2:], rtol=0, atol=1e-15)
+    # theta = 1: every pair rotates by the position; norms preserved
+    r1 = orc.rope(x, 2, 8, 1.0)
+    np.testing.assert_allclose(np.linalg.norm(r1, axis=1), np.linalg.norm(x, axis=1), rtol=1e-14)
+    p = 3
+    c, s = math.cos(p), math.sin(p)
+    np.testing.assert_allclose(r1[p, 2], x[p, 2] * c - x[p, 3] * s, rtol=1e-13)
+    np.testing.assert_array_equal(orc.rope(x, 2, 8, 500000.0)[0], x[0])  # position 0 untouched
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(2)
+    L, nh, hd = 7, 2, 8
+    q = rng.standard_normal((L, nh * hd))
+    k = np.tile(rng.standard_normal((1, nh * hd)), (L, 1))  # identical keys
+    v = rng.standard_normal((L, nh * hd))
+    o = orc.attention(q, k, v, nh, hd)
+    np.testing.assert_allclose(o, np.tile(v.mean(0), (L, 1)), rtol=1e-13)
+    # one dominant key per head: output = that key's value row
+    k2 = np.zeros((L, nh * hd))
+    k2[4] = 1e3 * q[0]
+    o2 = orc.attention(q, k2, v, nh, hd)
+    np.testing.assert_allclose(o2[0], v[4], rtol=1e-10)
+
+
+def test_swiglu_values():
+    g = np.array([0.0, 1.0, -1.0, 40.0])
+    u = np.array([3.0, 2.0, 2.0, 0.5])
+    h = orc.swiglu(g, u)
+    np.testing.assert_allclose(h, [0.0, 2.0 / (1 + math.exp(-1)), -2.0 / (1 + math.e), 20.0], rtol=1e-15)
+
+
+def test_embed_is_row_decode():
+    t = synth.q4k_blocks(9, 50, 512)
+    ids = np.array([3, 49, 0, 3], np.int32)
+    x = orc.embed(t, ids)
+    W = orc.dequant(orc.TYPE_Q4_K, t).reshape(50, 512)
+    np.testing.assert_array_equal(x, W[ids])
+    with pytest.raises(ValueError):
+        orc.embed(t, np.array([50], np.int32))
+
+
+# ---- confidence and commit --------------------------------------------------------------------
+
+def test_commit_tiny_handworked():
+    g = _golden("commit_tiny.txt")
+    logits = np.array([[float(v) for v in g[f"logits{i}"]] for i in range(4)])
+    ids, conf, t1, t2 = orc.row_confidence(logits)
+    assert ids.tolist() == [2, 0, 0, 6]
+    np.testing.assert_allclose(conf[[0, 1, 3]], [math.e ** 2 / (math.e ** 2 + 7), 0.125,
+                                                 math.e ** 5 / (2 * math.e ** 5 + 6)], rtol=1e-14)
+    assert t1[3] == t2[3] == 5.0
+    for k, key in [(2, "k2"), (3, "k3")]:
+        canvas = np.array([int(v) for v in g["canvas"]], np.int32)
+        conf_pos = conf.copy()
+        pos, tid = orc.commit_topk(canvas, 7, 0, 4, conf_pos, ids, k)
+        assert pos.tolist() == [int(v) for v in g[f"{key}_pos"]]
+        assert canvas.tolist() == [int(v) for v in g[f"{key}_canvas"]]
+    canvas = np.array([7, 7, 7, 7], np.int32)
+    pos, _ = orc.commit_topk(canvas, 7, 0, 4, np.array([0.3, 0.3, 0.1, 0.3]), np.zeros(4, np.int32), 2)
+    assert pos.tolist() == [0, 1]  # equal confidence -> lowest positions first
+
+
+def test_commit_invariants_random():
+    rng = np.random.default_rng(3)
+    L, mask = 148, 126336
+    for trial in range(20):
+        canvas = rng.integers(0, 1000, L).astype(np.int32)
+        masked = rng.random(L) < 0.6
+        canvas[masked] = mask
+        b0 = 20 + 32 * (trial % 4)
+        b1 = b0 + 32
+        conf = rng.random(L)
+        ids = rng.integers(0, 126464, L).astype(np.int32)
+        before = canvas.copy()
+        k = int(rng.integers(1, 8))
+        pos, tid = orc.commit_topk(canvas, mask, b0, b1, conf, ids, k)
+        cand = [p for p in range(b0, b1) if before[p] == mask]
+        assert len(pos) == min(k, len(cand))
+        assert all(b0 <= p < b1 and before[p] == mask for p in pos)
+        assert len(set(pos.tolist())) == len(pos)
+        rest = [p for p in cand if p not in set(pos.tolist())]
+        if rest and len(pos):
+            assert conf[pos].min() >= conf[rest].max()
+        np.testing.assert_array_equal(canvas[pos], ids[pos])
+        untouched = np.ones(L, bool)
+        untouched[pos] = False
+        np.testing.assert_array_equal(canvas[untouched], before[untouched])
+
+
+def test_transfer_counts():
+    assert orc.transfer_counts(32, 8).tolist() == [4] * 8
+    assert orc.transfer_counts(10, 4).tolist() == [3, 3, 2, 2]
+    assert orc.transfer_counts(3, 5).tolist() == [1, 1, 1, 0, 0]
+    for masked, steps in [(128, 32), (37, 8), (1, 1)]:
+        c = orc.transfer_counts(masked, steps)
+        assert c.sum() == masked and c.max() - c.min() <= 1 and np.all(np.diff(c) <= 0)
+
+
+def test_generator_is_deterministic_and_in_range():
+    a = synth.q4k_blocks(5, 3, 512)
+    b = synth.q4k_blocks(5, 3, 512)
+    np.testing.assert_array_equal(a, b)
+    d = a[..., 0:2].copy().view(np.uint16).ravel()
+    assert np.all((d >> 10) == 1)  # f16 exponent field 1 -> [2^-14, 2^-13)
+    x = synth.activations(1, 64, 1024)
+    assert abs(x.mean()) < 0.02 and abs(x.std() - 1) < 0.02
+    cv = synth.canvas(1)
+    assert cv.size == 148 and np.all(cv[20:] == 126336) and np.all(cv[:20] < 126000)
