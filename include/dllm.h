@@ -1,0 +1,167 @@
+/*
+ * dllm.h - C ABI of the GB300 (sm_103a) hot path of one LLaDA-style diffusion-LLM
+ * denoising step: Q8_K activation quantization, Q4_K / Q6_K quantized GEMMs on the
+ * tcgen05 tensor cores, the masked-rows-only LM head with softmax confidence and
+ * top-k token commit, and the per-layer linear stream.
+ *
+ * Sources (mojo-dllm pages; cited by page title and section):
+ *   [TS10]  Technical Specification, section 10 "Quantized Compute" (linear_q4k(x, weight,
+ *           out): Q4_K_M matmul directly on quantized weights, block decode, dot, f32 acc.)
+ *   [TS9]   Technical Specification, section 9.2 (unknown types fail explicitly, no silent
+ *           fallback) and section 27 (actionable errors).
+ *   [TS28]  Technical Specification, section 28 (preallocated, reusable runtime buffers).
+ *   [TS11]  Technical Specification, section 11 (LLaDA layer order) and 11.1 (bidirectional).
+ *   [TS12]  Technical Specification, sections 12-14 (diffusion loop, scheduler select/update,
+ *           softmax / argmax / top-k / scatter).
+ *   [DP-CD] Development plan, "Compute design" (Q8_K activations: int8, one f32 scale per
+ *           256 values, int sums per 16; weights decoded to unsigned bytes + per-16 scale +
+ *           per-16 offset; LM head only on the masked rows of the current block).
+ *   [DP-MF] Development plan, "Model facts" (d 4096, 32 x 128 MHA, FFN 12288 SwiGLU,
+ *           RMSNorm eps 1e-5, NORM RoPE theta 500000, vocab 126464, mask 126336).
+ *   [DP-CO] Development plan, "Corrections to the spec" (Q4_K / Q6_K matrices, F32 norms).
+ *   [RM-HW] README, "How it works" (logits only where the sampler looks; LLaDA low-confidence
+ *           remasking).
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers (global memory of the current device) unless a
+ *     parameter says "host". The caller owns every buffer, including workspaces; no
+ *     call allocates or frees device memory, and no call keeps a pointer after it
+ *     returns.
+ *   - Every call enqueues its kernels on `stream` and returns without synchronizing
+ *     (asynchronous; stream-ordered). Calls enqueue no host callbacks and no
+ *     allocations, so they may be captured into a CUDA graph by the caller.
+ *   - Return value: DLLM_OK or a negative-free positive status below. On error nothing is
+ *     launched and dllm_last_error() returns an actionable message (thread-local).
+ *   - Device-side failures (a bounded wait that ran out) are recorded in a device error
+ *     word; dllm_check(stream) synchronizes the stream and reports them.
+ *   - Shapes: k (reduction length) must be a multiple of 256 (one super-block).
+ */
+#ifndef DLLM_H
+#define DLLM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DLLM_API __attribute__((visibility("default")))
+#else
+#define DLLM_API
+#endif
+
+typedef struct CUstream_st* dllm_stream_t; /* same handle as cudaStream_t; NULL = legacy default */
+
+/* ---- status codes ([TS9], [TS27]) ---------------------------------------------------------- */
+enum {
+  DLLM_OK = 0,
+  DLLM_E_INVAL = 1,       /* NULL or non-device pointer, bad flag, bad range              */
+  DLLM_E_SHAPE = 2,       /* k % 256 != 0, sizes <= 0, sizes above a stated limit          */
+  DLLM_E_ALIGN = 3,       /* pointer not aligned as the call requires                      */
+  DLLM_E_TYPE = 4,        /* unsupported block type (only Q4_K and Q6_K have kernels)      */
+  DLLM_E_WORKSPACE = 5,   /* workspace smaller than the matching *_workspace_bytes()       */
+  DLLM_E_CUDA = 6,        /* a CUDA runtime call failed (message names it)                 */
+  DLLM_E_TIMEOUT = 7,     /* a device-side bounded wait ran out (reported by dllm_check)   */
+  DLLM_E_DEVICE = 8       /* current device is not sm_103 / lacks a feature               */
+};
+
+/* GGML block type ids of the two matrix formats with kernels ([DP-CO]). */
+enum { DLLM_Q4_K = 12, DLLM_Q6_K = 14 };
+
+/* Thread-local message of the last failing call on this host thread ("" if none). */
+DLLM_API const char* dllm_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+DLLM_API int dllm_version(void);
+
+/* Synchronize `stream`, then read and clear the device error word. Returns DLLM_OK,
+ * DLLM_E_TIMEOUT (a kernel's bounded wait ran out; the message names the kernel role) or
+ * DLLM_E_CUDA (a launch or execution error, message from the runtime). */
+DLLM_API int dllm_check(dllm_stream_t stream);
+
+/* ---- weight packing ------------------------------------------------------------------------
+ * The GEMMs read weights in a tile-major "packed" form made once at upload from the GGUF
+ * blocks (the pages' one-time repack at load, README "How it works", re-shaped for the GPU):
+ * rows are grouped in tiles of 128; for each (tile, super-block) the quant bytes and scale
+ * bytes of the 128 rows form one contiguous blob (one bulk copy), and the f16 super-block
+ * scales (d, and dmin for Q4_K) sit in a separate plane [tile][super-block][128 rows].
+ * The packed form holds exactly the GGUF bytes, re-ordered (zero extra bytes per row);
+ * rows beyond n up to the next multiple of 128 are zero.
+ *
+ * dllm_packed_bytes: bytes of the packed form of an n x k matrix (0 on bad arguments).
+ * dllm_pack_weights: `blocks` = device copy of the GGUF row-major block array
+ *   (n rows x k/256 blocks, 144 B per Q4_K block, 210 B per Q6_K block); `packed` must be
+ *   256-byte aligned and hold dllm_packed_bytes(type, n, k) bytes. Errors: DLLM_E_TYPE,
+ *   DLLM_E_SHAPE, DLLM_E_ALIGN, DLLM_E_INVAL, DLLM_E_WORKSPACE (packed_bytes too small). */
+DLLM_API size_t dllm_packed_bytes(int type, int64_t n, int64_t k);
+DLLM_API int dllm_pack_weights(int type, const void* blocks, int64_t n, int64_t k, void* packed,
+                               size_t packed_bytes, dllm_stream_t stream);
+
+/* ---- Q8_K activation quantization ([DP-CD]; RMSNorm [DP-MF]) -------------------------------
+ * For each of `rows` rows of x (f32, row stride ldx elements), optionally RMSNorm first:
+ *   xn = x / sqrt(mean(x^2) + eps) * norm_w          (norm_w == NULL: no normalization)
+ * then per 256 values: amax = max|xn|; d = amax / 127; q = clamp(rint(xn * (127 / amax)),
+ * -127, 127) (f32 multiply, round-half-even, IEEE division); amax == 0 gives d = 0, q = 0;
+ * bsum[g] = sum of the 16 codes of group g.
+ * Outputs (each optional, NULL = not written):
+ *   q    int8  [rows][k]         d    f32 [rows][k/256]      bsum int16 [rows][k/16]
+ *   act  the same codes in the tensor-core operand form read by the GEMMs, act_bytes
+ *        >= dllm_act_bytes(rows, k), 256-byte aligned. Layout (Lp = dllm_act_rows(rows),
+ *        planes at 1024-byte aligned offsets in this order):
+ *          A-plane f16 [k/64][Lp][64]: the int8 codes as exact f16 values; within each
+ *                  aligned group of 4 k-positions the order is (0, 2, 1, 3);
+ *          J-plane f16 [k/256][Lp/8][2][8][8]: bsum (16 per super-block) as exact f16, in
+ *                  8x8 core-matrix order (token-group, half, token, group);
+ *          D-plane f32 [k/256][Lp]: the scales d.
+ *        Rows rows..Lp-1 are written as zeros.
+ * Errors: DLLM_E_SHAPE (k % 256, rows <= 0, rows > 65536), DLLM_E_INVAL, DLLM_E_ALIGN
+ * (x not 16-byte aligned or ldx % 4), DLLM_E_WORKSPACE (act_bytes too small). */
+DLLM_API int64_t dllm_act_rows(int64_t rows);
+DLLM_API size_t dllm_act_bytes(int64_t rows, int64_t k);
+DLLM_API int dllm_quantize_act(const float* x, int64_t rows, int64_t k, int64_t ldx,
+                               const float* norm_w, float eps, int8_t* q, float* d, int16_t* bsum,
+                               void* act, size_t act_bytes, dllm_stream_t stream);
+
+/* ---- quantized GEMM ([TS10], [DP-CD]) --------------------------------------------------------
+ * y[i][j] (+)= sum_k W[j][k] * d_act[i][k/256] * q_act[i][k]       i < m tokens, j < n rows
+ * with W the exact decoded Q4_K (w = d*scale*q - dmin*min) or Q6_K (w = d*scale*(q-32))
+ * weights of `w_packed` (from dllm_pack_weights) and the activations of `act` (from
+ * dllm_quantize_act with the same m, k). Per super-block the integer sums run exactly on the
+ * tensor cores (integer values carried in f16 operands, f32 accumulators in tensor memory)
+ * and the f32 scale / offset epilogue applies d_act, d, dmin.
+ * y: f32, row stride ldy >= n (elements, ldy % 4 == 0). accumulate = 0: y = result;
+ * 1: y += result (residual add).
+ * ws: scratch for split-K partial sums, ws_bytes >= dllm_qgemm_workspace_bytes(type, m, n,
+ * k); may be NULL when that is 0. Deterministic: partials are summed in a fixed order.
+ * Errors: DLLM_E_TYPE, DLLM_E_SHAPE, DLLM_E_ALIGN, DLLM_E_INVAL, DLLM_E_WORKSPACE. */
+DLLM_API size_t dllm_qgemm_workspace_bytes(int type, int64_t m, int64_t n, int64_t k);
+DLLM_API int dllm_qgemm(int type, const void* act, int64_t m, int64_t k, const void* w_packed,
+                        int64_t n, float* y, int64_t ldy, int accumulate, void* ws, size_t ws_bytes,
+                        dllm_stream_t stream);
+DLLM_API int dllm_qgemm_q4k(const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
+                            float* y, int64_t ldy, int accumulate, void* ws, size_t ws_bytes,
+                            dllm_stream_t stream);
+DLLM_API int dllm_qgemm_q6k(const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
+                            float* y, int64_t ldy, int accumulate, void* ws, size_t ws_bytes,
+                            dllm_stream_t stream);
+
+/* Test hook ([DP-CD] integer sums): writes the exact per-super-block integer sums that the
+ * tensor cores accumulate, as int32 sums[2][k/256][m][n]:
+ *   Q4_K: sums[0] = sum_g scale * sum_i q4_i * a_i,      sums[1] = sum_g min * bsum_g
+ *   Q6_K: sums[0] = sum_g s_hi * sum_i (q6_i-32) * a_i, sums[1] = sum_g s_lo * sum_i (q6_i-32) * a_i
+ *         where the int8 group scale s = 16 * s_hi + s_lo, s_lo in [0, 15].
+ * Runs the same kernel as dllm_qgemm with one split; intended for small shapes. */
+DLLM_API int dllm_qgemm_intsums(int type, const void* act, int64_t m, int64_t k, const void* w_packed,
+                                int64_t n, int32_t* sums, dllm_stream_t stream);
+
+/* Test hook for failure detection: launches one kernel whose mbarrier wait can never
+ * complete, bounded by `limit_cycles` SM clock cycles; the kernel then records a timeout
+ * in the device error word and returns. dllm_check() afterwards reports DLLM_E_TIMEOUT. */
+DLLM_API int dllm_selftest_timeout(int64_t limit_cycles, dllm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DLLM_H */

@@ -1,0 +1,168 @@
+"""GB300 (sm_103a) hot path of one LLaDA-style diffusion-LLM denoising step.
+
+Thin Python binding over the C ABI in include/dllm.h (libdllm.so, built in-tree by
+``quantized_gemm_q8_gb300.build``). The functions here only marshal arguments: device
+memory and streams come from PyTorch, every step of the path runs in the library's CUDA
+kernels, and there is no CPU fallback - a missing library raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdllm.so")
+
+Q4_K = 12
+Q6_K = 14
+QK = 256
+
+OK, E_INVAL, E_SHAPE, E_ALIGN, E_TYPE, E_WORKSPACE, E_CUDA, E_TIMEOUT, E_DEVICE = range(9)
+
+
+class DllmError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[dllm status {code}] {msg}")
+        self.code = code
+
+
+_lock = threading.Lock()
+_lib = None
+
+P, I64, I32, SZ, F32, INT = C.c_void_p, C.c_int64, C.c_int32, C.c_size_t, C.c_float, C.c_int
+_SIGS = {
+    "dllm_last_error": ([], C.c_char_p),
+    "dllm_version": ([], INT),
+    "dllm_check": ([P], INT),
+    "dllm_packed_bytes": ([INT, I64, I64], SZ),
+    "dllm_pack_weights": ([INT, P, I64, I64, P, SZ, P], INT),
+    "dllm_act_rows": ([I64], I64),
+    "dllm_act_bytes": ([I64, I64], SZ),
+    "dllm_quantize_act": ([P, I64, I64, I64, P, F32, P, P, P, P, SZ, P], INT),
+    "dllm_qgemm_workspace_bytes": ([INT, I64, I64, I64], SZ),
+    "dllm_qgemm": ([INT, P, I64, I64, P, I64, P, I64, INT, P, SZ, P], INT),
+    "dllm_qgemm_q4k": ([P, I64, I64, P, I64, P, I64, INT, P, SZ, P], INT),
+    "dllm_qgemm_q6k": ([P, I64, I64, P, I64, P, I64, INT, P, SZ, P], INT),
+    "dllm_qgemm_intsums": ([INT, P, I64, I64, P, I64, P, P], INT),
+    "dllm_selftest_timeout": ([I64, P], INT),
+}
+
+
+def lib():
+    """The loaded C library (raises if it was not built: there is no fallback path)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; "
+                                   "g.build()'` (this package has no CPU fallback)")
+            l = C.CDLL(LIB_PATH)
+            for name, (args, res) in _SIGS.items():
+                f = getattr(l, name)
+                f.argtypes = args
+                f.restype = res
+            _lib = l
+    return _lib
+
+
+def last_error() -> str:
+    return lib().dllm_last_error().decode()
+
+
+def _ok(rc: int):
+    if rc != OK:
+        raise DllmError(rc, last_error())
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def check(stream=None):
+    """Synchronize the stream and raise if a kernel recorded a device-side timeout."""
+    _ok(lib().dllm_check(_stream(stream)))
+
+
+# --- weights -------------------------------------------------------------------------------
+
+def packed_bytes(type_id: int, n: int, k: int) -> int:
+    return int(lib().dllm_packed_bytes(type_id, n, k))
+
+
+def pack_weights(type_id: int, blocks: torch.Tensor, n: int, k: int, stream=None) -> torch.Tensor:
+    """GGUF block bytes (uint8 CUDA tensor, n x k/256 blocks) -> packed uint8 CUDA tensor."""
+    nbytes = packed_bytes(type_id, n, k)
+    if nbytes == 0:
+        raise DllmError(E_SHAPE, f"bad packed shape type={type_id} n={n} k={k}")
+    out = torch.empty(nbytes, dtype=torch.uint8, device=blocks.device)
+    _ok(lib().dllm_pack_weights(type_id, _ptr(blocks), n, k, _ptr(out), nbytes, _stream(stream)))
+    return out
+
+
+# --- activations ---------------------------------------------------------------------------
+
+def act_rows(rows: int) -> int:
+    return int(lib().dllm_act_rows(rows))
+
+
+def act_bytes(rows: int, k: int) -> int:
+    return int(lib().dllm_act_bytes(rows, k))
+
+
+def quantize_act(x: torch.Tensor, norm_w: torch.Tensor | None = None, eps: float = 1e-5,
+                 plain: bool = True, operand: bool = True, act: torch.Tensor | None = None, stream=None):
+    """Q8_K-quantize f32 rows of x (optionally RMSNorm-ed). Returns dict(q, d, bsum, act)."""
+    rows, k = x.shape
+    dev = x.device
+    out = {"q": None, "d": None, "bsum": None, "act": None}
+    if plain:
+        out["q"] = torch.empty((rows, k), dtype=torch.int8, device=dev)
+        out["d"] = torch.empty((rows, k // QK), dtype=torch.float32, device=dev)
+        out["bsum"] = torch.empty((rows, k // 16), dtype=torch.int16, device=dev)
+    nb = 0
+    if operand:
+        nb = act_bytes(rows, k)
+        out["act"] = act if act is not None else torch.empty(nb, dtype=torch.uint8, device=dev)
+    _ok(lib().dllm_quantize_act(_ptr(x), rows, k, x.stride(0), _ptr(norm_w), eps, _ptr(out["q"]),
+                                _ptr(out["d"]), _ptr(out["bsum"]), _ptr(out["act"]), nb, _stream(stream)))
+    return out
+
+
+# --- GEMM ----------------------------------------------------------------------------------
+
+def qgemm_workspace_bytes(type_id: int, m: int, n: int, k: int) -> int:
+    return int(lib().dllm_qgemm_workspace_bytes(type_id, m, n, k))
+
+
+def qgemm(type_id: int, act: torch.Tensor, m: int, k: int, w_packed: torch.Tensor, n: int,
+          y: torch.Tensor | None = None, accumulate: bool = False, ws: torch.Tensor | None = None,
+          stream=None) -> torch.Tensor:
+    """y[m, n] (+)= Q8_K activations x decoded Q4_K/Q6_K weights^T (f32)."""
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.float32, device=act.device)
+    wsb = qgemm_workspace_bytes(type_id, m, n, k)
+    if wsb and ws is None:
+        ws = torch.empty(wsb, dtype=torch.uint8, device=act.device)
+    _ok(lib().dllm_qgemm(type_id, _ptr(act), m, k, _ptr(w_packed), n, _ptr(y), y.stride(0), int(accumulate),
+                         _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return y
+
+
+def qgemm_intsums(type_id: int, act: torch.Tensor, m: int, k: int, w_packed: torch.Tensor, n: int,
+                  stream=None) -> torch.Tensor:
+    """Exact per-super-block integer sums int32 [2, k/256, m, n] (test hook)."""
+    sums = torch.zeros((2, k // QK, m, n), dtype=torch.int32, device=act.device)
+    _ok(lib().dllm_qgemm_intsums(type_id, _ptr(act), m, k, _ptr(w_packed), n, _ptr(sums), _stream(stream)))
+    return sums
+
+
+def selftest_timeout(limit_cycles: int, stream=None):
+    _ok(lib().dllm_selftest_timeout(limit_cycles, _stream(stream)))

@@ -1,0 +1,624 @@
+// C ABI of the library (include/dllm.h): status handling, weight packing, Q8_K activation
+// quantization, GEMM planning / dispatch, split-K reduction and test hooks.
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "qgemm.cuh"
+
+namespace dllm {
+
+__device__ int g_err_word = 0;
+
+int* err_word() {
+  static int* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+static thread_local char g_msg[1024] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DLLM_E_CUDA, "%s failed: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+static int cached_attr(cudaDeviceAttr attr, int* cache, int dflt) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return dflt;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess || v <= 0) return dflt;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  return cached_attr(cudaDevAttrMultiProcessorCount, cache, 152);
+}
+
+int check_device() {
+  static int major_c[64] = {0}, minor_c[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = cached_attr(cudaDevAttrComputeCapabilityMajor, major_c, 0);
+  int minor = cached_attr(cudaDevAttrComputeCapabilityMinor, minor_c, 0);
+  if (major != 10 || minor != 3)
+    return fail(DLLM_E_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev, major,
+                minor);
+  return DLLM_OK;
+}
+
+static bool is_device_ptr(const void* p) {
+  if (p == nullptr) return false;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+#define CHECK_DEV(ptr, name)                                                                      \
+  do {                                                                                            \
+    if (!is_device_ptr(ptr)) return fail(DLLM_E_INVAL, "%s: %s is NULL or not a device pointer", \
+                                         __func__, name);                                         \
+  } while (0)
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------------------------
+// Activation operand layout
+// ---------------------------------------------------------------------------------------------
+int64_t act_rows_padded(int64_t rows) {
+  if (rows <= 32) return 32;
+  if (rows <= 64) return 64;
+  if (rows <= 128) return 128;
+  if (rows <= 160) return 160;
+  return (rows + 127) / 128 * 128;
+}
+
+ActLayout act_layout(int64_t rows, int64_t k) {
+  ActLayout L;
+  L.rows = rows;
+  L.k = k;
+  L.lpad = act_rows_padded(rows);
+  L.nsb = k / QK;
+  L.off_a = 0;
+  L.off_j = align_up((size_t)L.lpad * k * 2, 1024);
+  L.off_d = align_up(L.off_j + (size_t)L.nsb * L.lpad * 32, 1024);
+  L.bytes = align_up(L.off_d + (size_t)L.nsb * L.lpad * 4, 1024);
+  return L;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int make_act_tmap(CUtensorMap* map, const void* act_a, int64_t lpad, int64_t k, int nt) {
+  auto enc = get_encode();
+  if (!enc) return fail(DLLM_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {64, (cuuint64_t)lpad, (cuuint64_t)(k / 64)};
+  cuuint64_t strides[2] = {128, (cuuint64_t)lpad * 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)nt, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(act_a), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DLLM_E_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return DLLM_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Weight packing (GGUF AoS blocks -> tile-major blobs + scale plane)
+// ---------------------------------------------------------------------------------------------
+static int block_bytes(int type) { return type == DLLM_Q4_K ? 144 : type == DLLM_Q6_K ? 210 : 0; }
+
+__global__ void pack_q4k_kernel(const uint8_t* __restrict__ src, int n, int nsb, uint8_t* __restrict__ blob,
+                                uint8_t* __restrict__ dd) {
+  const int ts = blockIdx.x;  // tile * nsb + sb
+  const int tile = ts / nsb, sb = ts % nsb, r = threadIdx.x;
+  const int64_t grow = (int64_t)tile * BM + r;
+  const bool valid = grow < n;
+  const uint8_t* b = src + (grow * nsb + sb) * 144;
+  uint8_t* o = blob + (size_t)ts * Q4K_BLOB;
+#pragma unroll
+  for (int h = 0; h < 8; ++h)
+    *reinterpret_cast<uint4*>(o + h * 2048 + r * 16) =
+        valid ? *reinterpret_cast<const uint4*>(b + 16 + 16 * h) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int w = 0; w < 3; ++w)
+    *reinterpret_cast<uint32_t*>(o + 16384 + w * 512 + r * 4) =
+        valid ? *reinterpret_cast<const uint32_t*>(b + 4 + 4 * w) : 0u;
+  *reinterpret_cast<uint32_t*>(dd + (size_t)ts * Q4K_DD + r * 4) =
+      valid ? *reinterpret_cast<const uint32_t*>(b) : 0u;
+}
+
+__global__ void pack_q6k_kernel(const uint8_t* __restrict__ src, int n, int nsb, uint8_t* __restrict__ blob,
+                                uint8_t* __restrict__ dd) {
+  const int ts = blockIdx.x;
+  const int tile = ts / nsb, sb = ts % nsb, r = threadIdx.x;
+  const int64_t grow = (int64_t)tile * BM + r;
+  const bool valid = grow < n;
+  const uint8_t* b = src + (grow * nsb + sb) * 210;
+  uint8_t* o = blob + (size_t)ts * Q6K_BLOB;
+  for (int i = 0; i < 128; ++i) o[(i >> 4) * 2048 + r * 16 + (i & 15)] = valid ? b[i] : 0;
+  for (int i = 0; i < 64; ++i) o[16384 + (i >> 4) * 2048 + r * 16 + (i & 15)] = valid ? b[128 + i] : 0;
+  for (int i = 0; i < 16; ++i) o[24576 + r * 16 + i] = valid ? b[192 + i] : 0;
+  uint8_t* d = dd + (size_t)ts * Q6K_DD + r * 2;
+  d[0] = valid ? b[208] : 0;
+  d[1] = valid ? b[209] : 0;
+}
+
+struct Packed {
+  size_t blob_bytes, dd_bytes;
+};
+static Packed packed_sizes(int type, int64_t n, int64_t k) {
+  const int64_t tiles = (n + BM - 1) / BM, nsb = k / QK;
+  Packed p;
+  p.blob_bytes = (size_t)tiles * nsb * (type == DLLM_Q4_K ? Q4K_BLOB : Q6K_BLOB);
+  p.dd_bytes = (size_t)tiles * nsb * (type == DLLM_Q4_K ? Q4K_DD : Q6K_DD);
+  return p;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Q8_K activation quantization (+ optional RMSNorm), writing the plain arrays and/or the
+// tensor-core operand planes.
+// ---------------------------------------------------------------------------------------------
+struct QuantOut {
+  int8_t* q;
+  float* d;
+  int16_t* bsum;
+  __half* act_a;
+  uint8_t* act_j;
+  float* act_d;
+  int lpad;
+};
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float s = 0.f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[i];
+  return s;
+}
+
+// Quantize one super-block held as 8 values per lane (lane covers k = 8*lane .. 8*lane+7)
+// and write all requested outputs for (row, sb).
+__device__ __forceinline__ void q8k_emit(float (&v)[8], int row, int rows, int sb, int64_t k, const QuantOut& o) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nsb = k / QK;
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  int qi[8];
+  float dsc = 0.f;
+  if (amax == 0.f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qi[i] = 0;
+  } else {
+    const float iscale = __fdiv_rn(127.f, amax);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float r = rintf(__fmul_rn(v[i], iscale));
+      r = fminf(127.f, fmaxf(-127.f, r));
+      qi[i] = (int)r;
+    }
+    dsc = __fdiv_rn(amax, 127.f);
+  }
+  int s8 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s8 += qi[i];
+  const int s16 = s8 + __shfl_xor_sync(0xffffffffu, s8, 1);  // group of 16 = lane pair
+  const int g = lane >> 1;
+  if (row < rows) {
+    if (o.q) {
+      uint32_t lo = (qi[0] & 0xFF) | ((qi[1] & 0xFF) << 8) | ((qi[2] & 0xFF) << 16) | ((uint32_t)(qi[3] & 0xFF) << 24);
+      uint32_t hi = (qi[4] & 0xFF) | ((qi[5] & 0xFF) << 8) | ((qi[6] & 0xFF) << 16) | ((uint32_t)(qi[7] & 0xFF) << 24);
+      *reinterpret_cast<uint2*>(o.q + (int64_t)row * k + (int64_t)sb * QK + 8 * lane) = make_uint2(lo, hi);
+    }
+    if (o.d && lane == 0) o.d[(int64_t)row * nsb + sb] = dsc;
+    if (o.bsum && (lane & 1) == 0) o.bsum[(int64_t)row * (k / 16) + (int64_t)sb * 16 + g] = (int16_t)s16;
+  }
+  if (o.act_a) {
+    // A-plane [k/64][lpad][64]; quarter q = lane/8, 16-byte chunk c = lane%8, order (0,2,1,3)
+    const int q = lane >> 3, c = lane & 7;
+    __half2 h0 = __floats2half2_rn((float)qi[0], (float)qi[2]);
+    __half2 h1 = __floats2half2_rn((float)qi[1], (float)qi[3]);
+    __half2 h2 = __floats2half2_rn((float)qi[4], (float)qi[6]);
+    __half2 h3 = __floats2half2_rn((float)qi[5], (float)qi[7]);
+    uint4 pk = make_uint4(h2u(h0), h2u(h1), h2u(h2), h2u(h3));
+    *reinterpret_cast<uint4*>(o.act_a + (((int64_t)sb * 4 + q) * o.lpad + row) * 64 + c * 8) = pk;
+    // J-plane [nsb][lpad/8][2][8][8]
+    if ((lane & 1) == 0) {
+      __half* j = reinterpret_cast<__half*>(o.act_j + ((int64_t)sb * o.lpad) * 32) + (row >> 3) * 128 +
+                  (g >> 3) * 64 + (row & 7) * 8 + (g & 7);
+      *j = __int2half_rn(s16);
+    }
+    if (lane == 0) o.act_d[(int64_t)sb * o.lpad + row] = dsc;
+  }
+}
+
+__global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restrict__ x, int rows, int64_t k,
+                                                           int64_t ldx, const float* __restrict__ norm_w, float eps,
+                                                           QuantOut o) {
+  __shared__ float red[8];
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nsb = (int)(k / QK);
+  if (row >= rows) {  // padding rows of the operand planes
+    float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int sb = warp; sb < nsb; sb += 8) q8k_emit(z, row, rows, sb, k, o);
+    return;
+  }
+  const float* xr = x + (int64_t)row * ldx;
+  float rstd = 1.f;
+  if (norm_w) {
+    float ss = 0.f;
+    for (int64_t i = threadIdx.x * 4; i < k; i += blockDim.x * 4) {
+      const float4 v = *reinterpret_cast<const float4*>(xr + i);
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+    ss = block_sum(ss, red);
+    rstd = 1.0f / sqrtf(ss / (float)k + eps);
+  }
+  for (int sb = warp; sb < nsb; sb += 8) {
+    const int64_t base = (int64_t)sb * QK + 8 * lane;
+    const float4 a = *reinterpret_cast<const float4*>(xr + base);
+    const float4 b = *reinterpret_cast<const float4*>(xr + base + 4);
+    float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    if (norm_w) {
+      const float4 wa = *reinterpret_cast<const float4*>(norm_w + base);
+      const float4 wb = *reinterpret_cast<const float4*>(norm_w + base + 4);
+      const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = (v[i] * rstd) * w[i];
+    }
+    q8k_emit(v, row, rows, sb, k, o);
+  }
+}
+
+// y (+)= sum of split partials, fixed order.
+__global__ void reduce_splits_kernel(const float* __restrict__ P, int splits, int64_t stride, int m, int n,
+                                     float* __restrict__ y, int64_t ldy, int accumulate) {
+  const int64_t total = (int64_t)m * n;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / n, c = i % n;
+    float s = 0.f;
+    for (int sp = 0; sp < splits; ++sp) s += P[sp * stride + i];
+    float* o = y + r * ldy + c;
+    *o = accumulate ? *o + s : s;
+  }
+}
+
+__global__ void selftest_timeout_kernel(long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing ever arrives on `bar`: the bounded wait must run out
+    if (!mbar_wait(b, 0, &abort_flag, limit)) atomicOr(&g_err_word, ERR_TIMEOUT_SELFTEST);
+    mbar_arrive(b);  // complete the phase so the barrier is left consistent
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// GEMM plan
+// ---------------------------------------------------------------------------------------------
+QgemmPlan plan_qgemm(int type, int64_t m, int64_t n, int64_t k) {
+  QgemmPlan P{};
+  P.lpad = (int)act_rows_padded(m);
+  P.nt = P.lpad <= 160 ? P.lpad : 128;
+  P.tiles_n = (int)((n + BM - 1) / BM);
+  P.tiles_m = P.lpad / P.nt;
+  P.nsb = (int)(k / QK);
+  const int nsm = num_sms();
+  const double w = type == DLLM_Q6_K ? 2.0 : 1.0625;  // MMA work per super-block
+  const double c_unit = 1.5;                           // fill + epilogue store, in super-block units
+  double best = 1e30;
+  for (int s = 1; s <= std::min(P.nsb, 32); ++s) {
+    const int sbps = (P.nsb + s - 1) / s;
+    const int sp = (P.nsb + sbps - 1) / sbps;
+    const long long units = (long long)P.tiles_n * P.tiles_m * sp;
+    const int grid = (int)std::min<long long>(units, nsm);
+    const long long waves = (units + grid - 1) / grid;
+    const double cost = waves * (sbps * w + c_unit) + (sp > 1 ? 0.02 * sp : 0.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      P.splits = sp;
+      P.sbps = sbps;
+      P.units = (int)units;
+      P.grid = grid;
+    }
+  }
+  P.ws_bytes = P.splits > 1 ? align_up((size_t)P.splits * m * n * 4, 256) : 0;
+  return P;
+}
+
+}  // namespace dllm
+
+using namespace dllm;
+
+extern "C" {
+
+DLLM_API const char* dllm_last_error(void) { return g_msg; }
+
+DLLM_API int dllm_version(void) { return 100; }
+
+DLLM_API int dllm_check(dllm_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int w = 0;
+  e = cudaMemcpyFromSymbol(&w, g_err_word, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "read device error word");
+  if (w) {
+    int z = 0;
+    cudaMemcpyToSymbol(g_err_word, &z, sizeof(int));
+    return fail(DLLM_E_TIMEOUT, "device-side bounded wait ran out (roles: %s%s%s%s%s%s)",
+                (w & ERR_TIMEOUT_PRODUCER) ? "producer " : "", (w & ERR_TIMEOUT_DECODE) ? "decode " : "",
+                (w & ERR_TIMEOUT_MMA) ? "mma " : "", (w & ERR_TIMEOUT_EPILOGUE) ? "epilogue " : "",
+                (w & ERR_TIMEOUT_SELFTEST) ? "selftest " : "", (w & ERR_TIMEOUT_OTHER) ? "other " : "");
+  }
+  return DLLM_OK;
+}
+
+DLLM_API size_t dllm_packed_bytes(int type, int64_t n, int64_t k) {
+  if (!block_bytes(type) || n <= 0 || k <= 0 || k % QK) return 0;
+  Packed p = packed_sizes(type, n, k);
+  return p.blob_bytes + p.dd_bytes;
+}
+
+DLLM_API int dllm_pack_weights(int type, const void* blocks, int64_t n, int64_t k, void* packed,
+                               size_t packed_bytes, dllm_stream_t stream) {
+  if (!block_bytes(type))
+    return fail(DLLM_E_TYPE, "dllm_pack_weights: unsupported block type %d: matrix kernels exist for Q4_K (12) and Q6_K (14)",
+                type);
+  if (n <= 0 || k <= 0 || k % QK || n > (1 << 24) || k > (1 << 20))
+    return fail(DLLM_E_SHAPE, "dllm_pack_weights: bad shape n=%lld k=%lld (k must be a positive multiple of 256)",
+                (long long)n, (long long)k);
+  int rc = check_device();
+  if (rc) return rc;
+  CHECK_DEV(blocks, "blocks");
+  CHECK_DEV(packed, "packed");
+  if (!aligned(packed, 256)) return fail(DLLM_E_ALIGN, "dllm_pack_weights: packed must be 256-byte aligned");
+  if (type == DLLM_Q4_K && !aligned(blocks, 16))
+    return fail(DLLM_E_ALIGN, "dllm_pack_weights: Q4_K blocks must be 16-byte aligned");
+  if (type == DLLM_Q6_K && !aligned(blocks, 2))
+    return fail(DLLM_E_ALIGN, "dllm_pack_weights: Q6_K blocks must be 2-byte aligned");
+  const size_t need = dllm_packed_bytes(type, n, k);
+  if (packed_bytes < need)
+    return fail(DLLM_E_WORKSPACE, "dllm_pack_weights: packed buffer has %zu bytes, needs %zu", packed_bytes, need);
+  Packed ps = packed_sizes(type, n, k);
+  const int nsb = (int)(k / QK), tiles = (int)((n + BM - 1) / BM);
+  uint8_t* blob = static_cast<uint8_t*>(packed);
+  uint8_t* dd = blob + ps.blob_bytes;
+  const uint8_t* src = static_cast<const uint8_t*>(blocks);
+  if (type == DLLM_Q4_K)
+    pack_q4k_kernel<<<tiles * nsb, BM, 0, (cudaStream_t)stream>>>(src, (int)n, nsb, blob, dd);
+  else
+    pack_q6k_kernel<<<tiles * nsb, BM, 0, (cudaStream_t)stream>>>(src, (int)n, nsb, blob, dd);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch pack kernel");
+}
+
+DLLM_API int64_t dllm_act_rows(int64_t rows) { return rows > 0 ? act_rows_padded(rows) : 0; }
+
+DLLM_API size_t dllm_act_bytes(int64_t rows, int64_t k) {
+  if (rows <= 0 || k <= 0 || k % QK) return 0;
+  return act_layout(rows, k).bytes;
+}
+
+DLLM_API int dllm_quantize_act(const float* x, int64_t rows, int64_t k, int64_t ldx, const float* norm_w, float eps,
+                               int8_t* q, float* d, int16_t* bsum, void* act, size_t act_bytes,
+                               dllm_stream_t stream) {
+  if (rows <= 0 || rows > 65536 || k <= 0 || k % QK || k > (1 << 20) || ldx < k)
+    return fail(DLLM_E_SHAPE, "dllm_quantize_act: bad shape rows=%lld k=%lld ldx=%lld (k %% 256 == 0, ldx >= k)",
+                (long long)rows, (long long)k, (long long)ldx);
+  int rc = check_device();
+  if (rc) return rc;
+  CHECK_DEV(x, "x");
+  if (!aligned(x, 16) || ldx % 4) return fail(DLLM_E_ALIGN, "dllm_quantize_act: x must be 16-byte aligned, ldx %% 4 == 0");
+  if (norm_w) {
+    CHECK_DEV(norm_w, "norm_w");
+    if (!aligned(norm_w, 16)) return fail(DLLM_E_ALIGN, "dllm_quantize_act: norm_w must be 16-byte aligned");
+  }
+  if (q) {
+    CHECK_DEV(q, "q");
+    if (!aligned(q, 8)) return fail(DLLM_E_ALIGN, "dllm_quantize_act: q must be 8-byte aligned");
+  }
+  if (d) CHECK_DEV(d, "d");
+  if (bsum) CHECK_DEV(bsum, "bsum");
+  QuantOut o{q, d, bsum, nullptr, nullptr, nullptr, 0};
+  int grid = (int)rows;
+  if (act) {
+    CHECK_DEV(act, "act");
+    if (!aligned(act, 256)) return fail(DLLM_E_ALIGN, "dllm_quantize_act: act must be 256-byte aligned");
+    ActLayout L = act_layout(rows, k);
+    if (act_bytes < L.bytes)
+      return fail(DLLM_E_WORKSPACE, "dllm_quantize_act: act buffer has %zu bytes, needs %zu", act_bytes, L.bytes);
+    uint8_t* base = static_cast<uint8_t*>(act);
+    o.act_a = reinterpret_cast<__half*>(base + L.off_a);
+    o.act_j = base + L.off_j;
+    o.act_d = reinterpret_cast<float*>(base + L.off_d);
+    o.lpad = (int)L.lpad;
+    grid = (int)L.lpad;
+  }
+  quantize_act_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(x, (int)rows, k, ldx, norm_w, eps, o);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch quantize_act");
+}
+
+DLLM_API size_t dllm_qgemm_workspace_bytes(int type, int64_t m, int64_t n, int64_t k) {
+  if (!block_bytes(type) || m <= 0 || n <= 0 || k <= 0 || k % QK) return 0;
+  return plan_qgemm(type, m, n, k).ws_bytes;
+}
+
+static int qgemm_common(const char* fn, int type, const void* act, int64_t m, int64_t k, const void* w_packed,
+                        int64_t n, float* y, int64_t ldy, int accumulate, void* ws, size_t ws_bytes,
+                        int32_t* dbg, cudaStream_t stream) {
+  if (!block_bytes(type))
+    return fail(DLLM_E_TYPE, "%s: unsupported block type %d: matrix kernels exist for Q4_K (12) and Q6_K (14)", fn,
+                type);
+  if (m <= 0 || m > 65536 || n <= 0 || n > (1 << 24) || k <= 0 || k % QK || k > (1 << 20))
+    return fail(DLLM_E_SHAPE, "%s: bad shape m=%lld n=%lld k=%lld (k must be a positive multiple of 256)", fn,
+                (long long)m, (long long)n, (long long)k);
+  if (accumulate != 0 && accumulate != 1) return fail(DLLM_E_INVAL, "%s: accumulate must be 0 or 1", fn);
+  int rc = check_device();
+  if (rc) return rc;
+  CHECK_DEV(act, "act");
+  CHECK_DEV(w_packed, "w_packed");
+  if (!aligned(act, 256) || !aligned(w_packed, 256))
+    return fail(DLLM_E_ALIGN, "%s: act and w_packed must be 256-byte aligned", fn);
+  if (y) {
+    CHECK_DEV(y, "y");
+    if (ldy < n) return fail(DLLM_E_SHAPE, "%s: ldy=%lld < n=%lld", fn, (long long)ldy, (long long)n);
+  }
+  QgemmPlan P = plan_qgemm(type, m, n, k);
+  if (dbg) {  // debug sums: one split, direct
+    P.splits = 1;
+    P.sbps = P.nsb;
+    P.units = P.tiles_n * P.tiles_m;
+    P.grid = std::min(P.units, num_sms());
+    P.ws_bytes = 0;
+  }
+  float* out = y;
+  int64_t ld = ldy;
+  int64_t stride = 0;
+  if (P.splits > 1) {
+    if (!ws || ws_bytes < P.ws_bytes)
+      return fail(DLLM_E_WORKSPACE, "%s: workspace has %zu bytes, needs %zu (dllm_qgemm_workspace_bytes)", fn,
+                  ws ? ws_bytes : (size_t)0, P.ws_bytes);
+    CHECK_DEV(ws, "ws");
+    out = static_cast<float*>(ws);
+    ld = n;
+    stride = m * n;
+  }
+  ActLayout L = act_layout(m, k);
+  const uint8_t* abase = static_cast<const uint8_t*>(act);
+  CUtensorMap map;
+  rc = make_act_tmap(&map, abase + L.off_a, L.lpad, k, P.nt);
+  if (rc) return rc;
+  Packed ps = packed_sizes(type, n, k);
+  QgemmParams prm{};
+  prm.wblob = static_cast<const uint8_t*>(w_packed);
+  prm.wdd = prm.wblob + ps.blob_bytes;
+  prm.act_j = abase + L.off_j;
+  prm.act_d = reinterpret_cast<const float*>(abase + L.off_d);
+  prm.nsb = P.nsb;
+  prm.n = (int)n;
+  prm.m = (int)m;
+  prm.lpad = P.lpad;
+  prm.tiles_n = P.tiles_n;
+  prm.tiles_m = P.tiles_m;
+  prm.splits = P.splits;
+  prm.sbps = P.sbps;
+  prm.units = P.units;
+  prm.y = out;
+  prm.ldy = ld;
+  prm.split_stride = stride;
+  prm.accumulate = P.splits > 1 ? 0 : accumulate;
+  prm.dbg = dbg;
+  prm.timeout = kDefaultTimeoutCycles;
+  prm.err = err_word();
+  if (!prm.err) return fail(DLLM_E_CUDA, "%s: cannot resolve the device error word", fn);
+  rc = type == DLLM_Q4_K ? launch_qgemm_q4k(P.nt, map, prm, P.grid, stream)
+                         : launch_qgemm_q6k(P.nt, map, prm, P.grid, stream);
+  if (rc) return rc;
+  if (P.splits > 1 && y) {
+    const int64_t total = m * n;
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4 * num_sms());
+    reduce_splits_kernel<<<blocks, 256, 0, stream>>>(out, P.splits, stride, (int)m, (int)n, y, ldy, accumulate);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch reduce_splits");
+  }
+  return DLLM_OK;
+}
+
+DLLM_API int dllm_qgemm(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n, float* y,
+                        int64_t ldy, int accumulate, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  if (!y) return fail(DLLM_E_INVAL, "dllm_qgemm: y is NULL");
+  return qgemm_common("dllm_qgemm", type, act, m, k, w_packed, n, y, ldy, accumulate, ws, ws_bytes, nullptr,
+                      (cudaStream_t)stream);
+}
+
+DLLM_API int dllm_qgemm_q4k(const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n, float* y,
+                            int64_t ldy, int accumulate, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  if (!y) return fail(DLLM_E_INVAL, "dllm_qgemm_q4k: y is NULL");
+  return qgemm_common("dllm_qgemm_q4k", DLLM_Q4_K, act, m, k, w_packed, n, y, ldy, accumulate, ws, ws_bytes, nullptr,
+                      (cudaStream_t)stream);
+}
+
+DLLM_API int dllm_qgemm_q6k(const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n, float* y,
+                            int64_t ldy, int accumulate, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  if (!y) return fail(DLLM_E_INVAL, "dllm_qgemm_q6k: y is NULL");
+  return qgemm_common("dllm_qgemm_q6k", DLLM_Q6_K, act, m, k, w_packed, n, y, ldy, accumulate, ws, ws_bytes, nullptr,
+                      (cudaStream_t)stream);
+}
+
+DLLM_API int dllm_qgemm_intsums(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
+                                int32_t* sums, dllm_stream_t stream) {
+  if (!is_device_ptr(sums)) return fail(DLLM_E_INVAL, "dllm_qgemm_intsums: sums is NULL or not a device pointer");
+  return qgemm_common("dllm_qgemm_intsums", type, act, m, k, w_packed, n, nullptr, n, 0, nullptr, 0, sums,
+                      (cudaStream_t)stream);
+}
+
+DLLM_API int dllm_selftest_timeout(int64_t limit_cycles, dllm_stream_t stream) {
+  if (limit_cycles <= 0 || limit_cycles > (int64_t)1 << 34)
+    return fail(DLLM_E_INVAL, "dllm_selftest_timeout: limit_cycles out of range");
+  int rc = check_device();
+  if (rc) return rc;
+  selftest_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((long long)limit_cycles);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch selftest_timeout");
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "dllm.h"
+
+namespace dllm {
+
+struct QgemmParams;
+
+// Status helpers: record an actionable message for dllm_last_error() and return the code.
+int fail(int code, const char* fmt, ...);
+int cuda_fail(cudaError_t e, const char* what);
+
+// Device properties of the current device (cached per device).
+int num_sms();
+int check_device();  // DLLM_OK if the current device is sm_103
+int* err_word();     // device address of the current device's error word (nullptr on failure)
+
+// Activation operand layout ("act" buffer of dllm_quantize_act).
+struct ActLayout {
+  int64_t rows, k, lpad, nsb;
+  size_t off_a, off_j, off_d, bytes;
+};
+ActLayout act_layout(int64_t rows, int64_t k);
+int64_t act_rows_padded(int64_t rows);
+
+// Tensor map over the A-plane of an act buffer (3-D: 64 x lpad x k/64, f16, 128-byte swizzle,
+// box 64 x nt x 1).
+int make_act_tmap(CUtensorMap* map, const void* act_a, int64_t lpad, int64_t k, int nt);
+
+// GEMM launch plan.
+struct QgemmPlan {
+  int nt, lpad, tiles_n, tiles_m, splits, sbps, units, grid, nsb;
+  size_t ws_bytes;
+};
+QgemmPlan plan_qgemm(int type, int64_t m, int64_t n, int64_t k);
+
+// Launch the tcgen05 GEMM kernel instantiated for (type, nt) (defined in qgemm_q4k.cu /
+// qgemm_q6k.cu). Returns DLLM_OK or a status.
+int launch_qgemm_q4k(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s);
+int launch_qgemm_q6k(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s);
+
+constexpr long long kDefaultTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+}  // namespace dllm

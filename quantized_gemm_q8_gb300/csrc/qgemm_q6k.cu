@@ -1,0 +1,29 @@
+// Instantiations and launcher of the tcgen05 quantized GEMM for Q6_K weights.
+#include "internal.h"
+#include "qgemm.cuh"
+
+namespace dllm {
+
+template <int NT>
+static int launch_one(const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s) {
+  constexpr int SMEM = QCfg<TYPE_Q6K, NT>::SMEM;
+  auto* k = &qgemm_kernel<TYPE_Q6K, NT>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(qgemm_q6k)");
+  k<<<grid, QG_THREADS, SMEM, s>>>(map, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch qgemm_q6k");
+  return DLLM_OK;
+}
+
+int launch_qgemm_q6k(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s) {
+  switch (nt) {
+    case 32: return launch_one<32>(map, p, grid, s);
+    case 64: return launch_one<64>(map, p, grid, s);
+    case 128: return launch_one<128>(map, p, grid, s);
+    case 160: return launch_one<160>(map, p, grid, s);
+    default: return fail(DLLM_E_SHAPE, "qgemm_q6k: unsupported token tile %d", nt);
+  }
+}
+
+}  // namespace dllm

@@ -1,0 +1,45 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, and exports every call that
+include/dllm.h declares (no compute calls: this runs on CPU)."""
+import ctypes
+import os
+import re
+
+import quantized_gemm_q8_gb300 as dl
+from quantized_gemm_q8_gb300 import build as dlbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for f in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names += re.findall(r"DLLM_API\s+[\w\s\*]+?\b(dllm_\w+)\s*\(", src)
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    dlbuild.build()
+    lib = ctypes.CDLL(dl.LIB_PATH)
+    names = _declared()
+    assert len(names) >= 10
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_declared_symbols():
+    names = set(_declared())
+    assert names <= set(dl._SIGS), sorted(names - set(dl._SIGS))
+
+
+def test_host_only_calls():
+    dlbuild.build()
+    L = dl.lib()
+    assert L.dllm_version() >= 100
+    assert L.dllm_packed_bytes(12, 4096, 4096) == 4096 * 16 * 144
+    assert L.dllm_packed_bytes(14, 126464, 4096) == 126464 * 16 * 210
+    assert L.dllm_packed_bytes(13, 128, 256) == 0
+    assert L.dllm_act_rows(148) == 160 and L.dllm_act_rows(16) == 32 and L.dllm_act_rows(512) == 512
+    assert L.dllm_act_bytes(148, 4096) >= 160 * 4096 * 2
+    assert L.dllm_act_bytes(148, 300) == 0
