@@ -30,6 +30,12 @@ int* err_word() {
 
 static thread_local char g_msg[1024] = "";
 
+#ifdef DLLM_TRACE
+// Trace builds only: device buffer of 8 x 256 clock64 stamps written by CTA 0 of each GEMM.
+static unsigned long long* g_trace = nullptr;
+extern "C" DLLM_API void dllm_trace_set(unsigned long long* buf) { g_trace = buf; }
+#endif
+
 int fail(int code, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -569,6 +575,9 @@ static int qgemm_common(const char* fn, int type, const void* act, int64_t m, in
   prm.dbg = dbg;
   prm.timeout = kDefaultTimeoutCycles;
   prm.err = err_word();
+#ifdef DLLM_TRACE
+  prm.trace = g_trace;
+#endif
   if (!prm.err) return fail(DLLM_E_CUDA, "%s: cannot resolve the device error word", fn);
   rc = type == DLLM_Q4_K ? launch_qgemm_q4k(P.nt, map, prm, P.grid, stream)
                          : launch_qgemm_q6k(P.nt, map, prm, P.grid, stream);
