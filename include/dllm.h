@@ -156,6 +156,28 @@ DLLM_API int dllm_qgemm_q6k(const void* act, int64_t m, int64_t k, const void* w
 DLLM_API int dllm_qgemm_intsums(int type, const void* act, int64_t m, int64_t k, const void* w_packed,
                                 int64_t n, int32_t* sums, dllm_stream_t stream);
 
+/* ---- masked-rows-only LM head + softmax confidence + top-k commit ([RM-HW], [DP-CD], [TS12]) --
+ * For the block positions p in [block_begin, block_end) (R = block_end - block_begin, 1..160):
+ *   1. h_p = RMSNorm(hidden[p]) * out_norm_w (eps; out_norm_w f32 [d], required), Q8_K;
+ *   2. logits_p = h_p x W_out^T over all `vocab` rows of the packed Q6_K head (the GEMM above);
+ *      the logits are reduced on the fly (never stored): per row, argmax id (lowest id on ties)
+ *      and confidence = softmax(logits_p)[argmax] = 1 / sum_v exp(logit_v - logit_max);
+ *   3. among the positions with canvas[p] == mask_id, the k_commit with the highest confidence
+ *      (ties: lowest position) get canvas[p] = argmax id.
+ * hidden: f32 [L][ldh] (row stride ldh >= d, ldh % 4 == 0). canvas: int32 [L], updated in place.
+ * out_pos / out_id (int32 [k_commit]) and out_conf (f32 [k_commit], may be NULL) receive the
+ * commits in selection order (descending confidence); entries past the number of masked
+ * positions are -1 / -1 / 0. row_id / row_conf (length R, may be NULL) receive every block row's
+ * argmax id and confidence (masked or not). ws: >= dllm_lmhead_workspace_bytes(R, vocab, d),
+ * 256-byte aligned. Errors: DLLM_E_SHAPE, DLLM_E_INVAL (block range, k_commit), DLLM_E_ALIGN,
+ * DLLM_E_WORKSPACE. */
+DLLM_API size_t dllm_lmhead_workspace_bytes(int64_t rows, int64_t vocab, int64_t d);
+DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d, int64_t ldh, const float* out_norm_w,
+                                       float eps, const void* w_out_packed, int64_t vocab, int32_t* canvas,
+                                       int32_t mask_id, int32_t block_begin, int32_t block_end, int32_t k_commit,
+                                       int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id,
+                                       float* row_conf, void* ws, size_t ws_bytes, dllm_stream_t stream);
+
 /* Test hook for failure detection: launches one kernel whose mbarrier wait can never
  * complete, bounded by `limit_cycles` SM clock cycles; the kernel then records a timeout
  * in the device error word and returns. dllm_check() afterwards reports DLLM_E_TIMEOUT. */

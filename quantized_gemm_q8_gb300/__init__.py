@@ -48,6 +48,9 @@ _SIGS = {
     "dllm_qgemm_q6k": ([P, I64, I64, P, I64, P, I64, INT, P, SZ, P], INT),
     "dllm_qgemm_intsums": ([INT, P, I64, I64, P, I64, P, P], INT),
     "dllm_selftest_timeout": ([I64, P], INT),
+    "dllm_lmhead_workspace_bytes": ([I64, I64, I64], SZ),
+    "dllm_lmhead_masked_select": ([P, I64, I64, I64, P, F32, P, I64, P, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P],
+                                  INT),
 }
 
 
@@ -166,3 +169,37 @@ def qgemm_intsums(type_id: int, act: torch.Tensor, m: int, k: int, w_packed: tor
 
 def selftest_timeout(limit_cycles: int, stream=None):
     _ok(lib().dllm_selftest_timeout(limit_cycles, _stream(stream)))
+
+
+# --- LM head + commit --------------------------------------------------------------------------
+
+def lmhead_workspace_bytes(rows: int, vocab: int, d: int) -> int:
+    return int(lib().dllm_lmhead_workspace_bytes(rows, vocab, d))
+
+
+def lmhead_masked_select(hidden: torch.Tensor, canvas: torch.Tensor, mask_id: int, block_begin: int,
+                         block_end: int, k_commit: int, out_norm_w: torch.Tensor, w_out_packed: torch.Tensor,
+                         vocab: int, eps: float = 1e-5, ws: torch.Tensor | None = None, stream=None) -> dict:
+    """Masked-rows-only LM head + softmax confidence + top-k commit; updates `canvas` in place.
+    Returns dict(pos, id, conf [k_commit], row_id, row_conf [block rows])."""
+    L, d = hidden.shape
+    R = block_end - block_begin
+    dev = hidden.device
+    out = {
+        "pos": torch.empty(max(k_commit, 1), dtype=torch.int32, device=dev),
+        "id": torch.empty(max(k_commit, 1), dtype=torch.int32, device=dev),
+        "conf": torch.empty(max(k_commit, 1), dtype=torch.float32, device=dev),
+        "row_id": torch.empty(R, dtype=torch.int32, device=dev),
+        "row_conf": torch.empty(R, dtype=torch.float32, device=dev),
+    }
+    nb = lmhead_workspace_bytes(R, vocab, d)
+    if ws is None:
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
+    _ok(lib().dllm_lmhead_masked_select(_ptr(hidden), L, d, hidden.stride(0), _ptr(out_norm_w), eps,
+                                        _ptr(w_out_packed), vocab, _ptr(canvas), mask_id, block_begin, block_end,
+                                        k_commit, _ptr(out["pos"]), _ptr(out["id"]), _ptr(out["conf"]),
+                                        _ptr(out["row_id"]), _ptr(out["row_conf"]), _ptr(ws), ws.numel(),
+                                        _stream(stream)))
+    for key in ("pos", "id", "conf"):
+        out[key] = out[key][:k_commit]
+    return out

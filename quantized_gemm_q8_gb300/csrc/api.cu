@@ -358,6 +358,112 @@ __global__ void selftest_timeout_kernel(long long limit) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// LM head: merge of the per-(tile, quadrant) softmax partials and top-k commit
+// ---------------------------------------------------------------------------------------------
+struct SoftPart {
+  float m;  // max logit
+  int a;    // its token id (lowest on ties)
+  float s;  // sum exp(logit - m)
+};
+
+__device__ __forceinline__ SoftPart soft_merge(SoftPart x, SoftPart y) {
+  if (y.m > x.m || (y.m == x.m && y.a < x.a)) {
+    const SoftPart t = x;
+    x = y;
+    y = t;
+  }
+  // x has the larger max (or the lower id at equal max)
+  x.s = x.s + (y.s == 0.f ? 0.f : y.s * expf(y.m - x.m));
+  return x;
+}
+
+// One CTA of 1024 threads: warp w merges rows w, w+32, ... over the P partials of each row,
+// then warp 0 picks the k masked positions of the block with the highest confidence (ties:
+// lowest position) and scatters their ids into the canvas.
+__global__ void __launch_bounds__(1024) lmhead_merge_commit_kernel(
+    const float* __restrict__ pmax, const int* __restrict__ parg, const float* __restrict__ psum, int P, int R,
+    int32_t* canvas, int32_t mask_id, int b0, int k, int32_t* out_pos, int32_t* out_id, float* out_conf,
+    int32_t* row_id, float* row_conf) {
+  __shared__ float conf_s[1024];
+  __shared__ int id_s[1024];
+  __shared__ int cand_s[1024];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int r = warp; r < R; r += 32) {
+    SoftPart acc{-INFINITY, 0x7fffffff, 0.f};
+    for (int i = lane; i < P; i += 32) {
+      const size_t o = (size_t)i * R + r;
+      acc = soft_merge(acc, SoftPart{pmax[o], parg[o], psum[o]});
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      SoftPart o{__shfl_xor_sync(0xffffffffu, acc.m, off), __shfl_xor_sync(0xffffffffu, acc.a, off),
+                 __shfl_xor_sync(0xffffffffu, acc.s, off)};
+      acc = soft_merge(acc, o);
+    }
+    if (lane == 0) {
+      const float c = 1.0f / acc.s;  // softmax probability of the argmax token
+      conf_s[r] = c;
+      id_s[r] = acc.a;
+      cand_s[r] = canvas[b0 + r] == mask_id;
+      if (row_id) row_id[r] = acc.a;
+      if (row_conf) row_conf[r] = c;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  for (int step = 0; step < k; ++step) {
+    float best = -1.f;
+    int bp = 0x7fffffff;
+    for (int r = lane; r < R; r += 32)
+      if (cand_s[r] && (conf_s[r] > best || (conf_s[r] == best && r < bp))) {
+        best = conf_s[r];
+        bp = r;
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+      const int op = __shfl_xor_sync(0xffffffffu, bp, off);
+      if (ob > best || (ob == best && op < bp)) {
+        best = ob;
+        bp = op;
+      }
+    }
+    if (lane == 0) {
+      if (bp != 0x7fffffff) {
+        cand_s[bp] = 0;
+        out_pos[step] = b0 + bp;
+        out_id[step] = id_s[bp];
+        if (out_conf) out_conf[step] = conf_s[bp];
+      } else {
+        out_pos[step] = -1;
+        out_id[step] = -1;
+        if (out_conf) out_conf[step] = 0.f;
+      }
+    }
+    __syncwarp();
+  }
+  if (lane == 0)
+    for (int step = 0; step < k; ++step)
+      if (out_pos[step] >= 0) canvas[out_pos[step]] = out_id[step];
+}
+
+struct LmheadWs {
+  size_t act, pmax, parg, psum, bytes;
+  int P;
+};
+static LmheadWs lmhead_ws(int64_t R, int64_t vocab, int64_t d) {
+  LmheadWs w;
+  const int64_t tiles = (vocab + BM - 1) / BM;
+  w.P = (int)(tiles * 4);
+  w.act = 0;
+  w.pmax = align_up(act_layout(R, d).bytes, 256);
+  w.parg = w.pmax + align_up((size_t)w.P * R * 4, 256);
+  w.psum = w.parg + align_up((size_t)w.P * R * 4, 256);
+  w.bytes = w.psum + align_up((size_t)w.P * R * 4, 256);
+  return w;
+}
+
+// ---------------------------------------------------------------------------------------------
 // GEMM plan
 // ---------------------------------------------------------------------------------------------
 QgemmPlan plan_qgemm(int type, int64_t m, int64_t n, int64_t k) {
@@ -390,6 +496,18 @@ QgemmPlan plan_qgemm(int type, int64_t m, int64_t n, int64_t k) {
   return P;
 }
 
+
+// Quantize `rows` rows of x into the operand form at `act` (no validation).
+int quantize_rows(const float* x, int64_t rows, int64_t k, int64_t ldx, const float* norm_w, float eps, void* act,
+                  cudaStream_t stream) {
+  ActLayout L = act_layout(rows, k);
+  uint8_t* base = static_cast<uint8_t*>(act);
+  QuantOut o{nullptr, nullptr, nullptr, reinterpret_cast<__half*>(base + L.off_a), base + L.off_j,
+             reinterpret_cast<float*>(base + L.off_d), (int)L.lpad};
+  quantize_act_kernel<<<(int)L.lpad, 256, 0, stream>>>(x, (int)rows, k, ldx, norm_w, eps, o);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch quantize_act");
+}
 }  // namespace dllm
 
 using namespace dllm;
@@ -508,6 +626,83 @@ DLLM_API size_t dllm_qgemm_workspace_bytes(int type, int64_t m, int64_t n, int64
   return plan_qgemm(type, m, n, k).ws_bytes;
 }
 
+// Launch one GEMM (no argument validation; callers validate). `P` is the plan; when
+// P.splits > 1 the kernel writes split partials [splits][m][n] to `partial`, otherwise it
+// writes y directly (mode 0) or the LM-head softmax partials (mode 1).
+struct GemmLaunch {
+  int type;
+  const void* act;
+  int64_t m, k;
+  const void* w;
+  int64_t n;
+  float* y;
+  int64_t ldy;
+  int accumulate;
+  float* partial;
+  int mode;
+  float* pmax;
+  int* parg;
+  float* psum;
+  int32_t* dbg;
+};
+
+static int launch_gemm(const GemmLaunch& g, const QgemmPlan& P, cudaStream_t stream) {
+  ActLayout L = act_layout(g.m, g.k);
+  const uint8_t* abase = static_cast<const uint8_t*>(g.act);
+  CUtensorMap map;
+  int rc = make_act_tmap(&map, abase + L.off_a, L.lpad, g.k, P.nt);
+  if (rc) return rc;
+  Packed ps = packed_sizes(g.type, g.n, g.k);
+  QgemmParams prm{};
+  prm.wblob = static_cast<const uint8_t*>(g.w);
+  prm.wdd = prm.wblob + ps.blob_bytes;
+  prm.act_j = abase + L.off_j;
+  prm.act_d = reinterpret_cast<const float*>(abase + L.off_d);
+  prm.nsb = P.nsb;
+  prm.n = (int)g.n;
+  prm.m = (int)g.m;
+  prm.lpad = P.lpad;
+  prm.tiles_n = P.tiles_n;
+  prm.tiles_m = P.tiles_m;
+  prm.splits = P.splits;
+  prm.sbps = P.sbps;
+  prm.units = P.units;
+  if (P.splits > 1) {
+    prm.y = g.partial;
+    prm.ldy = g.n;
+    prm.split_stride = g.m * g.n;
+    prm.accumulate = 0;
+  } else {
+    prm.y = g.y;
+    prm.ldy = g.ldy;
+    prm.split_stride = 0;
+    prm.accumulate = g.accumulate;
+  }
+  prm.mode = g.mode;
+  prm.pmax = g.pmax;
+  prm.parg = g.parg;
+  prm.psum = g.psum;
+  prm.dbg = g.dbg;
+  prm.timeout = kDefaultTimeoutCycles;
+  prm.err = err_word();
+  if (!prm.err) return fail(DLLM_E_CUDA, "cannot resolve the device error word");
+#ifdef DLLM_TRACE
+  prm.trace = g_trace;
+#endif
+  return g.type == DLLM_Q4_K ? launch_qgemm_q4k(P.nt, map, prm, P.grid, stream)
+                             : launch_qgemm_q6k(P.nt, map, prm, P.grid, stream);
+}
+
+static QgemmPlan plan_single_split(int type, int64_t m, int64_t n, int64_t k) {
+  QgemmPlan P = plan_qgemm(type, m, n, k);
+  P.splits = 1;
+  P.sbps = P.nsb;
+  P.units = P.tiles_n * P.tiles_m;
+  P.grid = std::min(P.units, num_sms());
+  P.ws_bytes = 0;
+  return P;
+}
+
 static int qgemm_common(const char* fn, int type, const void* act, int64_t m, int64_t k, const void* w_packed,
                         int64_t n, float* y, int64_t ldy, int accumulate, void* ws, size_t ws_bytes,
                         int32_t* dbg, cudaStream_t stream) {
@@ -528,64 +723,21 @@ static int qgemm_common(const char* fn, int type, const void* act, int64_t m, in
     CHECK_DEV(y, "y");
     if (ldy < n) return fail(DLLM_E_SHAPE, "%s: ldy=%lld < n=%lld", fn, (long long)ldy, (long long)n);
   }
-  QgemmPlan P = plan_qgemm(type, m, n, k);
-  if (dbg) {  // debug sums: one split, direct
-    P.splits = 1;
-    P.sbps = P.nsb;
-    P.units = P.tiles_n * P.tiles_m;
-    P.grid = std::min(P.units, num_sms());
-    P.ws_bytes = 0;
-  }
-  float* out = y;
-  int64_t ld = ldy;
-  int64_t stride = 0;
+  QgemmPlan P = dbg ? plan_single_split(type, m, n, k) : plan_qgemm(type, m, n, k);
   if (P.splits > 1) {
     if (!ws || ws_bytes < P.ws_bytes)
       return fail(DLLM_E_WORKSPACE, "%s: workspace has %zu bytes, needs %zu (dllm_qgemm_workspace_bytes)", fn,
                   ws ? ws_bytes : (size_t)0, P.ws_bytes);
     CHECK_DEV(ws, "ws");
-    out = static_cast<float*>(ws);
-    ld = n;
-    stride = m * n;
   }
-  ActLayout L = act_layout(m, k);
-  const uint8_t* abase = static_cast<const uint8_t*>(act);
-  CUtensorMap map;
-  rc = make_act_tmap(&map, abase + L.off_a, L.lpad, k, P.nt);
-  if (rc) return rc;
-  Packed ps = packed_sizes(type, n, k);
-  QgemmParams prm{};
-  prm.wblob = static_cast<const uint8_t*>(w_packed);
-  prm.wdd = prm.wblob + ps.blob_bytes;
-  prm.act_j = abase + L.off_j;
-  prm.act_d = reinterpret_cast<const float*>(abase + L.off_d);
-  prm.nsb = P.nsb;
-  prm.n = (int)n;
-  prm.m = (int)m;
-  prm.lpad = P.lpad;
-  prm.tiles_n = P.tiles_n;
-  prm.tiles_m = P.tiles_m;
-  prm.splits = P.splits;
-  prm.sbps = P.sbps;
-  prm.units = P.units;
-  prm.y = out;
-  prm.ldy = ld;
-  prm.split_stride = stride;
-  prm.accumulate = P.splits > 1 ? 0 : accumulate;
-  prm.dbg = dbg;
-  prm.timeout = kDefaultTimeoutCycles;
-  prm.err = err_word();
-#ifdef DLLM_TRACE
-  prm.trace = g_trace;
-#endif
-  if (!prm.err) return fail(DLLM_E_CUDA, "%s: cannot resolve the device error word", fn);
-  rc = type == DLLM_Q4_K ? launch_qgemm_q4k(P.nt, map, prm, P.grid, stream)
-                         : launch_qgemm_q6k(P.nt, map, prm, P.grid, stream);
+  GemmLaunch g{type, act, m, k, w_packed, n, y, ldy, accumulate, static_cast<float*>(ws), 0, nullptr, nullptr, nullptr, dbg};
+  rc = launch_gemm(g, P, stream);
   if (rc) return rc;
   if (P.splits > 1 && y) {
     const int64_t total = m * n;
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4 * num_sms());
-    reduce_splits_kernel<<<blocks, 256, 0, stream>>>(out, P.splits, stride, (int)m, (int)n, y, ldy, accumulate);
+    reduce_splits_kernel<<<blocks, 256, 0, stream>>>(static_cast<float*>(ws), P.splits, m * n, (int)m, (int)n, y,
+                                                     ldy, accumulate);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch reduce_splits");
   }
@@ -628,6 +780,69 @@ DLLM_API int dllm_selftest_timeout(int64_t limit_cycles, dllm_stream_t stream) {
   selftest_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((long long)limit_cycles);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch selftest_timeout");
+}
+
+
+DLLM_API size_t dllm_lmhead_workspace_bytes(int64_t rows, int64_t vocab, int64_t d) {
+  if (rows <= 0 || rows > 160 || vocab <= 0 || d <= 0 || d % QK) return 0;
+  return lmhead_ws(rows, vocab, d).bytes;
+}
+
+DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d, int64_t ldh, const float* out_norm_w,
+                                       float eps, const void* w_out_packed, int64_t vocab, int32_t* canvas,
+                                       int32_t mask_id, int32_t block_begin, int32_t block_end, int32_t k_commit,
+                                       int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id,
+                                       float* row_conf, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  const int64_t R = (int64_t)block_end - block_begin;
+  if (L <= 0 || d <= 0 || d % QK || d > (1 << 20) || ldh < d || vocab <= 0 || vocab > (1 << 24))
+    return fail(DLLM_E_SHAPE, "dllm_lmhead_masked_select: bad shape L=%lld d=%lld ldh=%lld vocab=%lld", (long long)L,
+                (long long)d, (long long)ldh, (long long)vocab);
+  if (block_begin < 0 || block_end > L || R <= 0 || R > 160)
+    return fail(DLLM_E_INVAL, "dllm_lmhead_masked_select: block [%d, %d) must lie in [0, L=%lld) and hold 1..160 positions",
+                block_begin, block_end, (long long)L);
+  if (k_commit < 0 || k_commit > R)
+    return fail(DLLM_E_INVAL, "dllm_lmhead_masked_select: k_commit=%d must be in [0, %lld]", k_commit, (long long)R);
+  int rc = check_device();
+  if (rc) return rc;
+  CHECK_DEV(hidden, "hidden");
+  CHECK_DEV(w_out_packed, "w_out_packed");
+  CHECK_DEV(canvas, "canvas");
+  if (k_commit > 0) {
+    CHECK_DEV(out_pos, "out_pos");
+    CHECK_DEV(out_id, "out_id");
+  }
+  if (out_conf) CHECK_DEV(out_conf, "out_conf");
+  if (row_id) CHECK_DEV(row_id, "row_id");
+  if (row_conf) CHECK_DEV(row_conf, "row_conf");
+  CHECK_DEV(out_norm_w, "out_norm_w");
+  if (!aligned(out_norm_w, 16)) return fail(DLLM_E_ALIGN, "dllm_lmhead_masked_select: out_norm_w must be 16-byte aligned");
+  if (!aligned(hidden, 16) || ldh % 4 || !aligned(w_out_packed, 256))
+    return fail(DLLM_E_ALIGN, "dllm_lmhead_masked_select: hidden 16-byte aligned with ldh %% 4 == 0, w_out_packed 256-byte aligned");
+  const LmheadWs W = lmhead_ws(R, vocab, d);
+  if (!ws || ws_bytes < W.bytes)
+    return fail(DLLM_E_WORKSPACE, "dllm_lmhead_masked_select: workspace has %zu bytes, needs %zu", ws ? ws_bytes : (size_t)0,
+                W.bytes);
+  CHECK_DEV(ws, "ws");
+  if (!aligned(ws, 256)) return fail(DLLM_E_ALIGN, "dllm_lmhead_masked_select: ws must be 256-byte aligned");
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  // 1) RMSNorm + Q8_K of the block's rows (contiguous in the residual stream)
+  rc = quantize_rows(hidden + (int64_t)block_begin * ldh, R, d, ldh, out_norm_w, eps, base + W.act, s);
+  if (rc) return rc;
+  // 2) Q6_K head GEMM with the softmax-partial epilogue (one split: logits complete per tile)
+  QgemmPlan P = plan_single_split(DLLM_Q6_K, R, vocab, d);
+  GemmLaunch g{DLLM_Q6_K, base + W.act, R, d, w_out_packed, vocab, nullptr, 0, 0, nullptr, 1,
+               reinterpret_cast<float*>(base + W.pmax), reinterpret_cast<int*>(base + W.parg),
+               reinterpret_cast<float*>(base + W.psum), nullptr};
+  rc = launch_gemm(g, P, s);
+  if (rc) return rc;
+  // 3) merge, confidence, top-k commit
+  lmhead_merge_commit_kernel<<<1, 1024, 0, s>>>(reinterpret_cast<float*>(base + W.pmax),
+                                                reinterpret_cast<int*>(base + W.parg),
+                                                reinterpret_cast<float*>(base + W.psum), W.P, (int)R, canvas, mask_id,
+                                                block_begin, k_commit, out_pos, out_id, out_conf, row_id, row_conf);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch lmhead_merge_commit");
 }
 
 }  // extern "C"

@@ -45,6 +45,10 @@ QgemmPlan plan_qgemm(int type, int64_t m, int64_t n, int64_t k);
 int launch_qgemm_q4k(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s);
 int launch_qgemm_q6k(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s);
 
+// Quantize rows of x into the operand form (internal, no validation).
+int quantize_rows(const float* x, int64_t rows, int64_t k, int64_t ldx, const float* norm_w, float eps, void* act,
+                  cudaStream_t stream);
+
 constexpr long long kDefaultTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 }  // namespace dllm

@@ -124,6 +124,13 @@ struct QgemmParams {
   int accumulate;
   int32_t* dbg;  // [2][nsb][m][n] or null
   int* err;      // device error word
+  // mode 1 (LM head): instead of y, per (weight tile, TMEM lane quadrant, token) softmax
+  // partials over the 32 weight rows of the quadrant: max logit, its row (lowest on ties),
+  // and sum_rows exp(logit - max); layout [tiles_n * 4][m].
+  int mode;
+  float* pmax;
+  int* parg;
+  float* psum;
 #ifdef DLLM_TRACE
   unsigned long long* trace;  // per-role clock64 stamps of CTA 0 (trace builds only)
 #endif
@@ -611,7 +618,32 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         if (lane == 0) mbar_arrive(BAR(C::BX_EMPTY + x));
       }
       if (!ok) break;
-      if (p.y != nullptr && grow < p.n) {
+      if (p.mode == 1) {
+#pragma unroll
+        for (int j = 0; j < NC; ++j) {
+          float v = grow < p.n ? acc[j] : -INFINITY;
+          int idx = grow;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, idx, off);
+            if (ov > v || (ov == v && oi < idx)) {
+              v = ov;
+              idx = oi;
+            }
+          }
+          float e = grow < p.n ? expf(acc[j] - v) : 0.f;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
+          const int tok = tokb + j;
+          if (lane == 0 && tok < p.m) {
+            const size_t o = ((size_t)tn * 4 + qd) * p.m + tok;
+            p.pmax[o] = v;
+            p.parg[o] = idx;
+            p.psum[o] = e;
+          }
+        }
+      } else if (p.y != nullptr && grow < p.n) {
         float* dst = p.y + (size_t)sp * p.split_stride + grow;
 #pragma unroll
         for (int j = 0; j < NC; ++j) {
