@@ -178,6 +178,59 @@ DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d
                                        int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id,
                                        float* row_conf, void* ws, size_t ws_bytes, dllm_stream_t stream);
 
+/* ---- LLaDA layer stream and full denoising step ([TS11], [DP-MF], [TS12]) -------------------
+ * Weights of one layer (device pointers). Q and K are packed as ONE Q4_K matrix of 2*d rows
+ * (rows 0..d-1 = Q, d..2d-1 = K); gate and up as ONE Q4_K matrix of 2*d_ff rows (rows
+ * 0..d_ff-1 = gate, d_ff..2*d_ff-1 = up); all from dllm_pack_weights. */
+typedef struct dllm_layer {
+  const void* wqk;         /* packed Q4_K [2d][d]      */
+  const void* wv;          /* packed Q6_K [d][d]       */
+  const void* wo;          /* packed Q4_K [d][d]       */
+  const void* wgu;         /* packed Q4_K [2 d_ff][d]  */
+  const void* wdown;       /* packed Q6_K [d][d_ff]    */
+  const float* attn_norm;  /* f32 [d]                  */
+  const float* ffn_norm;   /* f32 [d]                  */
+} dllm_layer;
+
+typedef struct dllm_model {
+  int32_t n_layers, d_model, n_heads, head_dim, d_ff, vocab, mask_id;
+  float eps, rope_theta;
+  const dllm_layer* layers; /* HOST array of n_layers entries holding device pointers          */
+  const void* tok_embd;     /* GGUF Q4_K blocks [vocab][d_model/256] (device, unpacked AoS)    */
+  const float* out_norm;    /* f32 [d_model] (device)                                          */
+  const void* w_out;        /* packed Q6_K [vocab][d_model] (device)                           */
+} dllm_model;
+
+enum { DLLM_STREAM_LINEAR = 0, DLLM_STREAM_FULL = 1 };
+
+/* dllm_step_linear_stream: the per-layer stream over all model->n_layers layers on L canvas
+ * rows; x is f32 [L][d_model] (row stride d_model, 16-byte aligned).
+ *   DLLM_STREAM_FULL:   x = embedding of canvas (int32 [L] token ids); every layer runs
+ *       x_n = RMSNorm(x) * attn_norm -> Q8_K -> [Q|K] (Q4_K), V (Q6_K) -> NORM RoPE on Q, K
+ *       (theta, positions 0..L-1) -> non-causal attention (softmax(QK^T/sqrt(hd)) V) -> Q8_K
+ *       -> O (Q4_K) -> x += O; RMSNorm(x) * ffn_norm -> Q8_K -> [gate|up] (Q4_K) ->
+ *       silu(gate) * up -> Q8_K -> down (Q6_K) -> x += down. On return x holds the final
+ *       residual stream (before the output norm).
+ *   DLLM_STREAM_LINEAR: x is the input and is updated in place by the same stream without
+ *       attention: the O projection consumes the V projection's output (canvas unused).
+ * ws: >= dllm_step_workspace_bytes(m, L, flags), 1024-byte aligned; it holds the quantized
+ * activations, the split-K partials of every projection and the attention buffers.
+ * Limits: d_model and d_ff multiples of 256, head_dim == 128, L <= 8192. */
+DLLM_API size_t dllm_step_workspace_bytes(const dllm_model* m, int64_t L, int flags);
+DLLM_API int dllm_step_linear_stream(const dllm_model* m, const int32_t* canvas, int64_t L, float* x, int flags,
+                                     void* ws, size_t ws_bytes, dllm_stream_t stream);
+
+/* dllm_denoise_step: one full denoising step = DLLM_STREAM_FULL forward over the canvas,
+ * then dllm_lmhead_masked_select on the block [block_begin, block_end) with k_commit
+ * commits (canvas updated in place; out_* as there). hidden_out (f32 [L][d_model], may be
+ * NULL) receives the final residual stream. ws: >= dllm_denoise_workspace_bytes(m, L,
+ * block_end - block_begin), 1024-byte aligned. */
+DLLM_API size_t dllm_denoise_workspace_bytes(const dllm_model* m, int64_t L, int32_t block_rows);
+DLLM_API int dllm_denoise_step(const dllm_model* m, int32_t* canvas, int64_t L, int32_t block_begin,
+                               int32_t block_end, int32_t k_commit, int32_t* out_pos, int32_t* out_id,
+                               float* out_conf, float* hidden_out, void* ws, size_t ws_bytes,
+                               dllm_stream_t stream);
+
 /* Test hook for failure detection: launches one kernel whose mbarrier wait can never
  * complete, bounded by `limit_cycles` SM clock cycles; the kernel then records a timeout
  * in the device error word and returns. dllm_check() afterwards reports DLLM_E_TIMEOUT. */

@@ -51,6 +51,10 @@ _SIGS = {
     "dllm_lmhead_workspace_bytes": ([I64, I64, I64], SZ),
     "dllm_lmhead_masked_select": ([P, I64, I64, I64, P, F32, P, I64, P, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P],
                                   INT),
+    "dllm_step_workspace_bytes": ([P, I64, INT], SZ),
+    "dllm_step_linear_stream": ([P, P, I64, P, INT, P, SZ, P], INT),
+    "dllm_denoise_workspace_bytes": ([P, I64, I32], SZ),
+    "dllm_denoise_step": ([P, P, I64, I32, I32, I32, P, P, P, P, P, SZ, P], INT),
 }
 
 
@@ -202,4 +206,108 @@ def lmhead_masked_select(hidden: torch.Tensor, canvas: torch.Tensor, mask_id: in
                                         _stream(stream)))
     for key in ("pos", "id", "conf"):
         out[key] = out[key][:k_commit]
+    return out
+
+
+# --- model, layer stream and denoising step ------------------------------------------------------
+
+STREAM_LINEAR = 0
+STREAM_FULL = 1
+
+
+class _Layer(C.Structure):
+    _fields_ = [("wqk", P), ("wv", P), ("wo", P), ("wgu", P), ("wdown", P), ("attn_norm", P), ("ffn_norm", P)]
+
+
+class _Model(C.Structure):
+    _fields_ = [("n_layers", I32), ("d_model", I32), ("n_heads", I32), ("head_dim", I32), ("d_ff", I32),
+                ("vocab", I32), ("mask_id", I32), ("eps", F32), ("rope_theta", F32), ("layers", C.POINTER(_Layer)),
+                ("tok_embd", P), ("out_norm", P), ("w_out", P)]
+
+
+class DeviceModel:
+    """Device copy of a LLaDA-shaped model: packed projections, norms, token table, head.
+
+    `layers` is a list of dicts of GGUF block arrays (numpy, as from synth.layer_weights);
+    `tok_embd` the Q4_K token table blocks; `head` a dict(w_out=Q6_K blocks, out_norm=f32).
+    The device tensors are kept alive by this object; `.ref` is the C struct pointer."""
+
+    def __init__(self, dims: dict, layers: list, tok_embd=None, head=None, device="cuda"):
+        import numpy as np
+
+        self.dims = dict(dims)
+        self._keep = []
+        d, f = dims["d_model"], dims["d_ff"]
+
+        def dev(a):
+            t = torch.from_numpy(np.ascontiguousarray(a)).to(device)
+            self._keep.append(t)
+            return t
+
+        def packed(type_id, blocks, n, k):
+            t = pack_weights(type_id, dev(blocks.reshape(-1)), n, k)
+            self._keep.append(t)
+            return t
+
+        arr = (_Layer * len(layers))()
+        for i, lw in enumerate(layers):
+            wqk = packed(Q4_K, np.concatenate([lw["wq"], lw["wk"]], axis=0), 2 * d, d)
+            wv = packed(Q6_K, lw["wv"], d, d)
+            wo = packed(Q4_K, lw["wo"], d, d)
+            wgu = packed(Q4_K, np.concatenate([lw["wgate"], lw["wup"]], axis=0), 2 * f, d)
+            wdn = packed(Q6_K, lw["wdown"], d, f)
+            an, fn = dev(lw["attn_norm"]), dev(lw["ffn_norm"])
+            arr[i] = _Layer(wqk.data_ptr(), wv.data_ptr(), wo.data_ptr(), wgu.data_ptr(), wdn.data_ptr(),
+                            an.data_ptr(), fn.data_ptr())
+            torch.cuda.synchronize()
+        self._layers = arr
+        te = dev(tok_embd.reshape(-1)).data_ptr() if tok_embd is not None else None
+        on = wout = None
+        if head is not None:
+            on = dev(head["out_norm"]).data_ptr()
+            wout = packed(Q6_K, head["w_out"], dims["vocab"], d).data_ptr()
+        self.struct = _Model(len(layers), d, dims["n_heads"], dims["head_dim"], f, dims["vocab"], dims["mask_id"],
+                             dims["eps"], dims["rope_theta"], arr, te, on, wout)
+        self.ref = C.byref(self.struct)
+        torch.cuda.synchronize()
+
+
+def step_workspace_bytes(model: DeviceModel, L: int, flags: int) -> int:
+    return int(lib().dllm_step_workspace_bytes(model.ref, L, flags))
+
+
+def step_linear_stream(model: DeviceModel, x: torch.Tensor, flags: int = STREAM_LINEAR,
+                       canvas: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None):
+    """Run the layer stream; x (f32 [L, d]) is updated in place (filled from the canvas when FULL)."""
+    L = x.shape[0]
+    nb = step_workspace_bytes(model, L, flags)
+    if ws is None:
+        ws = torch.empty(nb + 1024, dtype=torch.uint8, device=x.device)
+    wsp = (ws.data_ptr() + 1023) // 1024 * 1024
+    _ok(lib().dllm_step_linear_stream(model.ref, _ptr(canvas), L, _ptr(x), flags, C.c_void_p(wsp),
+                                      ws.numel() - (wsp - ws.data_ptr()), _stream(stream)))
+    return x
+
+
+def denoise_workspace_bytes(model: DeviceModel, L: int, block_rows: int) -> int:
+    return int(lib().dllm_denoise_workspace_bytes(model.ref, L, block_rows))
+
+
+def denoise_step(model: DeviceModel, canvas: torch.Tensor, block_begin: int, block_end: int, k_commit: int,
+                 hidden_out: torch.Tensor | None = None, ws: torch.Tensor | None = None, out: dict | None = None,
+                 stream=None) -> dict:
+    """One full denoising step (forward + masked LM head + commit); canvas updated in place."""
+    L = canvas.shape[0]
+    dev = canvas.device
+    if out is None:
+        out = {"pos": torch.empty(max(k_commit, 1), dtype=torch.int32, device=dev),
+               "id": torch.empty(max(k_commit, 1), dtype=torch.int32, device=dev),
+               "conf": torch.empty(max(k_commit, 1), dtype=torch.float32, device=dev)}
+    nb = denoise_workspace_bytes(model, L, block_end - block_begin)
+    if ws is None:
+        ws = torch.empty(nb + 1024, dtype=torch.uint8, device=dev)
+    wsp = (ws.data_ptr() + 1023) // 1024 * 1024
+    _ok(lib().dllm_denoise_step(model.ref, _ptr(canvas), L, block_begin, block_end, k_commit, _ptr(out["pos"]),
+                                _ptr(out["id"]), _ptr(out["conf"]), _ptr(hidden_out), C.c_void_p(wsp),
+                                ws.numel() - (wsp - ws.data_ptr()), _stream(stream)))
     return out

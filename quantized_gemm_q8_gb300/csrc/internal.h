@@ -40,6 +40,32 @@ struct QgemmPlan {
 };
 QgemmPlan plan_qgemm(int type, int64_t m, int64_t n, int64_t k);
 
+QgemmPlan plan_single_split(int type, int64_t m, int64_t n, int64_t k);
+
+// One GEMM launch (no argument validation; callers validate). When P.splits > 1 the kernel
+// writes split partials [splits][m][n] to `partial`, otherwise y (mode 0) or the LM-head
+// softmax partials (mode 1).
+struct GemmLaunch {
+  int type;
+  const void* act;
+  int64_t m, k;
+  const void* w;
+  int64_t n;
+  float* y;
+  int64_t ldy;
+  int accumulate;
+  float* partial;
+  int mode;
+  float* pmax;
+  int* parg;
+  float* psum;
+  int32_t* dbg;
+};
+int launch_gemm(const GemmLaunch& g, const QgemmPlan& P, cudaStream_t stream);
+size_t packed_blob_bytes(int type, int64_t n, int64_t k);
+bool device_ptr(const void* p);
+size_t align_up(size_t x, size_t a);
+
 // Launch the tcgen05 GEMM kernel instantiated for (type, nt) (defined in qgemm_q4k.cu /
 // qgemm_q6k.cu). Returns DLLM_OK or a status.
 int launch_qgemm_q4k(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s);

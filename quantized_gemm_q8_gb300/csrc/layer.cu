@@ -1,0 +1,456 @@
+// LLaDA layer stream and full denoising step (mojo-dllm Technical Specification, section 11:
+// RMSNorm, QKV projection, RoPE, bidirectional attention, output projection, residual,
+// RMSNorm, MLP, residual; Development plan, "Model facts": eps 1e-5, NORM RoPE theta 500000,
+// 32 x 128 MHA non-causal, SwiGLU FFN, untied output). Every projection is the tcgen05
+// quantized GEMM; the glue between them is fused into row kernels that consume the GEMMs'
+// split-K partials directly (fixed summation order), so no intermediate takes an extra pass.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "internal.h"
+#include "qgemm.cuh"
+#include "quant.cuh"
+
+namespace dllm {
+
+// ---------------------------------------------------------------------------------------------
+// RoPE table: cs[p][i] = (cos, sin) of p * theta^(-2i/hd), computed in f64 once per step.
+// ---------------------------------------------------------------------------------------------
+__global__ void rope_table_kernel(float2* cs, int L, int half, double theta, int hd) {
+  const int p = blockIdx.x, i = threadIdx.x;
+  if (p < L && i < half) {
+    const double ang = (double)p * pow(theta, -2.0 * (double)i / (double)hd);
+    double s, c;
+    sincos(ang, &s, &c);
+    cs[p * half + i] = make_float2((float)c, (float)s);
+  }
+}
+
+// Token embedding: x[p] = decoded Q4_K row ids[p] of the GGUF table (AoS blocks), f32.
+// w = d * scale * q - dmin * min is formed with one fused multiply-add.
+__global__ void embed_q4k_kernel(const uint8_t* __restrict__ table, int nsb, const int32_t* __restrict__ ids,
+                                 float* __restrict__ x, int d) {
+  const int p = blockIdx.x;
+  const int64_t row = ids[p];
+  for (int k = threadIdx.x; k < d; k += blockDim.x) {
+    const uint8_t* blk = table + (row * nsb + k / QK) * 144;
+    const int i = k % QK, j = i / 32;
+    const uint8_t* sc = blk + 4;
+    int scale, mn;
+    if (j < 4) {
+      scale = sc[j] & 63;
+      mn = sc[j + 4] & 63;
+    } else {
+      scale = (sc[j + 4] & 15) | ((sc[j - 4] >> 6) << 4);
+      mn = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
+    }
+    const uint8_t b = blk[16 + 32 * (i / 64) + (i % 32)];
+    const int q = ((i % 64) < 32) ? (b & 15) : (b >> 4);
+    const float dd = __half2float(*reinterpret_cast<const __half*>(blk));
+    const float dm = __half2float(*reinterpret_cast<const __half*>(blk + 2));
+    x[(int64_t)p * d + k] = fmaf(dd, (float)(scale * q), -dm * (float)mn);
+  }
+}
+
+// Sum of the split partials of the Q|K and V projections, with RoPE on Q and K (adjacent
+// pairs within each head, position = row index).
+__global__ void reduce_rope_kernel(const float* __restrict__ Pqk, int Sqk, const float* __restrict__ Pv, int Sv,
+                                   const float2* __restrict__ cs, int L, int d, int hd, float* __restrict__ Q,
+                                   float* __restrict__ K, float* __restrict__ V) {
+  const int p = blockIdx.x;
+  const int64_t sqk = (int64_t)L * 2 * d, sv = (int64_t)L * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {  // pair i: columns 2i, 2i+1 of [Q | K]
+    const int col = 2 * i;
+    float a0 = 0.f, a1 = 0.f;
+    for (int s = 0; s < Sqk; ++s) {
+      const float2 v = *reinterpret_cast<const float2*>(Pqk + s * sqk + (int64_t)p * 2 * d + col);
+      a0 += v.x;
+      a1 += v.y;
+    }
+    const float2 r = cs[p * (hd / 2) + (col % hd) / 2];
+    const float o0 = a0 * r.x - a1 * r.y, o1 = a0 * r.y + a1 * r.x;
+    float* dst = col < d ? Q + (int64_t)p * d + col : K + (int64_t)p * d + (col - d);
+    *reinterpret_cast<float2*>(dst) = make_float2(o0, o1);
+  }
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    float a = 0.f;
+    for (int s = 0; s < Sv; ++s) a += Pv[s * sv + (int64_t)p * d + c];
+    V[(int64_t)p * d + c] = a;
+  }
+}
+
+// Non-causal multi-head attention, f32, online softmax over key tiles of 32 (one key per lane):
+// O = softmax(Q K^T / sqrt(hd)) V per head. One CTA = one head x 16 queries (8 warps x 2).
+constexpr int ATT_QB = 16, ATT_KT = 32, ATT_HD = 128;
+__global__ void __launch_bounds__(256) attention_kernel(const float* __restrict__ Q, const float* __restrict__ K,
+                                                        const float* __restrict__ V, float* __restrict__ O, int L,
+                                                        int d, float scale) {
+  __shared__ float Kt[ATT_HD][ATT_KT + 1];
+  __shared__ float Vs[ATT_KT][ATT_HD];
+  __shared__ float Qs[ATT_QB][ATT_HD];
+  const int h = blockIdx.x, q0 = blockIdx.y * ATT_QB;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < ATT_QB * ATT_HD; i += blockDim.x) {
+    const int qi = i / ATT_HD, e = i % ATT_HD;
+    Qs[qi][e] = (q0 + qi < L) ? Q[(int64_t)(q0 + qi) * d + h * ATT_HD + e] * scale : 0.f;
+  }
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  for (int k0 = 0; k0 < L; k0 += ATT_KT) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < ATT_KT * ATT_HD; i += blockDim.x) {
+      const int kj = i / ATT_HD, e = i % ATT_HD;
+      const bool ok = k0 + kj < L;
+      Kt[e][kj] = ok ? K[(int64_t)(k0 + kj) * d + h * ATT_HD + e] : 0.f;
+      Vs[kj][e] = ok ? V[(int64_t)(k0 + kj) * d + h * ATT_HD + e] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int qq = 0; qq < 2; ++qq) {
+      const int qi = warp * 2 + qq;
+      float s0 = 0.f;
+#pragma unroll 8
+      for (int e = 0; e < ATT_HD; ++e) s0 = fmaf(Qs[qi][e], Kt[e][lane], s0);
+      if (k0 + lane >= L) s0 = -INFINITY;
+      float mx = s0;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mnew = fmaxf(m[qq], mx);
+      const float corr = expf(m[qq] - mnew);
+      const float p0 = expf(s0 - mnew);
+      float ps = p0;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+      l[qq] = l[qq] * corr + ps;
+      m[qq] = mnew;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[qq][c] *= corr;
+      for (int j = 0; j < ATT_KT; ++j) {
+        const float pj = __shfl_sync(0xffffffffu, p0, j);
+        const float4 vv = *reinterpret_cast<const float4*>(&Vs[j][lane * 4]);
+        acc[qq][0] = fmaf(pj, vv.x, acc[qq][0]);
+        acc[qq][1] = fmaf(pj, vv.y, acc[qq][1]);
+        acc[qq][2] = fmaf(pj, vv.z, acc[qq][2]);
+        acc[qq][3] = fmaf(pj, vv.w, acc[qq][3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int qq = 0; qq < 2; ++qq) {
+    const int qi = q0 + warp * 2 + qq;
+    if (qi < L) {
+      float4 o = make_float4(acc[qq][0] / l[qq], acc[qq][1] / l[qq], acc[qq][2] / l[qq], acc[qq][3] / l[qq]);
+      *reinterpret_cast<float4*>(O + (int64_t)qi * d + h * ATT_HD + lane * 4) = o;
+    }
+  }
+}
+
+// Fused row kernels: the source of each row is built from split partials, then quantized.
+enum RowMode : int {
+  ROW_RESID_NORM_QUANT = 0,  // x += sum_s P; act = Q8_K(RMSNorm(x) * w)
+  ROW_SUM_QUANT = 1,         // act = Q8_K(sum_s P)
+  ROW_SWIGLU_QUANT = 2,      // act = Q8_K(silu(sum_s G) * sum_s U), G|U side by side in P
+  ROW_RESID_ONLY = 3,        // x += sum_s P
+};
+
+struct RowArgs {
+  float* x;
+  const float* P;
+  int S;
+  int64_t pstride;
+  int ldp;
+  const float* norm_w;
+  float eps;
+  int rows, k;
+  QuantOut o;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(256) row_kernel(RowArgs a) {
+  __shared__ float red[8];
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nsb = a.k / QK;
+  if (row >= a.rows) {  // padding rows of the operand planes
+    if (MODE != ROW_RESID_ONLY) {
+      float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int sb = warp; sb < nsb; sb += 8) q8k_emit(z, row, a.rows, sb, a.k, a.o);
+    }
+    return;
+  }
+  const float* Pr = a.P + (int64_t)row * a.ldp;
+  if (MODE == ROW_RESID_NORM_QUANT || MODE == ROW_RESID_ONLY) {
+    float* xr = a.x + (int64_t)row * a.k;
+    float ss = 0.f;
+    for (int i = threadIdx.x * 4; i < a.k; i += blockDim.x * 4) {
+      float4 v = *reinterpret_cast<float4*>(xr + i);
+      for (int s = 0; s < a.S; ++s) {
+        const float4 pv = *reinterpret_cast<const float4*>(Pr + s * a.pstride + i);
+        v.x += pv.x;
+        v.y += pv.y;
+        v.z += pv.z;
+        v.w += pv.w;
+      }
+      *reinterpret_cast<float4*>(xr + i) = v;
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+    if (MODE == ROW_RESID_ONLY) return;
+    ss = block_sum(ss, red);  // also orders the x writes above before the reads below
+    const float rstd = 1.0f / sqrtf(ss / (float)a.k + a.eps);
+    for (int sb = warp; sb < nsb; sb += 8) {
+      const int base = sb * QK + 8 * lane;
+      const float4 v0 = *reinterpret_cast<const float4*>(xr + base);
+      const float4 v1 = *reinterpret_cast<const float4*>(xr + base + 4);
+      const float4 w0 = *reinterpret_cast<const float4*>(a.norm_w + base);
+      const float4 w1 = *reinterpret_cast<const float4*>(a.norm_w + base + 4);
+      float v[8] = {v0.x * rstd * w0.x, v0.y * rstd * w0.y, v0.z * rstd * w0.z, v0.w * rstd * w0.w,
+                    v1.x * rstd * w1.x, v1.y * rstd * w1.y, v1.z * rstd * w1.z, v1.w * rstd * w1.w};
+      q8k_emit(v, row, a.rows, sb, a.k, a.o);
+    }
+  } else {
+    for (int sb = warp; sb < nsb; sb += 8) {
+      const int base = sb * QK + 8 * lane;
+      float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      float u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int s = 0; s < a.S; ++s) {
+        const float* ps = Pr + s * a.pstride + base;
+        const float4 p0 = *reinterpret_cast<const float4*>(ps);
+        const float4 p1 = *reinterpret_cast<const float4*>(ps + 4);
+        v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
+        v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+        if (MODE == ROW_SWIGLU_QUANT) {
+          const float4 q0 = *reinterpret_cast<const float4*>(ps + a.k);
+          const float4 q1 = *reinterpret_cast<const float4*>(ps + a.k + 4);
+          u[0] += q0.x; u[1] += q0.y; u[2] += q0.z; u[3] += q0.w;
+          u[4] += q1.x; u[5] += q1.y; u[6] += q1.z; u[7] += q1.w;
+        }
+      }
+      if (MODE == ROW_SWIGLU_QUANT) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = v[i] / (1.0f + expf(-v[i])) * u[i];
+      }
+      q8k_emit(v, row, a.rows, sb, a.k, a.o);
+    }
+  }
+}
+
+static QuantOut quant_out(void* act, int64_t rows, int64_t k) {
+  ActLayout L = act_layout(rows, k);
+  uint8_t* base = static_cast<uint8_t*>(act);
+  return QuantOut{nullptr, nullptr, nullptr, reinterpret_cast<__half*>(base + L.off_a), base + L.off_j,
+                  reinterpret_cast<float*>(base + L.off_d), (int)L.lpad};
+}
+
+template <int MODE>
+static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, const float* w, float eps, int rows,
+                   int k, void* act, cudaStream_t s) {
+  RowArgs a{x, P, S, pstride, ldp, w, eps, rows, k, act ? quant_out(act, rows, k) : QuantOut{}};
+  const int grid = MODE == ROW_RESID_ONLY ? rows : (int)act_rows_padded(rows);
+  row_kernel<MODE><<<grid, 256, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch row kernel");
+}
+
+// ---------------------------------------------------------------------------------------------
+// Step workspace layout
+// ---------------------------------------------------------------------------------------------
+struct StepPlan {
+  QgemmPlan qk, v, o, gu, dn;
+  size_t x, act_d, act_ff, pqk, pv, po, pgu, pdn, q, k, vv, att, rope, lm, bytes;
+};
+
+static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead) {
+  const int64_t d = m->d_model, f = m->d_ff;
+  StepPlan S{};
+  S.qk = plan_qgemm(DLLM_Q4_K, L, 2 * d, d);
+  S.v = plan_qgemm(DLLM_Q6_K, L, d, d);
+  S.o = plan_qgemm(DLLM_Q4_K, L, d, d);
+  S.gu = plan_qgemm(DLLM_Q4_K, L, 2 * f, d);
+  S.dn = plan_qgemm(DLLM_Q6_K, L, d, f);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 1024);
+    return o;
+  };
+  const bool full = flags & DLLM_STREAM_FULL;
+  S.x = take(lmhead ? (size_t)L * d * 4 : 0);
+  S.act_d = take(act_layout(L, d).bytes);
+  S.act_ff = take(act_layout(L, f).bytes);
+  S.pqk = take((size_t)S.qk.splits * L * 2 * d * 4);
+  S.pv = take((size_t)S.v.splits * L * d * 4);
+  S.po = take((size_t)S.o.splits * L * d * 4);
+  S.pgu = take((size_t)S.gu.splits * L * 2 * f * 4);
+  S.pdn = take((size_t)S.dn.splits * L * d * 4);
+  S.q = take(full ? (size_t)L * d * 4 : 0);
+  S.k = take(full ? (size_t)L * d * 4 : 0);
+  S.vv = take(full ? (size_t)L * d * 4 : 0);
+  S.att = take(full ? (size_t)L * d * 4 : 0);
+  S.rope = take(full ? (size_t)L * (m->head_dim / 2) * 8 : 0);
+  S.lm = 0;
+  S.bytes = off;
+  return S;
+}
+
+static int check_model(const dllm_model* m, int64_t L, const char* fn) {
+  if (!m) return fail(DLLM_E_INVAL, "%s: model is NULL", fn);
+  if (m->n_layers <= 0 || m->d_model <= 0 || m->d_model % QK || m->d_ff <= 0 || m->d_ff % QK ||
+      m->head_dim != ATT_HD || m->n_heads * m->head_dim != m->d_model || m->vocab <= 0)
+    return fail(DLLM_E_SHAPE,
+                "%s: unsupported model shape (d_model %% 256 == 0, d_ff %% 256 == 0, head_dim == 128, "
+                "n_heads * head_dim == d_model): d=%d d_ff=%d heads=%d head_dim=%d",
+                fn, m->d_model, m->d_ff, m->n_heads, m->head_dim);
+  if (L <= 0 || L > 8192) return fail(DLLM_E_SHAPE, "%s: L=%lld must be in [1, 8192]", fn, (long long)L);
+  if (!m->layers) return fail(DLLM_E_INVAL, "%s: model->layers is NULL", fn);
+  for (int i = 0; i < m->n_layers; ++i) {
+    const dllm_layer& y = m->layers[i];
+    const void* ps[7] = {y.wqk, y.wv, y.wo, y.wgu, y.wdown, y.attn_norm, y.ffn_norm};
+    for (const void* p : ps)
+      if (!device_ptr(p)) return fail(DLLM_E_INVAL, "%s: layer %d has a NULL or non-device weight pointer", fn, i);
+  }
+  return DLLM_OK;
+}
+
+static int gemm(int type, const void* act, int64_t m, int64_t k, const void* w, int64_t n, float* out,
+                const QgemmPlan& P, cudaStream_t s) {
+  GemmLaunch g{type, act, m, k, w, n, out, n, 0, out, 0, nullptr, nullptr, nullptr, nullptr};
+  return launch_gemm(g, P, s);
+}
+
+// The forward pass over all layers; x is [L][d] (input for the linear stream, output always).
+static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float* x, int flags, uint8_t* ws,
+                   const StepPlan& S, cudaStream_t s) {
+  const int d = m->d_model, f = m->d_ff, hd = m->head_dim;
+  const bool full = flags & DLLM_STREAM_FULL;
+  float* Pqk = reinterpret_cast<float*>(ws + S.pqk);
+  float* Pv = reinterpret_cast<float*>(ws + S.pv);
+  float* Po = reinterpret_cast<float*>(ws + S.po);
+  float* Pgu = reinterpret_cast<float*>(ws + S.pgu);
+  float* Pdn = reinterpret_cast<float*>(ws + S.pdn);
+  void* actd = ws + S.act_d;
+  void* actf = ws + S.act_ff;
+  int rc;
+  if (full) {
+    rope_table_kernel<<<(int)L, hd / 2, 0, s>>>(reinterpret_cast<float2*>(ws + S.rope), (int)L, hd / 2,
+                                                (double)m->rope_theta, hd);
+    embed_q4k_kernel<<<(int)L, 256, 0, s>>>(static_cast<const uint8_t*>(m->tok_embd), d / QK, canvas, x, d);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch embedding");
+  }
+  // layer 0 input: RMSNorm + quantize of x
+  if ((rc = quantize_rows(x, L, d, d, m->layers[0].attn_norm, m->eps, actd, s))) return rc;
+  for (int li = 0; li < m->n_layers; ++li) {
+    const dllm_layer& Ly = m->layers[li];
+    if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wqk, 2 * d, Pqk, S.qk, s))) return rc;
+    if ((rc = gemm(DLLM_Q6_K, actd, L, d, Ly.wv, d, Pv, S.v, s))) return rc;
+    if (full) {
+      float* Q = reinterpret_cast<float*>(ws + S.q);
+      float* K = reinterpret_cast<float*>(ws + S.k);
+      float* V = reinterpret_cast<float*>(ws + S.vv);
+      float* A = reinterpret_cast<float*>(ws + S.att);
+      reduce_rope_kernel<<<(int)L, 256, 0, s>>>(Pqk, S.qk.splits, Pv, S.v.splits,
+                                                reinterpret_cast<const float2*>(ws + S.rope), (int)L, d, hd, Q, K, V);
+      dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB));
+      attention_kernel<<<ag, 256, 0, s>>>(Q, K, V, A, (int)L, d, 1.0f / sqrtf((float)hd));
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "launch attention");
+      if ((rc = quantize_rows(A, L, d, d, nullptr, m->eps, actd, s))) return rc;
+    } else {
+      // linear stream: the O projection consumes the V projection's output
+      if ((rc = run_row<ROW_SUM_QUANT>(nullptr, Pv, S.v.splits, L * d, d, nullptr, 0.f, (int)L, d, actd, s))) return rc;
+    }
+    if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wo, d, Po, S.o, s))) return rc;
+    if ((rc = run_row<ROW_RESID_NORM_QUANT>(x, Po, S.o.splits, L * d, d, Ly.ffn_norm, m->eps, (int)L, d, actd, s)))
+      return rc;
+    if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wgu, 2 * f, Pgu, S.gu, s))) return rc;
+    if ((rc = run_row<ROW_SWIGLU_QUANT>(nullptr, Pgu, S.gu.splits, L * 2 * f, 2 * f, nullptr, 0.f, (int)L, f, actf,
+                                        s)))
+      return rc;
+    if ((rc = gemm(DLLM_Q6_K, actf, L, f, Ly.wdown, d, Pdn, S.dn, s))) return rc;
+    if (li + 1 < m->n_layers) {
+      if ((rc = run_row<ROW_RESID_NORM_QUANT>(x, Pdn, S.dn.splits, L * d, d, m->layers[li + 1].attn_norm, m->eps,
+                                              (int)L, d, actd, s)))
+        return rc;
+    } else {
+      if ((rc = run_row<ROW_RESID_ONLY>(x, Pdn, S.dn.splits, L * d, d, nullptr, 0.f, (int)L, d, nullptr, s)))
+        return rc;
+    }
+  }
+  return DLLM_OK;
+}
+
+}  // namespace dllm
+
+using namespace dllm;
+
+extern "C" {
+
+DLLM_API size_t dllm_step_workspace_bytes(const dllm_model* m, int64_t L, int flags) {
+  if (!m || L <= 0 || m->d_model <= 0 || m->d_ff <= 0) return 0;
+  return step_plan(m, L, flags, false).bytes;
+}
+
+DLLM_API int dllm_step_linear_stream(const dllm_model* m, const int32_t* canvas, int64_t L, float* x, int flags,
+                                     void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  int rc = check_model(m, L, "dllm_step_linear_stream");
+  if (rc) return rc;
+  if (flags != DLLM_STREAM_LINEAR && flags != DLLM_STREAM_FULL)
+    return fail(DLLM_E_INVAL, "dllm_step_linear_stream: flags must be DLLM_STREAM_LINEAR or DLLM_STREAM_FULL");
+  if ((rc = check_device())) return rc;
+  if (!device_ptr(x)) return fail(DLLM_E_INVAL, "dllm_step_linear_stream: x is NULL or not a device pointer");
+  if (flags == DLLM_STREAM_FULL) {
+    if (!device_ptr(canvas)) return fail(DLLM_E_INVAL, "dllm_step_linear_stream: canvas is NULL or not a device pointer");
+    if (!device_ptr(m->tok_embd)) return fail(DLLM_E_INVAL, "dllm_step_linear_stream: model->tok_embd is not a device pointer");
+  }
+  if ((reinterpret_cast<uintptr_t>(x) & 15) != 0)
+    return fail(DLLM_E_ALIGN, "dllm_step_linear_stream: x must be 16-byte aligned");
+  const StepPlan S = step_plan(m, L, flags, false);
+  if (!ws || ws_bytes < S.bytes || !device_ptr(ws))
+    return fail(DLLM_E_WORKSPACE, "dllm_step_linear_stream: workspace has %zu bytes, needs %zu", ws ? ws_bytes : (size_t)0,
+                S.bytes);
+  if ((reinterpret_cast<uintptr_t>(ws) & 1023) != 0)
+    return fail(DLLM_E_ALIGN, "dllm_step_linear_stream: ws must be 1024-byte aligned");
+  return forward(m, canvas, L, x, flags, static_cast<uint8_t*>(ws), S, (cudaStream_t)stream);
+}
+
+DLLM_API size_t dllm_denoise_workspace_bytes(const dllm_model* m, int64_t L, int32_t block_rows) {
+  if (!m || L <= 0 || block_rows <= 0 || m->d_model <= 0) return 0;
+  const StepPlan S = step_plan(m, L, DLLM_STREAM_FULL, true);
+  return align_up(S.bytes, 1024) + dllm_lmhead_workspace_bytes(block_rows, m->vocab, m->d_model);
+}
+
+DLLM_API int dllm_denoise_step(const dllm_model* m, int32_t* canvas, int64_t L, int32_t block_begin, int32_t block_end,
+                               int32_t k_commit, int32_t* out_pos, int32_t* out_id, float* out_conf,
+                               float* hidden_out, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  int rc = check_model(m, L, "dllm_denoise_step");
+  if (rc) return rc;
+  if ((rc = check_device())) return rc;
+  if (!device_ptr(canvas) || !device_ptr(m->tok_embd) || !device_ptr(m->w_out) || !device_ptr(m->out_norm))
+    return fail(DLLM_E_INVAL, "dllm_denoise_step: canvas / tok_embd / w_out / out_norm must be device pointers");
+  const StepPlan S = step_plan(m, L, DLLM_STREAM_FULL, true);
+  const size_t need = dllm_denoise_workspace_bytes(m, L, block_end - block_begin);
+  if (block_end - block_begin <= 0 || need == 0)
+    return fail(DLLM_E_INVAL, "dllm_denoise_step: empty block [%d, %d)", block_begin, block_end);
+  if (!ws || ws_bytes < need || !device_ptr(ws))
+    return fail(DLLM_E_WORKSPACE, "dllm_denoise_step: workspace has %zu bytes, needs %zu", ws ? ws_bytes : (size_t)0,
+                need);
+  if ((reinterpret_cast<uintptr_t>(ws) & 1023) != 0)
+    return fail(DLLM_E_ALIGN, "dllm_denoise_step: ws must be 1024-byte aligned");
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  float* x = hidden_out ? hidden_out : reinterpret_cast<float*>(base + S.x);
+  if (hidden_out && !device_ptr(hidden_out))
+    return fail(DLLM_E_INVAL, "dllm_denoise_step: hidden_out is not a device pointer");
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((rc = forward(m, canvas, L, x, DLLM_STREAM_FULL, base, S, s))) return rc;
+  const size_t lm_off = align_up(S.bytes, 1024);
+  return dllm_lmhead_masked_select(x, L, m->d_model, m->d_model, m->out_norm, m->eps, m->w_out, m->vocab, canvas,
+                                   m->mask_id, block_begin, block_end, k_commit, out_pos, out_id, out_conf, nullptr,
+                                   nullptr, base + lm_off, ws_bytes - lm_off, stream);
+}
+
+}  // extern "C"
