@@ -231,6 +231,18 @@ DLLM_API int dllm_denoise_step(const dllm_model* m, int32_t* canvas, int64_t L, 
                                float* out_conf, float* hidden_out, void* ws, size_t ws_bytes,
                                dllm_stream_t stream);
 
+/* Benchmark hooks.
+ * dllm_launch_count: number of kernels this library has enqueued so far in this process (a
+ *   host-side counter; launches recorded during stream capture count once, at capture).
+ * dllm_qgemm_partials: the GEMM kernel alone, without the split-K reduction: writes the
+ *   plan's split partials f32 [splits][m][n] (their sum is dllm_qgemm's result) and stores
+ *   the number of splits in *splits (host pointer, may be NULL). partials_bytes >=
+ *   dllm_qgemm_partials_bytes(type, m, n, k). Used to time the tensor-core kernel alone. */
+DLLM_API long long dllm_launch_count(void);
+DLLM_API size_t dllm_qgemm_partials_bytes(int type, int64_t m, int64_t n, int64_t k);
+DLLM_API int dllm_qgemm_partials(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
+                                 float* partials, size_t partials_bytes, int32_t* splits, dllm_stream_t stream);
+
 /* Test hook for failure detection: launches one kernel whose mbarrier wait can never
  * complete, bounded by `limit_cycles` SM clock cycles; the kernel then records a timeout
  * in the device error word and returns. dllm_check() afterwards reports DLLM_E_TIMEOUT. */

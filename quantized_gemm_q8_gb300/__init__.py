@@ -55,6 +55,9 @@ _SIGS = {
     "dllm_step_linear_stream": ([P, P, I64, P, INT, P, SZ, P], INT),
     "dllm_denoise_workspace_bytes": ([P, I64, I32], SZ),
     "dllm_denoise_step": ([P, P, I64, I32, I32, I32, P, P, P, P, P, SZ, P], INT),
+    "dllm_launch_count": ([], C.c_longlong),
+    "dllm_qgemm_partials_bytes": ([INT, I64, I64, I64], SZ),
+    "dllm_qgemm_partials": ([INT, P, I64, I64, P, I64, P, SZ, P, P], INT),
 }
 
 
@@ -171,6 +174,23 @@ def qgemm_intsums(type_id: int, act: torch.Tensor, m: int, k: int, w_packed: tor
     return sums
 
 
+def launch_count() -> int:
+    """Kernels enqueued by the library so far in this process."""
+    return int(lib().dllm_launch_count())
+
+
+def qgemm_partials(type_id: int, act: torch.Tensor, m: int, k: int, w_packed: torch.Tensor, n: int,
+                   partials: torch.Tensor | None = None, stream=None):
+    """The GEMM kernel alone: split partials f32 [splits, m, n] (sum = qgemm result)."""
+    nb = int(lib().dllm_qgemm_partials_bytes(type_id, m, n, k))
+    if partials is None:
+        partials = torch.empty(nb // 4, dtype=torch.float32, device=act.device)
+    sp = C.c_int32(0)
+    _ok(lib().dllm_qgemm_partials(type_id, _ptr(act), m, k, _ptr(w_packed), n, _ptr(partials), partials.numel() * 4,
+                                  C.byref(sp), _stream(stream)))
+    return partials, sp.value
+
+
 def selftest_timeout(limit_cycles: int, stream=None):
     _ok(lib().dllm_selftest_timeout(limit_cycles, _stream(stream)))
 
@@ -232,12 +252,14 @@ class DeviceModel:
     `tok_embd` the Q4_K token table blocks; `head` a dict(w_out=Q6_K blocks, out_norm=f32).
     The device tensors are kept alive by this object; `.ref` is the C struct pointer."""
 
-    def __init__(self, dims: dict, layers: list, tok_embd=None, head=None, device="cuda"):
+    def __init__(self, dims: dict, layers, tok_embd=None, head=None, device="cuda", n_layers: int | None = None):
         import numpy as np
 
         self.dims = dict(dims)
         self._keep = []
         d, f = dims["d_model"], dims["d_ff"]
+        if n_layers is None:
+            n_layers = len(layers)
 
         def dev(a):
             t = torch.from_numpy(np.ascontiguousarray(a)).to(device)
@@ -249,7 +271,7 @@ class DeviceModel:
             self._keep.append(t)
             return t
 
-        arr = (_Layer * len(layers))()
+        arr = (_Layer * n_layers)()
         for i, lw in enumerate(layers):
             wqk = packed(Q4_K, np.concatenate([lw["wq"], lw["wk"]], axis=0), 2 * d, d)
             wv = packed(Q6_K, lw["wv"], d, d)
@@ -266,7 +288,7 @@ class DeviceModel:
         if head is not None:
             on = dev(head["out_norm"]).data_ptr()
             wout = packed(Q6_K, head["w_out"], dims["vocab"], d).data_ptr()
-        self.struct = _Model(len(layers), d, dims["n_heads"], dims["head_dim"], f, dims["vocab"], dims["mask_id"],
+        self.struct = _Model(n_layers, d, dims["n_heads"], dims["head_dim"], f, dims["vocab"], dims["mask_id"],
                              dims["eps"], dims["rope_theta"], arr, te, on, wout)
         self.ref = C.byref(self.struct)
         torch.cuda.synchronize()
@@ -311,3 +333,52 @@ def denoise_step(model: DeviceModel, canvas: torch.Tensor, block_begin: int, blo
                                 _ptr(out["id"]), _ptr(out["conf"]), _ptr(hidden_out), C.c_void_p(wsp),
                                 ws.numel() - (wsp - ws.data_ptr()), _stream(stream)))
     return out
+
+
+def model_from_seed(dims: dict, seed: int, device="cuda") -> DeviceModel:
+    """Seeded synthetic LLaDA-shaped model (generated, uploaded and packed one layer at a time)."""
+    from . import synth
+
+    gen = (synth.layer_weights(seed, i, dims) for i in range(dims["n_layers"]))
+    return DeviceModel(dims, gen, synth.embed_weights(seed, dims), synth.head_weights(seed, dims), device,
+                       n_layers=dims["n_layers"])
+
+
+class StepGraphs:
+    """One CUDA graph per block of the denoising step (forward + masked LM head + commit), all on
+    the same device canvas and output buffers; replay(step) runs the step of block
+    block_of(step). Workspace and outputs are allocated once, before capture."""
+
+    def __init__(self, model: DeviceModel, canvas: torch.Tensor, blocks: list, k_commit: int):
+        self.model, self.canvas, self.blocks, self.k = model, canvas, blocks, k_commit
+        dev = canvas.device
+        L = canvas.shape[0]
+        rows = max(b1 - b0 for b0, b1 in blocks)
+        nb = denoise_workspace_bytes(model, L, rows)
+        self.ws = torch.empty(nb + 1024, dtype=torch.uint8, device=dev)
+        self.out = {"pos": torch.empty(k_commit, dtype=torch.int32, device=dev),
+                    "id": torch.empty(k_commit, dtype=torch.int32, device=dev),
+                    "conf": torch.empty(k_commit, dtype=torch.float32, device=dev)}
+        self.stream = torch.cuda.Stream(device=dev)
+        self.graphs = []
+        self.launches_per_step = []
+        saved = canvas.clone()
+        with torch.cuda.stream(self.stream):
+            for b0, b1 in blocks:  # warm the library (attributes, tensor-map entry point) once
+                denoise_step(model, canvas, b0, b1, k_commit, ws=self.ws, out=self.out, stream=self.stream)
+        self.stream.synchronize()
+        check(self.stream)
+        for b0, b1 in blocks:
+            g = torch.cuda.CUDAGraph()
+            n0 = launch_count()
+            with torch.cuda.graph(g, stream=self.stream):
+                denoise_step(model, canvas, b0, b1, k_commit, ws=self.ws, out=self.out, stream=self.stream)
+            self.launches_per_step.append(launch_count() - n0)
+            self.graphs.append(g)
+        canvas.copy_(saved)
+        torch.cuda.synchronize()
+
+    def replay(self, block_index: int):
+        """Replay on self.stream (a graph replays on the caller's current stream)."""
+        with torch.cuda.stream(self.stream):
+            self.graphs[block_index].replay()

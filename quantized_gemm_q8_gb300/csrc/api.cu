@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -30,6 +31,8 @@ int* err_word() {
 }
 
 static thread_local char g_msg[1024] = "";
+static std::atomic<long long> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 #ifdef DLLM_TRACE
 // Trace builds only: device buffer of 8 x 256 clock64 stamps written by CTA 0 of each GEMM.
@@ -431,6 +434,7 @@ int quantize_rows(const float* x, int64_t rows, int64_t k, int64_t ldx, const fl
   QuantOut o{nullptr, nullptr, nullptr, reinterpret_cast<__half*>(base + L.off_a), base + L.off_j,
              reinterpret_cast<float*>(base + L.off_d), (int)L.lpad};
   quantize_act_kernel<<<(int)L.lpad, 256, 0, stream>>>(x, (int)rows, k, ldx, norm_w, eps, o);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch quantize_act");
 }
@@ -496,6 +500,7 @@ DLLM_API int dllm_pack_weights(int type, const void* blocks, int64_t n, int64_t 
     pack_q4k_kernel<<<tiles * nsb, BM, 0, (cudaStream_t)stream>>>(src, (int)n, nsb, blob, dd);
   else
     pack_q6k_kernel<<<tiles * nsb, BM, 0, (cudaStream_t)stream>>>(src, (int)n, nsb, blob, dd);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch pack kernel");
 }
@@ -543,6 +548,7 @@ DLLM_API int dllm_quantize_act(const float* x, int64_t rows, int64_t k, int64_t 
     grid = (int)L.lpad;
   }
   quantize_act_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(x, (int)rows, k, ldx, norm_w, eps, o);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch quantize_act");
 }
@@ -648,6 +654,7 @@ static int qgemm_common(const char* fn, int type, const void* act, int64_t m, in
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4 * num_sms());
     reduce_splits_kernel<<<blocks, 256, 0, stream>>>(static_cast<float*>(ws), P.splits, m * n, (int)m, (int)n, y,
                                                      ldy, accumulate);
+    note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch reduce_splits");
   }
@@ -692,6 +699,7 @@ DLLM_API int dllm_selftest_timeout(int64_t limit_cycles, dllm_stream_t stream) {
   int rc = check_device();
   if (rc) return rc;
   selftest_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((long long)limit_cycles);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch selftest_timeout");
 }
@@ -755,8 +763,41 @@ DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d
                                                 reinterpret_cast<int*>(base + W.parg),
                                                 reinterpret_cast<float*>(base + W.psum), W.P, (int)R, canvas, mask_id,
                                                 block_begin, k_commit, out_pos, out_id, out_conf, row_id, row_conf);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch lmhead_merge_commit");
+}
+
+
+DLLM_API long long dllm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+DLLM_API size_t dllm_qgemm_partials_bytes(int type, int64_t m, int64_t n, int64_t k) {
+  if (!block_bytes(type) || m <= 0 || n <= 0 || k <= 0 || k % QK) return 0;
+  const QgemmPlan P = plan_qgemm(type, m, n, k);
+  return align_up((size_t)P.splits * m * n * 4, 256);
+}
+
+DLLM_API int dllm_qgemm_partials(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
+                                 float* partials, size_t partials_bytes, int32_t* splits, dllm_stream_t stream) {
+  if (!block_bytes(type))
+    return fail(DLLM_E_TYPE, "dllm_qgemm_partials: unsupported block type %d", type);
+  if (m <= 0 || m > 65536 || n <= 0 || n > (1 << 24) || k <= 0 || k % QK || k > (1 << 20))
+    return fail(DLLM_E_SHAPE, "dllm_qgemm_partials: bad shape m=%lld n=%lld k=%lld", (long long)m, (long long)n,
+                (long long)k);
+  int rc = check_device();
+  if (rc) return rc;
+  CHECK_DEV(act, "act");
+  CHECK_DEV(w_packed, "w_packed");
+  CHECK_DEV(partials, "partials");
+  if (!aligned(act, 256) || !aligned(w_packed, 256))
+    return fail(DLLM_E_ALIGN, "dllm_qgemm_partials: act and w_packed must be 256-byte aligned");
+  const QgemmPlan P = plan_qgemm(type, m, n, k);
+  if (partials_bytes < (size_t)P.splits * m * n * 4)
+    return fail(DLLM_E_WORKSPACE, "dllm_qgemm_partials: buffer has %zu bytes, needs %zu", partials_bytes,
+                (size_t)P.splits * m * n * 4);
+  if (splits) *splits = P.splits;
+  GemmLaunch g{type, act, m, k, w_packed, n, partials, n, 0, partials, 0, nullptr, nullptr, nullptr, nullptr};
+  return launch_gemm(g, P, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -75,6 +75,9 @@ int launch_qgemm_q6k(int nt, const CUtensorMap& map, const QgemmParams& p, int g
 int quantize_rows(const float* x, int64_t rows, int64_t k, int64_t ldx, const float* norm_w, float eps, void* act,
                   cudaStream_t stream);
 
+// Count of kernel launches issued by this library (for benchmark bookkeeping).
+void note_launch();
+
 constexpr long long kDefaultTimeoutCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 }  // namespace dllm

@@ -252,6 +252,7 @@ static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, co
   RowArgs a{x, P, S, pstride, ldp, w, eps, rows, k, act ? quant_out(act, rows, k) : QuantOut{}};
   const int grid = MODE == ROW_RESID_ONLY ? rows : (int)act_rows_padded(rows);
   row_kernel<MODE><<<grid, 256, 0, s>>>(a);
+  note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch row kernel");
 }
@@ -338,7 +339,9 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
   if (full) {
     rope_table_kernel<<<(int)L, hd / 2, 0, s>>>(reinterpret_cast<float2*>(ws + S.rope), (int)L, hd / 2,
                                                 (double)m->rope_theta, hd);
+    note_launch();
     embed_q4k_kernel<<<(int)L, 256, 0, s>>>(static_cast<const uint8_t*>(m->tok_embd), d / QK, canvas, x, d);
+    note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch embedding");
   }
@@ -355,8 +358,10 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
       float* A = reinterpret_cast<float*>(ws + S.att);
       reduce_rope_kernel<<<(int)L, 256, 0, s>>>(Pqk, S.qk.splits, Pv, S.v.splits,
                                                 reinterpret_cast<const float2*>(ws + S.rope), (int)L, d, hd, Q, K, V);
+      note_launch();
       dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB));
       attention_kernel<<<ag, 256, 0, s>>>(Q, K, V, A, (int)L, d, 1.0f / sqrtf((float)hd));
+      note_launch();
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "launch attention");
       if ((rc = quantize_rows(A, L, d, d, nullptr, m->eps, actd, s))) return rc;

@@ -11,6 +11,7 @@ static int launch_one(const CUtensorMap& map, const QgemmParams& p, int grid, cu
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(qgemm_q4k)");
   k<<<grid, QG_THREADS, SMEM, s>>>(map, p);
+  note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch qgemm_q4k");
   return DLLM_OK;
