@@ -243,6 +243,20 @@ DLLM_API size_t dllm_qgemm_partials_bytes(int type, int64_t m, int64_t n, int64_
 DLLM_API int dllm_qgemm_partials(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
                                  float* partials, size_t partials_bytes, int32_t* splits, dllm_stream_t stream);
 
+/* ---- allocation-free GEMM (the pages have no counterpart to this entry point) ----------------
+ * For callers that cannot allocate device memory or hand over a workspace at call time (an
+ * inference server that reserves all device memory at start-up, a plugin interface that
+ * passes only inputs and outputs, a loop that must not call cudaMalloc because it can
+ * synchronize the device). Same result as dllm_qgemm, but the split-K partial sums live in a
+ * fixed 32 MiB array that the library holds in every GPU's memory until exit; m * n * 4 must
+ * not exceed 32 MiB (larger shapes return DLLM_E_SHAPE; the split count is reduced to 1 when
+ * the plan's partials would not fit). The first call on a device looks up that array's device
+ * address (once per device, with the device current); make it before any stream capture.
+ * Calls share the array: calls that overlap on the GPU race and must be serialized by the
+ * caller. No device memory is allocated or freed. */
+DLLM_API int dllm_qgemm_noalloc(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
+                                float* y, int64_t ldy, int accumulate, dllm_stream_t stream);
+
 /* Test hook for failure detection: launches one kernel whose mbarrier wait can never
  * complete, bounded by `limit_cycles` SM clock cycles; the kernel then records a timeout
  * in the device error word and returns. dllm_check() afterwards reports DLLM_E_TIMEOUT. */

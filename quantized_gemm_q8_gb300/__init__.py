@@ -58,6 +58,7 @@ _SIGS = {
     "dllm_launch_count": ([], C.c_longlong),
     "dllm_qgemm_partials_bytes": ([INT, I64, I64, I64], SZ),
     "dllm_qgemm_partials": ([INT, P, I64, I64, P, I64, P, SZ, P, P], INT),
+    "dllm_qgemm_noalloc": ([INT, P, I64, I64, P, I64, P, I64, INT, P], INT),
 }
 
 
@@ -172,6 +173,16 @@ def qgemm_intsums(type_id: int, act: torch.Tensor, m: int, k: int, w_packed: tor
     sums = torch.zeros((2, k // QK, m, n), dtype=torch.int32, device=act.device)
     _ok(lib().dllm_qgemm_intsums(type_id, _ptr(act), m, k, _ptr(w_packed), n, _ptr(sums), _stream(stream)))
     return sums
+
+
+def qgemm_noalloc(type_id: int, act: torch.Tensor, m: int, k: int, w_packed: torch.Tensor, n: int,
+                  y: torch.Tensor, accumulate: bool = False, stream=None) -> torch.Tensor:
+    """Same result as qgemm without any workspace: for callers that cannot allocate device
+    memory at call time; the library keeps the split-K partials in its own fixed 32 MiB array
+    (m * n * 4 bytes at most). Calls must not overlap on the GPU."""
+    _ok(lib().dllm_qgemm_noalloc(type_id, _ptr(act), m, k, _ptr(w_packed), n, _ptr(y), y.stride(0), int(accumulate),
+                                 _stream(stream)))
+    return y
 
 
 def launch_count() -> int:
