@@ -152,7 +152,11 @@ DLLM_API int dllm_qgemm_q6k(const void* act, int64_t m, int64_t k, const void* w
  *   Q4_K: sums[0] = sum_g scale * sum_i q4_i * a_i,      sums[1] = sum_g min * bsum_g
  *   Q6_K: sums[0] = sum_g s_hi * sum_i (q6_i-32) * a_i, sums[1] = sum_g s_lo * sum_i (q6_i-32) * a_i
  *         where the int8 group scale s = 16 * s_hi + s_lo, s_lo in [0, 15].
- * Runs the same kernel as dllm_qgemm with one split; intended for small shapes. */
+ * dllm_qgemm accumulates both parts of a super-block in one tensor-memory accumulator (Q4_K:
+ * the min part enters with f16 head and tail coefficients -min * dmin / d, 2^-22 relative;
+ * Q6_K: the hi operand carries 16 * s_hi * (q6-32)). This hook runs the same kernel twice
+ * with one split, each time with one part isolated, and copies out its exact integers;
+ * intended for small shapes. */
 DLLM_API int dllm_qgemm_intsums(int type, const void* act, int64_t m, int64_t k, const void* w_packed,
                                 int64_t n, int32_t* sums, dllm_stream_t stream);
 

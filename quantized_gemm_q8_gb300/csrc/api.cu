@@ -457,6 +457,10 @@ DLLM_API int dllm_check(dllm_stream_t stream) {
   if (w) {
     int z = 0;
     cudaMemcpyToSymbol(g_err_word, &z, sizeof(int));
+    if (w == ERR_RANGE)
+      return fail(DLLM_E_INVAL,
+                  "a Q4_K super-block has |dmin / d| above 4e6: its min term cannot be folded into the "
+                  "f16 tensor-core operands (the outputs of that launch are not valid)");
     return fail(DLLM_E_TIMEOUT, "device-side bounded wait ran out (roles: %s%s%s%s%s%s)",
                 (w & ERR_TIMEOUT_PRODUCER) ? "producer " : "", (w & ERR_TIMEOUT_DECODE) ? "decode " : "",
                 (w & ERR_TIMEOUT_MMA) ? "mma " : "", (w & ERR_TIMEOUT_EPILOGUE) ? "epilogue " : "",
@@ -599,6 +603,7 @@ int launch_gemm(const GemmLaunch& g, const QgemmPlan& P, cudaStream_t stream) {
   prm.parg = g.parg;
   prm.psum = g.psum;
   prm.dbg = g.dbg;
+  prm.dbg_mode = g.dbg_mode;
   prm.timeout = kDefaultTimeoutCycles;
   prm.err = err_word();
   if (!prm.err) return fail(DLLM_E_CUDA, "cannot resolve the device error word");
@@ -646,7 +651,17 @@ static int qgemm_common(const char* fn, int type, const void* act, int64_t m, in
                   ws ? ws_bytes : (size_t)0, P.ws_bytes);
     CHECK_DEV(ws, "ws");
   }
-  GemmLaunch g{type, act, m, k, w_packed, n, y, ldy, accumulate, static_cast<float*>(ws), 0, nullptr, nullptr, nullptr, dbg};
+  GemmLaunch g{type, act, m, k, w_packed, n, y, ldy, accumulate, static_cast<float*>(ws), 0, nullptr, nullptr, nullptr,
+               nullptr, 0};
+  if (dbg) {
+    // the integer sums: one launch per isolated part, each writing its own plane
+    for (int part = 0; part < 2; ++part) {
+      g.dbg = dbg + (size_t)part * P.nsb * m * n;
+      g.dbg_mode = part + 1;
+      if ((rc = launch_gemm(g, P, stream))) return rc;
+    }
+    return DLLM_OK;
+  }
   rc = launch_gemm(g, P, stream);
   if (rc) return rc;
   if (P.splits > 1 && y) {

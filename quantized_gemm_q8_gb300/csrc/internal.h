@@ -60,6 +60,7 @@ struct GemmLaunch {
   int* parg;
   float* psum;
   int32_t* dbg;
+  int dbg_mode;
 };
 int launch_gemm(const GemmLaunch& g, const QgemmPlan& P, cudaStream_t stream);
 size_t packed_blob_bytes(int type, int64_t n, int64_t k);

@@ -54,95 +54,151 @@ __global__ void embed_q4k_kernel(const uint8_t* __restrict__ table, int nsb, con
   }
 }
 
-// Sum of the split partials of the Q|K and V projections, with RoPE on Q and K (adjacent
-// pairs within each head, position = row index).
-__global__ void reduce_rope_kernel(const float* __restrict__ Pqk, int Sqk, const float* __restrict__ Pv, int Sv,
-                                   const float2* __restrict__ cs, int L, int d, int hd, float* __restrict__ Q,
-                                   float* __restrict__ K, float* __restrict__ V) {
-  const int p = blockIdx.x;
-  const int64_t sqk = (int64_t)L * 2 * d, sv = (int64_t)L * d;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {  // pair i: columns 2i, 2i+1 of [Q | K]
-    const int col = 2 * i;
-    float a0 = 0.f, a1 = 0.f;
-    for (int s = 0; s < Sqk; ++s) {
-      const float2 v = *reinterpret_cast<const float2*>(Pqk + s * sqk + (int64_t)p * 2 * d + col);
-      a0 += v.x;
-      a1 += v.y;
-    }
-    const float2 r = cs[p * (hd / 2) + (col % hd) / 2];
-    const float o0 = a0 * r.x - a1 * r.y, o1 = a0 * r.y + a1 * r.x;
-    float* dst = col < d ? Q + (int64_t)p * d + col : K + (int64_t)p * d + (col - d);
-    *reinterpret_cast<float2*>(dst) = make_float2(o0, o1);
+// Non-causal multi-head attention fused with the split-K sum and RoPE of its inputs:
+//   q, k = RoPE(sum_s Pqk[s]) (adjacent pairs within a head, position = row index),
+//   v = sum_s Pv[s],  O = softmax(q k^T / sqrt(hd)) v  per head,
+// in f32 with an online softmax over key tiles of 64. One CTA = one head x 32 queries; warp w
+// owns queries 4w..4w+3. Scores: a lane holds 4 queries x keys (lane, lane + 32), reading q as
+// broadcast float4 and k rows padded to 132 floats so a quarter-warp's float4 loads of 8
+// different keys hit distinct banks. PV: the warp's probabilities go through shared memory and a
+// lane accumulates 4 queries x dims 4*lane..4*lane+3.
+constexpr int ATT_QB = 32, ATT_KT = 64, ATT_HD = 128, ATT_KP = ATT_HD + 4;
+constexpr int ATT_SMEM = (ATT_KT * ATT_KP + ATT_KT * ATT_HD + ATT_QB * ATT_HD + ATT_QB * ATT_KT) * 4;
+
+struct AttArgs {
+  const float* Pqk;  // [Sqk][L][2d]: Q in columns 0..d-1, K in columns d..2d-1
+  int Sqk;
+  const float* Pv;   // [Sv][L][d]
+  int Sv;
+  const float2* cs;  // RoPE (cos, sin) table [L][hd/2]
+  float* O;          // [L][d]
+  int L, d;
+  float scale;
+};
+
+__device__ __forceinline__ float2 split_sum2(const float* P, int S, int64_t stride, int64_t off) {
+  float2 a = *reinterpret_cast<const float2*>(P + off);
+  for (int s = 1; s < S; ++s) {
+    const float2 v = *reinterpret_cast<const float2*>(P + s * stride + off);
+    a.x += v.x;
+    a.y += v.y;
   }
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    float a = 0.f;
-    for (int s = 0; s < Sv; ++s) a += Pv[s * sv + (int64_t)p * d + c];
-    V[(int64_t)p * d + c] = a;
-  }
+  return a;
 }
 
-// Non-causal multi-head attention, f32, online softmax over key tiles of 32 (one key per lane):
-// O = softmax(Q K^T / sqrt(hd)) V per head. One CTA = one head x 16 queries (8 warps x 2).
-constexpr int ATT_QB = 16, ATT_KT = 32, ATT_HD = 128;
-__global__ void __launch_bounds__(256) attention_kernel(const float* __restrict__ Q, const float* __restrict__ K,
-                                                        const float* __restrict__ V, float* __restrict__ O, int L,
-                                                        int d, float scale) {
-  __shared__ float Kt[ATT_HD][ATT_KT + 1];
-  __shared__ float Vs[ATT_KT][ATT_HD];
-  __shared__ float Qs[ATT_QB][ATT_HD];
+__device__ __forceinline__ float2 rope2(float2 v, float2 r) {
+  return make_float2(v.x * r.x - v.y * r.y, v.x * r.y + v.y * r.x);
+}
+
+__global__ void __launch_bounds__(256, 2) attention_kernel(AttArgs a) {
+  extern __shared__ float4 att_smem4[];
+  float* Ks = reinterpret_cast<float*>(att_smem4);  // [KT][KP]
+  float* Vs = Ks + ATT_KT * ATT_KP;                 // [KT][HD]
+  float* Qs = Vs + ATT_KT * ATT_HD;                 // [QB][HD]
+  float* Ps = Qs + ATT_QB * ATT_HD;                 // [QB][KT]
   const int h = blockIdx.x, q0 = blockIdx.y * ATT_QB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < ATT_QB * ATT_HD; i += blockDim.x) {
-    const int qi = i / ATT_HD, e = i % ATT_HD;
-    Qs[qi][e] = (q0 + qi < L) ? Q[(int64_t)(q0 + qi) * d + h * ATT_HD + e] * scale : 0.f;
+  const int L = a.L, d = a.d;
+  const int64_t sqk = (int64_t)L * 2 * d, sv = (int64_t)L * d;
+  constexpr int HP = ATT_HD / 2;
+  for (int i = threadIdx.x; i < ATT_QB * HP; i += blockDim.x) {
+    const int qi = i / HP, pr = i % HP, p = q0 + qi;
+    float2 o = make_float2(0.f, 0.f);
+    if (p < L) {
+      o = rope2(split_sum2(a.Pqk, a.Sqk, sqk, (int64_t)p * 2 * d + h * ATT_HD + 2 * pr), a.cs[p * HP + pr]);
+      o.x *= a.scale;
+      o.y *= a.scale;
+    }
+    *reinterpret_cast<float2*>(Qs + qi * ATT_HD + 2 * pr) = o;
   }
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  float m[4], l[4], acc[4][4];
+#pragma unroll
+  for (int qq = 0; qq < 4; ++qq) {
+    m[qq] = -INFINITY;
+    l[qq] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[qq][c] = 0.f;
+  }
+  const float* qw = Qs + warp * 4 * ATT_HD;
+  float* pw = Ps + warp * 4 * ATT_KT;
   for (int k0 = 0; k0 < L; k0 += ATT_KT) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < ATT_KT * ATT_HD; i += blockDim.x) {
-      const int kj = i / ATT_HD, e = i % ATT_HD;
-      const bool ok = k0 + kj < L;
-      Kt[e][kj] = ok ? K[(int64_t)(k0 + kj) * d + h * ATT_HD + e] : 0.f;
-      Vs[kj][e] = ok ? V[(int64_t)(k0 + kj) * d + h * ATT_HD + e] : 0.f;
+    __syncthreads();  // previous tile fully consumed
+    for (int i = threadIdx.x; i < ATT_KT * HP; i += blockDim.x) {
+      const int kj = i / HP, pr = i % HP, p = k0 + kj;
+      float2 kv = make_float2(0.f, 0.f), vv = make_float2(0.f, 0.f);
+      if (p < L) {
+        kv = rope2(split_sum2(a.Pqk, a.Sqk, sqk, (int64_t)p * 2 * d + d + h * ATT_HD + 2 * pr), a.cs[p * HP + pr]);
+        vv = split_sum2(a.Pv, a.Sv, sv, (int64_t)p * d + h * ATT_HD + 2 * pr);
+      }
+      *reinterpret_cast<float2*>(Ks + kj * ATT_KP + 2 * pr) = kv;
+      *reinterpret_cast<float2*>(Vs + kj * ATT_HD + 2 * pr) = vv;
     }
     __syncthreads();
+    // scores of 4 queries x keys (lane, lane + 32)
+    float sc[4][2];
 #pragma unroll
-    for (int qq = 0; qq < 2; ++qq) {
-      const int qi = warp * 2 + qq;
-      float s0 = 0.f;
-#pragma unroll 8
-      for (int e = 0; e < ATT_HD; ++e) s0 = fmaf(Qs[qi][e], Kt[e][lane], s0);
-      if (k0 + lane >= L) s0 = -INFINITY;
-      float mx = s0;
+    for (int qq = 0; qq < 4; ++qq) sc[qq][0] = sc[qq][1] = 0.f;
+    const float* k0r = Ks + lane * ATT_KP;
+    const float* k1r = Ks + (lane + 32) * ATT_KP;
+#pragma unroll 4
+    for (int e = 0; e < ATT_HD; e += 4) {
+      const float4 ka = *reinterpret_cast<const float4*>(k0r + e);
+      const float4 kb = *reinterpret_cast<const float4*>(k1r + e);
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        const float4 q = *reinterpret_cast<const float4*>(qw + qq * ATT_HD + e);
+        sc[qq][0] = fmaf(q.x, ka.x, fmaf(q.y, ka.y, fmaf(q.z, ka.z, fmaf(q.w, ka.w, sc[qq][0]))));
+        sc[qq][1] = fmaf(q.x, kb.x, fmaf(q.y, kb.y, fmaf(q.z, kb.z, fmaf(q.w, kb.w, sc[qq][1]))));
+      }
+    }
+    const bool v0 = k0 + lane < L, v1 = k0 + lane + 32 < L;
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      const float s0 = v0 ? sc[qq][0] : -INFINITY, s1 = v1 ? sc[qq][1] : -INFINITY;
+      float mx = fmaxf(s0, s1);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float mnew = fmaxf(m[qq], mx);
+      const float mnew = fmaxf(m[qq], mx);  // finite: key k0 is always valid
       const float corr = expf(m[qq] - mnew);
-      const float p0 = expf(s0 - mnew);
-      float ps = p0;
+      const float p0 = expf(s0 - mnew), p1 = expf(s1 - mnew);
+      float ps = p0 + p1;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
       l[qq] = l[qq] * corr + ps;
       m[qq] = mnew;
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[qq][c] *= corr;
-      for (int j = 0; j < ATT_KT; ++j) {
-        const float pj = __shfl_sync(0xffffffffu, p0, j);
-        const float4 vv = *reinterpret_cast<const float4*>(&Vs[j][lane * 4]);
-        acc[qq][0] = fmaf(pj, vv.x, acc[qq][0]);
-        acc[qq][1] = fmaf(pj, vv.y, acc[qq][1]);
-        acc[qq][2] = fmaf(pj, vv.z, acc[qq][2]);
-        acc[qq][3] = fmaf(pj, vv.w, acc[qq][3]);
+      pw[qq * ATT_KT + lane] = p0;
+      pw[qq * ATT_KT + lane + 32] = p1;
+    }
+    __syncwarp();
+    const int nk = min(ATT_KT, L - k0);
+    for (int j = 0; j < nk; j += 4) {  // keys past nk have p = 0 and zero V rows; nk rounds up to 4
+      float4 pj[4];
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) pj[qq] = *reinterpret_cast<const float4*>(pw + qq * ATT_KT + j);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float4 vv = *reinterpret_cast<const float4*>(Vs + (j + t) * ATT_HD + lane * 4);
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const float pv = t == 0 ? pj[qq].x : t == 1 ? pj[qq].y : t == 2 ? pj[qq].z : pj[qq].w;
+          acc[qq][0] = fmaf(pv, vv.x, acc[qq][0]);
+          acc[qq][1] = fmaf(pv, vv.y, acc[qq][1]);
+          acc[qq][2] = fmaf(pv, vv.z, acc[qq][2]);
+          acc[qq][3] = fmaf(pv, vv.w, acc[qq][3]);
+        }
       }
     }
+    __syncwarp();
   }
 #pragma unroll
-  for (int qq = 0; qq < 2; ++qq) {
-    const int qi = q0 + warp * 2 + qq;
+  for (int qq = 0; qq < 4; ++qq) {
+    const int qi = q0 + warp * 4 + qq;
     if (qi < L) {
-      float4 o = make_float4(acc[qq][0] / l[qq], acc[qq][1] / l[qq], acc[qq][2] / l[qq], acc[qq][3] / l[qq]);
-      *reinterpret_cast<float4*>(O + (int64_t)qi * d + h * ATT_HD + lane * 4) = o;
+      const float inv = 1.0f / l[qq];
+      *reinterpret_cast<float4*>(a.O + (int64_t)qi * d + h * ATT_HD + lane * 4) =
+          make_float4(acc[qq][0] * inv, acc[qq][1] * inv, acc[qq][2] * inv, acc[qq][3] * inv);
     }
   }
 }
@@ -262,7 +318,7 @@ static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, co
 // ---------------------------------------------------------------------------------------------
 struct StepPlan {
   QgemmPlan qk, v, o, gu, dn;
-  size_t x, act_d, act_ff, pqk, pv, po, pgu, pdn, q, k, vv, att, rope, lm, bytes;
+  size_t x, act_d, act_ff, pqk, pv, po, pgu, pdn, att, rope, lm, bytes;
 };
 
 static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead) {
@@ -288,9 +344,6 @@ static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead
   S.po = take((size_t)S.o.splits * L * d * 4);
   S.pgu = take((size_t)S.gu.splits * L * 2 * f * 4);
   S.pdn = take((size_t)S.dn.splits * L * d * 4);
-  S.q = take(full ? (size_t)L * d * 4 : 0);
-  S.k = take(full ? (size_t)L * d * 4 : 0);
-  S.vv = take(full ? (size_t)L * d * 4 : 0);
   S.att = take(full ? (size_t)L * d * 4 : 0);
   S.rope = take(full ? (size_t)L * (m->head_dim / 2) * 8 : 0);
   S.lm = 0;
@@ -352,17 +405,15 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
     if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wqk, 2 * d, Pqk, S.qk, s))) return rc;
     if ((rc = gemm(DLLM_Q6_K, actd, L, d, Ly.wv, d, Pv, S.v, s))) return rc;
     if (full) {
-      float* Q = reinterpret_cast<float*>(ws + S.q);
-      float* K = reinterpret_cast<float*>(ws + S.k);
-      float* V = reinterpret_cast<float*>(ws + S.vv);
       float* A = reinterpret_cast<float*>(ws + S.att);
-      reduce_rope_kernel<<<(int)L, 256, 0, s>>>(Pqk, S.qk.splits, Pv, S.v.splits,
-                                                reinterpret_cast<const float2*>(ws + S.rope), (int)L, d, hd, Q, K, V);
+      const AttArgs aa{Pqk, S.qk.splits, Pv, S.v.splits, reinterpret_cast<const float2*>(ws + S.rope), A, (int)L, d,
+                       1.0f / sqrtf((float)hd)};
+      cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
+      const dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB));
+      attention_kernel<<<ag, 256, ATT_SMEM, s>>>(aa);
       note_launch();
-      dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB));
-      attention_kernel<<<ag, 256, 0, s>>>(Q, K, V, A, (int)L, d, 1.0f / sqrtf((float)hd));
-      note_launch();
-      cudaError_t e = cudaGetLastError();
+      e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "launch attention");
       if ((rc = quantize_rows(A, L, d, d, nullptr, m->eps, actd, s))) return rc;
     } else {

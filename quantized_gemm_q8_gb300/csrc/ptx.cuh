@@ -16,6 +16,7 @@ enum : int {
   ERR_TIMEOUT_EPILOGUE = 1 << 3,
   ERR_TIMEOUT_SELFTEST = 1 << 4,
   ERR_TIMEOUT_OTHER = 1 << 5,
+  ERR_RANGE = 1 << 6,  // a Q4_K block whose dmin/d ratio cannot be folded (|dmin/d| > 4e6)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -43,20 +44,50 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of the phase of parity `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Suspending test: a thread whose phase is not complete sleeps until it completes or about
+// `ns` nanoseconds pass (the hint bounds how late a sleeping thread can notice completion).
+__device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait for the phase of parity `parity` to complete. Gives up (returns false) when
 // another role raised `abort` or after `limit` SM cycles, in which case it raises `abort`.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          long long limit) {
-  if (mbar_try_wait(bar, parity)) return true;
+// sleep_ns = 0 spins on the non-blocking test (lowest latency, but a spinning warp takes
+// issue slots from the warps doing the work); sleep_ns > 0 sleeps between tests.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, long long limit,
+                                          uint32_t sleep_ns = 0) {
+  if (mbar_test_wait(bar, parity)) return true;
   long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (sleep_ns ? mbar_try_wait_ns(bar, parity, sleep_ns) : mbar_test_wait(bar, parity)) return true;
     if (*abort) return false;
     if (clock64() - t0 > limit) {
       *abort = 1;
       return false;
     }
   }
+}
+// Warp-wide bounded wait: every lane waits; all lanes return the same result.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, long long limit,
+                                          uint32_t sleep_ns = 0) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit, sleep_ns));
 }
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -124,6 +155,30 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Warp-wide forms: every lane of the warp executes them with identical (warp-uniform) operands
+// and one elected lane issues, which keeps the operands in uniform registers.
+__device__ __forceinline__ void mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 q, %4, 0;\n elect.sync _|p, 0xffffffff;\n"
+      " @p tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, q;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 q, %4, 0;\n elect.sync _|p, 0xffffffff;\n"
+      " @p tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
+      " @p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+      : "memory");
+}
 // Arrive once on `bar` when all previously issued tcgen05 operations of this thread complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -154,6 +209,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
       "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
+}
+// Store 8 consecutive 32-bit columns of the warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

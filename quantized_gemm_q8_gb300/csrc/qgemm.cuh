@@ -13,29 +13,42 @@
 // operand B in shared memory (TMA, 128-byte swizzle). Keeping A out of shared memory halves
 // the shared-memory traffic per MMA, which bounds an M=128, N<=160 tile otherwise.
 //
-// Per super-block sb two accumulator "parts" are produced into TMEM slots of NT columns:
-//   Q4_K: part 0 = I = sum_k (scale_j * q4_k) * a_k           (16 MMAs, K = 256)
-//         part 1 = J = sum_g min_{g/2} * bsum16_g               (1 MMA, K = 16, A from smem)
-//         y += d_a * (d * I - dmin * J)
-//   Q6_K: the int8 group scale s = 16 * s_hi + s_lo (s_lo in [0,15]) so that both products
-//         s_hi * (q-32) and s_lo * (q-32) are exact f16 integers:
-//         part 0 = I_hi = sum s_hi (q-32) a,  part 1 = I_lo = sum s_lo (q-32) a   (16+16 MMAs)
-//         y += d_a * d * (16 * I_hi + I_lo)
-// The epilogue folds part p as y += (c_p * P) * d_a with c = (d, -dmin) or (16 d, d); it
-// drains a whole part into registers at once and frees the slot before the arithmetic.
+// Per super-block ONE accumulator part D is produced, in TMEM slot t & 1 (two slots of NT
+// columns: the epilogue drains super-block t while the tensor core fills t + 1):
+//   Q4_K: D = 2^-k * I - sum_g c_g * bsum16_g,   I = sum_k (scale_j * q4_k) * a_k,
+//         c_g = min_{g/2} * (dmin / d) * 2^-k,   y += d_a * (d * 2^k) * D
+//         The 16 MMAs of I read A = scale * q4 * 2^-k from tensor memory (exact f16 values); the
+//         min term is two more K = 16 MMAs from shared memory whose A operands are the f16
+//         head and tail of -c_g (their sum carries c_g to 2^-22 relative) against the exact
+//         f16 activation 16-sums. k >= 0 is the smallest shift keeping 63 * |dmin / d| * 2^-k
+//         below 2^14 (k = 0 for any realistic block). A row with d = 0 uses D = -sum min * bsum
+//         and y += d_a * dmin * D.
+//   Q6_K: the int8 group scale s = 16 * s_hi + s_lo (s_lo in [0,15]); per K-quarter 4 MMAs
+//         with A = 16 * s_hi * (q-32) and 4 with A = s_lo * (q-32) (both exact f16 integers)
+//         accumulate D = sum s (q-32) a;  y += d_a * d * D.
+// Integer sums are exact while every partial sum stays below 2^24 in magnitude (always for
+// Q6_K's separate hi and lo sums, the debug parts below, and random data; an all-extreme
+// block can exceed it and then rounds at 2^-24 relative). A debug mode runs the same kernel
+// with one part isolated (Q4_K: I or J; Q6_K: I_hi or I_lo) and writes the exact integers.
+// The epilogue loads the part into registers in groups, frees the slot once the last group is
+// loaded, and folds y += (f * D) * d_a.
 //
 // Warp roles (896 threads, 7 warpgroups): warps 0-15 epilogue (warp w reads TMEM lanes
-// 32*(w%4).. and quarter w/4 of the NT columns), warps 16-23 decode (two threads per weight
-// row = TMEM lane, one per half of each K-quarter), warp 24 producer (one thread issues bulk /
-// tensor copies), warp 25 MMA issuer (one thread) + TMEM owner, warps 26-27 idle. setmaxnreg
-// re-splits the 72-per-thread launch allocation: 88 epilogue, 56 decode, 40 control
-// (512*88 + 256*56 + 128*40 = 896*72).
+// 32*(w%4).. and quarter w/4 of the NT columns), warps 16-23 decode, warp 24 activation
+// producer, warp 25 MMA
+// issuer (whole warp, one elected lane issues) and TMEM owner, warp 26 weight producer, warp
+// 27 idle. The decode warps form two groups of four (one thread per weight row = TMEM lane
+// in each) that take alternate K-stages, so one group's tensor-memory stores drain while the
+// other decodes; each group also writes half of the Q4_K min-operand rows. setmaxnreg re-splits the 72-per-thread launch allocation: 88 epilogue, 56 decode,
+// 40 control (512*88 + 256*56 + 128*40 = 896*72).
 //
 // Rings (mbarrier-synchronized, every wait bounded):
-//   W  raw packed super-block of the 128 rows, smem (bulk copy)       producer -> decode
-//   X  per-super-block extras, smem: d/dmin plane, d_a, J operands    producer,decode -> MMA,epi
-//   B  activation quarter tile NT x 64 f16, smem, 128-byte swizzle    producer -> MMA
-//   A  decoded weight quarter 128 x 64 f16 (Q6_K: hi and lo), TMEM    decode -> MMA
+//   W  raw packed super-block of the 128 rows (+ Q4_K d/dmin), smem   weight producer -> decode
+//   E  per-super-block scales for the epilogue, smem: d/dmin, d_a    act. producer -> epilogue
+//   J  Q4_K min operands, smem: activation 16-sums (bulk copy) and     producer, decode -> MMA
+//      -c head and tail rows
+//   K  K-stage: activation tile (smem, TMA, 128-byte swizzle) and     producer, decode -> MMA
+//      decoded weights (TMEM), 64 TMEM columns
 //   S  accumulator slots, TMEM                                        MMA -> epilogue
 // K order inside each aligned group of 4 is (0,2,1,3) on both operands (the order in which
 // the nibble-to-f16 trick below produces weights); the activation operand is stored that way.
@@ -55,12 +68,15 @@ constexpr int Q6K_BLOB = 26624;  // 128 rows x (128 B ql + 64 B qh + 16 B scales
 constexpr int Q4K_DD = 512;      // 128 rows x (f16 d, f16 dmin)
 constexpr int Q6K_DD = 256;      // 128 rows x f16 d
 constexpr int QG_THREADS = 896;
-constexpr int QG_EPI_WARPS = 16, QG_DEC_WARP0 = 16, QG_DEC_WARPS = 8, QG_PROD_WARP = 24, QG_MMA_WARP = 25;
+constexpr int QG_EPI_WARPS = 16, QG_DEC_WARP0 = 16, QG_DEC_WARPS = 8, QG_PROD_WARP = 24, QG_MMA_WARP = 25,
+              QG_WPROD_WARP = 26;
 constexpr int QG_REGS_LAUNCH = 72;  // 65536 / 896 rounded down to a multiple of 8
 constexpr int QG_REGS_EPI = 88, QG_REGS_DEC = 56, QG_REGS_CTL = 40;
 static_assert(512 * QG_REGS_EPI + 256 * QG_REGS_DEC + 128 * QG_REGS_CTL <= QG_THREADS * QG_REGS_LAUNCH,
               "register split");
 constexpr int SMEM_LIMIT = 232448;
+// sleep hints (ns) of the waiting roles; the MMA warp spins
+constexpr uint32_t QG_SLEEP_DEC = 64, QG_SLEEP_EPI = 256, QG_SLEEP_PROD = 256;
 constexpr int TMEM_COLS = 512;
 
 __host__ __device__ constexpr int al128(int x) { return (x + 127) & ~127; }
@@ -72,36 +88,43 @@ struct QCfg {
   static constexpr int NC = NT / 4;  // columns per epilogue thread
   static constexpr int W_BYTES = Q4 ? Q4K_BLOB : Q6K_BLOB;
   static constexpr int DD_BYTES = Q4 ? Q4K_DD : Q6K_DD;
+  // a W slot: the blob, then (Q4_K) the super-block's d/dmin plane for the decode warps
+  static constexpr int W_SLOT = W_BYTES + (Q4 ? DD_BYTES : 0);
   // K-stage ring: one stage = QPS K-quarters (64 each) of both operands, 8 MMAs per stage:
   // Q4_K two quarters (one MMA chain), Q6_K one quarter (hi and lo chains).
   static constexpr int QPS = Q4 ? 2 : 1;
   static constexpr int SPS = 4 / QPS;  // stages per super-block
   // TMEM: accumulator slots, then the A operand of each stage (64 columns per stage)
-  static constexpr int NSLOT = NT >= 128 ? 2 : 4;
+  static constexpr int NSLOT = 2;
   static constexpr int ACOL = NSLOT * NT;
   static constexpr int ASTG = 64;
   static constexpr int K_STAGES = cmin(6, (TMEM_COLS - ACOL) / ASTG);
-  // shared memory
-  static constexpr int X_STAGES = 3;
-  static constexpr int X_DD = 0;
-  static constexpr int X_DA = al128(DD_BYTES);
-  static constexpr int X_BJ = X_DA + al128(NT * 4);
-  static constexpr int X_AJ = X_BJ + (Q4 ? NT * 32 : 0);
-  static constexpr int X_BYTES = al128(X_AJ + (Q4 ? 4096 : 0));
-  static constexpr int X_TX = DD_BYTES + NT * 4 + (Q4 ? NT * 32 : 0);
+  // shared memory: E ring (epilogue scales), J ring (Q4_K min operands)
+  static constexpr int E_STAGES = 6;
+  static constexpr int E_DD = 0;
+  static constexpr int E_DA = al128(DD_BYTES);
+  static constexpr int E_BYTES = al128(E_DA + NT * 4);
+  static constexpr int E_TX = DD_BYTES + NT * 4;
+  static constexpr int J_STAGES = Q4 ? 3 : 0;
+  static constexpr int J_BJ = 0;
+  static constexpr int J_AJ = al128(NT * 32);
+  static constexpr int J_BYTES = J_AJ + 8192;  // -c head, then tail, 128 rows x 16 f16 each
+  static constexpr int J_TX = NT * 32;
   static constexpr int B_QUARTER = NT * 128;
   static constexpr int B_STAGE = QPS * B_QUARTER;
-  static constexpr int SM_AVAIL = SMEM_LIMIT - 2048 - K_STAGES * B_STAGE - X_STAGES * X_BYTES;
-  static constexpr int W_STAGES = cmin(6, SM_AVAIL / W_BYTES);
+  static constexpr int SM_AVAIL = SMEM_LIMIT - 2048 - K_STAGES * B_STAGE - E_STAGES * E_BYTES - J_STAGES * J_BYTES;
+  static constexpr int W_STAGES = cmin(6, SM_AVAIL / W_SLOT);
   static constexpr int OFF_B = 0;
   static constexpr int OFF_W = OFF_B + K_STAGES * B_STAGE;
-  static constexpr int OFF_X = OFF_W + W_STAGES * W_BYTES;
-  static constexpr int OFF_BAR = OFF_X + X_STAGES * X_BYTES;
+  static constexpr int OFF_E = OFF_W + W_STAGES * W_SLOT;
+  static constexpr int OFF_J = OFF_E + E_STAGES * E_BYTES;
+  static constexpr int OFF_BAR = OFF_J + J_STAGES * J_BYTES;
   // barrier indices
   static constexpr int BK_FULL = 0, BK_EMPTY = BK_FULL + K_STAGES;
   static constexpr int BW_FULL = BK_EMPTY + K_STAGES, BW_EMPTY = BW_FULL + W_STAGES;
-  static constexpr int BX_FULL = BW_EMPTY + W_STAGES, BX_EMPTY = BX_FULL + X_STAGES;
-  static constexpr int BS_FULL = BX_EMPTY + X_STAGES, BS_EMPTY = BS_FULL + NSLOT;
+  static constexpr int BE_FULL = BW_EMPTY + W_STAGES, BE_EMPTY = BE_FULL + E_STAGES;
+  static constexpr int BJ_FULL = BE_EMPTY + E_STAGES, BJ_EMPTY = BJ_FULL + J_STAGES;
+  static constexpr int BS_FULL = BJ_EMPTY + J_STAGES, BS_EMPTY = BS_FULL + NSLOT;
   static constexpr int B_DONE = BS_EMPTY + NSLOT;
   static constexpr int NBAR = B_DONE + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -109,7 +132,7 @@ struct QCfg {
   static_assert(SMEM <= SMEM_LIMIT, "shared memory budget");
   static_assert(W_STAGES >= 2 && K_STAGES >= 2, "ring depth");
   static_assert(NT % 32 == 0 && NT >= 32 && NT <= 160, "token tile");
-  static_assert(OFF_W % 16 == 0 && OFF_X % 128 == 0, "alignment");
+  static_assert(OFF_W % 16 == 0 && OFF_E % 128 == 0 && OFF_J % 128 == 0, "alignment");
 };
 
 struct QgemmParams {
@@ -122,7 +145,8 @@ struct QgemmParams {
   float* y;  // may be null (debug sums only)
   long long ldy, split_stride;
   int accumulate;
-  int32_t* dbg;  // [2][nsb][m][n] or null
+  int32_t* dbg;   // debug: exact integer sums of one part, [nsb][m][n]
+  int dbg_mode;   // 0 off; 1 part 0 only (Q4_K I, Q6_K I_hi); 2 part 1 only (Q4_K J, Q6_K I_lo)
   int* err;      // device error word
   // mode 1 (LM head): instead of y, per (weight tile, TMEM lane quadrant, token) softmax
   // partials over the 32 weight rows of the quadrant: max logit, its row (lowest on ties),
@@ -168,33 +192,6 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
-// Q4_K: decode K-quarter q of row t (its 32 quant bytes: low nibbles = sub-block 2q, high
-// nibbles = sub-block 2q+1) into 32 words = 64 f16 values scale*q4, in TMEM column order
-// (word 4c + i = 16-byte chunk c, chunks 0-3 low nibbles, 4-7 high nibbles). The value is
-// produced exactly: the nibble is OR-ed into the f16 pattern 0x6400 (= 1024 + q, or 1024 + 16q
-// for a high nibble) and one fused multiply-add with (scale, -1024*scale) [or (scale/16,
-// -64*scale)] returns scale*q (an integer <= 945). Inside a chunk the k order is
-// (0,2,1,3, 4,6,5,7), the order in which the two nibble lanes of a 32-bit word come out.
-__device__ __forceinline__ void decode_q4k_quarter(const uint8_t* W, int t, int q, __half2 mlo, __half2 alo,
-                                                   __half2 mhi, __half2 ahi, uint32_t (&o)[2][16]) {
-  const uint4 v0 = *reinterpret_cast<const uint4*>(W + (2 * q) * 2048 + t * 16);
-  const uint4 v1 = *reinterpret_cast<const uint4*>(W + (2 * q + 1) * 2048 + t * 16);
-  const uint32_t x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const uint32_t w0 = x[2 * c], w1 = x[2 * c + 1];
-    const uint32_t w0s = w0 >> 8, w1s = w1 >> 8;
-    o[0][4 * c + 0] = hfma2u((w0 & 0x000F000Fu) | 0x64006400u, mlo, alo);
-    o[0][4 * c + 1] = hfma2u((w0s & 0x000F000Fu) | 0x64006400u, mlo, alo);
-    o[0][4 * c + 2] = hfma2u((w1 & 0x000F000Fu) | 0x64006400u, mlo, alo);
-    o[0][4 * c + 3] = hfma2u((w1s & 0x000F000Fu) | 0x64006400u, mlo, alo);
-    o[1][4 * c + 0] = hfma2u((w0 & 0x00F000F0u) | 0x64006400u, mhi, ahi);
-    o[1][4 * c + 1] = hfma2u((w0s & 0x00F000F0u) | 0x64006400u, mhi, ahi);
-    o[1][4 * c + 2] = hfma2u((w1 & 0x00F000F0u) | 0x64006400u, mhi, ahi);
-    o[1][4 * c + 3] = hfma2u((w1s & 0x00F000F0u) | 0x64006400u, mhi, ahi);
-  }
-}
-
 // Q4_K, one half of a K-quarter: h = 0 the low nibbles (chunks 0-3), h = 1 the high nibbles
 // (chunks 4-7) of the quarter's 32 quant bytes, as 16 words; (mul, add) as above for the
 // half's sub-block.
@@ -214,55 +211,77 @@ __device__ __forceinline__ void decode_q4k_half(const uint8_t* W, int t, int q, 
   }
 }
 
-// Q6_K: decode half tt of K-quarter q (half-block hq = q/2, t-slot 2(q%2)+tt) of row t into
-// 16 words of the hi operand (value s_hi*(q6-32)) and 16 words of the lo operand (value
-// s_lo*(q6-32)); both exact f16 integers (the int8 group scale s = 16*s_hi + s_lo, s_lo in
-// [0,15]). Even quarters take the low ql nibble and the f16 pattern 1024 + q6 (qh bits at 4-5),
-// odd quarters the high nibble and 1024 + 16*q6 (qh bits at 8-9) with the scale divided by 16.
-__device__ __forceinline__ void decode_q6k_half(const uint8_t* W, int t, int q, int tt, const int8_t* sc,
-                                                uint32_t (&hi)[16], uint32_t (&lo)[16]) {
+// Q6_K: piece ps (0 or 1) of half tt of K-quarter q (half-block hq = q/2, t-slot 2(q%2)+tt) of
+// row t, from one 16-byte load of ql and one of qh: 8 words of the hi operand
+// (hs * s_hi * (q6-32)) and 8 of the lo operand (ls * s_lo * (q6-32)), exact f16 integers (the
+// int8 group scale s = 16 * s_hi + s_lo, s_lo in [0,15]; hs in {0, 1, 16}, ls in {0, 1}).
+// Even quarters take the low ql nibble and the f16 pattern 1024 + q6 (qh bits at 4-5), odd
+// quarters the high nibble and 1024 + 16*q6 (qh bits at 8-9) with the scale divided by 16.
+__device__ __forceinline__ void decode_q6k_piece(const uint8_t* W, int t, int q, int tt, int ps, const int8_t* sc,
+                                                 float hs, float ls, uint32_t (&hi)[8], uint32_t (&lo)[8]) {
   const int hq = q >> 1, odd = q & 1;
-  uint32_t ql[8], qh[8];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint4 v = *reinterpret_cast<const uint4*>(W + (4 * hq + 2 * tt + i) * 2048 + t * 16);
-    ql[4 * i] = v.x;
-    ql[4 * i + 1] = v.y;
-    ql[4 * i + 2] = v.z;
-    ql[4 * i + 3] = v.w;
-    const uint4 u = *reinterpret_cast<const uint4*>(W + 16384 + (2 * hq + i) * 2048 + t * 16);
-    qh[4 * i] = u.x;
-    qh[4 * i + 1] = u.y;
-    qh[4 * i + 2] = u.z;
-    qh[4 * i + 3] = u.w;
-  }
+  const uint4 v = *reinterpret_cast<const uint4*>(W + (4 * hq + 2 * tt + ps) * 2048 + t * 16);
+  const uint4 u = *reinterpret_cast<const uint4*>(W + 16384 + (2 * hq + ps) * 2048 + t * 16);
+  const uint32_t ql[4] = {v.x, v.y, v.z, v.w}, qh[4] = {u.x, u.y, u.z, u.w};
   const uint32_t nmask = odd ? 0x00F000F0u : 0x000F000Fu;
   const uint32_t hmask = odd ? 0x03000300u : 0x00300030u;
   const float fm = odd ? 0.0625f : 1.0f;
   const float fa = odd ? -96.0f : -1056.0f;
   const int tslot = 2 * odd + tt;
   const int shift = tt ? 2 : 4;
+  const int s = sc[8 * hq + 2 * tslot + ps];
+  const float s_hi = hs == 0.f ? 0.f : (float)(s >> 4), s_lo = (float)(s & 15) * ls;
+  const __half2 mH = __float2half2_rn(s_hi * fm), aH = __float2half2_rn(s_hi * fa);
+  const __half2 mL = __float2half2_rn(s_lo * fm), aL = __float2half2_rn(s_lo * fa);
+  const __half2 h16 = __float2half2_rn(hs == 16.f ? 16.f : 1.f);
 #pragma unroll
-  for (int cp = 0; cp < 4; ++cp) {
-    const int s = sc[8 * hq + 2 * tslot + (cp >> 1)];
-    const int s_hi = s >> 4, s_lo = s & 15;
-    const __half2 mH = __float2half2_rn((float)s_hi * fm), aH = __float2half2_rn((float)s_hi * fa);
-    const __half2 mL = __float2half2_rn((float)s_lo * fm), aL = __float2half2_rn((float)s_lo * fa);
-    const uint32_t X0 = ql[2 * cp], X1 = ql[2 * cp + 1];
-    const uint32_t H0 = qh[2 * cp], H1 = qh[2 * cp + 1];
+  for (int c = 0; c < 2; ++c) {
+    const uint32_t X0 = ql[2 * c], X1 = ql[2 * c + 1];
+    const uint32_t H0 = qh[2 * c], H1 = qh[2 * c + 1];
     const uint32_t v0 = (X0 & nmask) | ((H0 << shift) & hmask) | 0x64006400u;
     const uint32_t v1 = ((X0 >> 8) & nmask) | (((H0 >> 8) << shift) & hmask) | 0x64006400u;
     const uint32_t v2 = (X1 & nmask) | ((H1 << shift) & hmask) | 0x64006400u;
     const uint32_t v3 = ((X1 >> 8) & nmask) | (((H1 >> 8) << shift) & hmask) | 0x64006400u;
-    hi[4 * cp + 0] = hfma2u(v0, mH, aH);
-    hi[4 * cp + 1] = hfma2u(v1, mH, aH);
-    hi[4 * cp + 2] = hfma2u(v2, mH, aH);
-    hi[4 * cp + 3] = hfma2u(v3, mH, aH);
-    lo[4 * cp + 0] = hfma2u(v0, mL, aL);
-    lo[4 * cp + 1] = hfma2u(v1, mL, aL);
-    lo[4 * cp + 2] = hfma2u(v2, mL, aL);
-    lo[4 * cp + 3] = hfma2u(v3, mL, aL);
+    hi[4 * c + 0] = h2u(__hmul2(u2h(hfma2u(v0, mH, aH)), h16));
+    hi[4 * c + 1] = h2u(__hmul2(u2h(hfma2u(v1, mH, aH)), h16));
+    hi[4 * c + 2] = h2u(__hmul2(u2h(hfma2u(v2, mH, aH)), h16));
+    hi[4 * c + 3] = h2u(__hmul2(u2h(hfma2u(v3, mH, aH)), h16));
+    lo[4 * c + 0] = hfma2u(v0, mL, aL);
+    lo[4 * c + 1] = hfma2u(v1, mL, aL);
+    lo[4 * c + 2] = hfma2u(v2, mL, aL);
+    lo[4 * c + 3] = hfma2u(v3, mL, aL);
   }
+}
+
+// Q4_K per-row fold of the min term into the scale-sum accumulator (see the top of the
+// file): A scale 2^-k (0 when d = 0), min coefficient -(dmin/d) * 2^-k (-1 when d = 0) and the
+// epilogue factor d * 2^k (dmin when d = 0). The decode and epilogue warps evaluate the same
+// function on the same f16 inputs. Sets *bad when the coefficient cannot be held (|dmin/d|
+// beyond 4e6; no real block comes near).
+struct Q4Fold {
+  float ascale, cmul, factor;
+};
+__device__ __forceinline__ Q4Fold q4k_fold(float d, float dmin, bool* bad) {
+  Q4Fold f;
+  if (d == 0.f) {
+    f.ascale = 0.f;
+    f.cmul = -1.f;
+    f.factor = dmin;
+    return f;
+  }
+  const float r = dmin / d;
+  float mag = 63.f * fabsf(r), sc = 1.f;
+  int k = 0;
+  while (mag > 16384.f && k < 14) {
+    mag *= 0.5f;
+    sc *= 0.5f;
+    ++k;
+  }
+  if (!(mag <= 16384.f)) *bad = true;
+  f.ascale = sc;
+  f.cmul = -r * sc;
+  f.factor = d / sc;
+  return f;
 }
 
 __device__ __forceinline__ void unit_coords(const QgemmParams& p, int u, int& tn, int& tm, int& sp, int& sb0,
@@ -290,16 +309,20 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::K_STAGES; ++i) {
-      mbar_init(BAR(C::BK_FULL + i), 1 + QG_DEC_WARPS);  // producer (with the B bytes) + decode warps
+      mbar_init(BAR(C::BK_FULL + i), 1 + QG_DEC_WARPS / 2);  // producer (with the B bytes) + a decode group
       mbar_init(BAR(C::BK_EMPTY + i), 1);
     }
     for (int i = 0; i < C::W_STAGES; ++i) {
       mbar_init(BAR(C::BW_FULL + i), 1);
       mbar_init(BAR(C::BW_EMPTY + i), QG_DEC_WARPS);
     }
-    for (int i = 0; i < C::X_STAGES; ++i) {
-      mbar_init(BAR(C::BX_FULL + i), C::Q4 ? 1 + QG_DEC_WARPS : 1);
-      mbar_init(BAR(C::BX_EMPTY + i), C::Q4 ? QG_EPI_WARPS + 1 : QG_EPI_WARPS);
+    for (int i = 0; i < C::E_STAGES; ++i) {
+      mbar_init(BAR(C::BE_FULL + i), 1);
+      mbar_init(BAR(C::BE_EMPTY + i), QG_EPI_WARPS);
+    }
+    for (int i = 0; i < C::J_STAGES; ++i) {
+      mbar_init(BAR(C::BJ_FULL + i), 1 + QG_DEC_WARPS);  // producer (activation sums, tx) + decode
+      mbar_init(BAR(C::BJ_EMPTY + i), 1);                // MMA commit
     }
     for (int i = 0; i < C::NSLOT; ++i) {
       mbar_init(BAR(C::BS_FULL + i), 1);
@@ -320,9 +343,10 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
 
   if (warp >= QG_PROD_WARP) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(QG_REGS_CTL));
-    if (warp == QG_PROD_WARP && lane == 0) {
-      // ---------------------------------------------------------- producer (one thread)
-      prefetch_tensormap(&tmap);
+    if (warp == QG_WPROD_WARP && lane == 0) {
+      // ---------------------------------------------------------- weight producer (one thread):
+      // raw packed super-blocks as far ahead as the W ring allows (HBM latency is hidden only
+      // by depth, so this runs independently of the activation stages)
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
@@ -330,25 +354,51 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         unit_coords(p, u, tn, tm, sp, sb0, sb1);
         const uint8_t* blob = p.wblob + (size_t)tn * p.nsb * C::W_BYTES;
         const uint8_t* dd = p.wdd + (size_t)tn * p.nsb * C::DD_BYTES;
-        const int tok0 = tm * NT;
         for (int sb = sb0; sb < sb1; ++sb, ++it) {
           const int w = it % C::W_STAGES;
-          if (!(ok = mbar_wait(BAR(C::BW_EMPTY + w), ((it / C::W_STAGES) & 1) ^ 1, abort_flag, lim))) break;
-          mbar_expect_tx(BAR(C::BW_FULL + w), C::W_BYTES);
-          bulk_g2s(sbase + C::OFF_W + w * C::W_BYTES, blob + (size_t)sb * C::W_BYTES, C::W_BYTES,
-                   BAR(C::BW_FULL + w));
+          if (!(ok = mbar_wait(BAR(C::BW_EMPTY + w), ((it / C::W_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_PROD))) break;
+          const uint32_t ws = sbase + C::OFF_W + w * C::W_SLOT;
+          mbar_expect_tx(BAR(C::BW_FULL + w), C::W_SLOT);
+          bulk_g2s(ws, blob + (size_t)sb * C::W_BYTES, C::W_BYTES, BAR(C::BW_FULL + w));
+          if (C::Q4) bulk_g2s(ws + C::W_BYTES, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES, BAR(C::BW_FULL + w));
           QTRACE(true, 1, it);
-          const int x = it % C::X_STAGES;
-          if (!(ok = mbar_wait(BAR(C::BX_EMPTY + x), ((it / C::X_STAGES) & 1) ^ 1, abort_flag, lim))) break;
-          const uint32_t xs = sbase + C::OFF_X + x * C::X_BYTES;
-          mbar_expect_tx(BAR(C::BX_FULL + x), C::X_TX);
-          bulk_g2s(xs + C::X_DD, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES, BAR(C::BX_FULL + x));
-          bulk_g2s(xs + C::X_DA, p.act_d + (size_t)sb * p.lpad + tok0, NT * 4, BAR(C::BX_FULL + x));
-          if (C::Q4)
-            bulk_g2s(xs + C::X_BJ, p.act_j + ((size_t)sb * p.lpad + tok0) * 32, NT * 32, BAR(C::BX_FULL + x));
+        }
+      }
+      if (!ok) {
+        atomicOr(p.err, ERR_TIMEOUT_PRODUCER);
+        const long long t0 = clock64();  // let issued copies land before the CTA can exit (~1 ms)
+        while (clock64() - t0 < 2000000) {
+        }
+      }
+    } else if (warp == QG_PROD_WARP && lane == 0) {
+      // ---------------------------------------------------------- activation producer (one
+      // thread): per super-block the epilogue scales (E), the Q4_K activation 16-sums (J), then
+      // the activation operand stages through the tensor map
+      prefetch_tensormap(&tmap);
+      int it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        int tn, tm, sp, sb0, sb1;
+        unit_coords(p, u, tn, tm, sp, sb0, sb1);
+        const uint8_t* dd = p.wdd + (size_t)tn * p.nsb * C::DD_BYTES;
+        const int tok0 = tm * NT;
+        for (int sb = sb0; sb < sb1; ++sb, ++it) {
+          const int e = it % C::E_STAGES;
+          if (!(ok = mbar_wait(BAR(C::BE_EMPTY + e), ((it / C::E_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_PROD))) break;
+          const uint32_t es = sbase + C::OFF_E + e * C::E_BYTES;
+          mbar_expect_tx(BAR(C::BE_FULL + e), C::E_TX);
+          bulk_g2s(es + C::E_DD, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES, BAR(C::BE_FULL + e));
+          bulk_g2s(es + C::E_DA, p.act_d + (size_t)sb * p.lpad + tok0, NT * 4, BAR(C::BE_FULL + e));
+          if constexpr (C::Q4) {
+            const int jx = it % C::J_STAGES;
+            if (!(ok = mbar_wait(BAR(C::BJ_EMPTY + jx), ((it / C::J_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_PROD))) break;
+            mbar_expect_tx(BAR(C::BJ_FULL + jx), C::J_TX);
+            bulk_g2s(sbase + C::OFF_J + jx * C::J_BYTES + C::J_BJ, p.act_j + ((size_t)sb * p.lpad + tok0) * 32,
+                     NT * 32, BAR(C::BJ_FULL + jx));
+          }
           for (int st = 0; st < C::SPS; ++st) {
             const int j = C::SPS * it + st, b = j % C::K_STAGES;
-            if (!(ok = mbar_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim))) break;
+            if (!(ok = mbar_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_PROD))) break;
             mbar_expect_tx(BAR(C::BK_FULL + b), C::B_STAGE);
 #pragma unroll
             for (int qq = 0; qq < C::QPS; ++qq)
@@ -367,156 +417,182 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         while (clock64() - t0 < 2000000) {
         }
       }
-    } else if (warp == QG_MMA_WARP && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer (one thread)
+    } else if (warp == QG_MMA_WARP) {
+      // ---------------------------------------------------------- MMA issuer (whole warp, one
+      // elected lane issues). Accumulator slot s (NT columns at s * NT) is written only after
+      // the epilogue drained its previous contents; se0/se1 count those waits.
       constexpr uint32_t IDESC = idesc_f16(BM, NT);
       int it = 0;
+      uint32_t se0 = 0, se1 = 0;
       bool ok = true;
+      auto wait_tc = [&](uint32_t bar, uint32_t parity) -> bool {
+        const bool r = warp_wait(bar, parity, abort_flag, lim);
+        tc_fence_after();
+        return r;
+      };
+      auto slot_free = [&](int s) -> bool {
+        const uint32_t n = s ? se1++ : se0++;
+        return wait_tc(BAR(C::BS_EMPTY + s), (n & 1) ^ 1);
+      };
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
         int tn, tm, sp, sb0, sb1;
         unit_coords(p, u, tn, tm, sp, sb0, sb1);
         for (int sb = sb0; sb < sb1; ++sb, ++it) {
-          const int c0 = 2 * it, c1 = 2 * it + 1;
-          const int s0 = c0 % C::NSLOT, s1 = c1 % C::NSLOT;
-          if (!(ok = mbar_wait(BAR(C::BS_EMPTY + s0), ((c0 / C::NSLOT) & 1) ^ 1, abort_flag, lim))) break;
-          tc_fence_after();
-          for (int st = 0; st < C::SPS; ++st) {
-            const int j = C::SPS * it + st, b = j % C::K_STAGES;
-            if (!(ok = mbar_wait(BAR(C::BK_FULL + b), (j / C::K_STAGES) & 1, abort_flag, lim))) break;
-            QTRACE(true, 2, j);
-            tc_fence_after();
-            const uint32_t acol = tmem + C::ACOL + b * C::ASTG;
-            const uint32_t bst = sbase + C::OFF_B + b * C::B_STAGE;
+          const int s = it & 1;
+          if (!(ok = slot_free(s))) break;  // super-block it - 2 drained
+          const uint32_t dslot = tmem + s * NT;
+          if constexpr (C::Q4) {
+            for (int st = 0; st < 2; ++st) {
+              const int j = 2 * it + st, b = j % C::K_STAGES;
+              if (!(ok = wait_tc(BAR(C::BK_FULL + b), (j / C::K_STAGES) & 1))) break;
+              QTRACE(lane == 0, 2, j);
+              const uint32_t acol = tmem + C::ACOL + b * C::ASTG;
+              const uint64_t bdesc = desc_sw128(sbase + C::OFF_B + b * C::B_STAGE);
 #pragma unroll
-            for (int qq = 0; qq < C::QPS; ++qq) {
-              const int q = st * C::QPS + qq;
-              const uint32_t baddr = bst + qq * C::B_QUARTER;
-              const uint32_t aq = acol + qq * 32;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16_ts(tmem + s0 * NT, aq + kk * 8, desc_sw128(baddr + kk * 32), IDESC, (q | kk) != 0);
-              if (q == 3) mma_commit(BAR(C::BS_FULL + s0));
-              if (!C::Q4) {
-                if (q == 0) {
-                  if (!(ok = mbar_wait(BAR(C::BS_EMPTY + s1), ((c1 / C::NSLOT) & 1) ^ 1, abort_flag, lim))) break;
-                  tc_fence_after();
-                }
+              for (int qq = 0; qq < 2; ++qq)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  mma_f16_ts(tmem + s1 * NT, aq + 32 + kk * 8, desc_sw128(baddr + kk * 32), IDESC, (q | kk) != 0);
-                if (q == 3) mma_commit(BAR(C::BS_FULL + s1));
-              }
+                  mma_f16_ts_warp(dslot, acol + qq * 32 + kk * 8, bdesc + (uint64_t)((qq * C::B_QUARTER + kk * 32) >> 4),
+                                  IDESC, (st | qq | kk) != 0);
+              mma_commit_warp(BAR(C::BK_EMPTY + b));
             }
             if (!ok) break;
-            mma_commit(BAR(C::BK_EMPTY + b));
+            // min term last: head and tail coefficients x activation 16-sums
+            const int jx = it % C::J_STAGES;
+            if (!(ok = wait_tc(BAR(C::BJ_FULL + jx), (it / C::J_STAGES) & 1))) break;
+            const uint32_t js = sbase + C::OFF_J + jx * C::J_BYTES;
+            const uint64_t bj = desc_noswz(js + C::J_BJ, 128, 256);
+            mma_f16_warp(dslot, desc_noswz(js + C::J_AJ, 128, 256), bj, IDESC, 1);
+            mma_f16_warp(dslot, desc_noswz(js + C::J_AJ + 4096, 128, 256), bj, IDESC, 1);
+            mma_commit_warp(BAR(C::BJ_EMPTY + jx));
+            QTRACE(lane == 0, 3, it);
+          } else {
+            for (int q = 0; q < 4; ++q) {
+              const int j = 4 * it + q, b = j % C::K_STAGES;
+              if (!(ok = wait_tc(BAR(C::BK_FULL + b), (j / C::K_STAGES) & 1))) break;
+              QTRACE(lane == 0, 2, j);
+              const uint32_t acol = tmem + C::ACOL + b * C::ASTG;
+              const uint64_t bdesc = desc_sw128(sbase + C::OFF_B + b * C::B_STAGE);
+#pragma unroll
+              for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_f16_ts_warp(dslot, acol + part * 32 + kk * 8, bdesc + (uint64_t)((kk * 32) >> 4), IDESC,
+                                  (q | part | kk) != 0);
+              mma_commit_warp(BAR(C::BK_EMPTY + b));
+            }
+            if (!ok) break;
           }
-          if (!ok) break;
-          if (C::Q4) {
-            const int x = it % C::X_STAGES;
-            if (!(ok = mbar_wait(BAR(C::BX_FULL + x), (it / C::X_STAGES) & 1, abort_flag, lim))) break;
-            if (!(ok = mbar_wait(BAR(C::BS_EMPTY + s1), ((c1 / C::NSLOT) & 1) ^ 1, abort_flag, lim))) break;
-            tc_fence_after();
-            const uint32_t xs = sbase + C::OFF_X + x * C::X_BYTES;
-            mma_f16(tmem + s1 * NT, desc_noswz(xs + C::X_AJ, 128, 256), desc_noswz(xs + C::X_BJ, 128, 256), IDESC,
-                    0);
-            mma_commit(BAR(C::BS_FULL + s1));
-            mma_commit(BAR(C::BX_EMPTY + x));
-          }
+          mma_commit_warp(BAR(C::BS_FULL + s));
         }
       }
-      if (!ok) atomicOr(p.err, ERR_TIMEOUT_MMA);
+      if (!ok && lane == 0) atomicOr(p.err, ERR_TIMEOUT_MMA);
       // all issued MMAs complete before the tensor memory is released
-      mma_commit(BAR(C::B_DONE));
+      mma_commit_warp(BAR(C::B_DONE));
       volatile int never = 0;
-      mbar_wait(BAR(C::B_DONE), 0, &never, lim);
+      warp_wait(BAR(C::B_DONE), 0, &never, lim);
     }
   } else if (warp >= QG_DEC_WARP0) {
-    // ------------------------------------------------------------ decode (thread = row = lane)
+    // ------------------------------------------------------------ decode: group g (warps 16-19 or
+    // 20-23), thread = weight row = TMEM lane; group g decodes the stages j with j % 2 == g
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(QG_REGS_DEC));
-    const int d = threadIdx.x - 32 * QG_DEC_WARP0;
-    const int t = d & 127, h = d >> 7;  // weight row (= TMEM lane, warp % 4 == t / 32), half
-    const uint32_t tlane = tmem + ((uint32_t)(t & ~31) << 16) + C::ACOL;
+    const int g = (warp - QG_DEC_WARP0) >> 2;
+    const int t = (warp & 3) * 32 + lane;
+    const uint32_t tlane = tmem + ((uint32_t)(warp & 3) * 32 << 16) + C::ACOL;
     int it = 0;
-    bool ok = true;
+    bool ok = true, bad = false;
     for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
       int tn, tm, sp, sb0, sb1;
       unit_coords(p, u, tn, tm, sp, sb0, sb1);
       for (int sb = sb0; sb < sb1; ++sb, ++it) {
         const int w = it % C::W_STAGES;
-        ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::BW_FULL + w), (it / C::W_STAGES) & 1, abort_flag, lim));
-        if (!ok) break;
-        const uint8_t* W = smem + C::OFF_W + w * C::W_BYTES;
+        if (!(ok = warp_wait(BAR(C::BW_FULL + w), (it / C::W_STAGES) & 1, abort_flag, lim, QG_SLEEP_DEC))) break;
+        QTRACE(t == 0 && g == 0, 8, it);
+        const uint8_t* W = smem + C::OFF_W + w * C::W_SLOT;
         if constexpr (C::Q4) {
+          // row t's fold of this super-block (see q4k_fold): the A operand carries scale * q * 2^-k
+          const __half2 ddv = *reinterpret_cast<const __half2*>(W + C::W_BYTES + t * 4);
+          const Q4Fold fo = q4k_fold(__low2float(ddv), __high2float(ddv), &bad);
+          const float ascale = p.dbg_mode == 1 ? 1.f : (p.dbg_mode == 2 ? 0.f : fo.ascale);
+          // stage g = quarters 2g, 2g+1 = sub-blocks 4g..4g+3; 6-bit scales: bytes 0-3 of scale
+          // word 0 are entries 0..3, entries 4..7 combine word 2's low nibbles and word 0's top bits
           const uint32_t sw0 = *reinterpret_cast<const uint32_t*>(W + 16384 + t * 4);
-          const uint32_t sw1 = *reinterpret_cast<const uint32_t*>(W + 16384 + 512 + t * 4);
-          const uint32_t sw2 = *reinterpret_cast<const uint32_t*>(W + 16384 + 1024 + t * 4);
-          // 6-bit fields: the bytes of *_lo4 are entries 0..3, of *_hi4 entries 4..7
-          const uint32_t sc_lo4 = sw0 & 0x3F3F3F3Fu;
-          const uint32_t mn_lo4 = sw1 & 0x3F3F3F3Fu;
-          const uint32_t sc_hi4 = (sw2 & 0x0F0F0F0Fu) | ((sw0 >> 2) & 0x30303030u);
-          const uint32_t mn_hi4 = ((sw2 >> 4) & 0x0F0F0F0Fu) | ((sw1 >> 2) & 0x30303030u);
-          // J operand row t: (min_0, min_0, min_1, min_1, ..., min_7, min_7) in 8x16 B core
-          // matrices (K-major, no swizzle), shared memory; half h writes core matrix h
-          const int x = it % C::X_STAGES;
-          ok = __all_sync(0xffffffffu,
-                          mbar_wait(BAR(C::BX_EMPTY + x), ((it / C::X_STAGES) & 1) ^ 1, abort_flag, lim));
-          if (!ok) break;
-          uint8_t* aj = smem + C::OFF_X + x * C::X_BYTES + C::X_AJ + (t >> 3) * 256 + (t & 7) * 16;
-          {
-            const uint32_t m4 = h ? mn_hi4 : mn_lo4;
-            uint4 o;
-            o.x = h2u(__float2half2_rn((float)(m4 & 0xFF)));
-            o.y = h2u(__float2half2_rn((float)((m4 >> 8) & 0xFF)));
-            o.z = h2u(__float2half2_rn((float)((m4 >> 16) & 0xFF)));
-            o.w = h2u(__float2half2_rn((float)(m4 >> 24)));
-            *reinterpret_cast<uint4*>(aj + h * 128) = o;
-          }
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(C::BX_FULL + x));
-#pragma unroll 1
-          for (int st = 0; st < 2; ++st) {
-            // quarters 2st, 2st+1: sub-blocks 4st..4st+3, scales are the bytes of sc_lo4 / sc_hi4
-            const uint32_t s4 = st ? sc_hi4 : sc_lo4;
-            const int j = 2 * it + st, b = j % C::K_STAGES;
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim));
-            if (!ok) break;
-            QTRACE(t == 0, 4, j);
-            tc_fence_after();
-            const uint32_t ta = tlane + b * C::ASTG;
+          const uint32_t s4 = g ? (((*reinterpret_cast<const uint32_t*>(W + 16384 + 1024 + t * 4)) & 0x0F0F0F0Fu) |
+                                   ((sw0 >> 2) & 0x30303030u))
+                                : (sw0 & 0x3F3F3F3Fu);
+          const int j = 2 * it + g, b = j % C::K_STAGES;
+          if (!(ok = warp_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_DEC))) break;
+          QTRACE(t == 0, 4, j);
+          tc_fence_after();
+          const uint32_t ta = tlane + b * C::ASTG;
 #pragma unroll
-            for (int qq = 0; qq < 2; ++qq) {
-              // sub-block 2q + h of quarter q = 2st + qq
-              const float sc = (float)((s4 >> (16 * qq + 8 * h)) & 0xFF);
+          for (int qq = 0; qq < 2; ++qq) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              // sub-block 2q + h of quarter q = 2g + qq; value scale * q4 * 2^-k
+              const float sc = (float)((s4 >> (16 * qq + 8 * h)) & 0xFF) * ascale;
               uint32_t o[16];
-              decode_q4k_half(W, t, 2 * st + qq, h, __float2half2_rn(h ? sc * 0.0625f : sc),
+              decode_q4k_half(W, t, 2 * g + qq, h, __float2half2_rn(h ? sc * 0.0625f : sc),
                               __float2half2_rn(h ? -64.f * sc : -1024.f * sc), o);
               tmem_st16(ta + 32 * qq + 16 * h, o);
             }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(BAR(C::BK_FULL + b));
-            QTRACE(t == 0, 5, j);
           }
+          {
+            // while the stores drain: row t's J operand (K-major 8x16 B core matrices, no
+            // swizzle; K = 16 groups of 16 values, group k pairs with min_{k/2}) holds the f16
+            // head and tail of c = cmul * min; group g writes core matrix g (mins 4g..4g+3)
+            const int jx = it % C::J_STAGES;
+            if (!(ok = warp_wait(BAR(C::BJ_EMPTY + jx), ((it / C::J_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_DEC))) break;
+            const float cmul = p.dbg_mode == 1 ? 0.f : (p.dbg_mode == 2 ? -1.f : fo.cmul);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(W + 16384 + 512 + t * 4);
+            // 6-bit mins: entries 0..3 are the bytes of word 1, entries 4..7 combine word 2's
+            // high nibbles with word 1's top bits
+            const uint32_t m4 =
+                g ? ((((*reinterpret_cast<const uint32_t*>(W + 16384 + 1024 + t * 4)) >> 4) & 0x0F0F0F0Fu) |
+                     ((w1 >> 2) & 0x30303030u))
+                  : (w1 & 0x3F3F3F3Fu);
+            uint32_t hd[4], tl[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float c = cmul * (float)((m4 >> (8 * i)) & 0xFF);
+              const __half ch = __float2half_rn(c);
+              const __half ct = __float2half_rn(c - __half2float(ch));
+              hd[i] = h2u(__halves2half2(ch, ch));
+              tl[i] = h2u(__halves2half2(ct, ct));
+            }
+            uint8_t* row = smem + C::OFF_J + jx * C::J_BYTES + C::J_AJ + (t >> 3) * 256 + (t & 7) * 16 + g * 128;
+            *reinterpret_cast<uint4*>(row) = make_uint4(hd[0], hd[1], hd[2], hd[3]);
+            *reinterpret_cast<uint4*>(row + 4096) = make_uint4(tl[0], tl[1], tl[2], tl[3]);
+            fence_proxy_async();
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(BAR(C::BK_FULL + b));
+            mbar_arrive(BAR(C::BJ_FULL + it % C::J_STAGES));
+          }
+          QTRACE(t == 0, 5, j);
         } else {
           const uint4 scv = *reinterpret_cast<const uint4*>(W + 24576 + t * 16);
           const int8_t* sc = reinterpret_cast<const int8_t*>(&scv);
+          const float hs = p.dbg_mode == 2 ? 0.f : (p.dbg_mode == 1 ? 1.f : 16.f);
+          const float ls = p.dbg_mode == 1 ? 0.f : 1.f;
 #pragma unroll 1
-          for (int q = 0; q < 4; ++q) {
+          for (int q = g; q < 4; q += 2) {
             const int j = 4 * it + q, b = j % C::K_STAGES;
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim));
-            if (!ok) break;
+            if (!(ok = warp_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_DEC))) break;
             QTRACE(t == 0, 4, j);
             tc_fence_after();
-            {
-              uint32_t hi[16], lo[16];
-              decode_q6k_half(W, t, q, h, sc, hi, lo);
-              tmem_st16(tlane + b * C::ASTG + 16 * h, hi);
-              tmem_st16(tlane + b * C::ASTG + 32 + 16 * h, lo);
-            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int ps = 0; ps < 2; ++ps) {
+                uint32_t hi[8], lo[8];
+                decode_q6k_piece(W, t, q, h, ps, sc, hs, ls, hi, lo);
+                tmem_st8(tlane + b * C::ASTG + 16 * h + 8 * ps, hi);
+                tmem_st8(tlane + b * C::ASTG + 32 + 16 * h + 8 * ps, lo);
+              }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -530,6 +606,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
       }
     }
     if (!ok && lane == 0) atomicOr(p.err, ERR_TIMEOUT_DECODE);
+    if (bad && lane == 0) atomicOr(p.err, ERR_RANGE);
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-15)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(QG_REGS_EPI));
@@ -539,6 +616,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
     const int row = 32 * qd + lane;
     const uint32_t tlane = tmem + ((uint32_t)(32 * qd) << 16) + hf * NC;
     int it = 0;
+    uint32_t sf0 = 0, sf1 = 0;  // full phases consumed per accumulator slot
     bool ok = true;
     for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
       int tn, tm, sp, sb0, sb1;
@@ -548,76 +626,75 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
       float acc[NC];
 #pragma unroll
       for (int i = 0; i < NC; ++i) acc[i] = 0.f;
-      for (int sb = sb0; sb < sb1; ++sb, ++it) {
-        const int x = it % C::X_STAGES;
-        ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::BX_FULL + x), (it / C::X_STAGES) & 1, abort_flag, lim));
-        if (!ok) break;
-        const uint8_t* X = smem + C::OFF_X + x * C::X_BYTES;
-        float cf[2];
+      // one accumulator part per super-block, in slot it & 1
+      const int nsbu = sb1 - sb0, it0 = it;
+#pragma unroll 1
+      for (int i = 0; i < nsbu; ++i) {
+        const int itp = it0 + i, sbp = sb0 + i;
+        const int s = itp & 1;
+        const int e = itp % C::E_STAGES;
+        if (!(ok = warp_wait(BAR(C::BE_FULL + e), (itp / C::E_STAGES) & 1, abort_flag, lim, QG_SLEEP_EPI))) break;
+        const uint8_t* E = smem + C::OFF_E + e * C::E_BYTES;
+        float cp;
         if constexpr (C::Q4) {
-          const __half2 dd = *reinterpret_cast<const __half2*>(X + C::X_DD + row * 4);
-          cf[0] = __low2float(dd);
-          cf[1] = -__high2float(dd);
+          const __half2 dd = *reinterpret_cast<const __half2*>(E + C::E_DD + row * 4);
+          bool bad = false;
+          cp = q4k_fold(__low2float(dd), __high2float(dd), &bad).factor;
         } else {
-          const float dv = __half2float(*reinterpret_cast<const __half*>(X + C::X_DD + row * 2));
-          cf[0] = 16.f * dv;
-          cf[1] = dv;
+          cp = __half2float(*reinterpret_cast<const __half*>(E + C::E_DD + row * 2));
         }
-        const float4* da4 = reinterpret_cast<const float4*>(X + C::X_DA) + hf * (NC / 4);
+        const float4* da4 = reinterpret_cast<const float4*>(E + C::E_DA) + hf * (NC / 4);
+        const uint32_t n = s ? sf1++ : sf0++;
+        if (!(ok = warp_wait(BAR(C::BS_FULL + s), n & 1, abort_flag, lim, QG_SLEEP_EPI))) break;
+        tc_fence_after();
+        QTRACE(warp == 0 && lane == 0, 6, itp);
+        // drain in groups of up to 2 x 8 columns; the slot is freed as soon as the last group
+        // is in registers, before its arithmetic
+        constexpr int G = 2;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const int cnt = 2 * it + part, s = cnt % C::NSLOT;
-          ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::BS_FULL + s), (cnt / C::NSLOT) & 1, abort_flag, lim));
-          if (!ok) break;
-          tc_fence_after();
-          QTRACE(warp == 0 && lane == 0, 6, cnt);
-          // drain the part in groups of up to 3 x 8 columns; the slot is freed as soon as the
-          // last group is in registers, before its arithmetic
-          const float cp = cf[part];
-          constexpr int G = 3;
+        for (int g0 = 0; g0 < NCH; g0 += G) {
+          uint32_t r[G][8];
 #pragma unroll
-          for (int g0 = 0; g0 < NCH; g0 += G) {
-            uint32_t r[G][8];
+          for (int c = 0; c < G; ++c)
+            if (g0 + c < NCH) tmem_ld8(tlane + s * NT + (g0 + c) * 8, r[c]);
+          tmem_ld_wait();
+          if (g0 + G >= NCH) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(C::BS_EMPTY + s));
+            QTRACE(warp == 0 && lane == 0, 7, itp);
+          }
 #pragma unroll
-            for (int c = 0; c < G; ++c)
-              if (g0 + c < NCH) tmem_ld8(tlane + s * NT + (g0 + c) * 8, r[c]);
-            tmem_ld_wait();
-            if (g0 + G >= NCH) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(BAR(C::BS_EMPTY + s));
-              QTRACE(warp == 0 && lane == 0, 7, cnt);
+          for (int c = 0; c < G; ++c) {
+            if (g0 + c >= NCH) break;
+            const int ch = g0 + c;
+#pragma unroll
+            for (int j4 = 0; j4 < 2; ++j4) {
+              const float4 dv = da4[ch * 2 + j4];
+              const int b = ch * 8 + 4 * j4;
+              float t0, t1, t2, t3;
+              fmul2(t0, t1, __uint_as_float(r[c][4 * j4]), __uint_as_float(r[c][4 * j4 + 1]), cp, cp);
+              fmul2(t2, t3, __uint_as_float(r[c][4 * j4 + 2]), __uint_as_float(r[c][4 * j4 + 3]), cp, cp);
+              ffma2(acc[b], acc[b + 1], t0, t1, dv.x, dv.y);
+              ffma2(acc[b + 2], acc[b + 3], t2, t3, dv.z, dv.w);
             }
+            if (p.dbg_mode != 0 && grow < p.n) {
+              // the isolated part's exact integers (Q4_K J is accumulated negated)
+              const float sgn = (C::Q4 && p.dbg_mode == 2) ? -1.f : 1.f;
 #pragma unroll
-            for (int c = 0; c < G; ++c) {
-              if (g0 + c >= NCH) break;
-              const int ch = g0 + c;
-#pragma unroll
-              for (int j4 = 0; j4 < 2; ++j4) {
-                const float4 dv = da4[ch * 2 + j4];
-                const int b = ch * 8 + 4 * j4;
-                float t0, t1, t2, t3;
-                fmul2(t0, t1, __uint_as_float(r[c][4 * j4]), __uint_as_float(r[c][4 * j4 + 1]), cp, cp);
-                fmul2(t2, t3, __uint_as_float(r[c][4 * j4 + 2]), __uint_as_float(r[c][4 * j4 + 3]), cp, cp);
-                ffma2(acc[b], acc[b + 1], t0, t1, dv.x, dv.y);
-                ffma2(acc[b + 2], acc[b + 3], t2, t3, dv.z, dv.w);
-              }
-              if (p.dbg != nullptr && grow < p.n) {
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                  const int tok = tokb + ch * 8 + jj;
-                  if (tok < p.m)
-                    p.dbg[(((size_t)part * p.nsb + sb) * p.m + tok) * p.n + grow] = (int32_t)__uint_as_float(r[c][jj]);
-                }
+              for (int jj = 0; jj < 8; ++jj) {
+                const int tok = tokb + ch * 8 + jj;
+                if (tok < p.m)
+                  p.dbg[((size_t)sbp * p.m + tok) * p.n + grow] = (int32_t)(sgn * __uint_as_float(r[c][jj]));
               }
             }
           }
         }
-        if (!ok) break;
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(C::BX_EMPTY + x));
+        if (lane == 0) mbar_arrive(BAR(C::BE_EMPTY + e));
       }
       if (!ok) break;
+      it = it0 + nsbu;
       if (p.mode == 1) {
 #pragma unroll
         for (int j = 0; j < NC; ++j) {
@@ -632,15 +709,15 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
               idx = oi;
             }
           }
-          float e = grow < p.n ? expf(acc[j] - v) : 0.f;
+          float ex = grow < p.n ? expf(acc[j] - v) : 0.f;
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
+          for (int off = 16; off > 0; off >>= 1) ex += __shfl_xor_sync(0xffffffffu, ex, off);
           const int tok = tokb + j;
           if (lane == 0 && tok < p.m) {
             const size_t o = ((size_t)tn * 4 + qd) * p.m + tok;
             p.pmax[o] = v;
             p.parg[o] = idx;
-            p.psum[o] = e;
+            p.psum[o] = ex;
           }
         }
       } else if (p.y != nullptr && grow < p.n) {

@@ -74,6 +74,24 @@ def test_linear_stream_llada_layer():
     _stream_ok(gx.cpu().numpy(), ref, 1)
 
 
+@pytest.mark.parametrize("L", [32, 512, 2048])
+def test_linear_stream_sweep(L):
+    # the canvas-length sweep of the LLaDA-8B-shaped layer stream; rows of a linear stream are
+    # independent, so the oracle runs on sampled rows (first, last and six seeded ones)
+    dims = dict(synth.LLADA, n_layers=1)
+    lws = [synth.layer_weights(synth.config_seed(5), 0, dims)]
+    x = synth.activations(synth.config_seed(5) + L, L, dims["d_model"])
+    model = dl.DeviceModel(dims, lws)
+    gx = torch.from_numpy(x.copy()).cuda()
+    dl.step_linear_stream(model, gx, dl.STREAM_LINEAR)
+    dl.check()
+    rows = np.unique(np.concatenate([[0, L - 1], np.random.default_rng(L).choice(L, 6, replace=False)]))
+    ref, _ = orc.layer(lws[0], np.asarray(x[rows], np.float64), dims, attention_on=False)
+    e = _row_errs(gx.cpu().numpy()[rows], ref)
+    # one tie-perturbed row allowed (see the module docstring)
+    assert int(np.sum(e > TOL)) <= 1 and e.max() <= 5e-2, (L, rows, e)
+
+
 def check_commits(gpos, gid, gcanvas, before, ref, conf_by_pos, k, row_err, gconf=None):
     """Commits must equal the oracle's up to confidence near-ties. Row p's confidence is trusted
     to tol_p = 1e-2 + 50 * row_err[p] (relative), row_err being that row's hidden-state error
