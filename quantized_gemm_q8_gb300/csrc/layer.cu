@@ -54,43 +54,56 @@ __global__ void embed_q4k_kernel(const uint8_t* __restrict__ table, int nsb, con
   }
 }
 
-// Non-causal multi-head attention fused with the split-K sum and RoPE of its inputs:
-//   q, k = RoPE(sum_s Pqk[s]) (adjacent pairs within a head, position = row index),
-//   v = sum_s Pv[s],  O = softmax(q k^T / sqrt(hd)) v  per head,
-// in f32 with an online softmax over key tiles of 64. One CTA = one head x 32 queries; warp w
-// owns queries 4w..4w+3. Scores: a lane holds 4 queries x keys (lane, lane + 32), reading q as
-// broadcast float4 and k rows padded to 132 floats so a quarter-warp's float4 loads of 8
-// different keys hit distinct banks. PV: the warp's probabilities go through shared memory and a
-// lane accumulates 4 queries x dims 4*lane..4*lane+3.
+// Q, K, V of one layer from the split-K partials of the Q|K and V projections: the splits are
+// summed in split order, RoPE rotates adjacent pairs of Q and K within each head (position =
+// row), Q is also scaled by 1/sqrt(hd). Out: QKV [L][3d] f32 (Q, K, V side by side). One thread
+// per output pair, all partial loads of a thread issued together.
+__global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __restrict__ Pqk, int Sqk,
+                                                              const float* __restrict__ Pv, int Sv,
+                                                              const float2* __restrict__ cs, int L, int d, int hd,
+                                                              float qscale, float* __restrict__ QKV) {
+  const int64_t npair = (int64_t)L * (3 * d / 2);
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= npair) return;
+  const int p = (int)(i / (3 * d / 2)), c = 2 * (int)(i % (3 * d / 2));  // row, column in [Q | K | V]
+  float2 a = make_float2(0.f, 0.f);
+  if (c < 2 * d) {
+    const float* src = Pqk + (int64_t)p * 2 * d + c;
+    const int64_t st = (int64_t)L * 2 * d;
+#pragma unroll 4
+    for (int sp = 0; sp < Sqk; ++sp) {
+      const float2 v = *reinterpret_cast<const float2*>(src + sp * st);
+      a.x += v.x;
+      a.y += v.y;
+    }
+    const float2 r = cs[p * (hd / 2) + (c % hd) / 2];
+    const float sc = c < d ? qscale : 1.f;
+    a = make_float2((a.x * r.x - a.y * r.y) * sc, (a.x * r.y + a.y * r.x) * sc);
+  } else {
+    const float* src = Pv + (int64_t)p * d + (c - 2 * d);
+    const int64_t st = (int64_t)L * d;
+#pragma unroll 4
+    for (int sp = 0; sp < Sv; ++sp) {
+      const float2 v = *reinterpret_cast<const float2*>(src + sp * st);
+      a.x += v.x;
+      a.y += v.y;
+    }
+  }
+  *reinterpret_cast<float2*>(QKV + (int64_t)p * 3 * d + c) = a;
+}
+
+// Non-causal multi-head attention O = softmax(q k^T) v per head on the reduced QKV ([L][3d],
+// q pre-scaled), f32 with an online softmax over key tiles of 64. One CTA = one head x 32
+// queries; warp w owns queries 4w..4w+3. Scores: a lane holds 4 queries x keys (lane,
+// lane + 32), reading q as broadcast float4 and k rows padded to 132 floats so a quarter-warp's
+// float4 loads of 8 different keys hit distinct banks. PV: the warp's probabilities go through
+// shared memory and a lane accumulates 4 queries x dims 4*lane..4*lane+3. Tiles are staged
+// with float4 loads, each thread's loads issued together.
 constexpr int ATT_QB = 32, ATT_KT = 64, ATT_HD = 128, ATT_KP = ATT_HD + 4;
 constexpr int ATT_SMEM = (ATT_KT * ATT_KP + ATT_KT * ATT_HD + ATT_QB * ATT_HD + ATT_QB * ATT_KT) * 4;
 
-struct AttArgs {
-  const float* Pqk;  // [Sqk][L][2d]: Q in columns 0..d-1, K in columns d..2d-1
-  int Sqk;
-  const float* Pv;   // [Sv][L][d]
-  int Sv;
-  const float2* cs;  // RoPE (cos, sin) table [L][hd/2]
-  float* O;          // [L][d]
-  int L, d;
-  float scale;
-};
-
-__device__ __forceinline__ float2 split_sum2(const float* P, int S, int64_t stride, int64_t off) {
-  float2 a = *reinterpret_cast<const float2*>(P + off);
-  for (int s = 1; s < S; ++s) {
-    const float2 v = *reinterpret_cast<const float2*>(P + s * stride + off);
-    a.x += v.x;
-    a.y += v.y;
-  }
-  return a;
-}
-
-__device__ __forceinline__ float2 rope2(float2 v, float2 r) {
-  return make_float2(v.x * r.x - v.y * r.y, v.x * r.y + v.y * r.x);
-}
-
-__global__ void __launch_bounds__(256, 2) attention_kernel(AttArgs a) {
+__global__ void __launch_bounds__(256, 2) attention_kernel(const float* __restrict__ QKV, float* __restrict__ O,
+                                                          int L, int d) {
   extern __shared__ float4 att_smem4[];
   float* Ks = reinterpret_cast<float*>(att_smem4);  // [KT][KP]
   float* Vs = Ks + ATT_KT * ATT_KP;                 // [KT][HD]
@@ -98,18 +111,20 @@ __global__ void __launch_bounds__(256, 2) attention_kernel(AttArgs a) {
   float* Ps = Qs + ATT_QB * ATT_HD;                 // [QB][KT]
   const int h = blockIdx.x, q0 = blockIdx.y * ATT_QB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int L = a.L, d = a.d;
-  const int64_t sqk = (int64_t)L * 2 * d, sv = (int64_t)L * d;
-  constexpr int HP = ATT_HD / 2;
-  for (int i = threadIdx.x; i < ATT_QB * HP; i += blockDim.x) {
-    const int qi = i / HP, pr = i % HP, p = q0 + qi;
-    float2 o = make_float2(0.f, 0.f);
-    if (p < L) {
-      o = rope2(split_sum2(a.Pqk, a.Sqk, sqk, (int64_t)p * 2 * d + h * ATT_HD + 2 * pr), a.cs[p * HP + pr]);
-      o.x *= a.scale;
-      o.y *= a.scale;
+  const int64_t ld = 3 * (int64_t)d;
+  constexpr int HV = ATT_HD / 4;  // float4 per head row
+  {
+    float4 v[ATT_QB * HV / 256];
+#pragma unroll
+    for (int r = 0; r < ATT_QB * HV / 256; ++r) {
+      const int i = threadIdx.x + 256 * r, qi = i / HV, c4 = i % HV, p = q0 + qi;
+      v[r] = p < L ? *reinterpret_cast<const float4*>(QKV + p * ld + h * ATT_HD + 4 * c4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    *reinterpret_cast<float2*>(Qs + qi * ATT_HD + 2 * pr) = o;
+#pragma unroll
+    for (int r = 0; r < ATT_QB * HV / 256; ++r) {
+      const int i = threadIdx.x + 256 * r;
+      *reinterpret_cast<float4*>(Qs + (i / HV) * ATT_HD + 4 * (i % HV)) = v[r];
+    }
   }
   float m[4], l[4], acc[4][4];
 #pragma unroll
@@ -123,15 +138,22 @@ __global__ void __launch_bounds__(256, 2) attention_kernel(AttArgs a) {
   float* pw = Ps + warp * 4 * ATT_KT;
   for (int k0 = 0; k0 < L; k0 += ATT_KT) {
     __syncthreads();  // previous tile fully consumed
-    for (int i = threadIdx.x; i < ATT_KT * HP; i += blockDim.x) {
-      const int kj = i / HP, pr = i % HP, p = k0 + kj;
-      float2 kv = make_float2(0.f, 0.f), vv = make_float2(0.f, 0.f);
-      if (p < L) {
-        kv = rope2(split_sum2(a.Pqk, a.Sqk, sqk, (int64_t)p * 2 * d + d + h * ATT_HD + 2 * pr), a.cs[p * HP + pr]);
-        vv = split_sum2(a.Pv, a.Sv, sv, (int64_t)p * d + h * ATT_HD + 2 * pr);
+    {
+      constexpr int R = ATT_KT * HV / 256;  // 8 float4 of K and of V per thread
+      float4 kv[R], vv[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int i = threadIdx.x + 256 * r, kj = i / HV, c4 = i % HV, p = k0 + kj;
+        const float* row = QKV + p * ld + h * ATT_HD + 4 * c4;
+        kv[r] = p < L ? *reinterpret_cast<const float4*>(row + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+        vv[r] = p < L ? *reinterpret_cast<const float4*>(row + 2 * d) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      *reinterpret_cast<float2*>(Ks + kj * ATT_KP + 2 * pr) = kv;
-      *reinterpret_cast<float2*>(Vs + kj * ATT_HD + 2 * pr) = vv;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int i = threadIdx.x + 256 * r, kj = i / HV, c4 = i % HV;
+        *reinterpret_cast<float4*>(Ks + kj * ATT_KP + 4 * c4) = kv[r];
+        *reinterpret_cast<float4*>(Vs + kj * ATT_HD + 4 * c4) = vv[r];
+      }
     }
     __syncthreads();
     // scores of 4 queries x keys (lane, lane + 32)
@@ -197,7 +219,7 @@ __global__ void __launch_bounds__(256, 2) attention_kernel(AttArgs a) {
     const int qi = q0 + warp * 4 + qq;
     if (qi < L) {
       const float inv = 1.0f / l[qq];
-      *reinterpret_cast<float4*>(a.O + (int64_t)qi * d + h * ATT_HD + lane * 4) =
+      *reinterpret_cast<float4*>(O + (int64_t)qi * d + h * ATT_HD + lane * 4) =
           make_float4(acc[qq][0] * inv, acc[qq][1] * inv, acc[qq][2] * inv, acc[qq][3] * inv);
     }
   }
@@ -223,76 +245,87 @@ struct RowArgs {
   QuantOut o;
 };
 
+// Residual modes (RESID_NORM_QUANT, RESID_ONLY): one CTA of 1024 threads per row (RMSNorm
+// needs the row's sum of squares); each thread's partial loads are issued together.
 template <int MODE>
-__global__ void __launch_bounds__(256) row_kernel(RowArgs a) {
-  __shared__ float red[8];
+__global__ void __launch_bounds__(1024) row_resid_kernel(RowArgs a) {
+  __shared__ float red[32];
   const int row = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
   const int nsb = a.k / QK;
   if (row >= a.rows) {  // padding rows of the operand planes
     if (MODE != ROW_RESID_ONLY) {
       float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int sb = warp; sb < nsb; sb += 8) q8k_emit(z, row, a.rows, sb, a.k, a.o);
+      for (int sb = warp; sb < nsb; sb += nwarp) q8k_emit(z, row, a.rows, sb, a.k, a.o);
     }
     return;
   }
   const float* Pr = a.P + (int64_t)row * a.ldp;
-  if (MODE == ROW_RESID_NORM_QUANT || MODE == ROW_RESID_ONLY) {
-    float* xr = a.x + (int64_t)row * a.k;
-    float ss = 0.f;
-    for (int i = threadIdx.x * 4; i < a.k; i += blockDim.x * 4) {
-      float4 v = *reinterpret_cast<float4*>(xr + i);
-      for (int s = 0; s < a.S; ++s) {
-        const float4 pv = *reinterpret_cast<const float4*>(Pr + s * a.pstride + i);
-        v.x += pv.x;
-        v.y += pv.y;
-        v.z += pv.z;
-        v.w += pv.w;
-      }
-      *reinterpret_cast<float4*>(xr + i) = v;
-      ss = fmaf(v.x, v.x, ss);
-      ss = fmaf(v.y, v.y, ss);
-      ss = fmaf(v.z, v.z, ss);
-      ss = fmaf(v.w, v.w, ss);
+  float* xr = a.x + (int64_t)row * a.k;
+  float ss = 0.f;
+  for (int i = threadIdx.x * 4; i < a.k; i += blockDim.x * 4) {
+    float4 v = *reinterpret_cast<float4*>(xr + i);
+#pragma unroll 4
+    for (int s = 0; s < a.S; ++s) {
+      const float4 pv = *reinterpret_cast<const float4*>(Pr + s * a.pstride + i);
+      v.x += pv.x;
+      v.y += pv.y;
+      v.z += pv.z;
+      v.w += pv.w;
     }
-    if (MODE == ROW_RESID_ONLY) return;
-    ss = block_sum(ss, red);  // also orders the x writes above before the reads below
-    const float rstd = 1.0f / sqrtf(ss / (float)a.k + a.eps);
-    for (int sb = warp; sb < nsb; sb += 8) {
-      const int base = sb * QK + 8 * lane;
-      const float4 v0 = *reinterpret_cast<const float4*>(xr + base);
-      const float4 v1 = *reinterpret_cast<const float4*>(xr + base + 4);
-      const float4 w0 = *reinterpret_cast<const float4*>(a.norm_w + base);
-      const float4 w1 = *reinterpret_cast<const float4*>(a.norm_w + base + 4);
-      float v[8] = {v0.x * rstd * w0.x, v0.y * rstd * w0.y, v0.z * rstd * w0.z, v0.w * rstd * w0.w,
-                    v1.x * rstd * w1.x, v1.y * rstd * w1.y, v1.z * rstd * w1.z, v1.w * rstd * w1.w};
-      q8k_emit(v, row, a.rows, sb, a.k, a.o);
-    }
-  } else {
-    for (int sb = warp; sb < nsb; sb += 8) {
-      const int base = sb * QK + 8 * lane;
-      float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      float u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int s = 0; s < a.S; ++s) {
-        const float* ps = Pr + s * a.pstride + base;
-        const float4 p0 = *reinterpret_cast<const float4*>(ps);
-        const float4 p1 = *reinterpret_cast<const float4*>(ps + 4);
-        v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
-        v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
-        if (MODE == ROW_SWIGLU_QUANT) {
-          const float4 q0 = *reinterpret_cast<const float4*>(ps + a.k);
-          const float4 q1 = *reinterpret_cast<const float4*>(ps + a.k + 4);
-          u[0] += q0.x; u[1] += q0.y; u[2] += q0.z; u[3] += q0.w;
-          u[4] += q1.x; u[5] += q1.y; u[6] += q1.z; u[7] += q1.w;
-        }
-      }
+    *reinterpret_cast<float4*>(xr + i) = v;
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+  if (MODE == ROW_RESID_ONLY) return;
+  ss = block_sum(ss, red);  // also orders the x writes above before the reads below
+  const float rstd = 1.0f / sqrtf(ss / (float)a.k + a.eps);
+  for (int sb = warp; sb < nsb; sb += nwarp) {
+    const int base = sb * QK + 8 * lane;
+    const float4 v0 = *reinterpret_cast<const float4*>(xr + base);
+    const float4 v1 = *reinterpret_cast<const float4*>(xr + base + 4);
+    const float4 w0 = *reinterpret_cast<const float4*>(a.norm_w + base);
+    const float4 w1 = *reinterpret_cast<const float4*>(a.norm_w + base + 4);
+    float v[8] = {v0.x * rstd * w0.x, v0.y * rstd * w0.y, v0.z * rstd * w0.z, v0.w * rstd * w0.w,
+                  v1.x * rstd * w1.x, v1.y * rstd * w1.y, v1.z * rstd * w1.z, v1.w * rstd * w1.w};
+    q8k_emit(v, row, a.rows, sb, a.k, a.o);
+  }
+}
+
+// Per-super-block modes (SUM_QUANT, SWIGLU_QUANT): warp (blockIdx.y * 8 + w) of row blockIdx.x
+// builds and quantizes one super-block; each lane's partial loads are issued together.
+template <int MODE>
+__global__ void __launch_bounds__(256) row_sb_kernel(RowArgs a) {
+  const int row = blockIdx.x;
+  const int sb = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int nsb = a.k / QK;
+  if (sb >= nsb) return;
+  float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (row < a.rows) {
+    const int base = sb * QK + 8 * lane;
+    const float* ps = a.P + (int64_t)row * a.ldp + base;
+    float u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll 4
+    for (int s = 0; s < a.S; ++s, ps += a.pstride) {
+      const float4 p0 = *reinterpret_cast<const float4*>(ps);
+      const float4 p1 = *reinterpret_cast<const float4*>(ps + 4);
+      v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
+      v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
       if (MODE == ROW_SWIGLU_QUANT) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = v[i] / (1.0f + expf(-v[i])) * u[i];
+        const float4 q0 = *reinterpret_cast<const float4*>(ps + a.k);
+        const float4 q1 = *reinterpret_cast<const float4*>(ps + a.k + 4);
+        u[0] += q0.x; u[1] += q0.y; u[2] += q0.z; u[3] += q0.w;
+        u[4] += q1.x; u[5] += q1.y; u[6] += q1.z; u[7] += q1.w;
       }
-      q8k_emit(v, row, a.rows, sb, a.k, a.o);
+    }
+    if (MODE == ROW_SWIGLU_QUANT) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = v[i] / (1.0f + expf(-v[i])) * u[i];
     }
   }
+  q8k_emit(v, row, a.rows, sb, a.k, a.o);  // padding rows quantize zeros
 }
 
 static QuantOut quant_out(void* act, int64_t rows, int64_t k) {
@@ -306,8 +339,13 @@ template <int MODE>
 static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, const float* w, float eps, int rows,
                    int k, void* act, cudaStream_t s) {
   RowArgs a{x, P, S, pstride, ldp, w, eps, rows, k, act ? quant_out(act, rows, k) : QuantOut{}};
-  const int grid = MODE == ROW_RESID_ONLY ? rows : (int)act_rows_padded(rows);
-  row_kernel<MODE><<<grid, 256, 0, s>>>(a);
+  if (MODE == ROW_RESID_NORM_QUANT || MODE == ROW_RESID_ONLY) {
+    const int grid = MODE == ROW_RESID_ONLY ? rows : (int)act_rows_padded(rows);
+    row_resid_kernel<MODE><<<grid, 1024, 0, s>>>(a);
+  } else {
+    const dim3 grid((unsigned)act_rows_padded(rows), (unsigned)((k / QK + 7) / 8));
+    row_sb_kernel<MODE><<<grid, 256, 0, s>>>(a);
+  }
   note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch row kernel");
@@ -318,7 +356,7 @@ static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, co
 // ---------------------------------------------------------------------------------------------
 struct StepPlan {
   QgemmPlan qk, v, o, gu, dn;
-  size_t x, act_d, act_ff, pqk, pv, po, pgu, pdn, att, rope, lm, bytes;
+  size_t x, act_d, act_ff, pqk, pv, po, pgu, pdn, qkv, att, rope, lm, bytes;
 };
 
 static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead) {
@@ -344,6 +382,7 @@ static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead
   S.po = take((size_t)S.o.splits * L * d * 4);
   S.pgu = take((size_t)S.gu.splits * L * 2 * f * 4);
   S.pdn = take((size_t)S.dn.splits * L * d * 4);
+  S.qkv = take(full ? (size_t)L * 3 * d * 4 : 0);
   S.att = take(full ? (size_t)L * d * 4 : 0);
   S.rope = take(full ? (size_t)L * (m->head_dim / 2) * 8 : 0);
   S.lm = 0;
@@ -406,12 +445,16 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
     if ((rc = gemm(DLLM_Q6_K, actd, L, d, Ly.wv, d, Pv, S.v, s))) return rc;
     if (full) {
       float* A = reinterpret_cast<float*>(ws + S.att);
-      const AttArgs aa{Pqk, S.qk.splits, Pv, S.v.splits, reinterpret_cast<const float2*>(ws + S.rope), A, (int)L, d,
-                       1.0f / sqrtf((float)hd)};
+      float* QKV = reinterpret_cast<float*>(ws + S.qkv);
+      const int64_t npair = L * (3 * d / 2);
+      qkv_reduce_rope_kernel<<<(unsigned)((npair + 255) / 256), 256, 0, s>>>(
+          Pqk, S.qk.splits, Pv, S.v.splits, reinterpret_cast<const float2*>(ws + S.rope), (int)L, d, hd,
+          1.0f / sqrtf((float)hd), QKV);
+      note_launch();
       cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM);
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
       const dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB));
-      attention_kernel<<<ag, 256, ATT_SMEM, s>>>(aa);
+      attention_kernel<<<ag, 256, ATT_SMEM, s>>>(QKV, A, (int)L, d);
       note_launch();
       e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "launch attention");
