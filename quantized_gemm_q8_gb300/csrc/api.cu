@@ -306,48 +306,58 @@ __device__ __forceinline__ SoftPart soft_merge(SoftPart x, SoftPart y) {
   return x;
 }
 
-// One CTA of 1024 threads: warp w merges rows w, w+32, ... over the P partials of each row,
-// then warp 0 picks the k masked positions of the block with the highest confidence (ties:
-// lowest position) and scatters their ids into the canvas.
-__global__ void __launch_bounds__(1024) lmhead_merge_commit_kernel(
+// Merge and commit, one launch: CTA r (256 threads) merges row r's P partials (contiguous,
+// [R][P]) into (argmax id, p_max = 1 / sum exp(l - l_max)) and stores them; the CTA that
+// finishes last (a counter, zeroed before the launch) picks the k masked positions of the
+// block with the highest confidence (ties: lowest position) and scatters their ids into the
+// canvas.
+__global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
     const float* __restrict__ pmax, const int* __restrict__ parg, const float* __restrict__ psum, int P, int R,
     int32_t* canvas, int32_t mask_id, int b0, int k, int32_t* out_pos, int32_t* out_id, float* out_conf,
-    int32_t* row_id, float* row_conf) {
-  __shared__ float conf_s[1024];
-  __shared__ int id_s[1024];
-  __shared__ int cand_s[1024];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < R; r += 32) {
-    SoftPart acc{-INFINITY, 0x7fffffff, 0.f};
-    for (int i = lane; i < P; i += 32) {
-      const size_t o = (size_t)i * R + r;
-      acc = soft_merge(acc, SoftPart{pmax[o], parg[o], psum[o]});
-    }
+    int32_t* row_id, float* row_conf, float* conf_ws, int* id_ws, unsigned int* done) {
+  __shared__ SoftPart red[8];
+  __shared__ bool last;
+  const int r = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  SoftPart acc{-INFINITY, 0x7fffffff, 0.f};
+  const size_t base = (size_t)r * P;
+  for (int i = threadIdx.x; i < P; i += blockDim.x)
+    acc = soft_merge(acc, SoftPart{pmax[base + i], parg[base + i], psum[base + i]});
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      SoftPart o{__shfl_xor_sync(0xffffffffu, acc.m, off), __shfl_xor_sync(0xffffffffu, acc.a, off),
-                 __shfl_xor_sync(0xffffffffu, acc.s, off)};
-      acc = soft_merge(acc, o);
-    }
-    if (lane == 0) {
-      const float c = 1.0f / acc.s;  // softmax probability of the argmax token
-      conf_s[r] = c;
-      id_s[r] = acc.a;
-      cand_s[r] = canvas[b0 + r] == mask_id;
-      if (row_id) row_id[r] = acc.a;
-      if (row_conf) row_conf[r] = c;
-    }
+  for (int off = 16; off > 0; off >>= 1) {
+    SoftPart o{__shfl_xor_sync(0xffffffffu, acc.m, off), __shfl_xor_sync(0xffffffffu, acc.a, off),
+               __shfl_xor_sync(0xffffffffu, acc.s, off)};
+    acc = soft_merge(acc, o);
+  }
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < 8; ++w) acc = soft_merge(acc, red[w]);
+    const float c = 1.0f / acc.s;  // softmax probability of the argmax token
+    conf_ws[r] = c;
+    id_ws[r] = acc.a;
+    if (row_id) row_id[r] = acc.a;
+    if (row_conf) row_conf[r] = c;
+    __threadfence();
+    last = atomicAdd(done, 1u) == (unsigned)(R - 1);
   }
   __syncthreads();
-  if (warp != 0) return;
+  if (!last || warp != 0) return;
+  __threadfence();
   for (int step = 0; step < k; ++step) {
     float best = -1.f;
     int bp = 0x7fffffff;
-    for (int r = lane; r < R; r += 32)
-      if (cand_s[r] && (conf_s[r] > best || (conf_s[r] == best && r < bp))) {
-        best = conf_s[r];
-        bp = r;
+    for (int q = lane; q < R; q += 32) {
+      const volatile float* cv = conf_ws;
+      const float cq = cv[q];
+      if (canvas[b0 + q] == mask_id && (cq > best || (cq == best && q < bp))) {
+        bool taken = false;
+        for (int s2 = 0; s2 < step; ++s2) taken |= out_pos[s2] == b0 + q;
+        if (!taken) {
+          best = cq;
+          bp = q;
+        }
       }
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float ob = __shfl_xor_sync(0xffffffffu, best, off);
@@ -358,11 +368,11 @@ __global__ void __launch_bounds__(1024) lmhead_merge_commit_kernel(
       }
     }
     if (lane == 0) {
+      const volatile int* iv = id_ws;
       if (bp != 0x7fffffff) {
-        cand_s[bp] = 0;
         out_pos[step] = b0 + bp;
-        out_id[step] = id_s[bp];
-        if (out_conf) out_conf[step] = conf_s[bp];
+        out_id[step] = iv[bp];
+        if (out_conf) out_conf[step] = best;
       } else {
         out_pos[step] = -1;
         out_id[step] = -1;
@@ -370,14 +380,16 @@ __global__ void __launch_bounds__(1024) lmhead_merge_commit_kernel(
       }
     }
     __syncwarp();
+    __threadfence_block();
   }
-  if (lane == 0)
+  if (lane == 0) {
     for (int step = 0; step < k; ++step)
       if (out_pos[step] >= 0) canvas[out_pos[step]] = out_id[step];
+  }
 }
 
 struct LmheadWs {
-  size_t act, pmax, parg, psum, bytes;
+  size_t act, pmax, parg, psum, conf, id, done, bytes;
   int P;
 };
 static LmheadWs lmhead_ws(int64_t R, int64_t vocab, int64_t d) {
@@ -388,7 +400,10 @@ static LmheadWs lmhead_ws(int64_t R, int64_t vocab, int64_t d) {
   w.pmax = align_up(act_layout(R, d).bytes, 256);
   w.parg = w.pmax + align_up((size_t)w.P * R * 4, 256);
   w.psum = w.parg + align_up((size_t)w.P * R * 4, 256);
-  w.bytes = w.psum + align_up((size_t)w.P * R * 4, 256);
+  w.conf = w.psum + align_up((size_t)w.P * R * 4, 256);
+  w.id = w.conf + align_up((size_t)R * 4, 256);
+  w.done = w.id + align_up((size_t)R * 4, 256);
+  w.bytes = w.done + 256;
   return w;
 }
 
@@ -774,12 +789,15 @@ DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d
   rc = launch_gemm(g, P, s);
   if (rc) return rc;
   // 3) merge, confidence, top-k commit
-  lmhead_merge_commit_kernel<<<1, 1024, 0, s>>>(reinterpret_cast<float*>(base + W.pmax),
-                                                reinterpret_cast<int*>(base + W.parg),
-                                                reinterpret_cast<float*>(base + W.psum), W.P, (int)R, canvas, mask_id,
-                                                block_begin, k_commit, out_pos, out_id, out_conf, row_id, row_conf);
+  unsigned int* done = reinterpret_cast<unsigned int*>(base + W.done);
+  cudaError_t e = cudaMemsetAsync(done, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess) return cuda_fail(e, "zero the merge counter");
+  lmhead_merge_commit_kernel<<<(int)R, 256, 0, s>>>(
+      reinterpret_cast<float*>(base + W.pmax), reinterpret_cast<int*>(base + W.parg),
+      reinterpret_cast<float*>(base + W.psum), W.P, (int)R, canvas, mask_id, block_begin, k_commit, out_pos, out_id,
+      out_conf, row_id, row_conf, reinterpret_cast<float*>(base + W.conf), reinterpret_cast<int*>(base + W.id), done);
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch lmhead_merge_commit");
 }
 

@@ -75,8 +75,22 @@ constexpr int QG_REGS_EPI = 88, QG_REGS_DEC = 56, QG_REGS_CTL = 40;
 static_assert(512 * QG_REGS_EPI + 256 * QG_REGS_DEC + 128 * QG_REGS_CTL <= QG_THREADS * QG_REGS_LAUNCH,
               "register split");
 constexpr int SMEM_LIMIT = 232448;
-// sleep hints (ns) of the waiting roles; the MMA warp spins
-constexpr uint32_t QG_SLEEP_DEC = 64, QG_SLEEP_EPI = 256, QG_SLEEP_PROD = 256;
+// sleep hints (ns) of the waiting roles (0 = spin); the hint bounds how late a sleeping warp
+// notices that its barrier completed, and a spinning warp takes issue slots from its SMSP
+#ifndef QG_SLEEP_MMA_NS
+#define QG_SLEEP_MMA_NS 0
+#endif
+#ifndef QG_SLEEP_DEC_NS
+#define QG_SLEEP_DEC_NS 64
+#endif
+#ifndef QG_SLEEP_EPI_NS
+#define QG_SLEEP_EPI_NS 256
+#endif
+#ifndef QG_SLEEP_PROD_NS
+#define QG_SLEEP_PROD_NS 256
+#endif
+constexpr uint32_t QG_SLEEP_MMA = QG_SLEEP_MMA_NS, QG_SLEEP_DEC = QG_SLEEP_DEC_NS, QG_SLEEP_EPI = QG_SLEEP_EPI_NS,
+                   QG_SLEEP_PROD = QG_SLEEP_PROD_NS;
 constexpr int TMEM_COLS = 512;
 
 __host__ __device__ constexpr int al128(int x) { return (x + 127) & ~127; }
@@ -150,7 +164,7 @@ struct QgemmParams {
   int* err;      // device error word
   // mode 1 (LM head): instead of y, per (weight tile, TMEM lane quadrant, token) softmax
   // partials over the 32 weight rows of the quadrant: max logit, its row (lowest on ties),
-  // and sum_rows exp(logit - max); layout [tiles_n * 4][m].
+  // and sum_rows exp(logit - max); layout [m][tiles_n * 4].
   int mode;
   float* pmax;
   int* parg;
@@ -426,7 +440,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
       uint32_t se0 = 0, se1 = 0;
       bool ok = true;
       auto wait_tc = [&](uint32_t bar, uint32_t parity) -> bool {
-        const bool r = warp_wait(bar, parity, abort_flag, lim);
+        const bool r = warp_wait(bar, parity, abort_flag, lim, QG_SLEEP_MMA);
         tc_fence_after();
         return r;
       };
@@ -525,15 +539,19 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           QTRACE(t == 0, 4, j);
           tc_fence_after();
           const uint32_t ta = tlane + b * C::ASTG;
+          // f16 multipliers (scale * 2^-k, and / 16 for the high nibbles) and addends: exact, from
+          // one integer-to-half conversion per sub-block
+          const __half2 asc = __float2half2_rn(ascale);
 #pragma unroll
           for (int qq = 0; qq < 2; ++qq) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               // sub-block 2q + h of quarter q = 2g + qq; value scale * q4 * 2^-k
-              const float sc = (float)((s4 >> (16 * qq + 8 * h)) & 0xFF) * ascale;
+              const __half2 sc = __hmul2(__half2half2(__int2half_rn((s4 >> (16 * qq + 8 * h)) & 0xFF)), asc);
+              const __half2 mul = h ? __hmul2(sc, __float2half2_rn(0.0625f)) : sc;
+              const __half2 add = __hmul2(sc, __float2half2_rn(h ? -64.f : -1024.f));
               uint32_t o[16];
-              decode_q4k_half(W, t, 2 * g + qq, h, __float2half2_rn(h ? sc * 0.0625f : sc),
-                              __float2half2_rn(h ? -64.f * sc : -1024.f * sc), o);
+              decode_q4k_half(W, t, 2 * g + qq, h, mul, add, o);
               tmem_st16(ta + 32 * qq + 16 * h, o);
             }
           }
@@ -565,7 +583,9 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             *reinterpret_cast<uint4*>(row + 4096) = make_uint4(tl[0], tl[1], tl[2], tl[3]);
             fence_proxy_async();
           }
+          QTRACE(t == 0, 10, j);
           tmem_st_wait();
+          QTRACE(t == 0, 11, j);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
@@ -714,7 +734,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           for (int off = 16; off > 0; off >>= 1) ex += __shfl_xor_sync(0xffffffffu, ex, off);
           const int tok = tokb + j;
           if (lane == 0 && tok < p.m) {
-            const size_t o = ((size_t)tn * 4 + qd) * p.m + tok;
+            const size_t o = (size_t)tok * (p.tiles_n * 4) + tn * 4 + qd;
             p.pmax[o] = v;
             p.parg[o] = idx;
             p.psum[o] = ex;
