@@ -338,12 +338,42 @@ ONLY_KERNELS = {  # name: (type, n, k) of one layer's GEMM at L = 148
 }
 
 
+def run_only_layer(args):
+    """One LLaDA-8B-shaped layer's full forward (embedding, attention, FFN) at L = 148 on a
+    one-layer model: the profiling target of the glue kernels (--steps launches after --warmup)."""
+    import torch
+
+    import quantized_gemm_q8_gb300 as dl
+    from quantized_gemm_q8_gb300 import synth
+
+    torch.cuda.set_device(0)
+    dims = dict(synth.LLADA, n_layers=1)
+    model = dl.model_from_seed(dims, synth.config_seed(4))
+    canvas = torch.from_numpy(synth.canvas(synth.config_seed(4))).cuda()
+    x = torch.empty((L_CANVAS, dims["d_model"]), dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        dl.step_linear_stream(model, x, dl.STREAM_FULL, canvas=canvas)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        dl.step_linear_stream(model, x, dl.STREAM_FULL, canvas=canvas)
+    e1.record()
+    torch.cuda.synchronize()
+    dl.check()
+    print(json.dumps({"kernel": "layer_full", "L": L_CANVAS, "ms_per_layer": e0.elapsed_time(e1) / max(args.steps, 1),
+                      "note": "one-layer model, embedding + layer; a profiling target"}))
+
+
 def run_only_kernel(args):
     """Time one GEMM of the step alone (the profiling target): --steps launches after --warmup."""
     import torch
 
     import quantized_gemm_q8_gb300 as dl
     from quantized_gemm_q8_gb300 import synth
+
+    if args.only_kernel == "layer_full":
+        return run_only_layer(args)
 
     ty_name, n, k = ONLY_KERNELS[args.only_kernel]
     ty = dl.Q4_K if ty_name == "q4k" else dl.Q6_K
@@ -378,7 +408,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only-kernel", choices=sorted(ONLY_KERNELS), default=None,
+    ap.add_argument("--only-kernel", choices=sorted(ONLY_KERNELS) + ["layer_full"], default=None,
                     help="time one GEMM of the step alone (profiling target) instead of the step")
     args = ap.parse_args()
     rank, local_rank, world = _env_dist()

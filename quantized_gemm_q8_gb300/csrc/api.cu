@@ -221,9 +221,12 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsb = (int)(k / QK);
+  // super-blocks of this CTA: all of the row (RMSNorm needs its sum of squares), or without a
+  // norm one per warp along gridDim.y
+  const int sbw = blockIdx.y * 8 + warp, sbstep = 8 * gridDim.y;
   if (row >= rows) {  // padding rows of the operand planes
     float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int sb = warp; sb < nsb; sb += 8) q8k_emit(z, row, rows, sb, k, o);
+    for (int sb = sbw; sb < nsb; sb += sbstep) q8k_emit(z, row, rows, sb, k, o);
     return;
   }
   const float* xr = x + (int64_t)row * ldx;
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
     ss = block_sum(ss, red);
     rstd = 1.0f / sqrtf(ss / (float)k + eps);
   }
-  for (int sb = warp; sb < nsb; sb += 8) {
+  for (int sb = sbw; sb < nsb; sb += sbstep) {
     const int64_t base = (int64_t)sb * QK + 8 * lane;
     const float4 a = *reinterpret_cast<const float4*>(xr + base);
     const float4 b = *reinterpret_cast<const float4*>(xr + base + 4);
@@ -448,7 +451,8 @@ int quantize_rows(const float* x, int64_t rows, int64_t k, int64_t ldx, const fl
   uint8_t* base = static_cast<uint8_t*>(act);
   QuantOut o{nullptr, nullptr, nullptr, reinterpret_cast<__half*>(base + L.off_a), base + L.off_j,
              reinterpret_cast<float*>(base + L.off_d), (int)L.lpad};
-  quantize_act_kernel<<<(int)L.lpad, 256, 0, stream>>>(x, (int)rows, k, ldx, norm_w, eps, o);
+  const dim3 grid((unsigned)L.lpad, norm_w ? 1u : (unsigned)((k / QK + 7) / 8));
+  quantize_act_kernel<<<grid, 256, 0, stream>>>(x, (int)rows, k, ldx, norm_w, eps, o);
   note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch quantize_act");

@@ -93,136 +93,170 @@ __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __res
 }
 
 // Non-causal multi-head attention O = softmax(q k^T) v per head on the reduced QKV ([L][3d],
-// q pre-scaled), f32 with an online softmax over key tiles of 64. One CTA = one head x 32
-// queries; warp w owns queries 4w..4w+3. Scores: a lane holds 4 queries x keys (lane,
-// lane + 32), reading q as broadcast float4 and k rows padded to 132 floats so a quarter-warp's
-// float4 loads of 8 different keys hit distinct banks. PV: the warp's probabilities go through
-// shared memory and a lane accumulates 4 queries x dims 4*lane..4*lane+3. Tiles are staged
-// with float4 loads, each thread's loads issued together.
-constexpr int ATT_QB = 32, ATT_KT = 64, ATT_HD = 128, ATT_KP = ATT_HD + 4;
-constexpr int ATT_SMEM = (ATT_KT * ATT_KP + ATT_KT * ATT_HD + ATT_QB * ATT_HD + ATT_QB * ATT_KT) * 4;
+// q pre-scaled), f32, split over chunks of 32 keys (flash-decoding style): CTA (head, 16
+// queries, chunk c) writes for each query the chunk's max score m_c, sum l_c = sum exp(s - m_c)
+// and unnormalized a_c = sum exp(s - m_c) v; attn_merge_quant_kernel combines the chunks. Small
+// CTAs (4 warps, 43 KB shared) let five share an SM. Warp w owns queries 4w..4w+3; lane = key
+// of the chunk for the scores (k rows padded to 132 floats: a quarter-warp's float4 loads of 8
+// keys hit distinct banks; q read as broadcast float4, query pairs as f32x2), and dims
+// 4*lane..4*lane+3 for the PV product (probabilities through shared memory).
+constexpr int ATT_QB = 16, ATT_KC = 32, ATT_HD = 128, ATT_KP = ATT_HD + 4, ATT_THREADS = 128;
+constexpr int ATT_SMEM = (ATT_KC * ATT_KP + ATT_KC * ATT_HD + ATT_QB * ATT_HD + ATT_QB * ATT_KC) * 4;
 
-__global__ void __launch_bounds__(256, 2) attention_kernel(const float* __restrict__ QKV, float* __restrict__ O,
-                                                          int L, int d) {
+__device__ __forceinline__ void fma2f(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%2,%3};\n mov.b64 rb, {%4,%5};\n mov.b64 rc, {%0,%1};\n"
+      " fma.rn.f32x2 rc, ra, rb, rc;\n mov.b64 {%0,%1}, rc;\n}\n"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+struct AttPart {
+  float* acc;  // [nchunk][L][d]   unnormalized chunk sums a_c
+  float* ml;   // [nchunk][L][heads][2]   (m_c, l_c)
+};
+
+__global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const float* __restrict__ QKV, AttPart part,
+                                                                       int L, int d, int heads) {
   extern __shared__ float4 att_smem4[];
-  float* Ks = reinterpret_cast<float*>(att_smem4);  // [KT][KP]
-  float* Vs = Ks + ATT_KT * ATT_KP;                 // [KT][HD]
-  float* Qs = Vs + ATT_KT * ATT_HD;                 // [QB][HD]
-  float* Ps = Qs + ATT_QB * ATT_HD;                 // [QB][KT]
-  const int h = blockIdx.x, q0 = blockIdx.y * ATT_QB;
+  float* Ks = reinterpret_cast<float*>(att_smem4);  // [KC][KP]
+  float* Vs = Ks + ATT_KC * ATT_KP;                 // [KC][HD]
+  float* Qs = Vs + ATT_KC * ATT_HD;                 // [QB][HD]
+  float* Ps = Qs + ATT_QB * ATT_HD;                 // [QB][KC]
+  const int h = blockIdx.x, q0 = blockIdx.y * ATT_QB, c = blockIdx.z, k0 = c * ATT_KC;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t ld = 3 * (int64_t)d;
   constexpr int HV = ATT_HD / 4;  // float4 per head row
   {
-    float4 v[ATT_QB * HV / 256];
+    constexpr int RQ = ATT_QB * HV / ATT_THREADS, RK = ATT_KC * HV / ATT_THREADS;
+    float4 qv[RQ], kv[RK], vv[RK];
 #pragma unroll
-    for (int r = 0; r < ATT_QB * HV / 256; ++r) {
-      const int i = threadIdx.x + 256 * r, qi = i / HV, c4 = i % HV, p = q0 + qi;
-      v[r] = p < L ? *reinterpret_cast<const float4*>(QKV + p * ld + h * ATT_HD + 4 * c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < RQ; ++r) {
+      const int i = threadIdx.x + ATT_THREADS * r, p = q0 + i / HV;
+      qv[r] = p < L ? *reinterpret_cast<const float4*>(QKV + p * ld + h * ATT_HD + 4 * (i % HV))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int r = 0; r < ATT_QB * HV / 256; ++r) {
-      const int i = threadIdx.x + 256 * r;
-      *reinterpret_cast<float4*>(Qs + (i / HV) * ATT_HD + 4 * (i % HV)) = v[r];
+    for (int r = 0; r < RK; ++r) {
+      const int i = threadIdx.x + ATT_THREADS * r, p = k0 + i / HV;
+      const float* row = QKV + p * ld + h * ATT_HD + 4 * (i % HV);
+      kv[r] = p < L ? *reinterpret_cast<const float4*>(row + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+      vv[r] = p < L ? *reinterpret_cast<const float4*>(row + 2 * d) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < RQ; ++r) {
+      const int i = threadIdx.x + ATT_THREADS * r;
+      *reinterpret_cast<float4*>(Qs + (i / HV) * ATT_HD + 4 * (i % HV)) = qv[r];
+    }
+#pragma unroll
+    for (int r = 0; r < RK; ++r) {
+      const int i = threadIdx.x + ATT_THREADS * r;
+      *reinterpret_cast<float4*>(Ks + (i / HV) * ATT_KP + 4 * (i % HV)) = kv[r];
+      *reinterpret_cast<float4*>(Vs + (i / HV) * ATT_HD + 4 * (i % HV)) = vv[r];
     }
   }
-  float m[4], l[4], acc[4][4];
+  __syncthreads();
+  // scores of 4 queries x key `lane`, as two f32x2 pairs of queries
+  const float* qw = Qs + warp * 4 * ATT_HD;
+  const float* kr = Ks + lane * ATT_KP;
+  float s01[2] = {0.f, 0.f}, s23[2] = {0.f, 0.f};
+#pragma unroll 4
+  for (int e = 0; e < ATT_HD; e += 4) {
+    const float4 k = *reinterpret_cast<const float4*>(kr + e);
+    const float4 a0 = *reinterpret_cast<const float4*>(qw + e);
+    const float4 a1 = *reinterpret_cast<const float4*>(qw + ATT_HD + e);
+    const float4 a2 = *reinterpret_cast<const float4*>(qw + 2 * ATT_HD + e);
+    const float4 a3 = *reinterpret_cast<const float4*>(qw + 3 * ATT_HD + e);
+    fma2f(s01[0], s01[1], a0.x, a1.x, k.x, k.x);
+    fma2f(s23[0], s23[1], a2.x, a3.x, k.x, k.x);
+    fma2f(s01[0], s01[1], a0.y, a1.y, k.y, k.y);
+    fma2f(s23[0], s23[1], a2.y, a3.y, k.y, k.y);
+    fma2f(s01[0], s01[1], a0.z, a1.z, k.z, k.z);
+    fma2f(s23[0], s23[1], a2.z, a3.z, k.z, k.z);
+    fma2f(s01[0], s01[1], a0.w, a1.w, k.w, k.w);
+    fma2f(s23[0], s23[1], a2.w, a3.w, k.w, k.w);
+  }
+  const bool valid = k0 + lane < L;
+  const float sc[4] = {s01[0], s01[1], s23[0], s23[1]};
+  float* pw = Ps + warp * 4 * ATT_KC;
+  float mq[4], lq[4];
 #pragma unroll
   for (int qq = 0; qq < 4; ++qq) {
-    m[qq] = -INFINITY;
-    l[qq] = 0.f;
+    const float sv = valid ? sc[qq] : -INFINITY;
+    float mx = sv;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[qq][c] = 0.f;
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float pr = expf(sv - mx);  // the chunk's key k0 is always valid, so mx is finite
+    float ps = pr;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    mq[qq] = mx;
+    lq[qq] = ps;
+    pw[qq * ATT_KC + lane] = pr;
   }
-  const float* qw = Qs + warp * 4 * ATT_HD;
-  float* pw = Ps + warp * 4 * ATT_KT;
-  for (int k0 = 0; k0 < L; k0 += ATT_KT) {
-    __syncthreads();  // previous tile fully consumed
-    {
-      constexpr int R = ATT_KT * HV / 256;  // 8 float4 of K and of V per thread
-      float4 kv[R], vv[R];
+  __syncwarp();
+  float acc[4][4];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int i = threadIdx.x + 256 * r, kj = i / HV, c4 = i % HV, p = k0 + kj;
-        const float* row = QKV + p * ld + h * ATT_HD + 4 * c4;
-        kv[r] = p < L ? *reinterpret_cast<const float4*>(row + d) : make_float4(0.f, 0.f, 0.f, 0.f);
-        vv[r] = p < L ? *reinterpret_cast<const float4*>(row + 2 * d) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+  for (int qq = 0; qq < 4; ++qq)
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int i = threadIdx.x + 256 * r, kj = i / HV, c4 = i % HV;
-        *reinterpret_cast<float4*>(Ks + kj * ATT_KP + 4 * c4) = kv[r];
-        *reinterpret_cast<float4*>(Vs + kj * ATT_HD + 4 * c4) = vv[r];
-      }
-    }
-    __syncthreads();
-    // scores of 4 queries x keys (lane, lane + 32)
-    float sc[4][2];
+    for (int i = 0; i < 4; ++i) acc[qq][i] = 0.f;
+#pragma unroll 2
+  for (int j = 0; j < ATT_KC; j += 4) {  // keys past L have p = 0 and zero V rows
+    float4 pj[4];
 #pragma unroll
-    for (int qq = 0; qq < 4; ++qq) sc[qq][0] = sc[qq][1] = 0.f;
-    const float* k0r = Ks + lane * ATT_KP;
-    const float* k1r = Ks + (lane + 32) * ATT_KP;
-#pragma unroll 4
-    for (int e = 0; e < ATT_HD; e += 4) {
-      const float4 ka = *reinterpret_cast<const float4*>(k0r + e);
-      const float4 kb = *reinterpret_cast<const float4*>(k1r + e);
+    for (int qq = 0; qq < 4; ++qq) pj[qq] = *reinterpret_cast<const float4*>(pw + qq * ATT_KC + j);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float4 vv = *reinterpret_cast<const float4*>(Vs + (j + t) * ATT_HD + lane * 4);
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
-        const float4 q = *reinterpret_cast<const float4*>(qw + qq * ATT_HD + e);
-        sc[qq][0] = fmaf(q.x, ka.x, fmaf(q.y, ka.y, fmaf(q.z, ka.z, fmaf(q.w, ka.w, sc[qq][0]))));
-        sc[qq][1] = fmaf(q.x, kb.x, fmaf(q.y, kb.y, fmaf(q.z, kb.z, fmaf(q.w, kb.w, sc[qq][1]))));
+        const float pv = t == 0 ? pj[qq].x : t == 1 ? pj[qq].y : t == 2 ? pj[qq].z : pj[qq].w;
+        fma2f(acc[qq][0], acc[qq][1], pv, pv, vv.x, vv.y);
+        fma2f(acc[qq][2], acc[qq][3], pv, pv, vv.z, vv.w);
       }
     }
-    const bool v0 = k0 + lane < L, v1 = k0 + lane + 32 < L;
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-      const float s0 = v0 ? sc[qq][0] : -INFINITY, s1 = v1 ? sc[qq][1] : -INFINITY;
-      float mx = fmaxf(s0, s1);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float mnew = fmaxf(m[qq], mx);  // finite: key k0 is always valid
-      const float corr = expf(m[qq] - mnew);
-      const float p0 = expf(s0 - mnew), p1 = expf(s1 - mnew);
-      float ps = p0 + p1;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-      l[qq] = l[qq] * corr + ps;
-      m[qq] = mnew;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[qq][c] *= corr;
-      pw[qq * ATT_KT + lane] = p0;
-      pw[qq * ATT_KT + lane + 32] = p1;
-    }
-    __syncwarp();
-    const int nk = min(ATT_KT, L - k0);
-    for (int j = 0; j < nk; j += 4) {  // keys past nk have p = 0 and zero V rows; nk rounds up to 4
-      float4 pj[4];
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq) pj[qq] = *reinterpret_cast<const float4*>(pw + qq * ATT_KT + j);
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const float4 vv = *reinterpret_cast<const float4*>(Vs + (j + t) * ATT_HD + lane * 4);
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          const float pv = t == 0 ? pj[qq].x : t == 1 ? pj[qq].y : t == 2 ? pj[qq].z : pj[qq].w;
-          acc[qq][0] = fmaf(pv, vv.x, acc[qq][0]);
-          acc[qq][1] = fmaf(pv, vv.y, acc[qq][1]);
-          acc[qq][2] = fmaf(pv, vv.z, acc[qq][2]);
-          acc[qq][3] = fmaf(pv, vv.w, acc[qq][3]);
-        }
-      }
-    }
-    __syncwarp();
   }
 #pragma unroll
   for (int qq = 0; qq < 4; ++qq) {
     const int qi = q0 + warp * 4 + qq;
     if (qi < L) {
-      const float inv = 1.0f / l[qq];
-      *reinterpret_cast<float4*>(O + (int64_t)qi * d + h * ATT_HD + lane * 4) =
-          make_float4(acc[qq][0] * inv, acc[qq][1] * inv, acc[qq][2] * inv, acc[qq][3] * inv);
+      *reinterpret_cast<float4*>(part.acc + ((int64_t)c * L + qi) * d + h * ATT_HD + lane * 4) =
+          make_float4(acc[qq][0], acc[qq][1], acc[qq][2], acc[qq][3]);
+      if (lane == 0)
+        *reinterpret_cast<float2*>(part.ml + (((int64_t)c * L + qi) * heads + h) * 2) = make_float2(mq[qq], lq[qq]);
     }
   }
+}
+
+// Merge the key chunks of the attention and quantize the output to Q8_K in one pass: warp
+// (blockIdx.y * 8 + w) of row blockIdx.x handles super-block sb (dims 256 sb .. = two heads);
+// lane's 8 dims belong to head 2 sb + lane / 16. O = sum_c e^(m_c - M) a_c / sum_c e^(m_c - M) l_c.
+__global__ void __launch_bounds__(256) attn_merge_quant_kernel(AttPart part, int nchunk, int L, int d, int heads,
+                                                               QuantOut o) {
+  const int row = blockIdx.x;
+  const int sb = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int nsb = d / QK;
+  if (sb >= nsb) return;
+  float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (row < L) {
+    const int dim = sb * QK + 8 * lane, h = dim / ATT_HD;
+    float M = -INFINITY;
+    for (int c = 0; c < nchunk; ++c) M = fmaxf(M, part.ml[(((int64_t)c * L + row) * heads + h) * 2]);
+    float den = 0.f;
+    for (int c = 0; c < nchunk; ++c) {
+      const float2 ml = *reinterpret_cast<const float2*>(part.ml + (((int64_t)c * L + row) * heads + h) * 2);
+      const float w = expf(ml.x - M);
+      den = fmaf(w, ml.y, den);
+      const float* ac = part.acc + ((int64_t)c * L + row) * d + dim;
+      const float4 a0 = *reinterpret_cast<const float4*>(ac);
+      const float4 a1 = *reinterpret_cast<const float4*>(ac + 4);
+      v[0] = fmaf(w, a0.x, v[0]); v[1] = fmaf(w, a0.y, v[1]); v[2] = fmaf(w, a0.z, v[2]); v[3] = fmaf(w, a0.w, v[3]);
+      v[4] = fmaf(w, a1.x, v[4]); v[5] = fmaf(w, a1.y, v[5]); v[6] = fmaf(w, a1.z, v[6]); v[7] = fmaf(w, a1.w, v[7]);
+    }
+    const float inv = 1.0f / den;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] *= inv;
+  }
+  q8k_emit(v, row, L, sb, d, o);  // padding rows quantize zeros
 }
 
 // Fused row kernels: the source of each row is built from split partials, then quantized.
@@ -356,7 +390,7 @@ static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, co
 // ---------------------------------------------------------------------------------------------
 struct StepPlan {
   QgemmPlan qk, v, o, gu, dn;
-  size_t x, act_d, act_ff, pqk, pv, po, pgu, pdn, qkv, att, rope, lm, bytes;
+  size_t x, act_d, act_ff, pqk, pv, po, pgu, pdn, qkv, att, attml, rope, lm, bytes;
 };
 
 static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead) {
@@ -383,7 +417,8 @@ static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead
   S.pgu = take((size_t)S.gu.splits * L * 2 * f * 4);
   S.pdn = take((size_t)S.dn.splits * L * d * 4);
   S.qkv = take(full ? (size_t)L * 3 * d * 4 : 0);
-  S.att = take(full ? (size_t)L * d * 4 : 0);
+  S.att = take(full ? (size_t)((L + 31) / 32) * L * d * 4 : 0);
+  S.attml = take(full ? (size_t)((L + 31) / 32) * L * m->n_heads * 8 : 0);
   S.rope = take(full ? (size_t)L * (m->head_dim / 2) * 8 : 0);
   S.lm = 0;
   S.bytes = off;
@@ -444,21 +479,25 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
     if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wqk, 2 * d, Pqk, S.qk, s))) return rc;
     if ((rc = gemm(DLLM_Q6_K, actd, L, d, Ly.wv, d, Pv, S.v, s))) return rc;
     if (full) {
-      float* A = reinterpret_cast<float*>(ws + S.att);
       float* QKV = reinterpret_cast<float*>(ws + S.qkv);
       const int64_t npair = L * (3 * d / 2);
       qkv_reduce_rope_kernel<<<(unsigned)((npair + 255) / 256), 256, 0, s>>>(
           Pqk, S.qk.splits, Pv, S.v.splits, reinterpret_cast<const float2*>(ws + S.rope), (int)L, d, hd,
           1.0f / sqrtf((float)hd), QKV);
       note_launch();
-      cudaError_t e = cudaFuncSetAttribute(attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM);
+      const int nchunk = (int)((L + ATT_KC - 1) / ATT_KC);
+      const AttPart ap{reinterpret_cast<float*>(ws + S.att), reinterpret_cast<float*>(ws + S.attml)};
+      cudaError_t e = cudaFuncSetAttribute(attention_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           ATT_SMEM);
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
-      const dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB));
-      attention_kernel<<<ag, 256, ATT_SMEM, s>>>(QKV, A, (int)L, d);
+      const dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB), (unsigned)nchunk);
+      attention_partial_kernel<<<ag, ATT_THREADS, ATT_SMEM, s>>>(QKV, ap, (int)L, d, m->n_heads);
+      note_launch();
+      const dim3 mg((unsigned)act_rows_padded(L), (unsigned)((d / QK + 7) / 8));
+      attn_merge_quant_kernel<<<mg, 256, 0, s>>>(ap, nchunk, (int)L, d, m->n_heads, quant_out(actd, L, d));
       note_launch();
       e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "launch attention");
-      if ((rc = quantize_rows(A, L, d, d, nullptr, m->eps, actd, s))) return rc;
     } else {
       // linear stream: the O projection consumes the V projection's output
       if ((rc = run_row<ROW_SUM_QUANT>(nullptr, Pv, S.v.splits, L * d, d, nullptr, 0.f, (int)L, d, actd, s))) return rc;
