@@ -218,6 +218,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
                                                            int64_t ldx, const float* __restrict__ norm_w, float eps,
                                                            QuantOut o) {
   __shared__ float red[8];
+  griddep_wait();
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsb = (int)(k / QK);
@@ -257,6 +258,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
     }
     q8k_emit(v, row, rows, sb, k, o);
   }
+  griddep_launch();
 }
 
 // y (+)= sum of split partials, fixed order.
@@ -320,6 +322,8 @@ __global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
     int32_t* row_id, float* row_conf, float* conf_ws, int* id_ws, unsigned int* done) {
   __shared__ SoftPart red[8];
   __shared__ bool last;
+  griddep_wait();
+  griddep_launch();
   const int r = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   SoftPart acc{-INFINITY, 0x7fffffff, 0.f};
   const size_t base = (size_t)r * P;
@@ -452,9 +456,9 @@ int quantize_rows(const float* x, int64_t rows, int64_t k, int64_t ldx, const fl
   QuantOut o{nullptr, nullptr, nullptr, reinterpret_cast<__half*>(base + L.off_a), base + L.off_j,
              reinterpret_cast<float*>(base + L.off_d), (int)L.lpad};
   const dim3 grid((unsigned)L.lpad, norm_w ? 1u : (unsigned)((k / QK + 7) / 8));
-  quantize_act_kernel<<<grid, 256, 0, stream>>>(x, (int)rows, k, ldx, norm_w, eps, o);
+  cudaError_t e = launch_pdl(quantize_act_kernel, grid, dim3(256), 0, stream, x, (int)rows, k, ldx, norm_w, eps, o);
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch quantize_act");
 }
 }  // namespace dllm
@@ -796,12 +800,13 @@ DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d
   unsigned int* done = reinterpret_cast<unsigned int*>(base + W.done);
   cudaError_t e = cudaMemsetAsync(done, 0, sizeof(unsigned int), s);
   if (e != cudaSuccess) return cuda_fail(e, "zero the merge counter");
-  lmhead_merge_commit_kernel<<<(int)R, 256, 0, s>>>(
-      reinterpret_cast<float*>(base + W.pmax), reinterpret_cast<int*>(base + W.parg),
-      reinterpret_cast<float*>(base + W.psum), W.P, (int)R, canvas, mask_id, block_begin, k_commit, out_pos, out_id,
-      out_conf, row_id, row_conf, reinterpret_cast<float*>(base + W.conf), reinterpret_cast<int*>(base + W.id), done);
+  e = launch_pdl(lmhead_merge_commit_kernel, dim3((unsigned)R), dim3(256), 0, s,
+                 reinterpret_cast<const float*>(base + W.pmax), reinterpret_cast<const int*>(base + W.parg),
+                 reinterpret_cast<const float*>(base + W.psum), W.P, (int)R, canvas, mask_id, (int)block_begin,
+                 (int)k_commit, out_pos, out_id, out_conf, row_id, row_conf, reinterpret_cast<float*>(base + W.conf),
+                 reinterpret_cast<int*>(base + W.id), done);
   note_launch();
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch lmhead_merge_commit");
 }
 

@@ -45,6 +45,24 @@ QgemmPlan plan_single_split(int type, int64_t m, int64_t n, int64_t k);
 // One GEMM launch (no argument validation; callers validate). When P.splits > 1 the kernel
 // writes split partials [splits][m][n] to `partial`, otherwise y (mode 0) or the LM-head
 // softmax partials (mode 1).
+// Launch with programmatic stream serialization: the kernel may start while its predecessor
+// drains; it synchronizes with griddep_wait() before touching the predecessor's data.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 struct GemmLaunch {
   int type;
   const void* act;

@@ -19,6 +19,8 @@ namespace dllm {
 // RoPE table: cs[p][i] = (cos, sin) of p * theta^(-2i/hd), computed in f64 once per step.
 // ---------------------------------------------------------------------------------------------
 __global__ void rope_table_kernel(float2* cs, int L, int half, double theta, int hd) {
+  griddep_wait();
+  griddep_launch();
   const int p = blockIdx.x, i = threadIdx.x;
   if (p < L && i < half) {
     const double ang = (double)p * pow(theta, -2.0 * (double)i / (double)hd);
@@ -32,6 +34,8 @@ __global__ void rope_table_kernel(float2* cs, int L, int half, double theta, int
 // w = d * scale * q - dmin * min is formed with one fused multiply-add.
 __global__ void embed_q4k_kernel(const uint8_t* __restrict__ table, int nsb, const int32_t* __restrict__ ids,
                                  float* __restrict__ x, int d) {
+  griddep_wait();
+  griddep_launch();
   const int p = blockIdx.x;
   const int64_t row = ids[p];
   for (int k = threadIdx.x; k < d; k += blockDim.x) {
@@ -62,6 +66,8 @@ __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __res
                                                               const float* __restrict__ Pv, int Sv,
                                                               const float2* __restrict__ cs, int L, int d, int hd,
                                                               float qscale, float* __restrict__ QKV) {
+  griddep_wait();
+  griddep_launch();
   const int64_t npair = (int64_t)L * (3 * d / 2);
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (i >= npair) return;
@@ -122,6 +128,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
   float* Vs = Ks + ATT_KC * ATT_KP;                 // [KC][HD]
   float* Qs = Vs + ATT_KC * ATT_HD;                 // [QB][HD]
   float* Ps = Qs + ATT_QB * ATT_HD;                 // [QB][KC]
+  griddep_wait();
   const int h = blockIdx.x, q0 = blockIdx.y * ATT_QB, c = blockIdx.z, k0 = c * ATT_KC;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t ld = 3 * (int64_t)d;
@@ -225,6 +232,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
         *reinterpret_cast<float2*>(part.ml + (((int64_t)c * L + qi) * heads + h) * 2) = make_float2(mq[qq], lq[qq]);
     }
   }
+  griddep_launch();
 }
 
 // Merge the key chunks of the attention and quantize the output to Q8_K in one pass: warp
@@ -232,6 +240,8 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
 // lane's 8 dims belong to head 2 sb + lane / 16. O = sum_c e^(m_c - M) a_c / sum_c e^(m_c - M) l_c.
 __global__ void __launch_bounds__(256) attn_merge_quant_kernel(AttPart part, int nchunk, int L, int d, int heads,
                                                                QuantOut o) {
+  griddep_wait();
+  griddep_launch();
   const int row = blockIdx.x;
   const int sb = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int nsb = d / QK;
@@ -284,6 +294,8 @@ struct RowArgs {
 template <int MODE>
 __global__ void __launch_bounds__(1024) row_resid_kernel(RowArgs a) {
   __shared__ float red[32];
+  griddep_wait();
+  griddep_launch();
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarp = blockDim.x >> 5;
   const int nsb = a.k / QK;
@@ -332,6 +344,8 @@ __global__ void __launch_bounds__(1024) row_resid_kernel(RowArgs a) {
 // builds and quantizes one super-block; each lane's partial loads are issued together.
 template <int MODE>
 __global__ void __launch_bounds__(256) row_sb_kernel(RowArgs a) {
+  griddep_wait();
+  griddep_launch();
   const int row = blockIdx.x;
   const int sb = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int nsb = a.k / QK;
@@ -373,15 +387,16 @@ template <int MODE>
 static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, const float* w, float eps, int rows,
                    int k, void* act, cudaStream_t s) {
   RowArgs a{x, P, S, pstride, ldp, w, eps, rows, k, act ? quant_out(act, rows, k) : QuantOut{}};
+  cudaError_t e;
   if (MODE == ROW_RESID_NORM_QUANT || MODE == ROW_RESID_ONLY) {
     const int grid = MODE == ROW_RESID_ONLY ? rows : (int)act_rows_padded(rows);
-    row_resid_kernel<MODE><<<grid, 1024, 0, s>>>(a);
+    e = launch_pdl(row_resid_kernel<MODE>, dim3(grid), dim3(1024), 0, s, a);
   } else {
     const dim3 grid((unsigned)act_rows_padded(rows), (unsigned)((k / QK + 7) / 8));
-    row_sb_kernel<MODE><<<grid, 256, 0, s>>>(a);
+    e = launch_pdl(row_sb_kernel<MODE>, grid, dim3(256), 0, s, a);
   }
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch row kernel");
 }
 
@@ -464,12 +479,14 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
   void* actf = ws + S.act_ff;
   int rc;
   if (full) {
-    rope_table_kernel<<<(int)L, hd / 2, 0, s>>>(reinterpret_cast<float2*>(ws + S.rope), (int)L, hd / 2,
-                                                (double)m->rope_theta, hd);
+    cudaError_t e = launch_pdl(rope_table_kernel, dim3((unsigned)L), dim3(hd / 2), 0, s,
+                               reinterpret_cast<float2*>(ws + S.rope), (int)L, hd / 2, (double)m->rope_theta, hd);
     note_launch();
-    embed_q4k_kernel<<<(int)L, 256, 0, s>>>(static_cast<const uint8_t*>(m->tok_embd), d / QK, canvas, x, d);
+    if (e == cudaSuccess)
+      e = launch_pdl(embed_q4k_kernel, dim3((unsigned)L), dim3(256), 0, s, static_cast<const uint8_t*>(m->tok_embd),
+                     d / QK, canvas, x, d);
     note_launch();
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch embedding");
   }
   // layer 0 input: RMSNorm + quantize of x
@@ -481,22 +498,26 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
     if (full) {
       float* QKV = reinterpret_cast<float*>(ws + S.qkv);
       const int64_t npair = L * (3 * d / 2);
-      qkv_reduce_rope_kernel<<<(unsigned)((npair + 255) / 256), 256, 0, s>>>(
-          Pqk, S.qk.splits, Pv, S.v.splits, reinterpret_cast<const float2*>(ws + S.rope), (int)L, d, hd,
-          1.0f / sqrtf((float)hd), QKV);
+      cudaError_t e = launch_pdl(qkv_reduce_rope_kernel, dim3((unsigned)((npair + 255) / 256)), dim3(256), 0, s,
+                                 (const float*)Pqk, S.qk.splits, (const float*)Pv, S.v.splits,
+                                 reinterpret_cast<const float2*>(ws + S.rope), (int)L, d, hd, 1.0f / sqrtf((float)hd),
+                                 QKV);
       note_launch();
+      if (e != cudaSuccess) return cuda_fail(e, "launch qkv reduce");
       const int nchunk = (int)((L + ATT_KC - 1) / ATT_KC);
       const AttPart ap{reinterpret_cast<float*>(ws + S.att), reinterpret_cast<float*>(ws + S.attml)};
-      cudaError_t e = cudaFuncSetAttribute(attention_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           ATT_SMEM);
+      e = cudaFuncSetAttribute(attention_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM);
       if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
       const dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB), (unsigned)nchunk);
-      attention_partial_kernel<<<ag, ATT_THREADS, ATT_SMEM, s>>>(QKV, ap, (int)L, d, m->n_heads);
+      e = launch_pdl(attention_partial_kernel, ag, dim3(ATT_THREADS), ATT_SMEM, s, (const float*)QKV, ap, (int)L, d,
+                     m->n_heads);
       note_launch();
       const dim3 mg((unsigned)act_rows_padded(L), (unsigned)((d / QK + 7) / 8));
-      attn_merge_quant_kernel<<<mg, 256, 0, s>>>(ap, nchunk, (int)L, d, m->n_heads, quant_out(actd, L, d));
+      if (e == cudaSuccess)
+        e = launch_pdl(attn_merge_quant_kernel, mg, dim3(256), 0, s, ap, nchunk, (int)L, d, m->n_heads,
+                       quant_out(actd, L, d));
       note_launch();
-      e = cudaGetLastError();
+      if (e == cudaSuccess) e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "launch attention");
     } else {
       // linear stream: the O projection consumes the V projection's output

@@ -55,28 +55,17 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Suspending test: a thread whose phase is not complete sleeps until it completes or about
-// `ns` nanoseconds pass (the hint bounds how late a sleeping thread can notice completion).
-__device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(ns)
-      : "memory");
-  return ok != 0;
-}
 // Bounded wait for the phase of parity `parity` to complete. Gives up (returns false) when
 // another role raised `abort` or after `limit` SM cycles, in which case it raises `abort`.
-// sleep_ns = 0 spins on the non-blocking test (lowest latency, but a spinning warp takes
-// issue slots from the warps doing the work); sleep_ns > 0 sleeps between tests.
+// sleep_ns = 0 polls back to back (lowest latency, but a polling warp takes issue slots from
+// the warps doing the work); sleep_ns > 0 naps about that long between polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, long long limit,
                                           uint32_t sleep_ns = 0) {
   if (mbar_test_wait(bar, parity)) return true;
   long long t0 = clock64();
   while (true) {
-    if (sleep_ns ? mbar_try_wait_ns(bar, parity, sleep_ns) : mbar_test_wait(bar, parity)) return true;
+    if (sleep_ns) __nanosleep(sleep_ns);
+    if (mbar_test_wait(bar, parity)) return true;
     if (*abort) return false;
     if (clock64() - t0 > limit) {
       *abort = 1;
@@ -96,6 +85,14 @@ __device__ __forceinline__ void fence_barrier_init() {
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+// ---- programmatic dependent launch --------------------------------------------------------
+// Wait until the preceding kernel of the stream has completed and its memory is visible (a
+// no-op for a kernel launched without the programmatic-serialization attribute).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel of the stream be scheduled once every CTA of this grid has done this or
+// exited (its CTAs start as resources free up; it still waits with griddep_wait for our writes).
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---- bulk copies (TMA engine) -------------------------------------------------------------
 // 1-D bulk copy global -> shared; dst, src 16-byte aligned, bytes % 16 == 0.

@@ -36,7 +36,7 @@
 // Warp roles (896 threads, 7 warpgroups): warps 0-15 epilogue (warp w reads TMEM lanes
 // 32*(w%4).. and quarter w/4 of the NT columns), warps 16-23 decode, warp 24 activation
 // producer, warp 25 MMA
-// issuer (whole warp, one elected lane issues) and TMEM owner, warp 26 weight producer, warp
+// issuer (one thread) and TMEM owner, warp 26 weight producer, warp
 // 27 idle. The decode warps form two groups of four (one thread per weight row = TMEM lane
 // in each) that take alternate K-stages, so one group's tensor-memory stores drain while the
 // other decodes; each group also writes half of the Q4_K min-operand rows. setmaxnreg re-splits the 72-per-thread launch allocation: 88 epilogue, 56 decode,
@@ -81,13 +81,13 @@ constexpr int SMEM_LIMIT = 232448;
 #define QG_SLEEP_MMA_NS 0
 #endif
 #ifndef QG_SLEEP_DEC_NS
-#define QG_SLEEP_DEC_NS 64
+#define QG_SLEEP_DEC_NS 32
 #endif
 #ifndef QG_SLEEP_EPI_NS
-#define QG_SLEEP_EPI_NS 256
+#define QG_SLEEP_EPI_NS 128
 #endif
 #ifndef QG_SLEEP_PROD_NS
-#define QG_SLEEP_PROD_NS 256
+#define QG_SLEEP_PROD_NS 64
 #endif
 constexpr uint32_t QG_SLEEP_MMA = QG_SLEEP_MMA_NS, QG_SLEEP_DEC = QG_SLEEP_DEC_NS, QG_SLEEP_EPI = QG_SLEEP_EPI_NS,
                    QG_SLEEP_PROD = QG_SLEEP_PROD_NS;
@@ -313,7 +313,8 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmap, const QgemmParams p) {
   using C = QCfg<TYPE, NT>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, by offset from the shared array (keeps shared-memory addressing)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -354,6 +355,9 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the next kernel of the stream may be scheduled now (its CTAs start as ours exit); only the
+  // roles that read the preceding kernel's outputs or write ours wait for it below
+  griddep_launch();
 
   if (warp >= QG_PROD_WARP) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(QG_REGS_CTL));
@@ -389,6 +393,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
       // thread): per super-block the epilogue scales (E), the Q4_K activation 16-sums (J), then
       // the activation operand stages through the tensor map
       prefetch_tensormap(&tmap);
+      griddep_wait();  // the activations are the preceding kernel's output
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
@@ -431,16 +436,17 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         while (clock64() - t0 < 2000000) {
         }
       }
-    } else if (warp == QG_MMA_WARP) {
-      // ---------------------------------------------------------- MMA issuer (whole warp, one
-      // elected lane issues). Accumulator slot s (NT columns at s * NT) is written only after
-      // the epilogue drained its previous contents; se0/se1 count those waits.
+    } else if (warp == QG_MMA_WARP && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer (one thread; a
+      // warp-wide issue was measured to replay each MMA once per lane). Accumulator slot s (NT
+      // columns at s * NT) is written only after the epilogue drained its previous contents;
+      // se0/se1 count those waits.
       constexpr uint32_t IDESC = idesc_f16(BM, NT);
       int it = 0;
       uint32_t se0 = 0, se1 = 0;
       bool ok = true;
       auto wait_tc = [&](uint32_t bar, uint32_t parity) -> bool {
-        const bool r = warp_wait(bar, parity, abort_flag, lim, QG_SLEEP_MMA);
+        const bool r = mbar_wait(bar, parity, abort_flag, lim, QG_SLEEP_MMA);
         tc_fence_after();
         return r;
       };
@@ -459,16 +465,16 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             for (int st = 0; st < 2; ++st) {
               const int j = 2 * it + st, b = j % C::K_STAGES;
               if (!(ok = wait_tc(BAR(C::BK_FULL + b), (j / C::K_STAGES) & 1))) break;
-              QTRACE(lane == 0, 2, j);
+              QTRACE(true, 2, j);
               const uint32_t acol = tmem + C::ACOL + b * C::ASTG;
               const uint64_t bdesc = desc_sw128(sbase + C::OFF_B + b * C::B_STAGE);
 #pragma unroll
               for (int qq = 0; qq < 2; ++qq)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  mma_f16_ts_warp(dslot, acol + qq * 32 + kk * 8, bdesc + (uint64_t)((qq * C::B_QUARTER + kk * 32) >> 4),
+                  mma_f16_ts(dslot, acol + qq * 32 + kk * 8, bdesc + (uint64_t)((qq * C::B_QUARTER + kk * 32) >> 4),
                                   IDESC, (st | qq | kk) != 0);
-              mma_commit_warp(BAR(C::BK_EMPTY + b));
+              mma_commit(BAR(C::BK_EMPTY + b));
             }
             if (!ok) break;
             // min term last: head and tail coefficients x activation 16-sums
@@ -476,35 +482,35 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             if (!(ok = wait_tc(BAR(C::BJ_FULL + jx), (it / C::J_STAGES) & 1))) break;
             const uint32_t js = sbase + C::OFF_J + jx * C::J_BYTES;
             const uint64_t bj = desc_noswz(js + C::J_BJ, 128, 256);
-            mma_f16_warp(dslot, desc_noswz(js + C::J_AJ, 128, 256), bj, IDESC, 1);
-            mma_f16_warp(dslot, desc_noswz(js + C::J_AJ + 4096, 128, 256), bj, IDESC, 1);
-            mma_commit_warp(BAR(C::BJ_EMPTY + jx));
-            QTRACE(lane == 0, 3, it);
+            mma_f16(dslot, desc_noswz(js + C::J_AJ, 128, 256), bj, IDESC, 1);
+            mma_f16(dslot, desc_noswz(js + C::J_AJ + 4096, 128, 256), bj, IDESC, 1);
+            mma_commit(BAR(C::BJ_EMPTY + jx));
+            QTRACE(true, 3, it);
           } else {
             for (int q = 0; q < 4; ++q) {
               const int j = 4 * it + q, b = j % C::K_STAGES;
               if (!(ok = wait_tc(BAR(C::BK_FULL + b), (j / C::K_STAGES) & 1))) break;
-              QTRACE(lane == 0, 2, j);
+              QTRACE(true, 2, j);
               const uint32_t acol = tmem + C::ACOL + b * C::ASTG;
               const uint64_t bdesc = desc_sw128(sbase + C::OFF_B + b * C::B_STAGE);
 #pragma unroll
               for (int part = 0; part < 2; ++part)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  mma_f16_ts_warp(dslot, acol + part * 32 + kk * 8, bdesc + (uint64_t)((kk * 32) >> 4), IDESC,
+                  mma_f16_ts(dslot, acol + part * 32 + kk * 8, bdesc + (uint64_t)((kk * 32) >> 4), IDESC,
                                   (q | part | kk) != 0);
-              mma_commit_warp(BAR(C::BK_EMPTY + b));
+              mma_commit(BAR(C::BK_EMPTY + b));
             }
             if (!ok) break;
           }
-          mma_commit_warp(BAR(C::BS_FULL + s));
+          mma_commit(BAR(C::BS_FULL + s));
         }
       }
-      if (!ok && lane == 0) atomicOr(p.err, ERR_TIMEOUT_MMA);
+      if (!ok) atomicOr(p.err, ERR_TIMEOUT_MMA);
       // all issued MMAs complete before the tensor memory is released
-      mma_commit_warp(BAR(C::B_DONE));
+      mma_commit(BAR(C::B_DONE));
       volatile int never = 0;
-      warp_wait(BAR(C::B_DONE), 0, &never, lim);
+      mbar_wait(BAR(C::B_DONE), 0, &never, lim);
     }
   } else if (warp >= QG_DEC_WARP0) {
     // ------------------------------------------------------------ decode: group g (warps 16-19 or
@@ -630,6 +636,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-15)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(QG_REGS_EPI));
+    griddep_wait();  // outputs may be read (accumulate) or still in use by the preceding kernel
     constexpr int NC = C::NC;
     constexpr int NCH = NC / 8;
     const int qd = warp & 3, hf = warp >> 2;

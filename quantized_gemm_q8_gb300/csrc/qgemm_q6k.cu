@@ -10,9 +10,9 @@ static int launch_one(const CUtensorMap& map, const QgemmParams& p, int grid, cu
   auto* k = &qgemm_kernel<TYPE_Q6K, NT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(qgemm_q6k)");
-  k<<<grid, QG_THREADS, SMEM, s>>>(map, p);
+  e = launch_pdl(k, dim3(grid), dim3(QG_THREADS), SMEM, s, map, p);
   note_launch();
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch qgemm_q6k");
   return DLLM_OK;
 }
