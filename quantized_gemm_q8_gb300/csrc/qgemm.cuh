@@ -178,7 +178,7 @@ struct QgemmParams {
 #ifdef DLLM_TRACE
 #define QTRACE(cond, slot, idx)                                                             \
   do {                                                                                      \
-    if ((cond) && blockIdx.x == 0 && (idx) < 256) p.trace[(slot) * 256 + (idx)] = clock64(); \
+    if ((cond) && blockIdx.x == 0 && (idx) < 256 && p.trace) p.trace[(slot) * 256 + (idx)] = clock64(); \
   } while (0)
 #else
 #define QTRACE(cond, slot, idx) \
@@ -269,9 +269,12 @@ __device__ __forceinline__ void decode_q6k_piece(const uint8_t* W, int t, int q,
 
 // Q4_K per-row fold of the min term into the scale-sum accumulator (see the top of the
 // file): A scale 2^-k (0 when d = 0), min coefficient -(dmin/d) * 2^-k (-1 when d = 0) and the
-// epilogue factor d * 2^k (dmin when d = 0). The decode and epilogue warps evaluate the same
-// function on the same f16 inputs. Sets *bad when the coefficient cannot be held (|dmin/d|
-// beyond 4e6; no real block comes near).
+// epilogue factor d * 2^k (dmin when d = 0), k the smallest shift >= 0 with
+// 63 |dmin/d| 2^-k <= 2^14. The decode and epilogue warps evaluate the same function on the
+// same f16 inputs, so both sides agree on k. Sets *bad when no k <= 14 suffices (|dmin/d|
+// beyond 4e6; no real block comes near). The ratio takes the fast division (within 2 ulp):
+// it only enters the min coefficient, which the J operand carries as an f16 head + tail pair
+// anyway; every power of two is built from exponent bits, so the fold has no loop.
 struct Q4Fold {
   float ascale, cmul, factor;
 };
@@ -283,18 +286,18 @@ __device__ __forceinline__ Q4Fold q4k_fold(float d, float dmin, bool* bad) {
     f.factor = dmin;
     return f;
   }
-  const float r = dmin / d;
-  float mag = 63.f * fabsf(r), sc = 1.f;
-  int k = 0;
-  while (mag > 16384.f && k < 14) {
-    mag *= 0.5f;
-    sc *= 0.5f;
-    ++k;
+  const float r = __fdividef(dmin, d);
+  const float mag = 63.f * fabsf(r);
+  const uint32_t mb = __float_as_uint(mag);
+  // mag = 2^e (1 + frac): mag * 2^-k <= 2^14 first holds at k = e - 14 (frac = 0) or e - 13
+  int k = mag <= 16384.f ? 0 : (int)(mb >> 23) - 141 + ((mb & 0x7FFFFFu) != 0u);
+  if (k > 14) {  // also NaN / inf ratios
+    k = 14;
+    *bad = true;
   }
-  if (!(mag <= 16384.f)) *bad = true;
-  f.ascale = sc;
-  f.cmul = -r * sc;
-  f.factor = d / sc;
+  f.ascale = __uint_as_float((uint32_t)(127 - k) << 23);
+  f.cmul = -r * f.ascale;
+  f.factor = d * __uint_as_float((uint32_t)(127 + k) << 23);
   return f;
 }
 
