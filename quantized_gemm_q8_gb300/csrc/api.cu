@@ -156,6 +156,23 @@ int make_act_tmap(CUtensorMap* map, const void* act_a, int64_t lpad, int64_t k, 
   return DLLM_OK;
 }
 
+// Tensor map over f16 planes [planes][rows][cols] (row-major), boxes of 64 columns x box_rows
+// rows of one plane, 128-byte swizzle (the K-major operand layout of the tensor cores); rows past
+// `rows` read as zeros.
+int make_planes_tmap(CUtensorMap* map, const void* base, int64_t planes, int64_t rows, int64_t cols, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return fail(DLLM_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)(rows * cols * 2)};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DLLM_E_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return DLLM_OK;
+}
+
 // ---------------------------------------------------------------------------------------------
 // Weight packing (GGUF AoS blocks -> tile-major blobs + scale plane)
 // ---------------------------------------------------------------------------------------------

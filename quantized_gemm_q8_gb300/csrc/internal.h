@@ -32,6 +32,7 @@ int64_t act_rows_padded(int64_t rows);
 // Tensor map over the A-plane of an act buffer (3-D: 64 x lpad x k/64, f16, 128-byte swizzle,
 // box 64 x nt x 1).
 int make_act_tmap(CUtensorMap* map, const void* act_a, int64_t lpad, int64_t k, int nt);
+int make_planes_tmap(CUtensorMap* map, const void* base, int64_t planes, int64_t rows, int64_t cols, int box_rows);
 
 // GEMM launch plan.
 struct QgemmPlan {

@@ -58,14 +58,24 @@ __global__ void embed_q4k_kernel(const uint8_t* __restrict__ table, int nsb, con
   }
 }
 
+// x = hi + lo for a pair of f32 values, packed as two f16x2 words
+__device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x, y);
+  const __half2 l = __floats2half2_rn(x - __low2float(h), y - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // Q, K, V of one layer from the split-K partials of the Q|K and V projections: the splits are
 // summed in split order, RoPE rotates adjacent pairs of Q and K within each head (position =
-// row), Q is also scaled by 1/sqrt(hd). Out: QKV [L][3d] f32 (Q, K, V side by side). One thread
-// per output pair, all partial loads of a thread issued together.
+// row), Q is also scaled by 1/sqrt(hd). Out: QKV [L][3d] f32 (Q, K, V side by side), or, when
+// `planes` is set (the tensor-core attention), six f16 planes [Qhi, Qlo, Khi, Klo, Vhi, Vlo][L][d]
+// with x = hi + lo. One thread per output pair, all partial loads of a thread issued together.
 __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __restrict__ Pqk, int Sqk,
                                                               const float* __restrict__ Pv, int Sv,
                                                               const float2* __restrict__ cs, int L, int d, int hd,
-                                                              float qscale, float* __restrict__ QKV) {
+                                                              float qscale, float* __restrict__ QKV,
+                                                              __half* __restrict__ planes) {
   griddep_wait();
   griddep_launch();
   const int64_t npair = (int64_t)L * (3 * d / 2);
@@ -95,7 +105,15 @@ __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __res
       a.y += v.y;
     }
   }
-  *reinterpret_cast<float2*>(QKV + (int64_t)p * 3 * d + c) = a;
+  if (planes) {
+    const int which = c / d, col = c % d;
+    uint32_t hi, lo;
+    split2(a.x, a.y, hi, lo);
+    *reinterpret_cast<uint32_t*>(planes + ((int64_t)(2 * which) * L + p) * d + col) = hi;
+    *reinterpret_cast<uint32_t*>(planes + ((int64_t)(2 * which + 1) * L + p) * d + col) = lo;
+  } else {
+    *reinterpret_cast<float2*>(QKV + (int64_t)p * 3 * d + c) = a;
+  }
 }
 
 // Non-causal multi-head attention O = softmax(q k^T) v per head on the reduced QKV ([L][3d],
@@ -233,6 +251,242 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
     }
   }
   griddep_launch();
+}
+
+// Tensor-core attention for canvases of up to TA_KEYS tokens. CTA (head, 128 queries), 8 warps;
+// warp w serves TMEM lane quarter w % 4 (query rows 32 (w % 4) ..) and half w / 4 of the columns.
+// Operands are f16 head/tail pairs x = hi + lo (qkv_reduce_rope_kernel writes the planes):
+//   Q, K    by TMA (128-byte swizzle, the K-major layout of the GEMM's activation operand),
+//           keys past L read as zeros;
+//   V^T     by a register transpose of the V planes into the no-swizzle K-major layout
+//           (core matrices of 8 rows x 16 bytes, 128 bytes apart along K, 8-row groups SBO apart).
+// One thread issues S = Q K^T (24 MMAs: M 128, N 160, K 16 x 8, terms hi*hi + hi*lo + lo*hi)
+// into TMEM; each row's softmax is exact (the two column halves meet through shared memory);
+// P goes back as head/tail planes over Q and K; O = P V (30 MMAs: M 128, N 128, K 16 x 10) and
+// each row is written unnormalized with (m, l) as the single chunk of attn_merge_quant_kernel.
+// The three-term products carry each product to ~2^-22 relative, far below the f32
+// accumulation's own rounding. Values must stay inside the f16 range.
+constexpr int TA_M = 128, TA_KEYS = 160, TA_HD = 128, TA_THREADS = 256, TA_BOXR = 32;
+constexpr int TA_ATOM_Q = TA_M * 128;                 // one 64-dim swizzled atom column of Q rows
+constexpr int TA_ATOM_K = TA_KEYS * 128;              // ... of K rows
+constexpr int TA_SBO_P = (TA_KEYS / 8) * 128;         // 8-row group stride of P (K = keys)
+constexpr int TA_SBO_V = (TA_KEYS / 8) * 128 + 16;    // ... of V^T, padded: spreads the staging stores
+constexpr int TA_VPL = (TA_HD / 8) * TA_SBO_V;        // one V^T plane
+constexpr int TA_PPL = (TA_M / 8) * TA_SBO_P;         // one P plane
+// Q[hl][atom] at (2 hl + atom) TA_ATOM_Q; K[hl][atom] after them; V^T hi, lo last
+constexpr int TA_OFF_Q = 0, TA_OFF_K = 4 * TA_ATOM_Q, TA_OFF_VH = TA_OFF_K + 4 * TA_ATOM_K;
+constexpr int TA_OFF_VL = TA_OFF_VH + TA_VPL;
+constexpr int TA_OFF_PH = 0, TA_OFF_PL = TA_PPL;      // P overwrites Q and K once S is complete
+constexpr int TA_OFF_RED = TA_OFF_PL + TA_PPL;        // row max / sum exchange, also over K
+constexpr int TA_OP = TA_HD + 4;                      // padded O row (floats) for the write-back
+constexpr int TA_SMEM = TA_OFF_VL + TA_VPL + 1024;    // + slack to align the base to 1024
+constexpr uint32_t TA_TX = (4 * TA_M + 4 * TA_KEYS) * 128;  // TMA bytes of Q and K
+static_assert(TA_OFF_RED + 2 * 2 * TA_M * 4 <= TA_OFF_VH, "P and the exchange fit over Q and K");
+static_assert(TA_M * TA_OP * 4 <= TA_OFF_RED, "O staging fits over the P planes");
+static_assert(TA_ATOM_Q % 1024 == 0 && TA_ATOM_K % 1024 == 0, "swizzle atoms 1024-byte aligned");
+static_assert(TA_SMEM + 64 <= 232448, "shared memory budget");
+constexpr int TA_COLS = 512;                          // S at columns [0, 160), O at [160, 288)
+
+__global__ void __launch_bounds__(TA_THREADS, 1)
+    attention_tc_kernel(const __grid_constant__ CUtensorMap qk_map, const __half* __restrict__ planes, AttPart part,
+                        int L, int d, int heads, int* err) {
+  extern __shared__ uint8_t ta_raw[];
+  __shared__ uint64_t ta_bar[3];
+  __shared__ uint32_t ta_tmem;
+  // 1024-byte aligned base (the swizzled operands), by offset from the shared array
+  uint8_t* ta_smem = ta_raw + ((1024u - (smem_u32(ta_raw) & 1023u)) & 1023u);
+  float(*ta_red)[2][TA_M] = reinterpret_cast<float(*)[2][TA_M]>(ta_smem + TA_OFF_RED);  // [max|sum][half][row]
+  const int h = blockIdx.x, q0 = blockIdx.y * TA_M;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qd = warp & 3, ch = warp >> 2, row = 32 * qd + lane;
+  const uint32_t sbase = smem_u32(ta_smem);
+  const uint32_t bar_in = smem_u32(&ta_bar[0]), bar_s = smem_u32(&ta_bar[1]), bar_o = smem_u32(&ta_bar[2]);
+  if (threadIdx.x == 0) {
+    mbar_init(bar_in, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    fence_barrier_init();
+    prefetch_tensormap(&qk_map);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&ta_tmem), TA_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  griddep_wait();  // the planes are the preceding kernel's output
+  if (threadIdx.x == 0) {
+    // Q (planes 0, 1) rows q0.., K (planes 2, 3) rows 0..: boxes of 64 dims x 32 rows
+    mbar_expect_tx(bar_in, TA_TX);
+#pragma unroll 1
+    for (int hl = 0; hl < 2; ++hl)
+#pragma unroll 1
+      for (int a = 0; a < 2; ++a) {
+        for (int b = 0; b < TA_M / TA_BOXR; ++b)
+          tma_g2s_3d(sbase + TA_OFF_Q + (2 * hl + a) * TA_ATOM_Q + b * TA_BOXR * 128, &qk_map, h * TA_HD + 64 * a,
+                     q0 + b * TA_BOXR, hl, bar_in);
+        for (int b = 0; b < TA_KEYS / TA_BOXR; ++b)
+          tma_g2s_3d(sbase + TA_OFF_K + (2 * hl + a) * TA_ATOM_K + b * TA_BOXR * 128, &qk_map, h * TA_HD + 64 * a,
+                     b * TA_BOXR, 2 + hl, bar_in);
+      }
+  }
+  // V^T (rows = dims, K = keys) by a register transpose of the V planes: item = (key pair, block
+  // of 8 dims), all of a thread's loads in flight, then (key, key + 1) pairs per 4-byte store
+  {
+    const int64_t pl = (int64_t)L * d;
+    constexpr int NIT = (TA_KEYS / 2) * (TA_HD / 8), PER = NIT / TA_THREADS;
+    static_assert(NIT % TA_THREADS == 0, "V^T staging split");
+    uint4 vh[PER][2], vl[PER][2];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int i = threadIdx.x + u * TA_THREADS;
+      const int k0 = 2 * (i / (TA_HD / 8)), nb = i % (TA_HD / 8);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        vh[u][e] = vl[u][e] = make_uint4(0u, 0u, 0u, 0u);
+        if (k0 + e < L) {
+          const __half* src = planes + (int64_t)(k0 + e) * d + h * TA_HD + 8 * nb;
+          vh[u][e] = *reinterpret_cast<const uint4*>(src + 4 * pl);
+          vl[u][e] = *reinterpret_cast<const uint4*>(src + 5 * pl);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int i = threadIdx.x + u * TA_THREADS;
+      const int k0 = 2 * (i / (TA_HD / 8)), nb = i % (TA_HD / 8);
+      const uint32_t* h0 = reinterpret_cast<const uint32_t*>(&vh[u][0]);
+      const uint32_t* h1 = reinterpret_cast<const uint32_t*>(&vh[u][1]);
+      const uint32_t* l0 = reinterpret_cast<const uint32_t*>(&vl[u][0]);
+      const uint32_t* l1 = reinterpret_cast<const uint32_t*>(&vl[u][1]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {  // dim 8 nb + e: key k0 in the low half, k0 + 1 in the high half
+        const int sh = 16 * (e & 1);
+        const uint32_t hw = ((h0[e >> 1] >> sh) & 0xFFFFu) | (((h1[e >> 1] >> sh) & 0xFFFFu) << 16);
+        const uint32_t lw = ((l0[e >> 1] >> sh) & 0xFFFFu) | (((l1[e >> 1] >> sh) & 0xFFFFu) << 16);
+        const int o = nb * TA_SBO_V + (k0 >> 3) * 128 + e * 16 + (k0 & 7) * 2;
+        *reinterpret_cast<uint32_t*>(ta_smem + TA_OFF_VH + o) = hw;
+        *reinterpret_cast<uint32_t*>(ta_smem + TA_OFF_VL + o) = lw;
+      }
+    }
+  }
+  fence_proxy_async();  // V^T is read by the tensor core
+  __syncthreads();
+  griddep_launch();
+  const uint32_t tmem = ta_tmem;
+  volatile int never = 0;
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    ok = mbar_wait(bar_in, 0, &never, kDefaultTimeoutCycles);
+    tc_fence_after();
+    constexpr uint32_t IDS = idesc_f16(TA_M, TA_KEYS);
+#pragma unroll 1
+    for (int kk = 0; kk < TA_HD / 16 && ok; ++kk) {
+      const int a = kk >> 2;
+      const uint32_t ko = (uint32_t)(kk & 3) * 32;  // K advance inside the 128-byte swizzled row
+      const uint64_t qh = desc_sw128(sbase + TA_OFF_Q + (0 + a) * TA_ATOM_Q + ko);
+      const uint64_t ql = desc_sw128(sbase + TA_OFF_Q + (2 + a) * TA_ATOM_Q + ko);
+      const uint64_t kh = desc_sw128(sbase + TA_OFF_K + (0 + a) * TA_ATOM_K + ko);
+      const uint64_t kl = desc_sw128(sbase + TA_OFF_K + (2 + a) * TA_ATOM_K + ko);
+      mma_f16(tmem, qh, kh, IDS, kk > 0);
+      mma_f16(tmem, qh, kl, IDS, 1);
+      mma_f16(tmem, ql, kh, IDS, 1);
+    }
+    mma_commit(bar_s);  // arrives even when the inputs timed out, so the waits below end
+  }
+  // this thread's row, its column half of S: keys [80 ch, 80 ch + 80)
+  ok = __all_sync(0xffffffffu, mbar_wait(bar_s, 0, &never, kDefaultTimeoutCycles));
+  tc_fence_after();
+  const uint32_t trow = tmem + ((uint32_t)(32 * qd) << 16);
+  constexpr int HK = TA_KEYS / 2;
+  float m = -INFINITY, l = 0.f;
+  {
+    uint32_t sv[HK];
+#pragma unroll
+    for (int c = 0; c < HK / 16; ++c) tmem_ld16(trow + HK * ch + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(sv + 16 * c));
+    tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < HK; ++k)
+      if (HK * ch + k < L) m = fmaxf(m, __uint_as_float(sv[k]));
+    ta_red[0][ch][row] = m;
+    __syncthreads();
+    m = fmaxf(ta_red[0][0][row], ta_red[0][1][row]);  // key 0 is real, so m is finite
+    // p = e^(s - m) as 2^((s - m) log2 e) (exp2f: 2 ulp)
+    constexpr float LOG2E = 1.4426950408889634f;
+    const float ml2 = m * LOG2E;
+#pragma unroll
+    for (int c = 0; c < HK / 8; ++c) {
+      float pv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int k = HK * ch + 8 * c + e;
+        pv[e] = k < L ? exp2f(fmaf(__uint_as_float(sv[8 * c + e]), LOG2E, -ml2)) : 0.f;
+        l += pv[e];
+      }
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split2(pv[2 * e], pv[2 * e + 1], hi[e], lo[e]);
+      const int o = (row >> 3) * TA_SBO_P + (HK / 8 * ch + c) * 128 + (row & 7) * 16;
+      *reinterpret_cast<uint4*>(ta_smem + TA_OFF_PH + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(ta_smem + TA_OFF_PL + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    ta_red[1][ch][row] = l;
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  l = ta_red[1][0][row] + ta_red[1][1][row];
+  if (threadIdx.x == 0) {
+    constexpr uint32_t IDO = idesc_f16(TA_M, TA_HD);
+#pragma unroll 1
+    for (int kk = 0; kk < TA_KEYS / 16 && ok; ++kk) {
+      const uint32_t ko = (uint32_t)kk * 256;
+      const uint64_t ph = desc_noswz(sbase + TA_OFF_PH + ko, 128, TA_SBO_P);
+      const uint64_t pl = desc_noswz(sbase + TA_OFF_PL + ko, 128, TA_SBO_P);
+      const uint64_t vh = desc_noswz(sbase + TA_OFF_VH + ko, 128, TA_SBO_V);
+      const uint64_t vl = desc_noswz(sbase + TA_OFF_VL + ko, 128, TA_SBO_V);
+      mma_f16(tmem + TA_KEYS, ph, vh, IDO, kk > 0);
+      mma_f16(tmem + TA_KEYS, ph, vl, IDO, 1);
+      mma_f16(tmem + TA_KEYS, pl, vh, IDO, 1);
+    }
+    mma_commit(bar_o);
+  }
+  ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_o, 0, &never, kDefaultTimeoutCycles));
+  tc_fence_after();
+  // O through shared memory (rows padded to TA_OP floats, over the finished P planes), then out
+  // row-contiguously: this thread's row, its half of the dims; all lanes load from TMEM
+  const int q = q0 + row;
+  {
+    float* os = reinterpret_cast<float*>(ta_smem);
+    uint32_t ov[TA_HD / 2];
+#pragma unroll
+    for (int c = 0; c < TA_HD / 32; ++c)
+      tmem_ld16(trow + TA_KEYS + (TA_HD / 2) * ch + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(ov + 16 * c));
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < TA_HD / 2; e += 4)
+      *reinterpret_cast<uint4*>(os + row * TA_OP + (TA_HD / 2) * ch + e) = make_uint4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
+    if (ok && ch == 0 && q < L) *reinterpret_cast<float2*>(part.ml + ((int64_t)q * heads + h) * 2) = make_float2(m, l);
+    __syncthreads();
+    if (ok) {
+      float* dst = part.acc + (int64_t)q0 * d + h * TA_HD;
+#pragma unroll 4
+      for (int i = threadIdx.x; i < TA_M * (TA_HD / 4); i += TA_THREADS) {
+        const int r = i / (TA_HD / 4), c4 = i % (TA_HD / 4);
+        if (q0 + r < L)
+          *reinterpret_cast<float4*>(dst + (int64_t)r * d + 4 * c4) = *reinterpret_cast<const float4*>(os + r * TA_OP + 4 * c4);
+      }
+    }
+  }
+  if (!ok && threadIdx.x == 0) atomicOr(err, ERR_TIMEOUT_OTHER);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TA_COLS);
+  }
 }
 
 // Merge the key chunks of the attention and quantize the output to Q8_K in one pass: warp
@@ -496,21 +750,38 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
     if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wqk, 2 * d, Pqk, S.qk, s))) return rc;
     if ((rc = gemm(DLLM_Q6_K, actd, L, d, Ly.wv, d, Pv, S.v, s))) return rc;
     if (full) {
+      // Q, K, V: f32 rows for the chunked attention, or (short canvases) the f16 head/tail planes
+      // of the tensor-core attention, in the same bytes
+      const bool tc_att = L <= TA_KEYS;
       float* QKV = reinterpret_cast<float*>(ws + S.qkv);
+      __half* planes = tc_att ? reinterpret_cast<__half*>(ws + S.qkv) : nullptr;
       const int64_t npair = L * (3 * d / 2);
       cudaError_t e = launch_pdl(qkv_reduce_rope_kernel, dim3((unsigned)((npair + 255) / 256)), dim3(256), 0, s,
                                  (const float*)Pqk, S.qk.splits, (const float*)Pv, S.v.splits,
                                  reinterpret_cast<const float2*>(ws + S.rope), (int)L, d, hd, 1.0f / sqrtf((float)hd),
-                                 QKV);
+                                 QKV, planes);
       note_launch();
       if (e != cudaSuccess) return cuda_fail(e, "launch qkv reduce");
-      const int nchunk = (int)((L + ATT_KC - 1) / ATT_KC);
       const AttPart ap{reinterpret_cast<float*>(ws + S.att), reinterpret_cast<float*>(ws + S.attml)};
-      e = cudaFuncSetAttribute(attention_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
-      const dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB), (unsigned)nchunk);
-      e = launch_pdl(attention_partial_kernel, ag, dim3(ATT_THREADS), ATT_SMEM, s, (const float*)QKV, ap, (int)L, d,
-                     m->n_heads);
+      int nchunk = 1;
+      if (tc_att) {  // whole rows per CTA on the tensor cores
+        int* err = err_word();
+        if (!err) return fail(DLLM_E_CUDA, "cannot resolve the device error word");
+        CUtensorMap qk_map;
+        if ((rc = make_planes_tmap(&qk_map, planes, 6, L, d, TA_BOXR))) return rc;
+        e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TA_SMEM);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
+        const dim3 ag(m->n_heads, (unsigned)((L + TA_M - 1) / TA_M));
+        e = launch_pdl(attention_tc_kernel, ag, dim3(TA_THREADS), TA_SMEM, s, qk_map, (const __half*)planes, ap,
+                       (int)L, d, m->n_heads, err);
+      } else {  // longer canvases: chunks of 32 keys, merged below
+        nchunk = (int)((L + ATT_KC - 1) / ATT_KC);
+        e = cudaFuncSetAttribute(attention_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
+        const dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB), (unsigned)nchunk);
+        e = launch_pdl(attention_partial_kernel, ag, dim3(ATT_THREADS), ATT_SMEM, s, (const float*)QKV, ap, (int)L,
+                       d, m->n_heads);
+      }
       note_launch();
       const dim3 mg((unsigned)act_rows_padded(L), (unsigned)((d / QK + 7) / 8));
       if (e == cudaSuccess)
