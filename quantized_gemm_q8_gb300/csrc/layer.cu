@@ -70,7 +70,7 @@ __device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t&
 // summed in split order, RoPE rotates adjacent pairs of Q and K within each head (position =
 // row), Q is also scaled by 1/sqrt(hd). Out: QKV [L][3d] f32 (Q, K, V side by side), or, when
 // `planes` is set (the tensor-core attention), six f16 planes [Qhi, Qlo, Khi, Klo, Vhi, Vlo][L][d]
-// with x = hi + lo. One thread per output pair, all partial loads of a thread issued together.
+// with x = hi + lo. All partial loads of a thread are issued together.
 __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __restrict__ Pqk, int Sqk,
                                                               const float* __restrict__ Pv, int Sv,
                                                               const float2* __restrict__ cs, int L, int d, int hd,
@@ -78,41 +78,48 @@ __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __res
                                                               __half* __restrict__ planes) {
   griddep_wait();
   griddep_launch();
-  const int64_t npair = (int64_t)L * (3 * d / 2);
+  // one thread per 4 consecutive columns (two RoPE pairs): 16-byte partial loads
+  const int64_t nquad = (int64_t)L * (3 * d / 4);
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (i >= npair) return;
-  const int p = (int)(i / (3 * d / 2)), c = 2 * (int)(i % (3 * d / 2));  // row, column in [Q | K | V]
-  float2 a = make_float2(0.f, 0.f);
+  if (i >= nquad) return;
+  const int p = (int)(i / (3 * d / 4)), c = 4 * (int)(i % (3 * d / 4));  // row, column in [Q | K | V]
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
   if (c < 2 * d) {
     const float* src = Pqk + (int64_t)p * 2 * d + c;
     const int64_t st = (int64_t)L * 2 * d;
 #pragma unroll 4
     for (int sp = 0; sp < Sqk; ++sp) {
-      const float2 v = *reinterpret_cast<const float2*>(src + sp * st);
+      const float4 v = *reinterpret_cast<const float4*>(src + sp * st);
       a.x += v.x;
       a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
     }
-    const float2 r = cs[p * (hd / 2) + (c % hd) / 2];
+    const float2 r0 = cs[p * (hd / 2) + (c % hd) / 2], r1 = cs[p * (hd / 2) + (c % hd) / 2 + 1];
     const float sc = c < d ? qscale : 1.f;
-    a = make_float2((a.x * r.x - a.y * r.y) * sc, (a.x * r.y + a.y * r.x) * sc);
+    a = make_float4((a.x * r0.x - a.y * r0.y) * sc, (a.x * r0.y + a.y * r0.x) * sc, (a.z * r1.x - a.w * r1.y) * sc,
+                    (a.z * r1.y + a.w * r1.x) * sc);
   } else {
     const float* src = Pv + (int64_t)p * d + (c - 2 * d);
     const int64_t st = (int64_t)L * d;
 #pragma unroll 4
     for (int sp = 0; sp < Sv; ++sp) {
-      const float2 v = *reinterpret_cast<const float2*>(src + sp * st);
+      const float4 v = *reinterpret_cast<const float4*>(src + sp * st);
       a.x += v.x;
       a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
     }
   }
   if (planes) {
     const int which = c / d, col = c % d;
-    uint32_t hi, lo;
-    split2(a.x, a.y, hi, lo);
-    *reinterpret_cast<uint32_t*>(planes + ((int64_t)(2 * which) * L + p) * d + col) = hi;
-    *reinterpret_cast<uint32_t*>(planes + ((int64_t)(2 * which + 1) * L + p) * d + col) = lo;
+    uint32_t h0, l0, h1, l1;
+    split2(a.x, a.y, h0, l0);
+    split2(a.z, a.w, h1, l1);
+    *reinterpret_cast<uint2*>(planes + ((int64_t)(2 * which) * L + p) * d + col) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(planes + ((int64_t)(2 * which + 1) * L + p) * d + col) = make_uint2(l0, l1);
   } else {
-    *reinterpret_cast<float2*>(QKV + (int64_t)p * 3 * d + c) = a;
+    *reinterpret_cast<float4*>(QKV + (int64_t)p * 3 * d + c) = a;
   }
 }
 
@@ -755,8 +762,8 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
       const bool tc_att = L <= TA_KEYS;
       float* QKV = reinterpret_cast<float*>(ws + S.qkv);
       __half* planes = tc_att ? reinterpret_cast<__half*>(ws + S.qkv) : nullptr;
-      const int64_t npair = L * (3 * d / 2);
-      cudaError_t e = launch_pdl(qkv_reduce_rope_kernel, dim3((unsigned)((npair + 255) / 256)), dim3(256), 0, s,
+      const int64_t nquad = L * (3 * d / 4);
+      cudaError_t e = launch_pdl(qkv_reduce_rope_kernel, dim3((unsigned)((nquad + 255) / 256)), dim3(256), 0, s,
                                  (const float*)Pqk, S.qk.splits, (const float*)Pv, S.v.splits,
                                  reinterpret_cast<const float2*>(ws + S.rope), (int)L, d, hd, 1.0f / sqrtf((float)hd),
                                  QKV, planes);
