@@ -751,13 +751,19 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           }
         }
       } else if (p.y != nullptr && grow < p.n) {
+        // two uniform branches: a plain store must not wait for a read of the old value
         float* dst = p.y + (size_t)sp * p.split_stride + grow;
+        if (p.accumulate) {
 #pragma unroll
-        for (int j = 0; j < NC; ++j) {
-          const int tok = tokb + j;
-          if (tok < p.m) {
-            float* o = dst + (size_t)tok * p.ldy;
-            *o = p.accumulate ? *o + acc[j] : acc[j];
+          for (int j = 0; j < NC; ++j) {
+            const int tok = tokb + j;
+            if (tok < p.m) dst[(size_t)tok * p.ldy] += acc[j];
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < NC; ++j) {
+            const int tok = tokb + j;
+            if (tok < p.m) dst[(size_t)tok * p.ldy] = acc[j];
           }
         }
       }
