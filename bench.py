@@ -401,6 +401,146 @@ def run_only_kernel(args):
                       "note": "weights L2-resident after the first launch (single copy): a profiling target"}))
 
 
+def run_configs(args):
+    """One JSON line per configuration other than the step (config 4, the default run): the
+    single Q4_K GEMM (config 1), the layer stream at L = 148 (2), the masked-rows LM head + commit
+    (3) and the canvas-length sweep of the layer stream (5), each against its roofline, and the
+    CPU oracle timed on configs 1-3."""
+    import numpy as np
+    import torch
+
+    import quantized_gemm_q8_gb300 as dl
+    from quantized_gemm_q8_gb300 import synth
+
+    torch.cuda.set_device(0)
+    peaks, peak_src = _peaks()
+    hbm, tens = peaks["hbm_gbs"], peaks["bf16_tflops"]
+    stream = torch.cuda.Stream()
+    lines = []
+
+    def timed(fn, reps):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        dl.check(stream)
+        return e0.elapsed_time(e1) / reps
+
+    # ---- config 1: quantize 16 x 4096 + Q4_K GEMM 4096 x 4096, 16 weight copies (151 MB) rotated
+    m1, n1, k1 = 16, 4096, 4096
+    seed1 = synth.config_seed(1)
+    wblk = synth.blocks(dl.Q4_K, seed1, n1, k1)
+    copies = [dl.pack_weights(dl.Q4_K, torch.from_numpy(wblk.reshape(-1)).cuda(), n1, k1) for _ in range(16)]
+    x1 = torch.from_numpy(synth.activations(seed1, m1, k1)).cuda()
+    act1 = torch.empty(dl.act_bytes(m1, k1), dtype=torch.uint8, device="cuda")
+    y1 = torch.empty((m1, n1), dtype=torch.float32, device="cuda")
+    ws1 = torch.empty(max(dl.qgemm_workspace_bytes(dl.Q4_K, m1, n1, k1), 1), dtype=torch.uint8, device="cuda")
+    per_graph = 64
+    with torch.cuda.stream(stream):
+        for i in range(3):  # warm-up, also loads the kernels
+            dl.quantize_act(x1, plain=False, act=act1, stream=stream)
+            dl.qgemm(dl.Q4_K, act1, m1, k1, copies[i % 16], n1, y=y1, ws=ws1, stream=stream)
+    torch.cuda.synchronize()
+    dl.check(stream)
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=stream):
+        for i in range(per_graph):
+            dl.quantize_act(x1, plain=False, act=act1, stream=stream)
+            dl.qgemm(dl.Q4_K, act1, m1, k1, copies[i % 16], n1, y=y1, ws=ws1, stream=stream)
+    g1.replay()
+    ms1 = timed(g1.replay, 8) / per_graph
+    bytes1 = n1 * k1 // 256 * 144 + m1 * (k1 + k1 // 256 * 4 + k1 // 16 * 2) + m1 * n1 * 4
+    ln1 = {"config": 1, "workload": "quantize 16x4096 + Q4_K GEMM 4096x4096 -> 16x4096 f32", "value": ms1 * 1e3,
+           "unit": "us/GEMM", "launch": f"CUDA graph of {per_graph} back-to-back calls, 16 weight copies rotated",
+           "roofline": {"bound": "hbm", "achieved": bytes1 / (ms1 * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                        "frac": bytes1 / (ms1 * 1e-3) / 1e9 / hbm, "algorithmic_bytes": bytes1},
+           "tops": 2.0 * m1 * n1 * k1 / (ms1 * 1e-3) / 1e12}
+    lines.append(ln1)
+    del copies, g1
+
+    # ---- configs 2 and 5: the layer stream (no attention) over a 4-layer model (560 MB of weights)
+    dims = dict(synth.LLADA, n_layers=4)
+    seed2 = synth.config_seed(2)
+    model = dl.model_from_seed(dims, seed2)
+    d, f = dims["d_model"], dims["d_ff"]
+    wbytes_layer = (4 * d * d + 2 * d * f) // 256 * 144 + (d * d + d * f) // 256 * 210
+    for L in (148, 32, 512, 2048):
+        x0 = torch.from_numpy(synth.activations(seed2 if L == 148 else synth.config_seed(5) + L, L, d)).cuda()
+        x = x0.clone()
+        ws = torch.empty(dl.step_workspace_bytes(model, L, dl.STREAM_LINEAR) + 1024, dtype=torch.uint8, device="cuda")
+
+        def run_stream():
+            x.copy_(x0, non_blocking=True)
+            dl.step_linear_stream(model, x, dl.STREAM_LINEAR, ws=ws, stream=stream)
+
+        run_stream()
+        reps = 20 if L <= 512 else 6
+        ms = timed(run_stream, reps) / dims["n_layers"]
+        ops = 2.0 * L * (4 * d * d + 3 * d * f)
+        t_roof = max(ops / (tens * 1e12), wbytes_layer / (hbm * 1e9)) * 1e3
+        bound = "tensor" if ops / (tens * 1e12) >= wbytes_layer / (hbm * 1e9) else "hbm"
+        lines.append({"config": 2 if L == 148 else 5, "workload": f"LLaDA-8B layer stream (no attention), L={L}",
+                      "value": ms, "unit": "ms/layer", "tops": ops / (ms * 1e-3) / 1e12,
+                      "roofline": {"bound": bound, "t_roof_ms": t_roof, "frac": t_roof / ms,
+                                   "peak": {"tensor_tflops": tens, "hbm_gbs": hbm}},
+                      "note": "per layer of a 4-layer pass; the input copy (L x 4096 f32) is inside the timed region"})
+    del model
+
+    # ---- config 3: masked-rows LM head 126464 x 4096 Q6_K + softmax confidence + top-4 commit
+    dims3 = dict(synth.LLADA)
+    seed3 = synth.config_seed(3)
+    head = synth.head_weights(seed3, dims3)
+    vocab = dims3["vocab"]
+    w_out = dl.pack_weights(dl.Q6_K, torch.from_numpy(head["w_out"].reshape(-1)).cuda(), vocab, d)
+    out_norm = torch.from_numpy(head["out_norm"]).cuda()
+    canvas0 = torch.from_numpy(synth.canvas(seed3)).cuda()
+    canvas = canvas0.clone()
+    hidden = torch.from_numpy(synth.activations(seed3, L_CANVAS, d)).cuda()
+    b0, b1 = PROMPT, PROMPT + BLOCK
+    ws3 = torch.empty(max(dl.lmhead_workspace_bytes(b1 - b0, vocab, d), 1), dtype=torch.uint8, device="cuda")
+
+    def run_head():
+        canvas.copy_(canvas0, non_blocking=True)
+        dl.lmhead_masked_select(hidden, canvas, dims3["mask_id"], b0, b1, K_COMMIT, out_norm, w_out, vocab,
+                                dims3["eps"], ws=ws3, stream=stream)
+
+    run_head()
+    ms3 = timed(run_head, 20)
+    bytes3 = vocab * d // 256 * 210
+    lines.append({"config": 3, "workload": "masked-rows LM head 126464x4096 Q6_K (32 block rows) + confidence + top-4",
+                  "value": ms3 * 1e3, "unit": "us/call",
+                  "roofline": {"bound": "hbm", "achieved": bytes3 / (ms3 * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                               "frac": bytes3 / (ms3 * 1e-3) / 1e9 / hbm, "algorithmic_bytes": bytes3}})
+
+    if not args.no_cpu_baseline:
+        import oracle as orc
+
+        t0 = time.perf_counter()
+        q, dq, _ = orc.quantize_q8k(synth.activations(seed1, m1, k1))
+        orc.qgemm(dl.Q4_K, wblk, q, dq)
+        ln1["cpu_baseline"] = {"value": 1e3 * (time.perf_counter() - t0), "unit": "ms/GEMM",
+                               "cores": orc.num_threads(), "kind": "oracle", "sample": "the whole config"}
+        lw = synth.layer_weights(seed2, 0, dims)
+        xa = np.asarray(synth.activations(seed2, L_CANVAS, d), np.float64)
+        t0 = time.perf_counter()
+        orc.layer(lw, xa, dims, attention_on=False)
+        lines[1]["cpu_baseline"] = {"value": 1e3 * (time.perf_counter() - t0), "unit": "ms/layer",
+                                    "cores": orc.num_threads(), "kind": "oracle", "sample": "one layer at L=148"}
+        cv = synth.canvas(seed3)
+        t0 = time.perf_counter()
+        orc.lmhead_commit(np.asarray(hidden.cpu().numpy(), np.float64), cv, dims3["mask_id"], b0, b1, K_COMMIT,
+                          head["out_norm"], head["w_out"], dims3["eps"])
+        lines[-1]["cpu_baseline"] = {"value": 1e3 * (time.perf_counter() - t0), "unit": "ms/call",
+                                     "cores": orc.num_threads(), "kind": "oracle", "sample": "the whole config"}
+    for ln in lines:
+        ln["peak_source"] = peak_src
+        print(json.dumps(ln), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,10 +550,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only-kernel", choices=sorted(ONLY_KERNELS) + ["layer_full"], default=None,
                     help="time one GEMM of the step alone (profiling target) instead of the step")
+    ap.add_argument("--configs", action="store_true",
+                    help="one JSON line per other configuration (1, 2, 3, 5) instead of the step")
     args = ap.parse_args()
     rank, local_rank, world = _env_dist()
     if args.only_kernel:
         run_only_kernel(args)
+    elif args.configs:
+        run_configs(args)
     elif args.impl == "reference":
         run_reference(args, rank)
     else:
