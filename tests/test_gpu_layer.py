@@ -168,6 +168,14 @@ def test_denoise_step_small_two_steps():
     print(f"denoise small: {exact}/2 steps with commits identical to the oracle's order")
 
 
+@pytest.mark.parametrize("L", [129, 160, 200])
+def test_denoise_step_small_canvas_edges(L):
+    # 129: a second 128-query tile holding one row; 160: the largest canvas of the tensor-core
+    # attention; 200: the chunked f32 attention and its multi-chunk merge
+    exact = _full_step_check(SMALL, 43 + L, L, 8, 40, 4, n_steps=1)
+    print(f"denoise small L={L}: {exact}/1 steps with commits identical to the oracle's order")
+
+
 def test_denoise_step_llada_shapes_two_layers():
     dims = dict(synth.LLADA, n_layers=2)
     exact = _full_step_check(dims, synth.config_seed(4), 148, 20, 52, 4, n_steps=2)
