@@ -511,10 +511,46 @@ def run_configs(args):
     run_head()
     ms3 = timed(run_head, 20)
     bytes3 = vocab * d // 256 * 210
-    lines.append({"config": 3, "workload": "masked-rows LM head 126464x4096 Q6_K (32 block rows) + confidence + top-4",
-                  "value": ms3 * 1e3, "unit": "us/call",
-                  "roofline": {"bound": "hbm", "achieved": bytes3 / (ms3 * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
-                               "frac": bytes3 / (ms3 * 1e-3) / 1e9 / hbm, "algorithmic_bytes": bytes3}})
+    ln3 = {"config": 3, "workload": "masked-rows LM head 126464x4096 Q6_K (32 block rows) + confidence + top-4",
+           "value": ms3 * 1e3, "unit": "us/call",
+           "roofline": {"bound": "hbm", "achieved": bytes3 / (ms3 * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                        "frac": bytes3 / (ms3 * 1e-3) / 1e9 / hbm, "algorithmic_bytes": bytes3}}
+    lines.append(ln3)
+
+    # ---- the same head over every masked position of the canvas (block = the whole canvas,
+    # 148 rows of which 128 masked): the tensor work per weight byte grows 4.6x
+    ws3b = torch.empty(max(dl.lmhead_workspace_bytes(L_CANVAS, vocab, d), 1), dtype=torch.uint8, device="cuda")
+
+    def run_head_all():
+        canvas.copy_(canvas0, non_blocking=True)
+        dl.lmhead_masked_select(hidden, canvas, dims3["mask_id"], 0, L_CANVAS, K_COMMIT, out_norm, w_out, vocab,
+                                dims3["eps"], ws=ws3b, stream=stream)
+
+    run_head_all()
+    ms3b = timed(run_head_all, 20)
+    flops3b = 2.0 * L_CANVAS * vocab * d
+    t_roof3b = max(bytes3 / (hbm * 1e9), flops3b / (tens * 1e12)) * 1e3
+    lines.append({"config": "3-all", "workload": "LM head over every masked position: 126464x4096 Q6_K, block = whole "
+                  "canvas (148 rows, 128 masked) + confidence + top-4",
+                  "value": ms3b * 1e3, "unit": "us/call", "tops": flops3b / (ms3b * 1e-3) / 1e12,
+                  "roofline": {"bound": "tensor" if flops3b / (tens * 1e12) > bytes3 / (hbm * 1e9) else "hbm",
+                               "t_roof_ms": t_roof3b, "frac": t_roof3b / ms3b,
+                               "peak": {"tensor_tflops": tens, "hbm_gbs": hbm}}})
+
+    # ---- the same, ranked by entropy (Dream's ranking): one more partial per (tile, row)
+    def run_head_ent():
+        canvas.copy_(canvas0, non_blocking=True)
+        dl.lmhead_select(hidden, canvas, dims3["mask_id"], 0, L_CANVAS, K_COMMIT, out_norm, w_out, vocab,
+                         dl.CONF_NEG_ENTROPY, dims3["eps"], ws=ws3b, stream=stream)
+
+    run_head_ent()
+    ms3e = timed(run_head_ent, 20)
+    lines.append({"config": "3-all-entropy", "workload": "LM head over every masked position ranked by entropy: "
+                  "126464x4096 Q6_K, block = whole canvas (148 rows, 128 masked) + -entropy + top-4",
+                  "value": ms3e * 1e3, "unit": "us/call", "tops": flops3b / (ms3e * 1e-3) / 1e12,
+                  "roofline": {"bound": "tensor" if flops3b / (tens * 1e12) > bytes3 / (hbm * 1e9) else "hbm",
+                               "t_roof_ms": t_roof3b, "frac": t_roof3b / ms3e,
+                               "peak": {"tensor_tflops": tens, "hbm_gbs": hbm}}})
 
     if not args.no_cpu_baseline:
         import oracle as orc
@@ -534,7 +570,7 @@ def run_configs(args):
         t0 = time.perf_counter()
         orc.lmhead_commit(np.asarray(hidden.cpu().numpy(), np.float64), cv, dims3["mask_id"], b0, b1, K_COMMIT,
                           head["out_norm"], head["w_out"], dims3["eps"])
-        lines[-1]["cpu_baseline"] = {"value": 1e3 * (time.perf_counter() - t0), "unit": "ms/call",
+        ln3["cpu_baseline"] = {"value": 1e3 * (time.perf_counter() - t0), "unit": "ms/call",
                                      "cores": orc.num_threads(), "kind": "oracle", "sample": "the whole config"}
     for ln in lines:
         ln["peak_source"] = peak_src

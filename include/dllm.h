@@ -176,6 +176,26 @@ DLLM_API int dllm_qgemm_intsums(int type, const void* act, int64_t m, int64_t k,
  * 256-byte aligned. Errors: DLLM_E_SHAPE, DLLM_E_INVAL (block range, k_commit), DLLM_E_ALIGN,
  * DLLM_E_WORKSPACE. */
 DLLM_API size_t dllm_lmhead_workspace_bytes(int64_t rows, int64_t vocab, int64_t d);
+
+/* Confidence used to rank the masked positions (dllm_lmhead_select):
+ *   DLLM_CONF_PMAX        softmax probability of the argmax token, 1 / sum_v exp(l_v - l_max)
+ *                         (LLaDA's low-confidence remasking: mojo-dllm "Each model's own sampler");
+ *   DLLM_CONF_NEG_ENTROPY minus the entropy of the row's softmax, sum_v p_v log p_v (natural log;
+ *                         Dream's entropy ranking, same page, and the "entropy" primitive of the
+ *                         sampling section). Committed tokens are the argmax in both (greedy).
+ * Like p_max, the fused epilogue reduces it on the fly: per partial it also keeps
+ * t = sum exp(l - m)(l - m), and -H = t / s - log s for the merged s = sum exp(l - l_max). */
+enum { DLLM_CONF_PMAX = 0, DLLM_CONF_NEG_ENTROPY = 1 };
+
+/* dllm_lmhead_select: dllm_lmhead_masked_select with the confidence chosen by conf_kind
+ * (DLLM_CONF_PMAX or DLLM_CONF_NEG_ENTROPY; anything else is DLLM_E_INVAL). out_conf and
+ * row_conf then hold that confidence. The block may be the whole canvas (every masked
+ * position, R up to 160). Same arguments, ownership and errors as below. */
+DLLM_API int dllm_lmhead_select(const float* hidden, int64_t L, int64_t d, int64_t ldh, const float* out_norm_w,
+                                float eps, const void* w_out_packed, int64_t vocab, int32_t* canvas, int32_t mask_id,
+                                int32_t block_begin, int32_t block_end, int32_t k_commit, int32_t conf_kind,
+                                int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id, float* row_conf,
+                                void* ws, size_t ws_bytes, dllm_stream_t stream);
 DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d, int64_t ldh, const float* out_norm_w,
                                        float eps, const void* w_out_packed, int64_t vocab, int32_t* canvas,
                                        int32_t mask_id, int32_t block_begin, int32_t block_end, int32_t k_commit,

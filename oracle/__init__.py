@@ -76,6 +76,7 @@ def _load():
                 "orc_swiglu": ([P, P, I64, P], None),
                 "orc_embed_q4k": ([P, I64, I64, P, I64, P], C.c_int),
                 "orc_row_confidence": ([P, I64, I64, P, P, P, P], None),
+                "orc_row_neg_entropy": ([P, I64, I64, P], None),
                 "orc_commit_topk": ([P, I64, I32, I64, I64, P, P, I64, P, P], C.c_int),
                 "orc_transfer_counts": ([I64, I64, P], None),
             }
@@ -252,6 +253,15 @@ def row_confidence(logits: np.ndarray):
     return ids, conf, t1, t2
 
 
+def row_neg_entropy(logits: np.ndarray) -> np.ndarray:
+    """Minus the entropy (natural log) of each row's softmax, f64: the entropy-ranking confidence."""
+    l = _c(logits, np.float64)
+    r, v = l.shape
+    out = np.empty(r, np.float64)
+    _load().orc_row_neg_entropy(_p(l), r, v, _p(out))
+    return out
+
+
 def commit_topk(canvas: np.ndarray, mask_id: int, b0: int, b1: int, conf_by_pos, ids_by_pos, k: int):
     """Commit in place; returns (positions, ids) in selection order."""
     cv = np.ascontiguousarray(canvas, np.int32)
@@ -322,8 +332,13 @@ def lmhead_logits(hidden_rows, out_norm, w_out, eps=1e-5):
     return qgemm(TYPE_Q6_K, w_out, q, d)
 
 
-def lmhead_commit(hidden, canvas, mask_id, b0, b1, k, out_norm, w_out, eps=1e-5):
-    """Masked-rows-only LM head + softmax confidence + top-k commit (canvas updated in place).
+CONF_PMAX, CONF_NEG_ENTROPY = 0, 1
+
+
+def lmhead_commit(hidden, canvas, mask_id, b0, b1, k, out_norm, w_out, eps=1e-5, conf_kind=CONF_PMAX):
+    """Masked-rows-only LM head + confidence + top-k commit (canvas updated in place). The
+    confidence is the argmax token's softmax probability (CONF_PMAX, LLaDA) or minus the
+    softmax entropy (CONF_NEG_ENTROPY, Dream's ranking); the committed token is the argmax.
 
     Returns dict(pos, id, conf, rows, ids_rows, conf_rows, top1, top2)."""
     rows = np.array([p for p in range(b0, b1) if canvas[p] == mask_id], dtype=np.int64)
@@ -334,6 +349,8 @@ def lmhead_commit(hidden, canvas, mask_id, b0, b1, k, out_norm, w_out, eps=1e-5)
     if rows.size:
         logits = lmhead_logits(np.asarray(hidden, np.float64)[rows], out_norm, w_out, eps)
         ids, conf, t1, t2 = row_confidence(logits)
+        if conf_kind == CONF_NEG_ENTROPY:
+            conf = row_neg_entropy(logits)
         conf_pos[rows] = conf
         ids_pos[rows] = ids
         res.update(ids_rows=ids, conf_rows=conf, top1=t1, top2=t2)

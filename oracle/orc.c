@@ -23,7 +23,10 @@
  *   - Development plan, "Model facts": RMSNorm eps 1e-5, RoPE theta 500000
  *     (adjacent-pair / NORM form), 32 x 128 MHA, non-causal, SwiGLU FFN.
  *   - Technical specification, section 12 (diffusion loop) and section 14
- *     (sampling primitives): softmax confidence, top-k selection, scatter.
+ *     (sampling primitives): softmax confidence, entropy, top-k selection,
+ *     scatter.
+ *   - README, "Each model's own sampler": LLaDA ranks masked positions by
+ *     the argmax token's probability, Dream by entropy.
  *   - README, "How it works": the LM head runs only on the masked positions
  *     of the current block.
  * The GGUF byte layouts of Q4_K / Q6_K are the public GGUF formats that the
@@ -444,6 +447,31 @@ void orc_row_confidence(const double* logits, int64_t rows, int64_t vocab,
     conf[r] = 1.0 / den;
     if (top1) top1[r] = b1;
     if (top2) top2[r] = b2;
+  }
+}
+
+/* ---------------------------------------------------------------------------
+ * Entropy of the softmax of one row of logits (f64, natural log), straight
+ * from its definition: p_v = exp(l_v) / sum_u exp(l_u) (computed with the row
+ * maximum subtracted, which leaves p unchanged), H = -sum_v p_v log p_v, with
+ * 0 log 0 = 0. neg_entropy[r] = -H is the confidence of the entropy ranking
+ * (README, "Each model's own sampler": Dream's entropy ranking).
+ * ------------------------------------------------------------------------- */
+void orc_row_neg_entropy(const double* logits, int64_t rows, int64_t vocab, double* neg_entropy) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    const double* l = logits + r * vocab;
+    double mx = l[0];
+    for (int64_t v = 1; v < vocab; ++v)
+      if (l[v] > mx) mx = l[v];
+    double den = 0.0;
+    for (int64_t v = 0; v < vocab; ++v) den += exp(l[v] - mx);
+    double h = 0.0;
+    for (int64_t v = 0; v < vocab; ++v) {
+      const double p = exp(l[v] - mx) / den;
+      if (p > 0.0) h -= p * log(p);
+    }
+    neg_entropy[r] = -h;
   }
 }
 

@@ -51,6 +51,8 @@ _SIGS = {
     "dllm_lmhead_workspace_bytes": ([I64, I64, I64], SZ),
     "dllm_lmhead_masked_select": ([P, I64, I64, I64, P, F32, P, I64, P, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P],
                                   INT),
+    "dllm_lmhead_select": ([P, I64, I64, I64, P, F32, P, I64, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P],
+                           INT),
     "dllm_step_workspace_bytes": ([P, I64, INT], SZ),
     "dllm_step_linear_stream": ([P, P, I64, P, INT, P, SZ, P], INT),
     "dllm_denoise_workspace_bytes": ([P, I64, I32], SZ),
@@ -212,11 +214,24 @@ def lmhead_workspace_bytes(rows: int, vocab: int, d: int) -> int:
     return int(lib().dllm_lmhead_workspace_bytes(rows, vocab, d))
 
 
+CONF_PMAX = 0         # confidence = softmax probability of the argmax token (LLaDA)
+CONF_NEG_ENTROPY = 1  # confidence = -entropy of the row's softmax (Dream's entropy ranking)
+
+
 def lmhead_masked_select(hidden: torch.Tensor, canvas: torch.Tensor, mask_id: int, block_begin: int,
                          block_end: int, k_commit: int, out_norm_w: torch.Tensor, w_out_packed: torch.Tensor,
                          vocab: int, eps: float = 1e-5, ws: torch.Tensor | None = None, stream=None) -> dict:
     """Masked-rows-only LM head + softmax confidence + top-k commit; updates `canvas` in place.
     Returns dict(pos, id, conf [k_commit], row_id, row_conf [block rows])."""
+    return lmhead_select(hidden, canvas, mask_id, block_begin, block_end, k_commit, out_norm_w, w_out_packed, vocab,
+                         CONF_PMAX, eps, ws, stream)
+
+
+def lmhead_select(hidden: torch.Tensor, canvas: torch.Tensor, mask_id: int, block_begin: int, block_end: int,
+                  k_commit: int, out_norm_w: torch.Tensor, w_out_packed: torch.Tensor, vocab: int,
+                  conf_kind: int = CONF_PMAX, eps: float = 1e-5, ws: torch.Tensor | None = None,
+                  stream=None) -> dict:
+    """lmhead_masked_select with the confidence chosen by conf_kind (CONF_PMAX, CONF_NEG_ENTROPY)."""
     L, d = hidden.shape
     R = block_end - block_begin
     dev = hidden.device
@@ -230,11 +245,10 @@ def lmhead_masked_select(hidden: torch.Tensor, canvas: torch.Tensor, mask_id: in
     nb = lmhead_workspace_bytes(R, vocab, d)
     if ws is None:
         ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
-    _ok(lib().dllm_lmhead_masked_select(_ptr(hidden), L, d, hidden.stride(0), _ptr(out_norm_w), eps,
-                                        _ptr(w_out_packed), vocab, _ptr(canvas), mask_id, block_begin, block_end,
-                                        k_commit, _ptr(out["pos"]), _ptr(out["id"]), _ptr(out["conf"]),
-                                        _ptr(out["row_id"]), _ptr(out["row_conf"]), _ptr(ws), ws.numel(),
-                                        _stream(stream)))
+    _ok(lib().dllm_lmhead_select(_ptr(hidden), L, d, hidden.stride(0), _ptr(out_norm_w), eps, _ptr(w_out_packed),
+                                 vocab, _ptr(canvas), mask_id, block_begin, block_end, k_commit, conf_kind,
+                                 _ptr(out["pos"]), _ptr(out["id"]), _ptr(out["conf"]), _ptr(out["row_id"]),
+                                 _ptr(out["row_conf"]), _ptr(ws), ws.numel(), _stream(stream)))
     for key in ("pos", "id", "conf"):
         out[key] = out[key][:k_commit]
     return out

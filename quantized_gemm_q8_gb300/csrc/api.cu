@@ -315,6 +315,7 @@ struct SoftPart {
   float m;  // max logit
   int a;    // its token id (lowest on ties)
   float s;  // sum exp(logit - m)
+  float t;  // sum exp(logit - m) (logit - m), for the entropy
 };
 
 __device__ __forceinline__ SoftPart soft_merge(SoftPart x, SoftPart y) {
@@ -323,40 +324,48 @@ __device__ __forceinline__ SoftPart soft_merge(SoftPart x, SoftPart y) {
     x = y;
     y = t;
   }
-  // x has the larger max (or the lower id at equal max)
-  x.s = x.s + (y.s == 0.f ? 0.f : y.s * expf(y.m - x.m));
+  // x has the larger max (or the lower id at equal max); y's sums move to x's max:
+  // exp(l - x.m) = f exp(l - y.m) and l - x.m = (l - y.m) + (y.m - x.m), f = exp(y.m - x.m)
+  if (y.s != 0.f) {
+    const float f = expf(y.m - x.m);
+    x.t = x.t + f * (y.t + (y.m - x.m) * y.s);
+    x.s = x.s + y.s * f;
+  }
   return x;
 }
 
 // Merge and commit, one launch: CTA r (256 threads) merges row r's P partials (contiguous,
-// [R][P]) into (argmax id, p_max = 1 / sum exp(l - l_max)) and stores them; the CTA that
+// [R][P]) into the argmax id and the row's confidence, and stores them; the CTA that
 // finishes last (a counter, zeroed before the launch) picks the k masked positions of the
 // block with the highest confidence (ties: lowest position) and scatters their ids into the
-// canvas.
+// canvas. Confidence: kind 0 p_max = 1 / sum exp(l - l_max); kind 1 the negative entropy
+// -H = sum p log p = t / s - log s with s = sum exp(l - l_max), t = sum exp(l - l_max)(l - l_max)
+// (pent holds the t partials; unused for kind 0).
 __global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
-    const float* __restrict__ pmax, const int* __restrict__ parg, const float* __restrict__ psum, int P, int R,
-    int32_t* canvas, int32_t mask_id, int b0, int k, int32_t* out_pos, int32_t* out_id, float* out_conf,
-    int32_t* row_id, float* row_conf, float* conf_ws, int* id_ws, unsigned int* done) {
+    const float* __restrict__ pmax, const int* __restrict__ parg, const float* __restrict__ psum,
+    const float* __restrict__ pent, int kind, int P, int R, int32_t* canvas, int32_t mask_id, int b0, int k,
+    int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id, float* row_conf, float* conf_ws, int* id_ws,
+    unsigned int* done) {
   __shared__ SoftPart red[8];
   __shared__ bool last;
   griddep_wait();
   griddep_launch();
   const int r = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  SoftPart acc{-INFINITY, 0x7fffffff, 0.f};
+  SoftPart acc{-INFINITY, 0x7fffffff, 0.f, 0.f};
   const size_t base = (size_t)r * P;
   for (int i = threadIdx.x; i < P; i += blockDim.x)
-    acc = soft_merge(acc, SoftPart{pmax[base + i], parg[base + i], psum[base + i]});
+    acc = soft_merge(acc, SoftPart{pmax[base + i], parg[base + i], psum[base + i], kind ? pent[base + i] : 0.f});
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     SoftPart o{__shfl_xor_sync(0xffffffffu, acc.m, off), __shfl_xor_sync(0xffffffffu, acc.a, off),
-               __shfl_xor_sync(0xffffffffu, acc.s, off)};
+               __shfl_xor_sync(0xffffffffu, acc.s, off), __shfl_xor_sync(0xffffffffu, acc.t, off)};
     acc = soft_merge(acc, o);
   }
   if (lane == 0) red[warp] = acc;
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int w = 1; w < 8; ++w) acc = soft_merge(acc, red[w]);
-    const float c = 1.0f / acc.s;  // softmax probability of the argmax token
+    const float c = kind ? acc.t / acc.s - logf(acc.s) : 1.0f / acc.s;
     conf_ws[r] = c;
     id_ws[r] = acc.a;
     if (row_id) row_id[r] = acc.a;
@@ -368,7 +377,7 @@ __global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
   if (!last || warp != 0) return;
   __threadfence();
   for (int step = 0; step < k; ++step) {
-    float best = -1.f;
+    float best = -INFINITY;  // below every confidence (p_max > 0, -entropy >= -log vocab)
     int bp = 0x7fffffff;
     for (int q = lane; q < R; q += 32) {
       const volatile float* cv = conf_ws;
@@ -413,7 +422,7 @@ __global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
 }
 
 struct LmheadWs {
-  size_t act, pmax, parg, psum, conf, id, done, bytes;
+  size_t act, pmax, parg, psum, pent, conf, id, done, bytes;
   int P;
 };
 static LmheadWs lmhead_ws(int64_t R, int64_t vocab, int64_t d) {
@@ -424,7 +433,8 @@ static LmheadWs lmhead_ws(int64_t R, int64_t vocab, int64_t d) {
   w.pmax = align_up(act_layout(R, d).bytes, 256);
   w.parg = w.pmax + align_up((size_t)w.P * R * 4, 256);
   w.psum = w.parg + align_up((size_t)w.P * R * 4, 256);
-  w.conf = w.psum + align_up((size_t)w.P * R * 4, 256);
+  w.pent = w.psum + align_up((size_t)w.P * R * 4, 256);
+  w.conf = w.pent + align_up((size_t)w.P * R * 4, 256);
   w.id = w.conf + align_up((size_t)R * 4, 256);
   w.done = w.id + align_up((size_t)R * 4, 256);
   w.bytes = w.done + 256;
@@ -642,6 +652,7 @@ int launch_gemm(const GemmLaunch& g, const QgemmPlan& P, cudaStream_t stream) {
   prm.pmax = g.pmax;
   prm.parg = g.parg;
   prm.psum = g.psum;
+  prm.pent = g.pent;
   prm.dbg = g.dbg;
   prm.dbg_mode = g.dbg_mode;
   prm.timeout = kDefaultTimeoutCycles;
@@ -765,20 +776,23 @@ DLLM_API size_t dllm_lmhead_workspace_bytes(int64_t rows, int64_t vocab, int64_t
   return lmhead_ws(rows, vocab, d).bytes;
 }
 
-DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d, int64_t ldh, const float* out_norm_w,
-                                       float eps, const void* w_out_packed, int64_t vocab, int32_t* canvas,
-                                       int32_t mask_id, int32_t block_begin, int32_t block_end, int32_t k_commit,
-                                       int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id,
-                                       float* row_conf, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+DLLM_API int dllm_lmhead_select(const float* hidden, int64_t L, int64_t d, int64_t ldh, const float* out_norm_w,
+                                float eps, const void* w_out_packed, int64_t vocab, int32_t* canvas, int32_t mask_id,
+                                int32_t block_begin, int32_t block_end, int32_t k_commit, int32_t conf_kind,
+                                int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id, float* row_conf,
+                                void* ws, size_t ws_bytes, dllm_stream_t stream) {
   const int64_t R = (int64_t)block_end - block_begin;
   if (L <= 0 || d <= 0 || d % QK || d > (1 << 20) || ldh < d || vocab <= 0 || vocab > (1 << 24))
-    return fail(DLLM_E_SHAPE, "dllm_lmhead_masked_select: bad shape L=%lld d=%lld ldh=%lld vocab=%lld", (long long)L,
+    return fail(DLLM_E_SHAPE, "dllm_lmhead_select: bad shape L=%lld d=%lld ldh=%lld vocab=%lld", (long long)L,
                 (long long)d, (long long)ldh, (long long)vocab);
   if (block_begin < 0 || block_end > L || R <= 0 || R > 160)
-    return fail(DLLM_E_INVAL, "dllm_lmhead_masked_select: block [%d, %d) must lie in [0, L=%lld) and hold 1..160 positions",
+    return fail(DLLM_E_INVAL, "dllm_lmhead_select: block [%d, %d) must lie in [0, L=%lld) and hold 1..160 positions",
                 block_begin, block_end, (long long)L);
   if (k_commit < 0 || k_commit > R)
-    return fail(DLLM_E_INVAL, "dllm_lmhead_masked_select: k_commit=%d must be in [0, %lld]", k_commit, (long long)R);
+    return fail(DLLM_E_INVAL, "dllm_lmhead_select: k_commit=%d must be in [0, %lld]", k_commit, (long long)R);
+  if (conf_kind != DLLM_CONF_PMAX && conf_kind != DLLM_CONF_NEG_ENTROPY)
+    return fail(DLLM_E_INVAL, "dllm_lmhead_select: conf_kind=%d must be DLLM_CONF_PMAX (0) or DLLM_CONF_NEG_ENTROPY (1)",
+                conf_kind);
   int rc = check_device();
   if (rc) return rc;
   CHECK_DEV(hidden, "hidden");
@@ -792,15 +806,15 @@ DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d
   if (row_id) CHECK_DEV(row_id, "row_id");
   if (row_conf) CHECK_DEV(row_conf, "row_conf");
   CHECK_DEV(out_norm_w, "out_norm_w");
-  if (!aligned(out_norm_w, 16)) return fail(DLLM_E_ALIGN, "dllm_lmhead_masked_select: out_norm_w must be 16-byte aligned");
+  if (!aligned(out_norm_w, 16)) return fail(DLLM_E_ALIGN, "dllm_lmhead_select: out_norm_w must be 16-byte aligned");
   if (!aligned(hidden, 16) || ldh % 4 || !aligned(w_out_packed, 256))
-    return fail(DLLM_E_ALIGN, "dllm_lmhead_masked_select: hidden 16-byte aligned with ldh %% 4 == 0, w_out_packed 256-byte aligned");
+    return fail(DLLM_E_ALIGN, "dllm_lmhead_select: hidden 16-byte aligned with ldh %% 4 == 0, w_out_packed 256-byte aligned");
   const LmheadWs W = lmhead_ws(R, vocab, d);
   if (!ws || ws_bytes < W.bytes)
-    return fail(DLLM_E_WORKSPACE, "dllm_lmhead_masked_select: workspace has %zu bytes, needs %zu", ws ? ws_bytes : (size_t)0,
+    return fail(DLLM_E_WORKSPACE, "dllm_lmhead_select: workspace has %zu bytes, needs %zu", ws ? ws_bytes : (size_t)0,
                 W.bytes);
   CHECK_DEV(ws, "ws");
-  if (!aligned(ws, 256)) return fail(DLLM_E_ALIGN, "dllm_lmhead_masked_select: ws must be 256-byte aligned");
+  if (!aligned(ws, 256)) return fail(DLLM_E_ALIGN, "dllm_lmhead_select: ws must be 256-byte aligned");
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* base = static_cast<uint8_t*>(ws);
   // 1) RMSNorm + Q8_K of the block's rows (contiguous in the residual stream)
@@ -811,6 +825,7 @@ DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d
   GemmLaunch g{DLLM_Q6_K, base + W.act, R, d, w_out_packed, vocab, nullptr, 0, 0, nullptr, 1,
                reinterpret_cast<float*>(base + W.pmax), reinterpret_cast<int*>(base + W.parg),
                reinterpret_cast<float*>(base + W.psum), nullptr};
+  g.pent = conf_kind == DLLM_CONF_NEG_ENTROPY ? reinterpret_cast<float*>(base + W.pent) : nullptr;
   rc = launch_gemm(g, P, s);
   if (rc) return rc;
   // 3) merge, confidence, top-k commit
@@ -819,12 +834,24 @@ DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d
   if (e != cudaSuccess) return cuda_fail(e, "zero the merge counter");
   e = launch_pdl(lmhead_merge_commit_kernel, dim3((unsigned)R), dim3(256), 0, s,
                  reinterpret_cast<const float*>(base + W.pmax), reinterpret_cast<const int*>(base + W.parg),
-                 reinterpret_cast<const float*>(base + W.psum), W.P, (int)R, canvas, mask_id, (int)block_begin,
+                 reinterpret_cast<const float*>(base + W.psum), reinterpret_cast<const float*>(base + W.pent),
+                 (int)conf_kind, W.P, (int)R, canvas, mask_id, (int)block_begin,
                  (int)k_commit, out_pos, out_id, out_conf, row_id, row_conf, reinterpret_cast<float*>(base + W.conf),
                  reinterpret_cast<int*>(base + W.id), done);
   note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch lmhead_merge_commit");
+}
+
+
+DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d, int64_t ldh, const float* out_norm_w,
+                                       float eps, const void* w_out_packed, int64_t vocab, int32_t* canvas,
+                                       int32_t mask_id, int32_t block_begin, int32_t block_end, int32_t k_commit,
+                                       int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id,
+                                       float* row_conf, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  return dllm_lmhead_select(hidden, L, d, ldh, out_norm_w, eps, w_out_packed, vocab, canvas, mask_id, block_begin,
+                            block_end, k_commit, DLLM_CONF_PMAX, out_pos, out_id, out_conf, row_id, row_conf, ws,
+                            ws_bytes, stream);
 }
 
 

@@ -80,6 +80,7 @@ struct GemmLaunch {
   float* psum;
   int32_t* dbg;
   int dbg_mode;
+  float* pent;  // mode 1: optional entropy partials
 };
 int launch_gemm(const GemmLaunch& g, const QgemmPlan& P, cudaStream_t stream);
 size_t packed_blob_bytes(int type, int64_t n, int64_t k);

@@ -164,11 +164,13 @@ struct QgemmParams {
   int* err;      // device error word
   // mode 1 (LM head): instead of y, per (weight tile, TMEM lane quadrant, token) softmax
   // partials over the 32 weight rows of the quadrant: max logit, its row (lowest on ties),
-  // and sum_rows exp(logit - max); layout [m][tiles_n * 4].
+  // sum_rows exp(logit - max) and (pent, optional) sum_rows exp(logit - max) (logit - max);
+  // layout [m][tiles_n * 4].
   int mode;
   float* pmax;
   int* parg;
   float* psum;
+  float* pent;
 #ifdef DLLM_TRACE
   unsigned long long* trace;  // per-role clock64 stamps of CTA 0 (trace builds only)
 #endif
@@ -739,15 +741,22 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
               idx = oi;
             }
           }
-          float ex = grow < p.n ? expf(acc[j] - v) : 0.f;
+          const float dl = acc[j] - v;
+          float ex = grow < p.n ? expf(dl) : 0.f;
+          float tx = grow < p.n ? ex * dl : 0.f;  // for the entropy: sum exp(l - max) (l - max)
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) ex += __shfl_xor_sync(0xffffffffu, ex, off);
+          if (p.pent != nullptr) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) tx += __shfl_xor_sync(0xffffffffu, tx, off);
+          }
           const int tok = tokb + j;
           if (lane == 0 && tok < p.m) {
             const size_t o = (size_t)tok * (p.tiles_n * 4) + tn * 4 + qd;
             p.pmax[o] = v;
             p.parg[o] = idx;
             p.psum[o] = ex;
+            if (p.pent != nullptr) p.pent[o] = tx;
           }
         }
       } else if (p.y != nullptr && grow < p.n) {

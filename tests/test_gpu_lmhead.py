@@ -1,7 +1,8 @@
 """GPU parity of the masked-rows-only LM head, softmax confidence and top-k commit.
 
-Bars: argmax ids and committed (position, id) pairs bit-exact; confidences within 1e-4
-relative. Logits are f32 on the GPU and f64 in the oracle, so an id can only legitimately
+Bars: argmax ids and committed (position, id) pairs bit-exact; p_max confidences within 1e-4
+relative, negative entropies within 2e-4 absolute (they are differences of O(log vocab) terms)
+except for rows whose Q8_K re-quantization lands on a rounding tie (see _run). Logits are f32 on the GPU and f64 in the oracle, so an id can only legitimately
 differ where the oracle's top-1 / top-2 logit gap is below the logit error; such rows are
 reported with their gap instead of failing (the seeded inputs used here have none).
 """
@@ -16,7 +17,7 @@ from quantized_gemm_q8_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 
-def _run(vocab, d, L, b0, b1, k, masked, seed, hidden_scale=1.0):
+def _run(vocab, d, L, b0, b1, k, masked, seed, hidden_scale=1.0, conf_kind=dl.CONF_PMAX):
     w = synth.q6k_blocks(seed, vocab, d)
     hidden = (synth.activations(seed + 1, L, d) * hidden_scale).astype(np.float32)
     norm_w = (1.0 + 0.1 * synth.activations(seed + 2, 1, d)[0]).astype(np.float32)
@@ -24,11 +25,11 @@ def _run(vocab, d, L, b0, b1, k, masked, seed, hidden_scale=1.0):
     mask_id = 7 if vocab < 1000 else synth.LLADA["mask_id"]
     canvas[masked] = mask_id
     ref_canvas = canvas.copy()
-    ref = orc.lmhead_commit(hidden, ref_canvas, mask_id, b0, b1, k, norm_w, w)
+    ref = orc.lmhead_commit(hidden, ref_canvas, mask_id, b0, b1, k, norm_w, w, conf_kind=conf_kind)
     pk = dl.pack_weights(dl.Q6_K, torch.from_numpy(w.reshape(-1)).cuda(), vocab, d)
     gcanvas = torch.from_numpy(canvas.copy()).cuda()
-    out = dl.lmhead_masked_select(torch.from_numpy(hidden).cuda(), gcanvas, mask_id, b0, b1, k,
-                                  torch.from_numpy(norm_w).cuda(), pk, vocab)
+    out = dl.lmhead_select(torch.from_numpy(hidden).cuda(), gcanvas, mask_id, b0, b1, k,
+                           torch.from_numpy(norm_w).cuda(), pk, vocab, conf_kind)
     dl.check()
     # per-row argmax / confidence for the masked rows the oracle computed
     rows = ref["rows"] - b0
@@ -38,7 +39,18 @@ def _run(vocab, d, L, b0, b1, k, masked, seed, hidden_scale=1.0):
         mism = np.nonzero(gid != ref["ids_rows"])[0]
         gaps = (ref["top1"] - ref["top2"])[mism]
         assert mism.size == 0, f"argmax differs at rows {rows[mism] + b0} with top-2 gaps {gaps}"
-        np.testing.assert_allclose(gconf, ref["conf_rows"], rtol=1e-4)
+        if conf_kind == dl.CONF_PMAX:
+            np.testing.assert_allclose(gconf, ref["conf_rows"], rtol=1e-4)
+        else:
+            # -entropy from f32 partials (t / s - log s, both terms O(log vocab)) agrees to 2e-4.
+            # A few rows may differ more: the head re-quantizes each row to Q8_K after an f32
+            # RMSNorm whose summation order differs from the oracle's, so a code that sits on a
+            # rounding tie can land one step apart (a few % of 4096-long rows). One code step
+            # moves every logit of the row by d_a * |w| (~1e-3 here) and the entropy by about
+            # as much; such rows are held to 5e-3 and to at most 5 % of the rows.
+            err = np.abs(gconf - ref["conf_rows"])
+            loose = err > 2e-4 + 1e-5 * np.abs(ref["conf_rows"])
+            assert err.max() <= 5e-3 and loose.sum() <= max(1, rows.size // 20), (err.max(), np.nonzero(loose))
     n = ref["pos"].size
     np.testing.assert_array_equal(out["pos"].cpu().numpy()[:n], ref["pos"])
     np.testing.assert_array_equal(out["id"].cpu().numpy()[:n], ref["id"])
@@ -68,3 +80,43 @@ def test_lmhead_full_llada_head():
     masked[20:] = True
     ref = _run(vocab, d, L, 20, 52, 4, masked, synth.config_seed(3))
     assert ref["pos"].size == 4
+
+
+def test_lmhead_every_masked_position():
+    # the head over the whole canvas (block = [0, L), R = 148 rows, 128 of them masked): the
+    # every-masked-position form of the same fused head, on the 160-token tile
+    L, d, vocab = 148, 4096, 126464
+    masked = np.zeros(L, bool)
+    masked[20:] = True
+    ref = _run(vocab, d, L, 0, L, 4, masked, synth.config_seed(3) + 7)
+    assert ref["pos"].size == 4 and ref["rows"].size == 128
+
+
+def test_lmhead_entropy_ranking_small():
+    # Dream's entropy ranking on a ragged vocabulary (1000 rows): the hidden scale spreads the
+    # rows' entropies so that the ranking is decided well above the f32 error
+    L, d, vocab = 40, 512, 1000
+    masked = np.zeros(L, bool)
+    masked[[8, 9, 11, 20, 21, 22, 30, 39]] = True
+    ref = _run(vocab, d, L, 8, 40, 4, masked, 13, hidden_scale=3.0, conf_kind=dl.CONF_NEG_ENTROPY)
+    assert ref["pos"].size == 4
+
+
+def test_lmhead_entropy_every_masked_position():
+    # the entropy ranking over every masked position of a LLaDA-8B-shaped canvas (128 masked of
+    # 148 rows, 126464 x 4096 Q6_K head)
+    L, d, vocab = 148, 4096, 126464
+    masked = np.zeros(L, bool)
+    masked[20:] = True
+    ref = _run(vocab, d, L, 0, L, 4, masked, synth.config_seed(3) + 9, conf_kind=dl.CONF_NEG_ENTROPY)
+    assert ref["pos"].size == 4 and ref["rows"].size == 128
+
+
+def test_lmhead_rejects_unknown_conf_kind():
+    L, d, vocab = 8, 256, 300
+    hidden = torch.zeros((L, d), device="cuda")
+    canvas = torch.zeros(L, dtype=torch.int32, device="cuda")
+    pk = dl.pack_weights(dl.Q6_K, torch.from_numpy(synth.q6k_blocks(1, vocab, d).reshape(-1)).cuda(), vocab, d)
+    with pytest.raises(RuntimeError, match="conf_kind"):
+        dl.lmhead_select(hidden, canvas, 7, 0, L, 2, torch.ones(d, device="cuda"), pk, vocab, 5)
+

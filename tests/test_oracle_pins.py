@@ -398,6 +398,44 @@ def test_commit_tiny_handworked():
     assert pos.tolist() == [0, 1]  # equal confidence -> lowest positions first
 
 
+def test_neg_entropy_closed_forms():
+    # uniform over V tokens: H = log V; two equal logits far above the rest: H = log 2; one
+    # logit 60 above 999 others: H = 999 e^-60 (60 + 1) to first order (below 1e-20)
+    V = 1000
+    ne = orc.row_neg_entropy(np.vstack([np.full(V, 0.37), np.r_[[3.0, 3.0], np.full(V - 2, -1e4)],
+                                        np.r_[[60.0], np.zeros(V - 1)]]))
+    np.testing.assert_allclose(ne[:2], [-math.log(V), -math.log(2.0)], rtol=1e-13)
+    assert -1e-20 < ne[2] <= 0.0
+
+
+def test_neg_entropy_matches_library_and_is_shift_invariant():
+    scipy_special = pytest.importorskip("scipy.special")
+    scipy_stats = pytest.importorskip("scipy.stats")
+    rng = np.random.default_rng(7)
+    logits = rng.normal(0.0, 3.0, size=(5, 777))
+    ref = -scipy_stats.entropy(scipy_special.softmax(logits, axis=1), axis=1)  # natural log
+    ne = orc.row_neg_entropy(logits)
+    np.testing.assert_allclose(ne, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(orc.row_neg_entropy(logits + 123.5), ne, rtol=1e-12, atol=1e-12)
+    assert np.all(ne <= 0.0) and np.all(ne >= -math.log(777) - 1e-12)
+
+
+def test_entropy_ranking_commit_order():
+    # the entropy ranking commits the most peaked rows first: one-hot-like < 2-way < 4-way
+    V = 16
+    rows = np.full((4, V), -1e4)
+    rows[0, :4] = 0.0          # uniform over 4
+    rows[1, 5] = 0.0           # one token
+    rows[2, [1, 9]] = 0.0      # uniform over 2
+    rows[3, :] = 0.0           # uniform over 16
+    ids, _, _, _ = orc.row_confidence(rows)
+    conf = orc.row_neg_entropy(rows)
+    canvas = np.array([7, 7, 7, 7], np.int32)
+    pos, tid = orc.commit_topk(canvas, 7, 0, 4, conf, ids, 3)
+    assert pos.tolist() == [1, 2, 0] and tid.tolist() == [5, 1, 0]
+    assert canvas.tolist() == [0, 5, 1, 7]
+
+
 def test_commit_invariants_random():
     rng = np.random.default_rng(3)
     L, mask = 148, 126336
