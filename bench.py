@@ -517,6 +517,20 @@ def run_configs(args):
                         "frac": bytes3 / (ms3 * 1e-3) / 1e9 / hbm, "algorithmic_bytes": bytes3}}
     lines.append(ln3)
 
+    # ---- config 3 with temperature sampling (T = 0.8): Gumbel-max draws in the same epilogue
+    def run_head_sample():
+        canvas.copy_(canvas0, non_blocking=True)
+        dl.lmhead_select(hidden, canvas, dims3["mask_id"], b0, b1, K_COMMIT, out_norm, w_out, vocab, dl.CONF_PMAX,
+                         dims3["eps"], ws=ws3, stream=stream, temperature=0.8, seed=42, step=0)
+
+    run_head_sample()
+    ms3s = timed(run_head_sample, 20)
+    lines.append({"config": "3-sample", "workload": "config 3 with temperature 0.8: Gumbel-max draws from counter-based "
+                  "SplitMix64 noise in the head's epilogue + probability of the draw + top-4",
+                  "value": ms3s * 1e3, "unit": "us/call",
+                  "roofline": {"bound": "hbm", "achieved": bytes3 / (ms3s * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                               "frac": bytes3 / (ms3s * 1e-3) / 1e9 / hbm, "algorithmic_bytes": bytes3}})
+
     # ---- the same head over every masked position of the canvas (block = the whole canvas,
     # 148 rows of which 128 masked): the tensor work per weight byte grows 4.6x
     ws3b = torch.empty(max(dl.lmhead_workspace_bytes(L_CANVAS, vocab, d), 1), dtype=torch.uint8, device="cuda")

@@ -188,14 +188,27 @@ DLLM_API size_t dllm_lmhead_workspace_bytes(int64_t rows, int64_t vocab, int64_t
 enum { DLLM_CONF_PMAX = 0, DLLM_CONF_NEG_ENTROPY = 1 };
 
 /* dllm_lmhead_select: dllm_lmhead_masked_select with the confidence chosen by conf_kind
- * (DLLM_CONF_PMAX or DLLM_CONF_NEG_ENTROPY; anything else is DLLM_E_INVAL). out_conf and
- * row_conf then hold that confidence. The block may be the whole canvas (every masked
- * position, R up to 160). Same arguments, ownership and errors as below. */
+ * (DLLM_CONF_PMAX or DLLM_CONF_NEG_ENTROPY; anything else is DLLM_E_INVAL) and an optional
+ * temperature (the specification's sampling section: temperature, categorical sampling,
+ * deterministic PRNG; "Fixed-seed runs are deterministic"). out_conf and row_conf hold the
+ * chosen confidence. The block may be the whole canvas (every masked position, R up to 160).
+ *   temperature == 0: greedy, the row's token is the argmax (as dllm_lmhead_masked_select).
+ *   temperature  > 0: the row's token is a draw from softmax(logits / temperature) by the
+ *       Gumbel-max rule, argmax_v (l_v / temperature + g_v), g_v = -log(-log u_v) (ties: lowest
+ *       id). u_v comes from counter-based SplitMix64 (Steele, Lea and Flood, "Fast splittable
+ *       pseudorandom number generators", OOPSLA 2014): z = mix(seed + (c + 1) 0x9E3779B97F4A7C15)
+ *       for the counter c = step * 2^40 + p * 2^24 + v (p the canvas position, v the token id),
+ *       u_v = (z >> 40 + 1/2) / 2^24. DLLM_CONF_PMAX is then the drawn token's probability
+ *       under the untempered softmax, exp(l_draw - l_max) / sum_v exp(l_v - l_max); the
+ *       entropy confidence does not depend on the draw. Same inputs give the same draws.
+ * Errors as below, plus DLLM_E_INVAL for a negative or non-finite temperature, or (sampling
+ * only) L > 65536 or step >= 2^24. */
 DLLM_API int dllm_lmhead_select(const float* hidden, int64_t L, int64_t d, int64_t ldh, const float* out_norm_w,
                                 float eps, const void* w_out_packed, int64_t vocab, int32_t* canvas, int32_t mask_id,
                                 int32_t block_begin, int32_t block_end, int32_t k_commit, int32_t conf_kind,
-                                int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id, float* row_conf,
-                                void* ws, size_t ws_bytes, dllm_stream_t stream);
+                                float temperature, uint64_t seed, uint32_t step, int32_t* out_pos, int32_t* out_id,
+                                float* out_conf, int32_t* row_id, float* row_conf, void* ws, size_t ws_bytes,
+                                dllm_stream_t stream);
 DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d, int64_t ldh, const float* out_norm_w,
                                        float eps, const void* w_out_packed, int64_t vocab, int32_t* canvas,
                                        int32_t mask_id, int32_t block_begin, int32_t block_end, int32_t k_commit,

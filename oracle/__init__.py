@@ -77,6 +77,8 @@ def _load():
                 "orc_embed_q4k": ([P, I64, I64, P, I64, P], C.c_int),
                 "orc_row_confidence": ([P, I64, I64, P, P, P, P], None),
                 "orc_row_neg_entropy": ([P, I64, I64, P], None),
+                "orc_splitmix64_at": ([C.c_uint64, C.c_uint64], C.c_uint64),
+                "orc_row_sample": ([P, I64, I64, C.c_double, C.c_uint64, C.c_uint32, P, P, P, P], None),
                 "orc_commit_topk": ([P, I64, I32, I64, I64, P, P, I64, P, P], C.c_int),
                 "orc_transfer_counts": ([I64, I64, P], None),
             }
@@ -262,6 +264,25 @@ def row_neg_entropy(logits: np.ndarray) -> np.ndarray:
     return out
 
 
+def splitmix64_at(seed: int, counter: int) -> int:
+    """Output number `counter` (from 0) of the SplitMix64 stream started at `seed`."""
+    return int(_load().orc_splitmix64_at(seed & 0xFFFFFFFFFFFFFFFF, counter & 0xFFFFFFFFFFFFFFFF))
+
+
+def row_sample(logits: np.ndarray, temperature: float, seed: int, step: int, pos) -> tuple:
+    """Gumbel-max draws from softmax(logits / temperature) per row (row r at canvas position
+    pos[r]): (id int32, probability of the id under softmax(logits) f64, perturbed-score gap)."""
+    l = _c(logits, np.float64)
+    r, v = l.shape
+    p = _c(np.asarray(pos, np.int64).reshape(r), np.int64)
+    ids = np.empty(r, np.int32)
+    conf = np.empty(r, np.float64)
+    gap = np.empty(r, np.float64)
+    _load().orc_row_sample(_p(l), r, v, float(temperature), seed & 0xFFFFFFFFFFFFFFFF, step, _p(p), _p(ids),
+                           _p(conf), _p(gap))
+    return ids, conf, gap
+
+
 def commit_topk(canvas: np.ndarray, mask_id: int, b0: int, b1: int, conf_by_pos, ids_by_pos, k: int):
     """Commit in place; returns (positions, ids) in selection order."""
     cv = np.ascontiguousarray(canvas, np.int32)
@@ -335,12 +356,15 @@ def lmhead_logits(hidden_rows, out_norm, w_out, eps=1e-5):
 CONF_PMAX, CONF_NEG_ENTROPY = 0, 1
 
 
-def lmhead_commit(hidden, canvas, mask_id, b0, b1, k, out_norm, w_out, eps=1e-5, conf_kind=CONF_PMAX):
+def lmhead_commit(hidden, canvas, mask_id, b0, b1, k, out_norm, w_out, eps=1e-5, conf_kind=CONF_PMAX,
+                  temperature=0.0, seed=0, step=0):
     """Masked-rows-only LM head + confidence + top-k commit (canvas updated in place). The
-    confidence is the argmax token's softmax probability (CONF_PMAX, LLaDA) or minus the
-    softmax entropy (CONF_NEG_ENTROPY, Dream's ranking); the committed token is the argmax.
+    committed token is the argmax (temperature 0) or a Gumbel-max draw from
+    softmax(logits / temperature) keyed by (seed, step, position, token). The confidence is
+    that token's probability under softmax(logits) (CONF_PMAX, LLaDA) or minus the softmax
+    entropy (CONF_NEG_ENTROPY, Dream's ranking).
 
-    Returns dict(pos, id, conf, rows, ids_rows, conf_rows, top1, top2)."""
+    Returns dict(pos, id, conf, rows, ids_rows, conf_rows, top1, top2[, sample_gap])."""
     rows = np.array([p for p in range(b0, b1) if canvas[p] == mask_id], dtype=np.int64)
     res = dict(rows=rows)
     L = canvas.size
@@ -349,6 +373,9 @@ def lmhead_commit(hidden, canvas, mask_id, b0, b1, k, out_norm, w_out, eps=1e-5,
     if rows.size:
         logits = lmhead_logits(np.asarray(hidden, np.float64)[rows], out_norm, w_out, eps)
         ids, conf, t1, t2 = row_confidence(logits)
+        if temperature > 0:
+            ids, conf, gap = row_sample(logits, temperature, seed, step, rows)
+            res.update(sample_gap=gap)
         if conf_kind == CONF_NEG_ENTROPY:
             conf = row_neg_entropy(logits)
         conf_pos[rows] = conf

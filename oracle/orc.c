@@ -27,6 +27,9 @@
  *     scatter.
  *   - README, "Each model's own sampler": LLaDA ranks masked positions by
  *     the argmax token's probability, Dream by entropy.
+ *   - Technical specification, "Fixed-seed runs are deterministic" and the
+ *     --seed / --temperature flags: temperature sampling from a seeded,
+ *     deterministic generator (here counter-based SplitMix64).
  *   - README, "How it works": the LM head runs only on the masked positions
  *     of the current block.
  * The GGUF byte layouts of Q4_K / Q6_K are the public GGUF formats that the
@@ -472,6 +475,61 @@ void orc_row_neg_entropy(const double* logits, int64_t rows, int64_t vocab, doub
       if (p > 0.0) h -= p * log(p);
     }
     neg_entropy[r] = -h;
+  }
+}
+
+/* ---------------------------------------------------------------------------
+ * Counter-based SplitMix64 (Steele, Lea and Flood, "Fast splittable
+ * pseudorandom number generators", OOPSLA 2014): the generator adds the
+ * golden-ratio increment 0x9E3779B97F4A7C15 to its state and returns the
+ * state through a 64-bit finalizer (xor-shift 30, multiply by
+ * 0xBF58476D1CE4E5B9, xor-shift 27, multiply by 0x94D049BB133111EB,
+ * xor-shift 31). Output number c (from 0) of the stream started at `seed`
+ * therefore depends on (seed, c) alone: mix(seed + (c + 1) * increment).
+ * ------------------------------------------------------------------------- */
+uint64_t orc_splitmix64_at(uint64_t seed, uint64_t c) {
+  uint64_t z = seed + (c + 1) * 0x9E3779B97F4A7C15ULL;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+  return z ^ (z >> 31);
+}
+
+/* ---------------------------------------------------------------------------
+ * Temperature sampling (specification, section 14: temperature, categorical
+ * sampling, deterministic PRNG) by the Gumbel-max rule: the draw
+ * argmax_v (l_v / T + g_v) with independent standard Gumbel g_v is
+ * distributed as softmax(l / T). g_v = -log(-log u_v), u_v uniform in (0, 1)
+ * from the top 24 bits of SplitMix64 output number
+ * c = step * 2^40 + position * 2^24 + v: u = (bits + 1/2) / 2^24. Per row:
+ * the drawn id (lowest on ties), its probability under the untempered
+ * softmax, exp(l_id - l_max) / sum_v exp(l_v - l_max), and the gap between
+ * the best and second-best perturbed scores (a diagnostic). f64 throughout.
+ * ------------------------------------------------------------------------- */
+void orc_row_sample(const double* logits, int64_t rows, int64_t vocab, double temperature, uint64_t seed,
+                    uint32_t step, const int64_t* pos, int32_t* id, double* conf, double* gap) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    const double* l = logits + r * vocab;
+    int64_t best = -1;
+    double s1 = -INFINITY, s2 = -INFINITY, mx = -INFINITY;
+    for (int64_t v = 0; v < vocab; ++v) {
+      const uint64_t c = ((uint64_t)step << 40) | ((uint64_t)pos[r] << 24) | (uint64_t)v;
+      const double u = ((double)(orc_splitmix64_at(seed, c) >> 40) + 0.5) / 16777216.0;
+      const double score = l[v] / temperature - log(-log(u));
+      if (score > s1) {
+        s2 = s1;
+        s1 = score;
+        best = v;
+      } else if (score > s2) {
+        s2 = score;
+      }
+      if (l[v] > mx) mx = l[v];
+    }
+    double den = 0.0;
+    for (int64_t v = 0; v < vocab; ++v) den += exp(l[v] - mx);
+    id[r] = (int32_t)best;
+    conf[r] = exp(l[best] - mx) / den;
+    gap[r] = s1 - s2;
   }
 }
 

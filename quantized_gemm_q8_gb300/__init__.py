@@ -33,6 +33,7 @@ _lock = threading.Lock()
 _lib = None
 
 P, I64, I32, SZ, F32, INT = C.c_void_p, C.c_int64, C.c_int32, C.c_size_t, C.c_float, C.c_int
+U64, U32 = C.c_uint64, C.c_uint32
 _SIGS = {
     "dllm_last_error": ([], C.c_char_p),
     "dllm_version": ([], INT),
@@ -51,8 +52,8 @@ _SIGS = {
     "dllm_lmhead_workspace_bytes": ([I64, I64, I64], SZ),
     "dllm_lmhead_masked_select": ([P, I64, I64, I64, P, F32, P, I64, P, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P],
                                   INT),
-    "dllm_lmhead_select": ([P, I64, I64, I64, P, F32, P, I64, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P],
-                           INT),
+    "dllm_lmhead_select": ([P, I64, I64, I64, P, F32, P, I64, P, I32, I32, I32, I32, I32, F32, U64, U32, P, P, P, P,
+                            P, P, SZ, P], INT),
     "dllm_step_workspace_bytes": ([P, I64, INT], SZ),
     "dllm_step_linear_stream": ([P, P, I64, P, INT, P, SZ, P], INT),
     "dllm_denoise_workspace_bytes": ([P, I64, I32], SZ),
@@ -229,9 +230,10 @@ def lmhead_masked_select(hidden: torch.Tensor, canvas: torch.Tensor, mask_id: in
 
 def lmhead_select(hidden: torch.Tensor, canvas: torch.Tensor, mask_id: int, block_begin: int, block_end: int,
                   k_commit: int, out_norm_w: torch.Tensor, w_out_packed: torch.Tensor, vocab: int,
-                  conf_kind: int = CONF_PMAX, eps: float = 1e-5, ws: torch.Tensor | None = None,
-                  stream=None) -> dict:
-    """lmhead_masked_select with the confidence chosen by conf_kind (CONF_PMAX, CONF_NEG_ENTROPY)."""
+                  conf_kind: int = CONF_PMAX, eps: float = 1e-5, ws: torch.Tensor | None = None, stream=None,
+                  temperature: float = 0.0, seed: int = 0, step: int = 0) -> dict:
+    """lmhead_masked_select with the confidence chosen by conf_kind (CONF_PMAX, CONF_NEG_ENTROPY)
+    and, for temperature > 0, Gumbel-max draws keyed by (seed, step, position, token)."""
     L, d = hidden.shape
     R = block_end - block_begin
     dev = hidden.device
@@ -247,7 +249,7 @@ def lmhead_select(hidden: torch.Tensor, canvas: torch.Tensor, mask_id: int, bloc
         ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=dev)
     _ok(lib().dllm_lmhead_select(_ptr(hidden), L, d, hidden.stride(0), _ptr(out_norm_w), eps, _ptr(w_out_packed),
                                  vocab, _ptr(canvas), mask_id, block_begin, block_end, k_commit, conf_kind,
-                                 _ptr(out["pos"]), _ptr(out["id"]), _ptr(out["conf"]), _ptr(out["row_id"]),
+                                 temperature, seed, step, _ptr(out["pos"]), _ptr(out["id"]), _ptr(out["conf"]), _ptr(out["row_id"]),
                                  _ptr(out["row_conf"]), _ptr(ws), ws.numel(), _stream(stream)))
     for key in ("pos", "id", "conf"):
         out[key] = out[key][:k_commit]

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -334,38 +335,66 @@ __device__ __forceinline__ SoftPart soft_merge(SoftPart x, SoftPart y) {
   return x;
 }
 
+// One Gumbel-max partial: best perturbed score, its token id (lowest on ties), its logit.
+struct SampPart {
+  float sc;
+  int a;
+  float l;
+};
+__device__ __forceinline__ SampPart samp_merge(SampPart x, SampPart y) {
+  return (y.sc > x.sc || (y.sc == x.sc && y.a < x.a)) ? y : x;
+}
+
 // Merge and commit, one launch: CTA r (256 threads) merges row r's P partials (contiguous,
 // [R][P]) into the argmax id and the row's confidence, and stores them; the CTA that
 // finishes last (a counter, zeroed before the launch) picks the k masked positions of the
 // block with the highest confidence (ties: lowest position) and scatters their ids into the
 // canvas. Confidence: kind 0 p_max = 1 / sum exp(l - l_max); kind 1 the negative entropy
 // -H = sum p log p = t / s - log s with s = sum exp(l - l_max), t = sum exp(l - l_max)(l - l_max)
-// (pent holds the t partials; unused for kind 0).
+// (pent holds the t partials; unused for kind 0). With sampling (pscore non-null) the row's
+// token is the Gumbel-max draw instead of the argmax, and kind 0 is its probability
+// exp(l_draw - l_max) / s.
 __global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
     const float* __restrict__ pmax, const int* __restrict__ parg, const float* __restrict__ psum,
-    const float* __restrict__ pent, int kind, int P, int R, int32_t* canvas, int32_t mask_id, int b0, int k,
+    const float* __restrict__ pent, const float* __restrict__ pscore, const int* __restrict__ pidx,
+    const float* __restrict__ plogit, int kind, int P, int R, int32_t* canvas, int32_t mask_id, int b0, int k,
     int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id, float* row_conf, float* conf_ws, int* id_ws,
     unsigned int* done) {
   __shared__ SoftPart red[8];
+  __shared__ SampPart sred[8];
   __shared__ bool last;
   griddep_wait();
   griddep_launch();
   const int r = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   SoftPart acc{-INFINITY, 0x7fffffff, 0.f, 0.f};
+  SampPart sacc{-INFINITY, 0x7fffffff, 0.f};
+  const bool sample = pscore != nullptr;
   const size_t base = (size_t)r * P;
-  for (int i = threadIdx.x; i < P; i += blockDim.x)
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
     acc = soft_merge(acc, SoftPart{pmax[base + i], parg[base + i], psum[base + i], kind ? pent[base + i] : 0.f});
+    if (sample) sacc = samp_merge(sacc, SampPart{pscore[base + i], pidx[base + i], plogit[base + i]});
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     SoftPart o{__shfl_xor_sync(0xffffffffu, acc.m, off), __shfl_xor_sync(0xffffffffu, acc.a, off),
                __shfl_xor_sync(0xffffffffu, acc.s, off), __shfl_xor_sync(0xffffffffu, acc.t, off)};
     acc = soft_merge(acc, o);
+    SampPart so{__shfl_xor_sync(0xffffffffu, sacc.sc, off), __shfl_xor_sync(0xffffffffu, sacc.a, off),
+                __shfl_xor_sync(0xffffffffu, sacc.l, off)};
+    sacc = samp_merge(sacc, so);
   }
-  if (lane == 0) red[warp] = acc;
+  if (lane == 0) {
+    red[warp] = acc;
+    sred[warp] = sacc;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < 8; ++w) acc = soft_merge(acc, red[w]);
-    const float c = kind ? acc.t / acc.s - logf(acc.s) : 1.0f / acc.s;
+    for (int w = 1; w < 8; ++w) {
+      acc = soft_merge(acc, red[w]);
+      sacc = samp_merge(sacc, sred[w]);
+    }
+    if (sample) acc.a = sacc.a;  // the committed token is the draw
+    const float c = kind ? acc.t / acc.s - logf(acc.s) : (sample ? expf(sacc.l - acc.m) : 1.0f) / acc.s;
     conf_ws[r] = c;
     id_ws[r] = acc.a;
     if (row_id) row_id[r] = acc.a;
@@ -422,7 +451,7 @@ __global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
 }
 
 struct LmheadWs {
-  size_t act, pmax, parg, psum, pent, conf, id, done, bytes;
+  size_t act, pmax, parg, psum, pent, pscore, pidx, plogit, conf, id, done, bytes;
   int P;
 };
 static LmheadWs lmhead_ws(int64_t R, int64_t vocab, int64_t d) {
@@ -434,7 +463,10 @@ static LmheadWs lmhead_ws(int64_t R, int64_t vocab, int64_t d) {
   w.parg = w.pmax + align_up((size_t)w.P * R * 4, 256);
   w.psum = w.parg + align_up((size_t)w.P * R * 4, 256);
   w.pent = w.psum + align_up((size_t)w.P * R * 4, 256);
-  w.conf = w.pent + align_up((size_t)w.P * R * 4, 256);
+  w.pscore = w.pent + align_up((size_t)w.P * R * 4, 256);
+  w.pidx = w.pscore + align_up((size_t)w.P * R * 4, 256);
+  w.plogit = w.pidx + align_up((size_t)w.P * R * 4, 256);
+  w.conf = w.plogit + align_up((size_t)w.P * R * 4, 256);
   w.id = w.conf + align_up((size_t)R * 4, 256);
   w.done = w.id + align_up((size_t)R * 4, 256);
   w.bytes = w.done + 256;
@@ -653,6 +685,13 @@ int launch_gemm(const GemmLaunch& g, const QgemmPlan& P, cudaStream_t stream) {
   prm.parg = g.parg;
   prm.psum = g.psum;
   prm.pent = g.pent;
+  prm.inv_temp = g.inv_temp;
+  prm.seed = g.seed;
+  prm.step = g.step;
+  prm.pos0 = g.pos0;
+  prm.pscore = g.pscore;
+  prm.pidx = g.pidx;
+  prm.plogit = g.plogit;
   prm.dbg = g.dbg;
   prm.dbg_mode = g.dbg_mode;
   prm.timeout = kDefaultTimeoutCycles;
@@ -779,8 +818,9 @@ DLLM_API size_t dllm_lmhead_workspace_bytes(int64_t rows, int64_t vocab, int64_t
 DLLM_API int dllm_lmhead_select(const float* hidden, int64_t L, int64_t d, int64_t ldh, const float* out_norm_w,
                                 float eps, const void* w_out_packed, int64_t vocab, int32_t* canvas, int32_t mask_id,
                                 int32_t block_begin, int32_t block_end, int32_t k_commit, int32_t conf_kind,
-                                int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id, float* row_conf,
-                                void* ws, size_t ws_bytes, dllm_stream_t stream) {
+                                float temperature, uint64_t seed, uint32_t step, int32_t* out_pos, int32_t* out_id,
+                                float* out_conf, int32_t* row_id, float* row_conf, void* ws, size_t ws_bytes,
+                                dllm_stream_t stream) {
   const int64_t R = (int64_t)block_end - block_begin;
   if (L <= 0 || d <= 0 || d % QK || d > (1 << 20) || ldh < d || vocab <= 0 || vocab > (1 << 24))
     return fail(DLLM_E_SHAPE, "dllm_lmhead_select: bad shape L=%lld d=%lld ldh=%lld vocab=%lld", (long long)L,
@@ -793,6 +833,10 @@ DLLM_API int dllm_lmhead_select(const float* hidden, int64_t L, int64_t d, int64
   if (conf_kind != DLLM_CONF_PMAX && conf_kind != DLLM_CONF_NEG_ENTROPY)
     return fail(DLLM_E_INVAL, "dllm_lmhead_select: conf_kind=%d must be DLLM_CONF_PMAX (0) or DLLM_CONF_NEG_ENTROPY (1)",
                 conf_kind);
+  if (!std::isfinite(temperature) || temperature < 0.f)
+    return fail(DLLM_E_INVAL, "dllm_lmhead_select: temperature must be finite and >= 0 (0 = greedy)");
+  if (temperature > 0.f && (L > 65536 || step >= (1u << 24)))
+    return fail(DLLM_E_INVAL, "dllm_lmhead_select: sampling needs L <= 65536 and step < 2^24 (the noise counter)");
   int rc = check_device();
   if (rc) return rc;
   CHECK_DEV(hidden, "hidden");
@@ -826,6 +870,14 @@ DLLM_API int dllm_lmhead_select(const float* hidden, int64_t L, int64_t d, int64
                reinterpret_cast<float*>(base + W.pmax), reinterpret_cast<int*>(base + W.parg),
                reinterpret_cast<float*>(base + W.psum), nullptr};
   g.pent = conf_kind == DLLM_CONF_NEG_ENTROPY ? reinterpret_cast<float*>(base + W.pent) : nullptr;
+  const bool sample = temperature > 0.f;
+  g.inv_temp = sample ? 1.0f / temperature : 0.f;
+  g.seed = seed;
+  g.step = (int)step;
+  g.pos0 = block_begin;
+  g.pscore = sample ? reinterpret_cast<float*>(base + W.pscore) : nullptr;
+  g.pidx = sample ? reinterpret_cast<int*>(base + W.pidx) : nullptr;
+  g.plogit = sample ? reinterpret_cast<float*>(base + W.plogit) : nullptr;
   rc = launch_gemm(g, P, s);
   if (rc) return rc;
   // 3) merge, confidence, top-k commit
@@ -835,7 +887,7 @@ DLLM_API int dllm_lmhead_select(const float* hidden, int64_t L, int64_t d, int64
   e = launch_pdl(lmhead_merge_commit_kernel, dim3((unsigned)R), dim3(256), 0, s,
                  reinterpret_cast<const float*>(base + W.pmax), reinterpret_cast<const int*>(base + W.parg),
                  reinterpret_cast<const float*>(base + W.psum), reinterpret_cast<const float*>(base + W.pent),
-                 (int)conf_kind, W.P, (int)R, canvas, mask_id, (int)block_begin,
+                 g.pscore, g.pidx, g.plogit, (int)conf_kind, W.P, (int)R, canvas, mask_id, (int)block_begin,
                  (int)k_commit, out_pos, out_id, out_conf, row_id, row_conf, reinterpret_cast<float*>(base + W.conf),
                  reinterpret_cast<int*>(base + W.id), done);
   note_launch();
@@ -850,8 +902,8 @@ DLLM_API int dllm_lmhead_masked_select(const float* hidden, int64_t L, int64_t d
                                        int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id,
                                        float* row_conf, void* ws, size_t ws_bytes, dllm_stream_t stream) {
   return dllm_lmhead_select(hidden, L, d, ldh, out_norm_w, eps, w_out_packed, vocab, canvas, mask_id, block_begin,
-                            block_end, k_commit, DLLM_CONF_PMAX, out_pos, out_id, out_conf, row_id, row_conf, ws,
-                            ws_bytes, stream);
+                            block_end, k_commit, DLLM_CONF_PMAX, 0.f, 0, 0, out_pos, out_id, out_conf, row_id,
+                            row_conf, ws, ws_bytes, stream);
 }
 
 

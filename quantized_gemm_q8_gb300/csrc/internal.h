@@ -81,6 +81,13 @@ struct GemmLaunch {
   int32_t* dbg;
   int dbg_mode;
   float* pent;  // mode 1: optional entropy partials
+  // mode 1: Gumbel-max sampling when inv_temp > 0 (partials pscore / pidx / plogit)
+  float inv_temp;
+  unsigned long long seed;
+  int step, pos0;
+  float* pscore;
+  int* pidx;
+  float* plogit;
 };
 int launch_gemm(const GemmLaunch& g, const QgemmPlan& P, cudaStream_t stream);
 size_t packed_blob_bytes(int type, int64_t n, int64_t k);
@@ -91,6 +98,7 @@ size_t align_up(size_t x, size_t a);
 // qgemm_q6k.cu). Returns DLLM_OK or a status.
 int launch_qgemm_q4k(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s);
 int launch_qgemm_q6k(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s);
+int launch_qgemm_q6k_sample(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s);
 
 // Quantize rows of x into the operand form (internal, no validation).
 int quantize_rows(const float* x, int64_t rows, int64_t k, int64_t ldx, const float* norm_w, float eps, void* act,

@@ -171,6 +171,15 @@ struct QgemmParams {
   int* parg;
   float* psum;
   float* pent;
+  // mode 1 sampling (inv_temp > 0): per partial also the Gumbel-max draw over its rows: the
+  // best score l * inv_temp + g (g from the counter (step, pos0 + token, row), see
+  // gumbel_noise), its row (lowest on ties) and that row's logit
+  float inv_temp;
+  unsigned long long seed;
+  int step, pos0;
+  float* pscore;
+  int* pidx;
+  float* plogit;
 #ifdef DLLM_TRACE
   unsigned long long* trace;  // per-role clock64 stamps of CTA 0 (trace builds only)
 #endif
@@ -303,6 +312,20 @@ __device__ __forceinline__ Q4Fold q4k_fold(float d, float dmin, bool* bad) {
   return f;
 }
 
+// Gumbel noise of one (row, vocabulary entry) of a sampling step: counter-based SplitMix64
+// (Steele, Lea and Flood, "Fast splittable pseudorandom number generators"): the output for
+// counter c of the stream `seed` is mix(seed + (c + 1) * 0x9E3779B97F4A7C15). Counter
+// c = step * 2^40 + position * 2^24 + vocabulary id; its top 24 bits give the uniform
+// u = (bits + 1/2) / 2^24 in (0, 1), and g = -log(-log u).
+__device__ __forceinline__ float gumbel_noise(unsigned long long seed, unsigned long long c) {
+  unsigned long long z = seed + (c + 1ull) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  const float u = ((float)(z >> 40) + 0.5f) * 5.9604644775390625e-8f;  // 2^-24
+  return -logf(-logf(u));
+}
+
 __device__ __forceinline__ void unit_coords(const QgemmParams& p, int u, int& tn, int& tm, int& sp, int& sb0,
                                             int& sb1) {
   tn = u % p.tiles_n;
@@ -313,7 +336,9 @@ __device__ __forceinline__ void unit_coords(const QgemmParams& p, int u, int& tn
   sb1 = min(p.nsb, sb0 + p.sbps);
 }
 
-template <int TYPE, int NT>
+// SAMPLE: the LM-head epilogue also makes the Gumbel-max draws (mode 1 with inv_temp > 0); a
+// separate instantiation, so the other kernels carry none of its code.
+template <int TYPE, int NT, bool SAMPLE = false>
 __global__ void __launch_bounds__(QG_THREADS, 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tmap, const QgemmParams p) {
   using C = QCfg<TYPE, NT>;
@@ -751,6 +776,34 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             for (int off = 16; off > 0; off >>= 1) tx += __shfl_xor_sync(0xffffffffu, tx, off);
           }
           const int tok = tokb + j;
+          if constexpr (SAMPLE) {
+            // Gumbel-max draw: the best perturbed score of the quadrant's rows
+            float sc = -INFINITY, sl = 0.f;
+            int si = grow;
+            if (grow < p.n) {
+              const unsigned long long c = ((unsigned long long)p.step << 40) |
+                                           ((unsigned long long)(p.pos0 + tok) << 24) | (unsigned long long)grow;
+              sc = acc[j] * p.inv_temp + gumbel_noise(p.seed, c);
+              sl = acc[j];
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+              const float os = __shfl_xor_sync(0xffffffffu, sc, off);
+              const int oi = __shfl_xor_sync(0xffffffffu, si, off);
+              const float ol = __shfl_xor_sync(0xffffffffu, sl, off);
+              if (os > sc || (os == sc && oi < si)) {
+                sc = os;
+                si = oi;
+                sl = ol;
+              }
+            }
+            if (lane == 0 && tok < p.m) {
+              const size_t o = (size_t)tok * (p.tiles_n * 4) + tn * 4 + qd;
+              p.pscore[o] = sc;
+              p.pidx[o] = si;
+              p.plogit[o] = sl;
+            }
+          }
           if (lane == 0 && tok < p.m) {
             const size_t o = (size_t)tok * (p.tiles_n * 4) + tn * 4 + qd;
             p.pmax[o] = v;

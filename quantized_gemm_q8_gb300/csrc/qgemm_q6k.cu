@@ -18,6 +18,7 @@ static int launch_one(const CUtensorMap& map, const QgemmParams& p, int grid, cu
 }
 
 int launch_qgemm_q6k(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s) {
+  if (p.mode == 1 && p.inv_temp > 0.f) return launch_qgemm_q6k_sample(nt, map, p, grid, s);
   switch (nt) {
     case 32: return launch_one<32>(map, p, grid, s);
     case 64: return launch_one<64>(map, p, grid, s);

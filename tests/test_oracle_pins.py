@@ -436,6 +436,52 @@ def test_entropy_ranking_commit_order():
     assert canvas.tolist() == [0, 5, 1, 7]
 
 
+def test_splitmix64_published_first_output():
+    g = _golden("splitmix64.txt")
+    assert orc.splitmix64_at(int(g["seed"][0]), 0) == int(g["first_output"][0], 16)
+
+
+def test_splitmix64_counter_form_is_the_stream():
+    # output c of the stream = output 0 of the stream started c increments later
+    gamma = 0x9E3779B97F4A7C15
+    for seed, c in [(0, 1), (12345, 7), (2**63 + 5, 1000)]:
+        assert orc.splitmix64_at(seed, c) == orc.splitmix64_at((seed + c * gamma) % 2**64, 0)
+    outs = {orc.splitmix64_at(99, c) for c in range(4096)}
+    assert len(outs) == 4096  # a bijective finalizer over distinct states
+
+
+def test_gumbel_max_draws_follow_softmax_over_temperature():
+    # 40000 draws (one per canvas position) from V = 5 logits at T = 0.7: the frequencies match
+    # softmax(l / T) (chi-square, 4 degrees of freedom, far below the 1e-4 critical value 23.5)
+    l = np.array([0.0, 1.0, -0.5, 2.0, 0.3])
+    n, T = 40000, 0.7
+    ids, conf, _ = orc.row_sample(np.tile(l, (n, 1)), T, 2024, 5, np.arange(n))
+    p = np.exp(l / T) / np.exp(l / T).sum()
+    cnt = np.bincount(ids, minlength=5)
+    chi2 = float(((cnt - n * p) ** 2 / (n * p)).sum())
+    assert chi2 < 23.5, (cnt, n * p, chi2)
+    # the confidence is the drawn token's probability under the untempered softmax
+    np.testing.assert_allclose(conf, (np.exp(l) / np.exp(l).sum())[ids], rtol=1e-13)
+
+
+def test_gumbel_max_limits():
+    rng = np.random.default_rng(3)
+    logits = rng.normal(0.0, 1.0, size=(64, 50))
+    # T -> 0: the draw is the argmax (logit gaps / T dwarf the noise)
+    ids0 = orc.row_confidence(logits)[0]
+    ids, _, _ = orc.row_sample(logits, 1e-7, 7, 0, np.arange(64))
+    assert np.array_equal(ids, ids0)
+    # equal logits: every token is drawn, each with probability 1 / V
+    ids, conf, _ = orc.row_sample(np.zeros((20000, 4)), 1.3, 11, 2, np.arange(20000))
+    np.testing.assert_allclose(conf, 0.25, rtol=1e-15)
+    assert np.all(np.abs(np.bincount(ids, minlength=4) / 20000 - 0.25) < 0.02)
+    # the draw depends on (seed, step, position) and on nothing else
+    a, _, _ = orc.row_sample(logits, 0.9, 5, 1, np.arange(64))
+    b, _, _ = orc.row_sample(logits, 0.9, 5, 1, np.arange(64))
+    c, _, _ = orc.row_sample(logits, 0.9, 5, 2, np.arange(64))
+    assert np.array_equal(a, b) and not np.array_equal(a, c)
+
+
 def test_commit_invariants_random():
     rng = np.random.default_rng(3)
     L, mask = 148, 126336
