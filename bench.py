@@ -172,6 +172,19 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def job_timing(ms_local, steps, world, dist=None, device="cpu"):
+    """Whole-job timing of N replicas: the slowest rank's timed region (max over ranks), its
+    per-step time, and the job-wide ms per step (N replicas complete N * steps steps in that
+    time). `dist` is torch.distributed with an initialized process group when world > 1."""
+    import torch
+
+    t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    if dist is not None and world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, ms_max / steps, ms_max / (steps * world)
+
+
 def run_ours(args, rank, local_rank, world):
     import numpy as np
     import torch
@@ -219,13 +232,7 @@ def run_ours(args, rank, local_rank, world):
     if dist:
         dist.barrier()
     dl.check(stream)
-    ms_total = ev0.elapsed_time(ev1)
-    t = torch.tensor([ms_total], device="cuda")
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    ms_per_step = ms_max / args.steps
-    value = ms_max / (args.steps * world)  # job-wide: N replicas complete N*K steps in ms_max
+    ms_max, ms_per_step, value = job_timing(ev0.elapsed_time(ev1), args.steps, world, dist, "cuda")
 
     # ---- end-to-end through the public call with host buffers (H2D canvas, D2H commits) ----
     canvas_h = torch.from_numpy(synth.canvas(seed)).pin_memory()
