@@ -268,6 +268,31 @@ DLLM_API int dllm_denoise_step(const dllm_model* m, int32_t* canvas, int64_t L, 
                                float* out_conf, float* hidden_out, void* ws, size_t ws_bytes,
                                dllm_stream_t stream);
 
+/* ---- inter-step K/V cache ("--dual-cache": mojo-dllm README status table, opt-in and not
+ * exact; specification section 23, "Future Caching Research": inter-step cache, which must report
+ * speedup, memory and output divergence) ------------------------------------------------------
+ * dllm_kv_cache_bytes: size of the cache, f32 [n_layers][2][L][d_model] (per layer K after RoPE,
+ *   then V, for every canvas row); caller-owned device memory, 16-byte aligned.
+ * dllm_denoise_step_cached: one denoising step with the cache.
+ *   refresh = 1: exactly dllm_denoise_step, and every layer's K and V of all L rows are stored in
+ *       kv_cache (the first step of a block);
+ *   refresh = 0: only the block's rows [block_begin, block_end) (1..160 rows) run through the
+ *       layers: embedding, projections, RoPE at their canvas positions, attention of their
+ *       queries over all L keys and values taken from kv_cache (the block's own rows replaced by
+ *       their fresh K and V, which are also written back), O, FFN; then the head and commit
+ *       on the block as in dllm_denoise_step. Rows outside the block keep the K and V of the
+ *       last refresh, so the result is an approximation of the uncached step.
+ *   hidden_out (may be NULL): f32 [L][d_model]; a cached step writes the block's rows only.
+ *   ws: >= dllm_denoise_cached_workspace_bytes(m, L, block_end - block_begin), 1024-byte aligned.
+ * Errors: as dllm_denoise_step, plus DLLM_E_WORKSPACE for a short kv_cache, DLLM_E_ALIGN for a
+ * misaligned one and DLLM_E_INVAL for refresh not 0 or 1. */
+DLLM_API size_t dllm_kv_cache_bytes(const dllm_model* m, int64_t L);
+DLLM_API size_t dllm_denoise_cached_workspace_bytes(const dllm_model* m, int64_t L, int32_t block_rows);
+DLLM_API int dllm_denoise_step_cached(const dllm_model* m, int32_t* canvas, int64_t L, int32_t block_begin,
+                                      int32_t block_end, int32_t k_commit, int32_t refresh, float* kv_cache,
+                                      size_t kv_bytes, int32_t* out_pos, int32_t* out_id, float* out_conf,
+                                      float* hidden_out, void* ws, size_t ws_bytes, dllm_stream_t stream);
+
 /* Benchmark hooks.
  * dllm_launch_count: number of kernels this library has enqueued so far in this process (a
  *   host-side counter; launches recorded during stream capture count once, at capture).

@@ -347,6 +347,56 @@ def layer(lw: dict, x, dims: dict, attention_on: bool, with_qk: bool = True):
     return x, ex
 
 
+def layer_block(lw: dict, xb, dims: dict, k_cache: np.ndarray, v_cache: np.ndarray, b0: int):
+    """One LLaDA layer on the block rows xb (canvas positions b0 .. b0 + R - 1) of a cached step
+    (the inter-step K/V cache, "--dual-cache"): the block's Q, K, V are projected as in `layer`,
+    RoPE uses the rows' canvas positions, the fresh K (after RoPE) and V overwrite the block's rows
+    of k_cache / v_cache ([L][d], in place), and the block's queries attend to all L cached rows.
+    Everything after the attention is `layer` on the block rows. Returns the block's x_out."""
+    eps, nh, hd = dims["eps"], dims["n_heads"], dims["head_dim"]
+    xb = np.asarray(xb, np.float64)
+    L, R = k_cache.shape[0], xb.shape[0]
+    q1, d1, _ = quantize_act(xb, lw["attn_norm"], eps)
+    q = qgemm(TYPE_Q4_K, lw["wq"], q1, d1)
+    k = qgemm(TYPE_Q4_K, lw["wk"], q1, d1)
+    v = qgemm(TYPE_Q6_K, lw["wv"], q1, d1)
+
+    def at_positions(a):  # rows placed at their canvas positions, so RoPE rotates by position
+        full = np.zeros((L, a.shape[1]))
+        full[b0:b0 + R] = a
+        return full
+
+    q_full = rope(at_positions(q), nh, hd, dims["rope_theta"])
+    k_cache[b0:b0 + R] = rope(at_positions(k), nh, hd, dims["rope_theta"])[b0:b0 + R]
+    v_cache[b0:b0 + R] = v
+    o = attention(q_full, k_cache, v_cache, nh, hd)[b0:b0 + R]  # only the block's query rows are kept
+    q2, d2, _ = quantize_act(o)
+    x = xb + qgemm(TYPE_Q4_K, lw["wo"], q2, d2)
+    q3, d3, _ = quantize_act(x, lw["ffn_norm"], eps)
+    h = swiglu(qgemm(TYPE_Q4_K, lw["wgate"], q3, d3), qgemm(TYPE_Q4_K, lw["wup"], q3, d3))
+    q4, d4, _ = quantize_act(h)
+    return x + qgemm(TYPE_Q6_K, lw["wdown"], q4, d4)
+
+
+def forward_cached(lws, table, canvas, dims: dict, b0: int, b1: int, refresh: bool, cache: list):
+    """The residual stream of a cached step: refresh runs every layer on all rows and stores each
+    layer's (K after RoPE, V) in `cache` (a list, filled in place); otherwise only rows [b0, b1)
+    run, through layer_block. Returns x [L][d] (rows outside the block are zero for a cached step)."""
+    if refresh:
+        x = embed(table, canvas)
+        cache.clear()
+        for lw in lws:
+            x, ex = layer(lw, x, dims, attention_on=True)
+            cache.append((ex["k_rope"].copy(), ex["v"].copy()))
+        return x
+    xb = embed(table, np.asarray(canvas)[b0:b1])
+    for lw, (kc, vc) in zip(lws, cache):
+        xb = layer_block(lw, xb, dims, kc, vc, b0)
+    x = np.zeros((np.asarray(canvas).size, xb.shape[1]))
+    x[b0:b1] = xb
+    return x
+
+
 def lmhead_logits(hidden_rows, out_norm, w_out, eps=1e-5):
     """Logits (f64) of the given hidden rows: RMSNorm -> Q8_K -> Q6_K head."""
     q, d, _ = quantize_act(hidden_rows, out_norm, eps)

@@ -58,6 +58,9 @@ _SIGS = {
     "dllm_step_linear_stream": ([P, P, I64, P, INT, P, SZ, P], INT),
     "dllm_denoise_workspace_bytes": ([P, I64, I32], SZ),
     "dllm_denoise_step": ([P, P, I64, I32, I32, I32, P, P, P, P, P, SZ, P], INT),
+    "dllm_kv_cache_bytes": ([P, I64], SZ),
+    "dllm_denoise_cached_workspace_bytes": ([P, I64, I32], SZ),
+    "dllm_denoise_step_cached": ([P, P, I64, I32, I32, I32, I32, P, SZ, P, P, P, P, P, SZ, P], INT),
     "dllm_launch_count": ([], C.c_longlong),
     "dllm_qgemm_partials_bytes": ([INT, I64, I64, I64], SZ),
     "dllm_qgemm_partials": ([INT, P, I64, I64, P, I64, P, SZ, P, P], INT),
@@ -362,6 +365,36 @@ def denoise_step(model: DeviceModel, canvas: torch.Tensor, block_begin: int, blo
     return out
 
 
+def kv_cache_bytes(model: DeviceModel, L: int) -> int:
+    return int(lib().dllm_kv_cache_bytes(model.ref, L))
+
+
+def denoise_cached_workspace_bytes(model: DeviceModel, L: int, block_rows: int) -> int:
+    return int(lib().dllm_denoise_cached_workspace_bytes(model.ref, L, block_rows))
+
+
+def denoise_step_cached(model: DeviceModel, canvas: torch.Tensor, block_begin: int, block_end: int, k_commit: int,
+                        refresh: bool, kv_cache: torch.Tensor, hidden_out: torch.Tensor | None = None,
+                        ws: torch.Tensor | None = None, out: dict | None = None, stream=None) -> dict:
+    """One denoising step with the inter-step K/V cache: refresh=True runs the full step and fills
+    kv_cache; refresh=False recomputes only the block's rows against the cached K/V."""
+    L = canvas.shape[0]
+    dev = canvas.device
+    if out is None:
+        out = {"pos": torch.empty(max(k_commit, 1), dtype=torch.int32, device=dev),
+               "id": torch.empty(max(k_commit, 1), dtype=torch.int32, device=dev),
+               "conf": torch.empty(max(k_commit, 1), dtype=torch.float32, device=dev)}
+    nb = denoise_cached_workspace_bytes(model, L, block_end - block_begin)
+    if ws is None:
+        ws = torch.empty(nb + 1024, dtype=torch.uint8, device=dev)
+    wsp = (ws.data_ptr() + 1023) // 1024 * 1024
+    _ok(lib().dllm_denoise_step_cached(model.ref, _ptr(canvas), L, block_begin, block_end, k_commit, int(refresh),
+                                       _ptr(kv_cache), kv_cache.numel() * kv_cache.element_size(), _ptr(out["pos"]),
+                                       _ptr(out["id"]), _ptr(out["conf"]), _ptr(hidden_out), C.c_void_p(wsp),
+                                       ws.numel() - (wsp - ws.data_ptr()), _stream(stream)))
+    return out
+
+
 def model_from_seed(dims: dict, seed: int, device="cuda") -> DeviceModel:
     """Seeded synthetic LLaDA-shaped model (generated, uploaded and packed one layer at a time)."""
     from . import synth
@@ -409,3 +442,47 @@ class StepGraphs:
         """Replay on self.stream (a graph replays on the caller's current stream)."""
         with torch.cuda.stream(self.stream):
             self.graphs[block_index].replay()
+
+
+class CachedStepGraphs:
+    """Two CUDA graphs per block for the inter-step K/V cache: the refreshing step (full forward,
+    cache filled) and the cached step (block rows only); replay(block, refresh). One cache,
+    workspace and output set, allocated before capture."""
+
+    def __init__(self, model: DeviceModel, canvas: torch.Tensor, blocks: list, k_commit: int):
+        self.model, self.canvas, self.blocks, self.k = model, canvas, blocks, k_commit
+        dev = canvas.device
+        L = canvas.shape[0]
+        rows = max(b1 - b0 for b0, b1 in blocks)
+        nb = denoise_cached_workspace_bytes(model, L, rows)
+        self.ws = torch.empty(nb + 1024, dtype=torch.uint8, device=dev)
+        self.kv = torch.empty(kv_cache_bytes(model, L) // 4, dtype=torch.float32, device=dev)
+        self.out = {"pos": torch.empty(k_commit, dtype=torch.int32, device=dev),
+                    "id": torch.empty(k_commit, dtype=torch.int32, device=dev),
+                    "conf": torch.empty(k_commit, dtype=torch.float32, device=dev)}
+        self.stream = torch.cuda.Stream(device=dev)
+        self.graphs = {}
+        saved = canvas.clone()
+
+        def step(b0, b1, refresh):
+            denoise_step_cached(model, canvas, b0, b1, k_commit, refresh, self.kv, ws=self.ws, out=self.out,
+                                stream=self.stream)
+
+        with torch.cuda.stream(self.stream):
+            for b0, b1 in blocks:  # warm the library once; the refresh fills the cache first
+                step(b0, b1, True)
+                step(b0, b1, False)
+        self.stream.synchronize()
+        check(self.stream)
+        for i, (b0, b1) in enumerate(blocks):
+            for refresh in (True, False):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=self.stream):
+                    step(b0, b1, refresh)
+                self.graphs[(i, refresh)] = g
+        canvas.copy_(saved)
+        torch.cuda.synchronize()
+
+    def replay(self, block_index: int, refresh: bool):
+        with torch.cuda.stream(self.stream):
+            self.graphs[(block_index, refresh)].replay()

@@ -68,14 +68,16 @@ __device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t&
 
 // Q, K, V of one layer from the split-K partials of the Q|K and V projections: the splits are
 // summed in split order, RoPE rotates adjacent pairs of Q and K within each head (position =
-// row), Q is also scaled by 1/sqrt(hd). Out: QKV [L][3d] f32 (Q, K, V side by side), or, when
-// `planes` is set (the tensor-core attention), six f16 planes [Qhi, Qlo, Khi, Klo, Vhi, Vlo][L][d]
-// with x = hi + lo. All partial loads of a thread are issued together.
+// pos0 + row), Q is also scaled by 1/sqrt(hd). Out: QKV [L][3d] f32 (Q, K, V side by side), or,
+// when `planes` is set (the tensor-core attention), six f16 planes [Qhi, Qlo, Khi, Klo, Vhi,
+// Vlo][L][d] with x = hi + lo. With kcache / vcache set, K (after RoPE) and V also go to rows
+// pos0 + row of those [*][d] caches. All partial loads of a thread are issued together.
 __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __restrict__ Pqk, int Sqk,
                                                               const float* __restrict__ Pv, int Sv,
                                                               const float2* __restrict__ cs, int L, int d, int hd,
                                                               float qscale, float* __restrict__ QKV,
-                                                              __half* __restrict__ planes) {
+                                                              __half* __restrict__ planes, int pos0,
+                                                              float* __restrict__ kcache, float* __restrict__ vcache) {
   griddep_wait();
   griddep_launch();
   // one thread per 4 consecutive columns (two RoPE pairs): 16-byte partial loads
@@ -95,7 +97,8 @@ __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __res
       a.z += v.z;
       a.w += v.w;
     }
-    const float2 r0 = cs[p * (hd / 2) + (c % hd) / 2], r1 = cs[p * (hd / 2) + (c % hd) / 2 + 1];
+    const int64_t rp = (int64_t)(pos0 + p) * (hd / 2) + (c % hd) / 2;
+    const float2 r0 = cs[rp], r1 = cs[rp + 1];
     const float sc = c < d ? qscale : 1.f;
     a = make_float4((a.x * r0.x - a.y * r0.y) * sc, (a.x * r0.y + a.y * r0.x) * sc, (a.z * r1.x - a.w * r1.y) * sc,
                     (a.z * r1.y + a.w * r1.x) * sc);
@@ -111,6 +114,10 @@ __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __res
       a.w += v.w;
     }
   }
+  if (kcache && c >= d) {
+    float* dst = (c < 2 * d ? kcache : vcache) + (int64_t)(pos0 + p) * d + (c % d);
+    *reinterpret_cast<float4*>(dst) = a;
+  }
   if (planes) {
     const int which = c / d, col = c % d;
     uint32_t h0, l0, h1, l1;
@@ -123,10 +130,12 @@ __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __res
   }
 }
 
-// Non-causal multi-head attention O = softmax(q k^T) v per head on the reduced QKV ([L][3d],
-// q pre-scaled), f32, split over chunks of 32 keys (flash-decoding style): CTA (head, 16
-// queries, chunk c) writes for each query the chunk's max score m_c, sum l_c = sum exp(s - m_c)
-// and unnormalized a_c = sum exp(s - m_c) v; attn_merge_quant_kernel combines the chunks. Small
+// Non-causal multi-head attention O = softmax(q k^T) v per head, f32, split over chunks of 32
+// keys (flash-decoding style): Lq query rows (q pre-scaled, row stride ldq) against Lk key and
+// value rows (row stride ldkv); for self-attention on the reduced QKV ([L][3d]) q = QKV,
+// k = QKV + d, v = QKV + 2d. CTA (head, 16 queries, chunk c) writes for each query the chunk's
+// max score m_c, sum l_c = sum exp(s - m_c) and unnormalized a_c = sum exp(s - m_c) v;
+// attn_merge_quant_kernel combines the chunks. Small
 // CTAs (4 warps, 43 KB shared) let five share an SM. Warp w owns queries 4w..4w+3; lane = key
 // of the chunk for the scores (k rows padded to 132 floats: a quarter-warp's float4 loads of 8
 // keys hit distinct banks; q read as broadcast float4, query pairs as f32x2), and dims
@@ -142,12 +151,15 @@ __device__ __forceinline__ void fma2f(float& d0, float& d1, float a0, float a1, 
 }
 
 struct AttPart {
-  float* acc;  // [nchunk][L][d]   unnormalized chunk sums a_c
-  float* ml;   // [nchunk][L][heads][2]   (m_c, l_c)
+  float* acc;  // [nchunk][Lq][d]   unnormalized chunk sums a_c
+  float* ml;   // [nchunk][Lq][heads][2]   (m_c, l_c)
 };
 
-__global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const float* __restrict__ QKV, AttPart part,
-                                                                       int L, int d, int heads) {
+__global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const float* __restrict__ Qm, int64_t ldq,
+                                                                       const float* __restrict__ Km,
+                                                                       const float* __restrict__ Vm, int64_t ldkv,
+                                                                       AttPart part, int Lq, int Lk, int d,
+                                                                       int heads) {
   extern __shared__ float4 att_smem4[];
   float* Ks = reinterpret_cast<float*>(att_smem4);  // [KC][KP]
   float* Vs = Ks + ATT_KC * ATT_KP;                 // [KC][HD]
@@ -156,7 +168,6 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
   griddep_wait();
   const int h = blockIdx.x, q0 = blockIdx.y * ATT_QB, c = blockIdx.z, k0 = c * ATT_KC;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ld = 3 * (int64_t)d;
   constexpr int HV = ATT_HD / 4;  // float4 per head row
   {
     constexpr int RQ = ATT_QB * HV / ATT_THREADS, RK = ATT_KC * HV / ATT_THREADS;
@@ -164,15 +175,15 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
 #pragma unroll
     for (int r = 0; r < RQ; ++r) {
       const int i = threadIdx.x + ATT_THREADS * r, p = q0 + i / HV;
-      qv[r] = p < L ? *reinterpret_cast<const float4*>(QKV + p * ld + h * ATT_HD + 4 * (i % HV))
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      qv[r] = p < Lq ? *reinterpret_cast<const float4*>(Qm + p * ldq + h * ATT_HD + 4 * (i % HV))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int r = 0; r < RK; ++r) {
       const int i = threadIdx.x + ATT_THREADS * r, p = k0 + i / HV;
-      const float* row = QKV + p * ld + h * ATT_HD + 4 * (i % HV);
-      kv[r] = p < L ? *reinterpret_cast<const float4*>(row + d) : make_float4(0.f, 0.f, 0.f, 0.f);
-      vv[r] = p < L ? *reinterpret_cast<const float4*>(row + 2 * d) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const int64_t off = p * ldkv + h * ATT_HD + 4 * (i % HV);
+      kv[r] = p < Lk ? *reinterpret_cast<const float4*>(Km + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+      vv[r] = p < Lk ? *reinterpret_cast<const float4*>(Vm + off) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int r = 0; r < RQ; ++r) {
@@ -207,7 +218,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
     fma2f(s01[0], s01[1], a0.w, a1.w, k.w, k.w);
     fma2f(s23[0], s23[1], a2.w, a3.w, k.w, k.w);
   }
-  const bool valid = k0 + lane < L;
+  const bool valid = k0 + lane < Lk;
   const float sc[4] = {s01[0], s01[1], s23[0], s23[1]};
   float* pw = Ps + warp * 4 * ATT_KC;
   float mq[4], lq[4];
@@ -232,7 +243,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[qq][i] = 0.f;
 #pragma unroll 2
-  for (int j = 0; j < ATT_KC; j += 4) {  // keys past L have p = 0 and zero V rows
+  for (int j = 0; j < ATT_KC; j += 4) {  // keys past Lk have p = 0 and zero V rows
     float4 pj[4];
 #pragma unroll
     for (int qq = 0; qq < 4; ++qq) pj[qq] = *reinterpret_cast<const float4*>(pw + qq * ATT_KC + j);
@@ -250,11 +261,11 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
 #pragma unroll
   for (int qq = 0; qq < 4; ++qq) {
     const int qi = q0 + warp * 4 + qq;
-    if (qi < L) {
-      *reinterpret_cast<float4*>(part.acc + ((int64_t)c * L + qi) * d + h * ATT_HD + lane * 4) =
+    if (qi < Lq) {
+      *reinterpret_cast<float4*>(part.acc + ((int64_t)c * Lq + qi) * d + h * ATT_HD + lane * 4) =
           make_float4(acc[qq][0], acc[qq][1], acc[qq][2], acc[qq][3]);
       if (lane == 0)
-        *reinterpret_cast<float2*>(part.ml + (((int64_t)c * L + qi) * heads + h) * 2) = make_float2(mq[qq], lq[qq]);
+        *reinterpret_cast<float2*>(part.ml + (((int64_t)c * Lq + qi) * heads + h) * 2) = make_float2(mq[qq], lq[qq]);
     }
   }
   griddep_launch();
@@ -669,8 +680,11 @@ struct StepPlan {
   size_t x, act_d, act_ff, pqk, pv, po, pgu, pdn, qkv, att, attml, rope, lm, bytes;
 };
 
-static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead) {
+// L rows run through the layers; Lk (0: L) is the canvas length, i.e. the attention's keys, the
+// RoPE positions and the hidden-state rows (Lk > L: the block rows of a cached step).
+static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead, int64_t Lk = 0) {
   const int64_t d = m->d_model, f = m->d_ff;
+  if (Lk <= 0) Lk = L;
   StepPlan S{};
   S.qk = plan_qgemm(DLLM_Q4_K, L, 2 * d, d);
   S.v = plan_qgemm(DLLM_Q6_K, L, d, d);
@@ -684,7 +698,7 @@ static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead
     return o;
   };
   const bool full = flags & DLLM_STREAM_FULL;
-  S.x = take(lmhead ? (size_t)L * d * 4 : 0);
+  S.x = take(lmhead ? (size_t)Lk * d * 4 : 0);
   S.act_d = take(act_layout(L, d).bytes);
   S.act_ff = take(act_layout(L, f).bytes);
   S.pqk = take((size_t)S.qk.splits * L * 2 * d * 4);
@@ -693,9 +707,9 @@ static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead
   S.pgu = take((size_t)S.gu.splits * L * 2 * f * 4);
   S.pdn = take((size_t)S.dn.splits * L * d * 4);
   S.qkv = take(full ? (size_t)L * 3 * d * 4 : 0);
-  S.att = take(full ? (size_t)((L + 31) / 32) * L * d * 4 : 0);
-  S.attml = take(full ? (size_t)((L + 31) / 32) * L * m->n_heads * 8 : 0);
-  S.rope = take(full ? (size_t)L * (m->head_dim / 2) * 8 : 0);
+  S.att = take(full ? (size_t)((Lk + 31) / 32) * L * d * 4 : 0);
+  S.attml = take(full ? (size_t)((Lk + 31) / 32) * L * m->n_heads * 8 : 0);
+  S.rope = take(full ? (size_t)Lk * (m->head_dim / 2) * 8 : 0);
   S.lm = 0;
   S.bytes = off;
   return S;
@@ -727,8 +741,9 @@ static int gemm(int type, const void* act, int64_t m, int64_t k, const void* w, 
 }
 
 // The forward pass over all layers; x is [L][d] (input for the linear stream, output always).
+// kv (optional, full stream only): per layer K (after RoPE) then V of every row, [layers][2][L][d].
 static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float* x, int flags, uint8_t* ws,
-                   const StepPlan& S, cudaStream_t s) {
+                   const StepPlan& S, cudaStream_t s, float* kv = nullptr) {
   const int d = m->d_model, f = m->d_ff, hd = m->head_dim;
   const bool full = flags & DLLM_STREAM_FULL;
   float* Pqk = reinterpret_cast<float*>(ws + S.pqk);
@@ -763,10 +778,11 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
       float* QKV = reinterpret_cast<float*>(ws + S.qkv);
       __half* planes = tc_att ? reinterpret_cast<__half*>(ws + S.qkv) : nullptr;
       const int64_t nquad = L * (3 * d / 4);
+      float* kc = kv ? kv + (int64_t)li * 2 * L * d : nullptr;
       cudaError_t e = launch_pdl(qkv_reduce_rope_kernel, dim3((unsigned)((nquad + 255) / 256)), dim3(256), 0, s,
                                  (const float*)Pqk, S.qk.splits, (const float*)Pv, S.v.splits,
                                  reinterpret_cast<const float2*>(ws + S.rope), (int)L, d, hd, 1.0f / sqrtf((float)hd),
-                                 QKV, planes);
+                                 QKV, planes, 0, kc, kc ? kc + L * d : nullptr);
       note_launch();
       if (e != cudaSuccess) return cuda_fail(e, "launch qkv reduce");
       const AttPart ap{reinterpret_cast<float*>(ws + S.att), reinterpret_cast<float*>(ws + S.attml)};
@@ -786,8 +802,9 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
         e = cudaFuncSetAttribute(attention_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
         const dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB), (unsigned)nchunk);
-        e = launch_pdl(attention_partial_kernel, ag, dim3(ATT_THREADS), ATT_SMEM, s, (const float*)QKV, ap, (int)L,
-                       d, m->n_heads);
+        e = launch_pdl(attention_partial_kernel, ag, dim3(ATT_THREADS), ATT_SMEM, s, (const float*)QKV,
+                       (int64_t)3 * d, (const float*)(QKV + d), (const float*)(QKV + 2 * d), (int64_t)3 * d, ap,
+                       (int)L, (int)L, d, m->n_heads);
       }
       note_launch();
       const dim3 mg((unsigned)act_rows_padded(L), (unsigned)((d / QK + 7) / 8));
@@ -815,6 +832,82 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
         return rc;
     } else {
       if ((rc = run_row<ROW_RESID_ONLY>(x, Pdn, S.dn.splits, L * d, d, nullptr, 0.f, (int)L, d, nullptr, s)))
+        return rc;
+    }
+  }
+  return DLLM_OK;
+}
+
+// The forward pass of a cached step over the block rows only (LLaDA's inter-step K/V cache,
+// "--dual-cache"): rows [b0, b0 + R) of the canvas (length L) run through every layer; their
+// queries attend to all L keys and values, which come from kv ([layers][2][L][d], K after
+// RoPE, then V) written by the last refreshing step, with the block's own rows overwritten by
+// their fresh K and V. x is [L][d]; only rows [b0, b0 + R) are computed. Not exact: the cached
+// rows outside the block do not see the block's new tokens until the next refresh.
+static int forward_block(const dllm_model* m, const int32_t* canvas, int64_t L, int64_t b0, int64_t R, float* x,
+                         float* kv, uint8_t* ws, const StepPlan& S, cudaStream_t s) {
+  const int d = m->d_model, f = m->d_ff, hd = m->head_dim;
+  float* Pqk = reinterpret_cast<float*>(ws + S.pqk);
+  float* Pv = reinterpret_cast<float*>(ws + S.pv);
+  float* Po = reinterpret_cast<float*>(ws + S.po);
+  float* Pgu = reinterpret_cast<float*>(ws + S.pgu);
+  float* Pdn = reinterpret_cast<float*>(ws + S.pdn);
+  void* actd = ws + S.act_d;
+  void* actf = ws + S.act_ff;
+  float* xb = x + b0 * d;
+  int rc;
+  cudaError_t e = launch_pdl(rope_table_kernel, dim3((unsigned)L), dim3(hd / 2), 0, s,
+                             reinterpret_cast<float2*>(ws + S.rope), (int)L, hd / 2, (double)m->rope_theta, hd);
+  note_launch();
+  if (e == cudaSuccess)
+    e = launch_pdl(embed_q4k_kernel, dim3((unsigned)R), dim3(256), 0, s, static_cast<const uint8_t*>(m->tok_embd),
+                   d / QK, canvas + b0, xb, d);
+  note_launch();
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch embedding");
+  if ((rc = quantize_rows(xb, R, d, d, m->layers[0].attn_norm, m->eps, actd, s))) return rc;
+  const int nchunk = (int)((L + ATT_KC - 1) / ATT_KC);
+  e = cudaFuncSetAttribute(attention_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
+  for (int li = 0; li < m->n_layers; ++li) {
+    const dllm_layer& Ly = m->layers[li];
+    float* kc = kv + (int64_t)li * 2 * L * d;
+    float* vc = kc + L * d;
+    if ((rc = gemm(DLLM_Q4_K, actd, R, d, Ly.wqk, 2 * d, Pqk, S.qk, s))) return rc;
+    if ((rc = gemm(DLLM_Q6_K, actd, R, d, Ly.wv, d, Pv, S.v, s))) return rc;
+    float* QKV = reinterpret_cast<float*>(ws + S.qkv);
+    const int64_t nquad = R * (3 * d / 4);
+    e = launch_pdl(qkv_reduce_rope_kernel, dim3((unsigned)((nquad + 255) / 256)), dim3(256), 0, s, (const float*)Pqk,
+                   S.qk.splits, (const float*)Pv, S.v.splits, reinterpret_cast<const float2*>(ws + S.rope), (int)R, d,
+                   hd, 1.0f / sqrtf((float)hd), QKV, (__half*)nullptr, (int)b0, kc, vc);
+    note_launch();
+    if (e != cudaSuccess) return cuda_fail(e, "launch qkv reduce");
+    const AttPart ap{reinterpret_cast<float*>(ws + S.att), reinterpret_cast<float*>(ws + S.attml)};
+    const dim3 ag(m->n_heads, (unsigned)((R + ATT_QB - 1) / ATT_QB), (unsigned)nchunk);
+    e = launch_pdl(attention_partial_kernel, ag, dim3(ATT_THREADS), ATT_SMEM, s, (const float*)QKV, (int64_t)3 * d,
+                   (const float*)kc, (const float*)vc, (int64_t)d, ap, (int)R, (int)L, d, m->n_heads);
+    note_launch();
+    const dim3 mg((unsigned)act_rows_padded(R), (unsigned)((d / QK + 7) / 8));
+    if (e == cudaSuccess)
+      e = launch_pdl(attn_merge_quant_kernel, mg, dim3(256), 0, s, ap, nchunk, (int)R, d, m->n_heads,
+                     quant_out(actd, R, d));
+    note_launch();
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch attention");
+    if ((rc = gemm(DLLM_Q4_K, actd, R, d, Ly.wo, d, Po, S.o, s))) return rc;
+    if ((rc = run_row<ROW_RESID_NORM_QUANT>(xb, Po, S.o.splits, R * d, d, Ly.ffn_norm, m->eps, (int)R, d, actd, s)))
+      return rc;
+    if ((rc = gemm(DLLM_Q4_K, actd, R, d, Ly.wgu, 2 * f, Pgu, S.gu, s))) return rc;
+    if ((rc = run_row<ROW_SWIGLU_QUANT>(nullptr, Pgu, S.gu.splits, R * 2 * f, 2 * f, nullptr, 0.f, (int)R, f, actf,
+                                        s)))
+      return rc;
+    if ((rc = gemm(DLLM_Q6_K, actf, R, f, Ly.wdown, d, Pdn, S.dn, s))) return rc;
+    if (li + 1 < m->n_layers) {
+      if ((rc = run_row<ROW_RESID_NORM_QUANT>(xb, Pdn, S.dn.splits, R * d, d, m->layers[li + 1].attn_norm, m->eps,
+                                              (int)R, d, actd, s)))
+        return rc;
+    } else {
+      if ((rc = run_row<ROW_RESID_ONLY>(xb, Pdn, S.dn.splits, R * d, d, nullptr, 0.f, (int)R, d, nullptr, s)))
         return rc;
     }
   }
@@ -885,6 +978,62 @@ DLLM_API int dllm_denoise_step(const dllm_model* m, int32_t* canvas, int64_t L, 
   cudaStream_t s = (cudaStream_t)stream;
   if ((rc = forward(m, canvas, L, x, DLLM_STREAM_FULL, base, S, s))) return rc;
   const size_t lm_off = align_up(S.bytes, 1024);
+  return dllm_lmhead_masked_select(x, L, m->d_model, m->d_model, m->out_norm, m->eps, m->w_out, m->vocab, canvas,
+                                   m->mask_id, block_begin, block_end, k_commit, out_pos, out_id, out_conf, nullptr,
+                                   nullptr, base + lm_off, ws_bytes - lm_off, stream);
+}
+
+DLLM_API size_t dllm_kv_cache_bytes(const dllm_model* m, int64_t L) {
+  if (!m || L <= 0 || m->d_model <= 0 || m->n_layers <= 0) return 0;
+  return (size_t)m->n_layers * 2 * (size_t)L * m->d_model * 4;
+}
+
+DLLM_API size_t dllm_denoise_cached_workspace_bytes(const dllm_model* m, int64_t L, int32_t block_rows) {
+  if (!m || L <= 0 || block_rows <= 0 || block_rows > L || m->d_model <= 0 || m->d_ff <= 0) return 0;
+  const StepPlan F = step_plan(m, L, DLLM_STREAM_FULL, true);
+  const StepPlan B = step_plan(m, block_rows, DLLM_STREAM_FULL, true, L);
+  return align_up(std::max(F.bytes, B.bytes), 1024) + dllm_lmhead_workspace_bytes(block_rows, m->vocab, m->d_model);
+}
+
+DLLM_API int dllm_denoise_step_cached(const dllm_model* m, int32_t* canvas, int64_t L, int32_t block_begin,
+                                      int32_t block_end, int32_t k_commit, int32_t refresh, float* kv_cache,
+                                      size_t kv_bytes, int32_t* out_pos, int32_t* out_id, float* out_conf,
+                                      float* hidden_out, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  int rc = check_model(m, L, "dllm_denoise_step_cached");
+  if (rc) return rc;
+  if ((rc = check_device())) return rc;
+  if (!device_ptr(canvas) || !device_ptr(m->tok_embd) || !device_ptr(m->w_out) || !device_ptr(m->out_norm))
+    return fail(DLLM_E_INVAL, "dllm_denoise_step_cached: canvas / tok_embd / w_out / out_norm must be device pointers");
+  if (refresh != 0 && refresh != 1) return fail(DLLM_E_INVAL, "dllm_denoise_step_cached: refresh must be 0 or 1");
+  const int64_t R = (int64_t)block_end - block_begin;
+  if (block_begin < 0 || block_end > L || R <= 0 || R > 160)
+    return fail(DLLM_E_INVAL, "dllm_denoise_step_cached: block [%d, %d) must lie in [0, L=%lld) and hold 1..160 rows",
+                block_begin, block_end, (long long)L);
+  const size_t kv_need = dllm_kv_cache_bytes(m, L);
+  if (!kv_cache || kv_bytes < kv_need || !device_ptr(kv_cache))
+    return fail(DLLM_E_WORKSPACE, "dllm_denoise_step_cached: kv_cache has %zu bytes, needs %zu (dllm_kv_cache_bytes)",
+                kv_cache ? kv_bytes : (size_t)0, kv_need);
+  if ((reinterpret_cast<uintptr_t>(kv_cache) & 15) != 0)
+    return fail(DLLM_E_ALIGN, "dllm_denoise_step_cached: kv_cache must be 16-byte aligned");
+  const size_t need = dllm_denoise_cached_workspace_bytes(m, L, (int32_t)R);
+  if (!ws || ws_bytes < need || !device_ptr(ws))
+    return fail(DLLM_E_WORKSPACE, "dllm_denoise_step_cached: workspace has %zu bytes, needs %zu",
+                ws ? ws_bytes : (size_t)0, need);
+  if ((reinterpret_cast<uintptr_t>(ws) & 1023) != 0)
+    return fail(DLLM_E_ALIGN, "dllm_denoise_step_cached: ws must be 1024-byte aligned");
+  if (hidden_out && (!device_ptr(hidden_out) || (reinterpret_cast<uintptr_t>(hidden_out) & 15) != 0))
+    return fail(DLLM_E_INVAL, "dllm_denoise_step_cached: hidden_out must be a 16-byte aligned device pointer");
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const StepPlan F = step_plan(m, L, DLLM_STREAM_FULL, true);
+  const StepPlan B = step_plan(m, R, DLLM_STREAM_FULL, true, L);
+  float* x = hidden_out ? hidden_out : reinterpret_cast<float*>(base + F.x);  // F.x == B.x == 0
+  cudaStream_t s = (cudaStream_t)stream;
+  if (refresh)
+    rc = forward(m, canvas, L, x, DLLM_STREAM_FULL, base, F, s, kv_cache);
+  else
+    rc = forward_block(m, canvas, L, block_begin, R, x, kv_cache, base, B, s);
+  if (rc) return rc;
+  const size_t lm_off = align_up(std::max(F.bytes, B.bytes), 1024);
   return dllm_lmhead_masked_select(x, L, m->d_model, m->d_model, m->out_norm, m->eps, m->w_out, m->vocab, canvas,
                                    m->mask_id, block_begin, block_end, k_commit, out_pos, out_id, out_conf, nullptr,
                                    nullptr, base + lm_off, ws_bytes - lm_off, stream);

@@ -180,3 +180,54 @@ def test_denoise_step_llada_shapes_two_layers():
     dims = dict(synth.LLADA, n_layers=2)
     exact = _full_step_check(dims, synth.config_seed(4), 148, 20, 52, 4, n_steps=2)
     print(f"denoise LLaDA shapes: {exact}/2 steps with commits identical to the oracle's order")
+
+
+def _cached_steps_check(dims, seed, L, b0, b1, k, n_steps):
+    """Inter-step K/V cache: step 0 refreshes, the following steps recompute the block only.
+    Each step starts from the oracle's canvas; the GPU's cache holds its own K/V from its refresh.
+    Block rows of the hidden state are held to the layer-stream bar, commits to check_commits."""
+    lws = _layers(seed, dims, dims["n_layers"])
+    table = synth.embed_weights(seed, dims)
+    head = synth.head_weights(seed, dims)
+    head["out_norm"] = (1.0 + 0.2 * synth.activations(seed + 300, 1, dims["d_model"])[0]).astype(np.float32)
+    canvas = synth.canvas(seed, prompt_len=b0, gen_len=L - b0, mask_id=dims["mask_id"],
+                          prompt_max=min(126000, dims["vocab"] - 10))
+    model = dl.DeviceModel(dims, lws, table, head)
+    kv = torch.empty(dl.kv_cache_bytes(model, L) // 4, dtype=torch.float32, device="cuda")
+    hid = torch.zeros((L, dims["d_model"]), device="cuda")
+    ref_canvas = canvas.copy()
+    cache = []
+    exact = 0
+    for step in range(n_steps):
+        refresh = step == 0
+        before = ref_canvas.copy()
+        gcanvas = torch.from_numpy(before.copy()).cuda()
+        x = orc.forward_cached(lws, table, ref_canvas, dims, b0, b1, refresh, cache)
+        ref = orc.lmhead_commit(x, ref_canvas, dims["mask_id"], b0, b1, k, head["out_norm"], head["w_out"],
+                                dims["eps"])
+        conf_by_pos = np.full(L, -1.0)
+        conf_by_pos[ref["rows"]] = ref["conf_rows"]
+        out = dl.denoise_step_cached(model, gcanvas, b0, b1, k, refresh, kv, hidden_out=hid)
+        dl.check()
+        gh = hid.cpu().numpy()
+        rows = slice(0, L) if refresh else slice(b0, b1)
+        _stream_ok(gh[rows], x[rows], dims["n_layers"], f"cached step {step}")
+        errs = np.zeros(L)
+        errs[rows] = _row_errs(gh[rows], x[rows])
+        exact += check_commits(out["pos"].cpu().numpy(), out["id"].cpu().numpy(), gcanvas.cpu().numpy(), before,
+                               ref, conf_by_pos, k, errs, out["conf"].cpu().numpy())
+    return exact
+
+
+def test_dual_cache_small_four_steps():
+    # refresh, then three block-only steps; 200 rows also puts the cached keys in several chunks
+    for L in (40, 200):
+        exact = _cached_steps_check(SMALL, 61 + L, L, 8, 40, 4, n_steps=4)
+        print(f"dual cache small L={L}: {exact}/4 steps with commits identical to the oracle's order")
+
+
+def test_dual_cache_llada_shapes_two_layers():
+    dims = dict(synth.LLADA, n_layers=2)
+    exact = _cached_steps_check(dims, synth.config_seed(4) + 5, 148, 20, 52, 4, n_steps=3)
+    print(f"dual cache LLaDA shapes: {exact}/3 steps with commits identical to the oracle's order")
+

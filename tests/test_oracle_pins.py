@@ -482,6 +482,50 @@ def test_gumbel_max_limits():
     assert np.array_equal(a, b) and not np.array_equal(a, c)
 
 
+TINY = dict(n_layers=2, d_model=256, n_heads=2, head_dim=128, d_ff=512, vocab=300, mask_id=297, eps=1e-5,
+            rope_theta=500000.0)
+
+
+def _tiny_model(seed):
+    lws = [synth.layer_weights(seed, i, TINY) for i in range(TINY["n_layers"])]
+    for i, lw in enumerate(lws):  # norm weights away from 1 so that every norm matters
+        lw["attn_norm"] = (1.0 + 0.2 * synth.activations(seed + 10 + i, 1, TINY["d_model"])[0]).astype(np.float32)
+        lw["ffn_norm"] = (1.0 + 0.2 * synth.activations(seed + 20 + i, 1, TINY["d_model"])[0]).astype(np.float32)
+    table = synth.embed_weights(seed, TINY)
+    canvas = synth.canvas(seed, prompt_len=8, gen_len=16, mask_id=TINY["mask_id"], prompt_max=290)
+    return lws, table, canvas
+
+
+def test_cached_step_right_after_refresh_equals_the_full_forward():
+    # nothing has changed since the refresh, so the cached K/V equal the fresh ones and the block
+    # rows of the cached step reproduce the uncached forward (to rounding)
+    lws, table, canvas = _tiny_model(71)
+    cache = []
+    x_full = orc.forward_cached(lws, table, canvas, TINY, 8, 16, True, cache)
+    x_blk = orc.forward_cached(lws, table, canvas, TINY, 8, 16, False, cache)
+    np.testing.assert_allclose(x_blk[8:16], x_full[8:16], rtol=1e-12, atol=1e-12)
+    assert np.all(x_blk[:8] == 0) and np.all(x_blk[16:] == 0)
+
+
+def test_cached_step_sees_the_block_but_not_stale_rows():
+    lws, table, canvas = _tiny_model(72)
+    cache = []
+    orc.forward_cached(lws, table, canvas, TINY, 8, 16, True, cache)
+    # a token outside the block changes after the refresh: the cached step cannot see it
+    outside = canvas.copy()
+    outside[20] = 5
+    a = orc.forward_cached(lws, table, canvas, TINY, 8, 16, False, [(k.copy(), v.copy()) for k, v in cache])
+    b = orc.forward_cached(lws, table, outside, TINY, 8, 16, False, [(k.copy(), v.copy()) for k, v in cache])
+    np.testing.assert_array_equal(a[8:16], b[8:16])
+    fresh = orc.forward_cached(lws, table, outside, TINY, 8, 16, True, [])
+    assert np.abs(fresh[8:16] - a[8:16]).max() > 1e-6  # the uncached step does see it
+    # a token inside the block changes: the cached step recomputes the block and sees it
+    inside = canvas.copy()
+    inside[10] = 5
+    c = orc.forward_cached(lws, table, inside, TINY, 8, 16, False, [(k.copy(), v.copy()) for k, v in cache])
+    assert np.abs(c[8:16] - a[8:16]).max() > 1e-6
+
+
 def test_commit_invariants_random():
     rng = np.random.default_rng(3)
     L, mask = 148, 126336
