@@ -43,3 +43,21 @@ def test_host_only_calls():
     assert L.dllm_act_rows(148) == 160 and L.dllm_act_rows(16) == 32 and L.dllm_act_rows(512) == 512
     assert L.dllm_act_bytes(148, 4096) >= 160 * 4096 * 2
     assert L.dllm_act_bytes(148, 300) == 0
+
+
+def test_host_only_size_queries_of_the_cache_and_the_head():
+    # size queries read only the model's dimensions: no device is touched
+    dlbuild.build()
+    L = dl.lib()
+    m = dl._Model(n_layers=32, d_model=4096, n_heads=32, head_dim=128, d_ff=12288, vocab=126464, mask_id=126336,
+                  eps=1e-5, rope_theta=500000.0)
+    ref = ctypes.byref(m)
+    assert L.dllm_kv_cache_bytes(ref, 148) == 32 * 2 * 148 * 4096 * 4  # f32 K and V per layer
+    assert L.dllm_kv_cache_bytes(ref, 0) == 0
+    blk = L.dllm_denoise_cached_workspace_bytes(ref, 148, 32)
+    assert blk >= L.dllm_denoise_workspace_bytes(ref, 148, 32) > 0
+    assert L.dllm_denoise_cached_workspace_bytes(ref, 148, 149) == 0  # more block rows than the canvas
+    # the head's workspace holds, per row and tile quadrant, the softmax, entropy and draw partials
+    P = (126464 + 127) // 128 * 4
+    assert L.dllm_lmhead_workspace_bytes(32, 126464, 4096) >= 7 * P * 32 * 4
+    assert L.dllm_lmhead_workspace_bytes(161, 126464, 4096) == 0
