@@ -282,6 +282,9 @@ DLLM_API int dllm_denoise_step(const dllm_model* m, int32_t* canvas, int64_t L, 
  *       their fresh K and V, which are also written back), O, FFN; then the head and commit
  *       on the block as in dllm_denoise_step. Rows outside the block keep the K and V of the
  *       last refresh, so the result is an approximation of the uncached step.
+ *   A cached step reads what the last refreshing step on this cache stored (same model, same L):
+ *   the first step on a cache must refresh, and a cached step before any refresh computes from
+ *   undefined cache contents (no fault: every access stays inside the buffer).
  *   hidden_out (may be NULL): f32 [L][d_model]; a cached step writes the block's rows only.
  *   ws: >= dllm_denoise_cached_workspace_bytes(m, L, block_end - block_begin), 1024-byte aligned.
  * Errors: as dllm_denoise_step, plus DLLM_E_WORKSPACE for a short kv_cache, DLLM_E_ALIGN for a
