@@ -20,7 +20,16 @@ Readings where the pages are silent:
 * the "linear stream" workload has no attention: the O projection consumes
   the V projection's output;
 * confidence = softmax probability of the argmax token; ties in the argmax go
-  to the lowest token id, ties in top-k to the lowest position.
+  to the lowest token id, ties in top-k to the lowest position;
+* the entropy confidence (README, "Each model's own sampler": Dream's entropy
+  ranking) is minus the natural-log entropy of the row's softmax;
+* temperature sampling (specification section 14: temperature, categorical
+  sampling, deterministic PRNG) is the Gumbel-max draw with noise from
+  counter-based SplitMix64 keyed by (seed, step, position, token); the draw's
+  confidence is its probability under the untempered softmax;
+* the inter-step K/V cache (README status table, "--dual-cache"; specification
+  section 23) refreshes every layer's K and V on a block's first step and then
+  recomputes only the block's rows against them.
 """
 from __future__ import annotations
 
