@@ -499,8 +499,8 @@ uint64_t orc_splitmix64_at(uint64_t seed, uint64_t c) {
  * sampling, deterministic PRNG) by the Gumbel-max rule: the draw
  * argmax_v (l_v / T + g_v) with independent standard Gumbel g_v is
  * distributed as softmax(l / T). g_v = -log(-log u_v), u_v uniform in (0, 1)
- * from the top 24 bits of SplitMix64 output number
- * c = step * 2^40 + position * 2^24 + v: u = (bits + 1/2) / 2^24. Per row:
+ * from the top 23 bits of SplitMix64 output number
+ * c = step * 2^40 + position * 2^24 + v: u = (bits + 1/2) / 2^23. Per row:
  * the drawn id (lowest on ties), its probability under the untempered
  * softmax, exp(l_id - l_max) / sum_v exp(l_v - l_max), and the gap between
  * the best and second-best perturbed scores (a diagnostic). f64 throughout.
@@ -514,7 +514,7 @@ void orc_row_sample(const double* logits, int64_t rows, int64_t vocab, double te
     double s1 = -INFINITY, s2 = -INFINITY, mx = -INFINITY;
     for (int64_t v = 0; v < vocab; ++v) {
       const uint64_t c = ((uint64_t)step << 40) | ((uint64_t)pos[r] << 24) | (uint64_t)v;
-      const double u = ((double)(orc_splitmix64_at(seed, c) >> 40) + 0.5) / 16777216.0;
+      const double u = ((double)(orc_splitmix64_at(seed, c) >> 41) + 0.5) / 8388608.0;
       const double score = l[v] / temperature - log(-log(u));
       if (score > s1) {
         s2 = s1;

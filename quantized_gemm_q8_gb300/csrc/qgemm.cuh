@@ -315,14 +315,15 @@ __device__ __forceinline__ Q4Fold q4k_fold(float d, float dmin, bool* bad) {
 // Gumbel noise of one (row, vocabulary entry) of a sampling step: counter-based SplitMix64
 // (Steele, Lea and Flood, "Fast splittable pseudorandom number generators"): the output for
 // counter c of the stream `seed` is mix(seed + (c + 1) * 0x9E3779B97F4A7C15). Counter
-// c = step * 2^40 + position * 2^24 + vocabulary id; its top 24 bits give the uniform
-// u = (bits + 1/2) / 2^24 in (0, 1), and g = -log(-log u).
+// c = step * 2^40 + position * 2^24 + vocabulary id; its top 23 bits give the uniform
+// u = (bits + 1/2) / 2^23, exact in f32 and strictly inside (0, 1) (with 24 bits the top value
+// would round to 1 and give infinite noise), and g = -log(-log u).
 __device__ __forceinline__ float gumbel_noise(unsigned long long seed, unsigned long long c) {
   unsigned long long z = seed + (c + 1ull) * 0x9E3779B97F4A7C15ull;
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
   z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
   z ^= z >> 31;
-  const float u = ((float)(z >> 40) + 0.5f) * 5.9604644775390625e-8f;  // 2^-24
+  const float u = ((float)(z >> 41) + 0.5f) * 1.1920928955078125e-7f;  // 2^-23
   return -logf(-logf(u));
 }
 
