@@ -198,9 +198,10 @@ enum { DLLM_CONF_PMAX = 0, DLLM_CONF_NEG_ENTROPY = 1 };
  *       id). u_v comes from counter-based SplitMix64 (Steele, Lea and Flood, "Fast splittable
  *       pseudorandom number generators", OOPSLA 2014): z = mix(seed + (c + 1) 0x9E3779B97F4A7C15)
  *       for the counter c = step * 2^40 + p * 2^24 + v (p the canvas position, v the token id),
- *       u_v = ((z >> 41) + 1/2) / 2^23 (23 bits: exact in f32 and strictly inside (0, 1)). DLLM_CONF_PMAX is then the drawn token's probability
- *       under the untempered softmax, exp(l_draw - l_max) / sum_v exp(l_v - l_max); the
- *       entropy confidence does not depend on the draw. Same inputs give the same draws.
+ *       u_v = ((z >> 41) + 1/2) / 2^23 (23 bits: exact in f32 and strictly inside (0, 1)).
+ *       DLLM_CONF_PMAX is then the drawn token's probability under the untempered softmax,
+ *       exp(l_draw - l_max) / sum_v exp(l_v - l_max); the entropy confidence does not depend on
+ *       the draw. Same inputs give the same draws.
  * Errors as below, plus DLLM_E_INVAL for a negative or non-finite temperature, or (sampling
  * only) L > 65536 or step >= 2^24. */
 DLLM_API int dllm_lmhead_select(const float* hidden, int64_t L, int64_t d, int64_t ldh, const float* out_norm_w,
