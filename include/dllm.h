@@ -190,8 +190,9 @@ enum { DLLM_CONF_PMAX = 0, DLLM_CONF_NEG_ENTROPY = 1 };
 /* dllm_lmhead_select: dllm_lmhead_masked_select with the confidence chosen by conf_kind
  * (DLLM_CONF_PMAX or DLLM_CONF_NEG_ENTROPY; anything else is DLLM_E_INVAL) and an optional
  * temperature (the specification's sampling section: temperature, categorical sampling,
- * deterministic PRNG; "Fixed-seed runs are deterministic"). out_conf and row_conf hold the
- * chosen confidence. The block may be the whole canvas (every masked position, R up to 160).
+ * deterministic PRNG; its section 30, definition of done: a fixed seed gives the same run).
+ * out_conf and row_conf hold the chosen confidence. The block may be the whole canvas (every
+ * masked position, R up to 160).
  *   temperature == 0: greedy, the row's token is the argmax (as dllm_lmhead_masked_select).
  *   temperature  > 0: the row's token is a draw from softmax(logits / temperature) by the
  *       Gumbel-max rule, argmax_v (l_v / temperature + g_v), g_v = -log(-log u_v) (ties: lowest

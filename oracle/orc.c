@@ -27,7 +27,8 @@
  *     scatter.
  *   - README, "Each model's own sampler": LLaDA ranks masked positions by
  *     the argmax token's probability, Dream by entropy.
- *   - Technical specification, "Fixed-seed runs are deterministic" and the
+ *   - Technical specification, section 30 (definition of done: a fixed seed
+ *     gives the same run every time), section 14 (sampling) and the
  *     --seed / --temperature flags: temperature sampling from a seeded,
  *     deterministic generator (here counter-based SplitMix64).
  *   - README, "How it works": the LM head runs only on the masked positions
@@ -169,8 +170,9 @@ int orc_dequant(int type, const uint8_t* blocks, int64_t nblocks, double* out) {
  *   else iscale = 127 / amax (f32 division), q = clamp(rint(x * iscale),
  *   -127, 127) with a single f32 multiply and round-half-even, d = amax / 127.
  *   bsum[g] = sum of the 16 codes of group g (exact integer).
- * The pages fix only "int8 with one f32 scale per 256 plus int sums per 16";
- * the symmetric 127/amax rule is this build's reading of it.
+ * Development plan, "Compute design", fixes the format (8-bit codes, a single
+ * f32 scale for each 256 values, integer sums for each 16) but not the
+ * rounding rule; the symmetric 127/amax rule above is this build's reading.
  * ------------------------------------------------------------------------- */
 void orc_quantize_q8k(const float* x, int64_t rows, int64_t k, int64_t ldx,
                       int8_t* q, float* d, int16_t* bsum) {
