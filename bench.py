@@ -28,7 +28,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "ms/denoising step at L=148 (LLaDA-8B shapes); Q4_K GEMM TOPS vs roofline"
 WORKLOAD = "llada8b_denoise_step_L148"
-L_CANVAS, PROMPT, GEN, BLOCK, K_COMMIT = 148, 20, 128, 32, 4
+# the pages' benchmark protocol: 20 prompt + 128 generated tokens, blocks of 32, 32 steps (the
+# library's schedule then commits 4 tokens per step)
+L_CANVAS, PROMPT, GEN, BLOCK, STEPS = 148, 20, 128, 32, 32
 SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -48,8 +50,14 @@ def _peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def _blocks():
-    return [(PROMPT + BLOCK * b, PROMPT + BLOCK * (b + 1)) for b in range(GEN // BLOCK)]
+def _schedule():
+    """(schedule, kinds, kind index per step): the library's transfer schedule of the protocol,
+    its distinct (block_begin, block_end, k) step kinds, and each step's kind."""
+    import quantized_gemm_q8_gb300 as dl
+
+    sched = dl.schedule(PROMPT, GEN, BLOCK, STEPS)
+    kinds = sorted(set(sched))
+    return sched, kinds, [kinds.index(t) for t in sched]
 
 
 class ClockSampler:
@@ -135,13 +143,14 @@ def oracle_step_sample(dims, seed, n_layers_sample=2):
         x, _ = orc.layer(lw, x, dims, attention_on=True)
     t2 = time.perf_counter()
     cv = canvas.copy()
-    orc.lmhead_commit(x, cv, dims["mask_id"], PROMPT, PROMPT + BLOCK, K_COMMIT, head["out_norm"], head["w_out"],
-                      dims["eps"])
+    b0, b1, k = _schedule()[0][0]
+    orc.lmhead_commit(x, cv, dims["mask_id"], b0, b1, k, head["out_norm"], head["w_out"], dims["eps"])
     t3 = time.perf_counter()
     per_layer = (t2 - t1) / n_layers_sample
     ms = 1e3 * ((t1 - t0) + dims["n_layers"] * per_layer + (t3 - t2))
-    desc = (f"embedding + {n_layers_sample} of {dims['n_layers']} layers (L=148, with attention) + masked LM head "
-            f"(32 rows x 126464 x 4096) of one step, layer time scaled x{dims['n_layers']}/{n_layers_sample}")
+    desc = (f"estimate: embedding + {n_layers_sample} of {dims['n_layers']} layers (L=148, with attention) + masked "
+            f"LM head (32 rows x 126464 x 4096) of one step, measured; the layer time scaled "
+            f"x{dims['n_layers']}/{n_layers_sample} to the full depth")
     return ms, orc.num_threads(), desc
 
 
@@ -165,7 +174,9 @@ def run_reference(args, rank):
         "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random LLaDA-8B-shaped weights)",
         "config": {"workload": WORKLOAD, "L": L_CANVAS, "layers": dims["n_layers"], "block": BLOCK,
-                   "k_commit": K_COMMIT, "l2": "weights (4.9 GB) > L2"},
+                   "k_commit": _schedule()[0][0][2], "l2": "weights (4.9 GB) > L2",
+                   "value_kind": "estimate: 2 of the 32 layers timed, scaled to 32 (a full oracle step takes "
+                                 "about half a minute per layer pair on these cores)"},
         "cpu_baseline": {"kind": "oracle", "value": value, "unit": "ms/step", "cores": cores, "sample": desc},
         "e2e": {"value": value, "unit": "ms/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -203,12 +214,11 @@ def run_ours(args, rank, local_rank, world):
     model = dl.model_from_seed(dims, seed)
     canvas0 = torch.from_numpy(synth.canvas(seed)).cuda()
     canvas = canvas0.clone()
-    blocks = _blocks()
-    graphs = dl.StepGraphs(model, canvas, blocks, K_COMMIT)
-    steps_per_block = 32 // len(blocks)  # 32 steps, 8 per block
+    sched, kinds, kind_of = _schedule()
+    graphs = dl.StepGraphs(model, canvas, kinds)
 
-    def block_of(s):
-        return (s // steps_per_block) % len(blocks)
+    def block_of(s):  # the graph of step s of the protocol's schedule (repeated past its end)
+        return kind_of[s % len(sched)]
 
     stream = graphs.stream
     torch.cuda.synchronize()
@@ -236,7 +246,8 @@ def run_ours(args, rank, local_rank, world):
 
     # ---- end-to-end through the public call with host buffers (H2D canvas, D2H commits) ----
     canvas_h = torch.from_numpy(synth.canvas(seed)).pin_memory()
-    out_h = torch.empty(2 * K_COMMIT, dtype=torch.int32).pin_memory()
+    kmax = max(k for _, _, k in kinds)
+    out_h = torch.empty(2 * kmax, dtype=torch.int32).pin_memory()
     out_dev = torch.cat([graphs.out["pos"], graphs.out["id"]])
     e2e_steps = min(args.steps, 32)
     torch.cuda.synchronize()
@@ -248,7 +259,8 @@ def run_ours(args, rank, local_rank, world):
             torch.cat([graphs.out["pos"], graphs.out["id"]], out=out_dev)
             out_h.copy_(out_dev, non_blocking=True)
         stream.synchronize()
-        pos, ids = out_h[:K_COMMIT].numpy(), out_h[K_COMMIT:].numpy()
+        k = sched[s % len(sched)][2]
+        pos, ids = out_h[:k].numpy(), out_h[kmax:kmax + k].numpy()
         for p, i in zip(pos, ids):
             if p >= 0:
                 canvas_h[p] = int(i)
@@ -310,11 +322,12 @@ def run_ours(args, rank, local_rank, world):
         "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded random LLaDA-8B-shaped Q4_K/Q6_K weights, 20 random prompt ids + 128 masks)",
         "config": {"workload": WORKLOAD, "L": L, "layers": dims["n_layers"], "d_model": d, "d_ff": f,
-                   "vocab": dims["vocab"], "block": BLOCK, "k_commit": K_COMMIT, "graph": "one CUDA graph per block",
+                   "vocab": dims["vocab"], "block": BLOCK, "k_commit": sched[0][2],
+                   "schedule": f"dllm_schedule({PROMPT}, {GEN}, {BLOCK}, {STEPS})", "graph": "one CUDA graph per block",
                    "l2": "no flush: weights read per step (4.9 GB) exceed L2",
                    "parallelism": f"replicas x{world}",
                    "arith": "Q8_K x Q4_K/Q6_K integer sums exact in f16 tcgen05 MMA, f32 accumulate/epilogue"},
-        "tok_per_s": K_COMMIT * world / (value * 1e-3),
+        "tok_per_s": (sum(k for _, _, k in sched) / len(sched)) * world / (value * 1e-3),
         "step_roofline_ms": t_roof_ms, "step_roofline_frac": t_roof_ms / ms_per_step,
         "algorithmic_tops": ops_step / (ms_per_step * 1e-3) / 1e12,
         "gpu_launches": int(graphs.launches_per_step[0]) * args.steps,
@@ -507,7 +520,7 @@ def run_configs(args):
     canvas0 = torch.from_numpy(synth.canvas(seed3)).cuda()
     canvas = canvas0.clone()
     hidden = torch.from_numpy(synth.activations(seed3, L_CANVAS, d)).cuda()
-    b0, b1 = PROMPT, PROMPT + BLOCK
+    b0, b1, K_COMMIT = _schedule()[0][0]  # the protocol's first step: block 0, 4 commits
     ws3 = torch.empty(max(dl.lmhead_workspace_bytes(b1 - b0, vocab, d), 1), dtype=torch.uint8, device="cuda")
 
     def run_head():
@@ -602,18 +615,17 @@ def run_configs(args):
     canvas_a = torch.from_numpy(synth.canvas(seed4)).cuda()
     canvas_b = canvas_a.clone()
     start = canvas_a.clone()
-    blocks = _blocks()
-    spb = 32 // len(blocks)
-    plain = dl.StepGraphs(model4, canvas_a, blocks, K_COMMIT)
-    cached = dl.CachedStepGraphs(model4, canvas_b, blocks, K_COMMIT)
+    sched, kinds, kind_of = _schedule()
+    plain = dl.StepGraphs(model4, canvas_a, kinds)
+    cached = dl.CachedStepGraphs(model4, canvas_b, kinds)
 
     def run_plain():
-        for st in range(32):
-            plain.replay(st // spb)
+        for st in range(len(sched)):
+            plain.replay(kind_of[st])
 
-    def run_cached():
-        for st in range(32):
-            cached.replay(st // spb, st % spb == 0)
+    def run_cached():  # a block's first step refreshes the cache
+        for st in range(len(sched)):
+            cached.replay(kind_of[st], st == 0 or sched[st][0] != sched[st - 1][0])
 
     def timed_on(st, fn):
         torch.cuda.synchronize()
@@ -661,6 +673,12 @@ def main():
                     help="one JSON line per other configuration (1, 2, 3, 5) instead of the step")
     args = ap.parse_args()
     rank, local_rank, world = _env_dist()
+    if args.gpus != world and args.impl == "ours" and not (args.only_kernel or args.configs):
+        # N replicas come from the launcher (one process per GPU); a plain run would measure one GPU
+        sys.stderr.write(f"bench.py --gpus {args.gpus}: WORLD_SIZE is {world}; launch N > 1 replicas with "
+                         f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py --gpus "
+                         f"{args.gpus} ...\n")
+        sys.exit(2)
     if args.only_kernel:
         run_only_kernel(args)
     elif args.configs:

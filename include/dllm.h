@@ -298,6 +298,26 @@ DLLM_API int dllm_denoise_step_cached(const dllm_model* m, int32_t* canvas, int6
                                       size_t kv_bytes, int32_t* out_pos, int32_t* out_id, float* out_conf,
                                       float* hidden_out, void* ws, size_t ws_bytes, dllm_stream_t stream);
 
+/* ---- transfer schedule (Development plan, "Benchmark protocol": 128 generated tokens in
+ * blocks of 32 over 32 steps, 4 commits per step, transfer counts checked against the reference
+ * generator; Technical Specification, section 13 "Scheduler Interface": select the positions
+ * to commit, then update the canvas) -------------------------------------------------------
+ * Host-only calls: no device work, no stream; outputs are HOST arrays owned by the caller.
+ * dllm_transfer_counts: how many of a block's `masked` masked positions are committed at each
+ *   of its `steps` steps: floor(masked / steps) at every step, plus one more at each of the
+ *   first masked % steps steps. counts: int32 [steps]; the counts sum to `masked`.
+ *   Errors: DLLM_E_INVAL (masked outside [0, 2^30], steps outside [1, 2^20], counts NULL).
+ * dllm_schedule: the whole generation of gen_len positions after prompt_len, in blocks of
+ *   block_len over `steps` steps: step s works on block b = s / (steps / blocks), the positions
+ *   [prompt_len + b * block_len, prompt_len + (b + 1) * block_len), and commits k[s] tokens, the
+ *   dllm_transfer_counts(block_len, steps / blocks) entry of its place in the block (every
+ *   position of a block is masked when the block starts). block_begin, block_end, k: int32
+ *   [steps]. Errors: DLLM_E_INVAL (a size out of range, gen_len not a multiple of block_len,
+ *   steps not a multiple of the block count, a NULL output). */
+DLLM_API int dllm_transfer_counts(int64_t masked, int64_t steps, int32_t* counts);
+DLLM_API int dllm_schedule(int64_t prompt_len, int64_t gen_len, int64_t block_len, int64_t steps,
+                           int32_t* block_begin, int32_t* block_end, int32_t* k);
+
 /* Benchmark hooks.
  * dllm_launch_count: number of kernels this library has enqueued so far in this process (a
  *   host-side counter; launches recorded during stream capture count once, at capture).

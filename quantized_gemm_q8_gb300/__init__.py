@@ -65,6 +65,8 @@ _SIGS = {
     "dllm_qgemm_partials_bytes": ([INT, I64, I64, I64], SZ),
     "dllm_qgemm_partials": ([INT, P, I64, I64, P, I64, P, SZ, P, P], INT),
     "dllm_qgemm_noalloc": ([INT, P, I64, I64, P, I64, P, I64, INT, P], INT),
+    "dllm_transfer_counts": ([I64, I64, P], INT),
+    "dllm_schedule": ([I64, I64, I64, I64, P, P, P], INT),
 }
 
 
@@ -210,6 +212,23 @@ def qgemm_partials(type_id: int, act: torch.Tensor, m: int, k: int, w_packed: to
 
 def selftest_timeout(limit_cycles: int, stream=None):
     _ok(lib().dllm_selftest_timeout(limit_cycles, _stream(stream)))
+
+
+# --- transfer schedule (host only) -----------------------------------------------------------
+
+def transfer_counts(masked: int, steps: int) -> list:
+    """Tokens committed at each of a block's `steps` steps for `masked` masked positions."""
+    arr = (C.c_int32 * max(steps, 1))()
+    _ok(lib().dllm_transfer_counts(masked, steps, arr))
+    return [int(v) for v in arr[:steps]]
+
+
+def schedule(prompt_len: int, gen_len: int, block_len: int, steps: int) -> list:
+    """[(block_begin, block_end, k)] for each step of the whole generation."""
+    n = max(steps, 1)
+    b0, b1, k = (C.c_int32 * n)(), (C.c_int32 * n)(), (C.c_int32 * n)()
+    _ok(lib().dllm_schedule(prompt_len, gen_len, block_len, steps, b0, b1, k))
+    return [(int(b0[s]), int(b1[s]), int(k[s])) for s in range(steps)]
 
 
 # --- LM head + commit --------------------------------------------------------------------------
@@ -405,84 +424,87 @@ def model_from_seed(dims: dict, seed: int, device="cuda") -> DeviceModel:
 
 
 class StepGraphs:
-    """One CUDA graph per block of the denoising step (forward + masked LM head + commit), all on
-    the same device canvas and output buffers; replay(step) runs the step of block
-    block_of(step). Workspace and outputs are allocated once, before capture."""
+    """One CUDA graph per kind of denoising step (forward + masked LM head + commit), all on the
+    same device canvas and output buffers. A kind is (block_begin, block_end, k_commit), e.g. the
+    distinct entries of `schedule(...)`; replay(i) runs kind i. Workspace and outputs are
+    allocated once, before capture."""
 
-    def __init__(self, model: DeviceModel, canvas: torch.Tensor, blocks: list, k_commit: int):
-        self.model, self.canvas, self.blocks, self.k = model, canvas, blocks, k_commit
+    def __init__(self, model: DeviceModel, canvas: torch.Tensor, kinds: list):
+        self.model, self.canvas, self.kinds = model, canvas, list(kinds)
         dev = canvas.device
         L = canvas.shape[0]
-        rows = max(b1 - b0 for b0, b1 in blocks)
+        rows = max(b1 - b0 for b0, b1, _ in self.kinds)
+        kmax = max(max(k for _, _, k in self.kinds), 1)
         nb = denoise_workspace_bytes(model, L, rows)
         self.ws = torch.empty(nb + 1024, dtype=torch.uint8, device=dev)
-        self.out = {"pos": torch.empty(k_commit, dtype=torch.int32, device=dev),
-                    "id": torch.empty(k_commit, dtype=torch.int32, device=dev),
-                    "conf": torch.empty(k_commit, dtype=torch.float32, device=dev)}
+        self.out = {"pos": torch.empty(kmax, dtype=torch.int32, device=dev),
+                    "id": torch.empty(kmax, dtype=torch.int32, device=dev),
+                    "conf": torch.empty(kmax, dtype=torch.float32, device=dev)}
         self.stream = torch.cuda.Stream(device=dev)
         self.graphs = []
         self.launches_per_step = []
         saved = canvas.clone()
         with torch.cuda.stream(self.stream):
-            for b0, b1 in blocks:  # warm the library (attributes, tensor-map entry point) once
-                denoise_step(model, canvas, b0, b1, k_commit, ws=self.ws, out=self.out, stream=self.stream)
+            for b0, b1, k in self.kinds:  # warm the library (attributes, tensor-map entry point) once
+                denoise_step(model, canvas, b0, b1, k, ws=self.ws, out=self.out, stream=self.stream)
         self.stream.synchronize()
         check(self.stream)
-        for b0, b1 in blocks:
+        for b0, b1, k in self.kinds:
             g = torch.cuda.CUDAGraph()
             n0 = launch_count()
             with torch.cuda.graph(g, stream=self.stream):
-                denoise_step(model, canvas, b0, b1, k_commit, ws=self.ws, out=self.out, stream=self.stream)
+                denoise_step(model, canvas, b0, b1, k, ws=self.ws, out=self.out, stream=self.stream)
             self.launches_per_step.append(launch_count() - n0)
             self.graphs.append(g)
         canvas.copy_(saved)
         torch.cuda.synchronize()
 
-    def replay(self, block_index: int):
+    def replay(self, kind_index: int):
         """Replay on self.stream (a graph replays on the caller's current stream)."""
         with torch.cuda.stream(self.stream):
-            self.graphs[block_index].replay()
+            self.graphs[kind_index].replay()
 
 
 class CachedStepGraphs:
-    """Two CUDA graphs per block for the inter-step K/V cache: the refreshing step (full forward,
-    cache filled) and the cached step (block rows only); replay(block, refresh). One cache,
-    workspace and output set, allocated before capture."""
+    """Two CUDA graphs per kind of step (block_begin, block_end, k_commit) for the inter-step K/V
+    cache: the refreshing step (full forward, cache filled) and the cached step (block rows
+    only); replay(kind, refresh). One cache, workspace and output set, allocated before capture."""
 
-    def __init__(self, model: DeviceModel, canvas: torch.Tensor, blocks: list, k_commit: int):
-        self.model, self.canvas, self.blocks, self.k = model, canvas, blocks, k_commit
+    def __init__(self, model: DeviceModel, canvas: torch.Tensor, kinds: list):
+        self.model, self.canvas, self.kinds = model, canvas, list(kinds)
         dev = canvas.device
         L = canvas.shape[0]
-        rows = max(b1 - b0 for b0, b1 in blocks)
+        rows = max(b1 - b0 for b0, b1, _ in self.kinds)
+        kmax = max(max(k for _, _, k in self.kinds), 1)
         nb = denoise_cached_workspace_bytes(model, L, rows)
         self.ws = torch.empty(nb + 1024, dtype=torch.uint8, device=dev)
         self.kv = torch.empty(kv_cache_bytes(model, L) // 4, dtype=torch.float32, device=dev)
-        self.out = {"pos": torch.empty(k_commit, dtype=torch.int32, device=dev),
-                    "id": torch.empty(k_commit, dtype=torch.int32, device=dev),
-                    "conf": torch.empty(k_commit, dtype=torch.float32, device=dev)}
+        self.out = {"pos": torch.empty(kmax, dtype=torch.int32, device=dev),
+                    "id": torch.empty(kmax, dtype=torch.int32, device=dev),
+                    "conf": torch.empty(kmax, dtype=torch.float32, device=dev)}
         self.stream = torch.cuda.Stream(device=dev)
         self.graphs = {}
         saved = canvas.clone()
 
-        def step(b0, b1, refresh):
-            denoise_step_cached(model, canvas, b0, b1, k_commit, refresh, self.kv, ws=self.ws, out=self.out,
+        def step(b0, b1, k, refresh):
+            denoise_step_cached(model, canvas, b0, b1, k, refresh, self.kv, ws=self.ws, out=self.out,
                                 stream=self.stream)
 
         with torch.cuda.stream(self.stream):
-            for b0, b1 in blocks:  # warm the library once; the refresh fills the cache first
-                step(b0, b1, True)
-                step(b0, b1, False)
+            for b0, b1, k in self.kinds:  # warm the library once; the refresh fills the cache first
+                step(b0, b1, k, True)
+                step(b0, b1, k, False)
         self.stream.synchronize()
         check(self.stream)
-        for i, (b0, b1) in enumerate(blocks):
+        for i, (b0, b1, k) in enumerate(self.kinds):
             for refresh in (True, False):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=self.stream):
-                    step(b0, b1, refresh)
+                    step(b0, b1, k, refresh)
                 self.graphs[(i, refresh)] = g
         canvas.copy_(saved)
         torch.cuda.synchronize()
 
-    def replay(self, block_index: int, refresh: bool):
+    def replay(self, kind_index: int, refresh: bool):
         with torch.cuda.stream(self.stream):
-            self.graphs[(block_index, refresh)].replay()
+            self.graphs[(kind_index, refresh)].replay()
