@@ -140,23 +140,43 @@ DLLM_API size_t dllm_qgemm_workspace_bytes(int type, int64_t m, int64_t n, int64
 DLLM_API int dllm_qgemm(int type, const void* act, int64_t m, int64_t k, const void* w_packed,
                         int64_t n, float* y, int64_t ldy, int accumulate, void* ws, size_t ws_bytes,
                         dllm_stream_t stream);
-DLLM_API int dllm_qgemm_q4k(const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
-                            float* y, int64_t ldy, int accumulate, void* ws, size_t ws_bytes,
-                            dllm_stream_t stream);
-DLLM_API int dllm_qgemm_q6k(const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
-                            float* y, int64_t ldy, int accumulate, void* ws, size_t ws_bytes,
-                            dllm_stream_t stream);
+
+/* The same GEMM on plain Q8_K activations, the form the pages' Q8_K blocks take ([DP-CD]: int8
+ * codes, one f32 scale per 256 values, int sums per 16):
+ *   q int8 [m][k], d f32 [m][k/256], bsum int16 [m][k/16] (e.g. dllm_quantize_act's q, d, bsum).
+ * dllm_pack_act builds the operand form `act` (layout as in dllm_quantize_act, act_bytes >=
+ *   dllm_act_bytes(rows, k), 256-byte aligned) from them; codes, scales and sums are copied
+ *   exactly. bsum must hold the sums of the codes: a group whose sum differs is recorded in the
+ *   device error word and dllm_check reports DLLM_E_INVAL (the outputs made from it are not
+ *   valid). Alignment: q 8-byte, d 4-byte, bsum 2-byte.
+ * dllm_qgemm_q4k / dllm_qgemm_q6k: dllm_pack_act into the start of ws, then dllm_qgemm with the
+ *   rest of ws as its split-K workspace; ws >= dllm_qgemm_plain_workspace_bytes(type, m, n, k),
+ *   256-byte aligned. Same results as dllm_qgemm on the operand form of the same codes.
+ * Errors: as dllm_qgemm, plus those of dllm_pack_act. */
+DLLM_API int dllm_pack_act(const int8_t* q, const float* d, const int16_t* bsum, int64_t rows, int64_t k, void* act,
+                           size_t act_bytes, dllm_stream_t stream);
+DLLM_API size_t dllm_qgemm_plain_workspace_bytes(int type, int64_t m, int64_t n, int64_t k);
+DLLM_API int dllm_qgemm_q4k(const int8_t* q, const float* d, const int16_t* bsum, int64_t m, int64_t k,
+                            const void* w_packed, int64_t n, float* y, int64_t ldy, int accumulate, void* ws,
+                            size_t ws_bytes, dllm_stream_t stream);
+DLLM_API int dllm_qgemm_q6k(const int8_t* q, const float* d, const int16_t* bsum, int64_t m, int64_t k,
+                            const void* w_packed, int64_t n, float* y, int64_t ldy, int accumulate, void* ws,
+                            size_t ws_bytes, dllm_stream_t stream);
 
 /* Test hook ([DP-CD] integer sums): writes the exact per-super-block integer sums that the
  * tensor cores accumulate, as int32 sums[2][k/256][m][n]:
  *   Q4_K: sums[0] = sum_g scale * sum_i q4_i * a_i,      sums[1] = sum_g min * bsum_g
  *   Q6_K: sums[0] = sum_g s_hi * sum_i (q6_i-32) * a_i, sums[1] = sum_g s_lo * sum_i (q6_i-32) * a_i
  *         where the int8 group scale s = 16 * s_hi + s_lo, s_lo in [0, 15].
- * dllm_qgemm accumulates both parts of a super-block in one tensor-memory accumulator (Q4_K:
- * the min part enters with f16 head and tail coefficients -min * dmin / d, 2^-22 relative;
- * Q6_K: the hi operand carries 16 * s_hi * (q6-32)). This hook runs the same kernel twice
- * with one split, each time with one part isolated, and copies out its exact integers;
- * intended for small shapes. */
+ * dllm_qgemm accumulates all parts of a super-block in one tensor-memory accumulator (Q4_K:
+ * the integer chain uses re-centred quants, I' = sum_g scale * sum_i (q4_i - 8) * a_i, whose
+ * partial sums stay below 2^24 for every input, and the offset 8 * scale and the min part
+ * enter with f16 head and tail coefficients 8 * scale - min * dmin / d, 2^-22 relative;
+ * Q6_K: the hi operand carries s_hi * (q6-32) and the lo operand s_lo * (q6-32) / 16, and the
+ * epilogue applies 16 d). This hook runs the same kernel once per
+ * part with one split, each time with one part isolated, and copies out its exact integers
+ * (Q4_K: I', J, then the offset part added to I' to give sums[0] = I); intended for small
+ * shapes. */
 DLLM_API int dllm_qgemm_intsums(int type, const void* act, int64_t m, int64_t k, const void* w_packed,
                                 int64_t n, int32_t* sums, dllm_stream_t stream);
 
@@ -254,10 +274,34 @@ enum { DLLM_STREAM_LINEAR = 0, DLLM_STREAM_FULL = 1 };
  *       attention: the O projection consumes the V projection's output (canvas unused).
  * ws: >= dllm_step_workspace_bytes(m, L, flags), 1024-byte aligned; it holds the quantized
  * activations, the split-K partials of every projection and the attention buffers.
- * Limits: d_model and d_ff multiples of 256, head_dim == 128, L <= 8192. */
+ * Limits: d_model and d_ff multiples of 256, d_model <= 16384, head_dim == 128, L <= 8192. */
 DLLM_API size_t dllm_step_workspace_bytes(const dllm_model* m, int64_t L, int flags);
 DLLM_API int dllm_step_linear_stream(const dllm_model* m, const int32_t* canvas, int64_t L, float* x, int flags,
                                      void* ws, size_t ws_bytes, dllm_stream_t stream);
+
+/* Test hook: dllm_step_linear_stream that also copies out the intermediates of one layer, so
+ * that each stage of the layer can be checked on its own input (the Development plan's
+ * correctness ladder: RMSNorm, RoPE, softmax, attention, one layer). Every tap is optional
+ * (NULL = not captured) and caller-owned device memory; "operand" taps are dllm_act_bytes(L, k)
+ * bytes in the operand form of dllm_quantize_act. */
+typedef struct dllm_taps {
+  int32_t layer;   /* the layer whose intermediates are captured, 0 .. n_layers - 1              */
+  float* x_in;     /* f32 [L][d]: the layer's input residual stream                                */
+  void* act_attn;  /* operand of RMSNorm(x) * attn_norm (the Q|K and V projections' input), k = d */
+  float* q;        /* f32 [L][d]: Q after RoPE, times 1/sqrt(head_dim) (DLLM_STREAM_FULL only)    */
+  float* k;        /* f32 [L][d]: K after RoPE (DLLM_STREAM_FULL only)                            */
+  float* v;        /* f32 [L][d]: V (DLLM_STREAM_FULL only)                                        */
+  float* attn;     /* f32 [L][d], 16-byte aligned: the O projection's input before Q8_K (the
+                      attention output; the V projection for DLLM_STREAM_LINEAR)                   */
+  void* act_o;     /* operand of that input, k = d                                                 */
+  float* x_mid;    /* f32 [L][d]: the residual stream after the O residual add                     */
+  void* act_ffn;   /* operand of RMSNorm(x_mid) * ffn_norm (the gate|up input), k = d              */
+  float* h;        /* f32 [L][d_ff], 16-byte aligned: silu(gate) * up before Q8_K                  */
+  void* act_down;  /* operand of h (the down projection's input), k = d_ff                         */
+  float* x_out;    /* f32 [L][d]: the residual stream after the down residual add                  */
+} dllm_taps;
+DLLM_API int dllm_step_taps(const dllm_model* m, const int32_t* canvas, int64_t L, float* x, int flags,
+                            const dllm_taps* taps, void* ws, size_t ws_bytes, dllm_stream_t stream);
 
 /* dllm_denoise_step: one full denoising step = DLLM_STREAM_FULL forward over the canvas,
  * then dllm_lmhead_masked_select on the block [block_begin, block_end) with k_commit
@@ -340,7 +384,9 @@ DLLM_API int dllm_qgemm_partials(int type, const void* act, int64_t m, int64_t k
  * the plan's partials would not fit). The first call on a device looks up that array's device
  * address (once per device, with the device current); make it before any stream capture.
  * Calls share the array: calls that overlap on the GPU race and must be serialized by the
- * caller. No device memory is allocated or freed. */
+ * caller. No device memory is allocated or freed. The looked-up address is kept for the life of
+ * the process and does not survive a device reset: after cudaDeviceReset on a device, do not
+ * call this entry point on that device again. */
 DLLM_API int dllm_qgemm_noalloc(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
                                 float* y, int64_t ldy, int accumulate, dllm_stream_t stream);
 

@@ -45,8 +45,10 @@ _SIGS = {
     "dllm_quantize_act": ([P, I64, I64, I64, P, F32, P, P, P, P, SZ, P], INT),
     "dllm_qgemm_workspace_bytes": ([INT, I64, I64, I64], SZ),
     "dllm_qgemm": ([INT, P, I64, I64, P, I64, P, I64, INT, P, SZ, P], INT),
-    "dllm_qgemm_q4k": ([P, I64, I64, P, I64, P, I64, INT, P, SZ, P], INT),
-    "dllm_qgemm_q6k": ([P, I64, I64, P, I64, P, I64, INT, P, SZ, P], INT),
+    "dllm_pack_act": ([P, P, P, I64, I64, P, SZ, P], INT),
+    "dllm_qgemm_plain_workspace_bytes": ([INT, I64, I64, I64], SZ),
+    "dllm_qgemm_q4k": ([P, P, P, I64, I64, P, I64, P, I64, INT, P, SZ, P], INT),
+    "dllm_qgemm_q6k": ([P, P, P, I64, I64, P, I64, P, I64, INT, P, SZ, P], INT),
     "dllm_qgemm_intsums": ([INT, P, I64, I64, P, I64, P, P], INT),
     "dllm_selftest_timeout": ([I64, P], INT),
     "dllm_lmhead_workspace_bytes": ([I64, I64, I64], SZ),
@@ -65,6 +67,7 @@ _SIGS = {
     "dllm_qgemm_partials_bytes": ([INT, I64, I64, I64], SZ),
     "dllm_qgemm_partials": ([INT, P, I64, I64, P, I64, P, SZ, P, P], INT),
     "dllm_qgemm_noalloc": ([INT, P, I64, I64, P, I64, P, I64, INT, P], INT),
+    "dllm_step_taps": ([P, P, I64, P, INT, P, P, SZ, P], INT),
     "dllm_transfer_counts": ([I64, I64, P], INT),
     "dllm_schedule": ([I64, I64, I64, I64, P, P, P], INT),
 }
@@ -172,6 +175,33 @@ def qgemm(type_id: int, act: torch.Tensor, m: int, k: int, w_packed: torch.Tenso
         ws = torch.empty(wsb, dtype=torch.uint8, device=act.device)
     _ok(lib().dllm_qgemm(type_id, _ptr(act), m, k, _ptr(w_packed), n, _ptr(y), y.stride(0), int(accumulate),
                          _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return y
+
+
+def pack_act(q: torch.Tensor, d: torch.Tensor, bsum: torch.Tensor, act: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """Operand form of plain Q8_K arrays (q int8 [rows, k], d f32 [rows, k/256], bsum int16)."""
+    rows, k = q.shape
+    nb = act_bytes(rows, k)
+    if act is None:
+        act = torch.empty(nb, dtype=torch.uint8, device=q.device)
+    _ok(lib().dllm_pack_act(_ptr(q), _ptr(d), _ptr(bsum), rows, k, _ptr(act), act.numel(), _stream(stream)))
+    return act
+
+
+def qgemm_plain(type_id: int, q: torch.Tensor, d: torch.Tensor, bsum: torch.Tensor, w_packed: torch.Tensor, n: int,
+                y: torch.Tensor | None = None, accumulate: bool = False, ws: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """y[m, n] (+)= plain Q8_K activations x decoded weights^T (dllm_qgemm_q4k / dllm_qgemm_q6k)."""
+    m, k = q.shape
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.float32, device=q.device)
+    nb = int(lib().dllm_qgemm_plain_workspace_bytes(type_id, m, n, k))
+    if ws is None:
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=q.device)
+    fn = lib().dllm_qgemm_q4k if type_id == Q4_K else lib().dllm_qgemm_q6k
+    _ok(fn(_ptr(q), _ptr(d), _ptr(bsum), m, k, _ptr(w_packed), n, _ptr(y), y.stride(0), int(accumulate), _ptr(ws),
+           ws.numel(), _stream(stream)))
     return y
 
 
@@ -358,6 +388,37 @@ def step_linear_stream(model: DeviceModel, x: torch.Tensor, flags: int = STREAM_
     _ok(lib().dllm_step_linear_stream(model.ref, _ptr(canvas), L, _ptr(x), flags, C.c_void_p(wsp),
                                       ws.numel() - (wsp - ws.data_ptr()), _stream(stream)))
     return x
+
+
+class _Taps(C.Structure):
+    _fields_ = [("layer", I32), ("x_in", P), ("act_attn", P), ("q", P), ("k", P), ("v", P), ("attn", P), ("act_o", P),
+                ("x_mid", P), ("act_ffn", P), ("h", P), ("act_down", P), ("x_out", P)]
+
+
+TAP_NAMES = ("x_in", "act_attn", "q", "k", "v", "attn", "act_o", "x_mid", "act_ffn", "h", "act_down", "x_out")
+
+
+def step_taps(model: DeviceModel, x: torch.Tensor, flags: int, layer: int, canvas: torch.Tensor | None = None,
+              names=TAP_NAMES, stream=None) -> dict:
+    """step_linear_stream that also captures layer `layer`'s intermediates (test hook). Returns
+    a dict of device tensors: f32 [L, d] / [L, d_ff] for x_in, q, k, v, attn, x_mid, h, x_out,
+    and uint8 operand-form buffers for act_attn, act_o, act_ffn, act_down."""
+    L = x.shape[0]
+    d, f = model.dims["d_model"], model.dims["d_ff"]
+    dev = x.device
+    out = {}
+    for nm in names:
+        if nm.startswith("act_"):
+            out[nm] = torch.zeros(act_bytes(L, f if nm == "act_down" else d), dtype=torch.uint8, device=dev)
+        else:
+            out[nm] = torch.zeros((L, f if nm == "h" else d), dtype=torch.float32, device=dev)
+    taps = _Taps(layer, *[out[nm].data_ptr() if nm in out else None for nm in TAP_NAMES])
+    nb = step_workspace_bytes(model, L, flags)
+    ws = torch.empty(nb + 1024, dtype=torch.uint8, device=dev)
+    wsp = (ws.data_ptr() + 1023) // 1024 * 1024
+    _ok(lib().dllm_step_taps(model.ref, _ptr(canvas), L, _ptr(x), flags, C.byref(taps), C.c_void_p(wsp),
+                             ws.numel() - (wsp - ws.data_ptr()), _stream(stream)))
+    return out
 
 
 def denoise_workspace_bytes(model: DeviceModel, L: int, block_rows: int) -> int:

@@ -279,6 +279,42 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
   griddep_launch();
 }
 
+// Plain Q8_K arrays -> the operand form: warp (blockIdx.y * 8 + w) of row blockIdx.x copies
+// super-block sb (lane = codes 8*lane .. 8*lane+7); padding rows are written as zeros. Each lane
+// pair checks that its group's 16-sum matches the codes and records ERR_BSUM if not.
+__global__ void __launch_bounds__(256) pack_act_kernel(const int8_t* __restrict__ q, const float* __restrict__ d,
+                                                       const int16_t* __restrict__ bsum, int rows, int64_t k,
+                                                       QuantOut o, int* err) {
+  griddep_wait();
+  griddep_launch();
+  const int row = blockIdx.x;
+  const int sb = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  const int64_t nsb = k / QK;
+  if (sb >= nsb) return;
+  int qi[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  int s16 = 0;
+  float dsc = 0.f;
+  if (row < rows) {
+    const uint2 w = *reinterpret_cast<const uint2*>(q + (int64_t)row * k + (int64_t)sb * QK + 8 * lane);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      qi[i] = (int)(int8_t)(w.x >> (8 * i));
+      qi[4 + i] = (int)(int8_t)(w.y >> (8 * i));
+    }
+    s16 = bsum[(int64_t)row * (k / 16) + (int64_t)sb * 16 + (lane >> 1)];
+    dsc = d[(int64_t)row * nsb + sb];
+    int s8 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s8 += qi[i];
+    if (s8 + __shfl_xor_sync(0xffffffffu, s8, 1) != s16 && (lane & 1) == 0) atomicOr(err, ERR_BSUM);
+  }
+  QuantOut a = o;
+  a.q = nullptr;
+  a.d = nullptr;
+  a.bsum = nullptr;
+  q8k_store(qi, s16, dsc, row, rows, sb, k, a);
+}
+
 // y (+)= sum of split partials, fixed order.
 __global__ void reduce_splits_kernel(const float* __restrict__ P, int splits, int64_t stride, int m, int n,
                                      float* __restrict__ y, int64_t ldy, int accumulate) {
@@ -539,10 +575,14 @@ DLLM_API int dllm_check(dllm_stream_t stream) {
   if (w) {
     int z = 0;
     cudaMemcpyToSymbol(g_err_word, &z, sizeof(int));
-    if (w == ERR_RANGE)
-      return fail(DLLM_E_INVAL,
-                  "a Q4_K super-block has |dmin / d| above 4e6: its min term cannot be folded into the "
-                  "f16 tensor-core operands (the outputs of that launch are not valid)");
+    if ((w & ~(ERR_RANGE | ERR_BSUM)) == 0)
+      return fail(DLLM_E_INVAL, "%s%s",
+                  (w & ERR_RANGE) ? "a Q4_K super-block has |dmin / d| above 4e6: its min term cannot be folded into "
+                                    "the f16 tensor-core operands (the outputs of that launch are not valid). "
+                                  : "",
+                  (w & ERR_BSUM) ? "plain Q8_K input to dllm_pack_act has a 16-value sum (bsum) that does not match "
+                                   "its codes (the operand and the GEMM outputs made from it are not valid). "
+                                 : "");
     return fail(DLLM_E_TIMEOUT, "device-side bounded wait ran out (roles: %s%s%s%s%s%s)",
                 (w & ERR_TIMEOUT_PRODUCER) ? "producer " : "", (w & ERR_TIMEOUT_DECODE) ? "decode " : "",
                 (w & ERR_TIMEOUT_MMA) ? "mma " : "", (w & ERR_TIMEOUT_EPILOGUE) ? "epilogue " : "",
@@ -744,9 +784,11 @@ static int qgemm_common(const char* fn, int type, const void* act, int64_t m, in
   GemmLaunch g{type, act, m, k, w_packed, n, y, ldy, accumulate, static_cast<float*>(ws), 0, nullptr, nullptr, nullptr,
                nullptr, 0};
   if (dbg) {
-    // the integer sums: one launch per isolated part, each writing its own plane
-    for (int part = 0; part < 2; ++part) {
-      g.dbg = dbg + (size_t)part * P.nsb * m * n;
+    // the integer sums: one launch per isolated part, each writing its own plane; Q4_K's plane 0
+    // is I' (re-centred quants) and a third launch adds the offset part 8 * sum scale * bsum
+    const int parts = type == DLLM_Q4_K ? 3 : 2;
+    for (int part = 0; part < parts; ++part) {
+      g.dbg = dbg + (size_t)(part == 1) * P.nsb * m * n;
       g.dbg_mode = part + 1;
       if ((rc = launch_gemm(g, P, stream))) return rc;
     }
@@ -754,16 +796,18 @@ static int qgemm_common(const char* fn, int type, const void* act, int64_t m, in
   }
   rc = launch_gemm(g, P, stream);
   if (rc) return rc;
-  if (P.splits > 1 && y) {
-    const int64_t total = m * n;
-    const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4 * num_sms());
-    reduce_splits_kernel<<<blocks, 256, 0, stream>>>(static_cast<float*>(ws), P.splits, m * n, (int)m, (int)n, y,
-                                                     ldy, accumulate);
-    note_launch();
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "launch reduce_splits");
-  }
+  if (P.splits > 1 && y) return launch_reduce_splits(static_cast<float*>(ws), P.splits, m * n, m, n, y, ldy, accumulate, stream);
   return DLLM_OK;
+}
+
+int launch_reduce_splits(const float* P, int splits, int64_t stride, int64_t m, int64_t n, float* y, int64_t ldy,
+                         int accumulate, cudaStream_t stream) {
+  const int64_t total = m * n;
+  const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4 * num_sms());
+  reduce_splits_kernel<<<blocks, 256, 0, stream>>>(P, splits, stride, (int)m, (int)n, y, ldy, accumulate);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch reduce_splits");
 }
 
 }  // namespace dllm
@@ -777,18 +821,81 @@ DLLM_API int dllm_qgemm(int type, const void* act, int64_t m, int64_t k, const v
                       (cudaStream_t)stream);
 }
 
-DLLM_API int dllm_qgemm_q4k(const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n, float* y,
-                            int64_t ldy, int accumulate, void* ws, size_t ws_bytes, dllm_stream_t stream) {
-  if (!y) return fail(DLLM_E_INVAL, "dllm_qgemm_q4k: y is NULL");
-  return qgemm_common("dllm_qgemm_q4k", DLLM_Q4_K, act, m, k, w_packed, n, y, ldy, accumulate, ws, ws_bytes, nullptr,
-                      (cudaStream_t)stream);
+DLLM_API int dllm_pack_act(const int8_t* q, const float* d, const int16_t* bsum, int64_t rows, int64_t k, void* act,
+                           size_t act_bytes, dllm_stream_t stream) {
+  if (rows <= 0 || rows > 65536 || k <= 0 || k % QK || k > (1 << 20))
+    return fail(DLLM_E_SHAPE, "dllm_pack_act: bad shape rows=%lld k=%lld (k must be a positive multiple of 256)",
+                (long long)rows, (long long)k);
+  int rc = check_device();
+  if (rc) return rc;
+  CHECK_DEV(q, "q");
+  CHECK_DEV(d, "d");
+  CHECK_DEV(bsum, "bsum");
+  CHECK_DEV(act, "act");
+  if (!aligned(q, 8) || !aligned(d, 4) || !aligned(bsum, 2))
+    return fail(DLLM_E_ALIGN, "dllm_pack_act: q must be 8-byte, d 4-byte and bsum 2-byte aligned");
+  if (!aligned(act, 256)) return fail(DLLM_E_ALIGN, "dllm_pack_act: act must be 256-byte aligned");
+  const ActLayout L = act_layout(rows, k);
+  if (act_bytes < L.bytes)
+    return fail(DLLM_E_WORKSPACE, "dllm_pack_act: act buffer has %zu bytes, needs %zu (dllm_act_bytes)", act_bytes,
+                L.bytes);
+  int* err = err_word();
+  if (!err) return fail(DLLM_E_CUDA, "cannot resolve the device error word");
+  uint8_t* base = static_cast<uint8_t*>(act);
+  QuantOut o{nullptr, nullptr, nullptr, reinterpret_cast<__half*>(base + L.off_a), base + L.off_j,
+             reinterpret_cast<float*>(base + L.off_d), (int)L.lpad};
+  const dim3 grid((unsigned)L.lpad, (unsigned)((k / QK + 7) / 8));
+  cudaError_t e = launch_pdl(pack_act_kernel, grid, dim3(256), 0, (cudaStream_t)stream, q, d, bsum, (int)rows, k, o,
+                             err);
+  note_launch();
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch pack_act");
 }
 
-DLLM_API int dllm_qgemm_q6k(const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n, float* y,
-                            int64_t ldy, int accumulate, void* ws, size_t ws_bytes, dllm_stream_t stream) {
-  if (!y) return fail(DLLM_E_INVAL, "dllm_qgemm_q6k: y is NULL");
-  return qgemm_common("dllm_qgemm_q6k", DLLM_Q6_K, act, m, k, w_packed, n, y, ldy, accumulate, ws, ws_bytes, nullptr,
-                      (cudaStream_t)stream);
+DLLM_API size_t dllm_qgemm_plain_workspace_bytes(int type, int64_t m, int64_t n, int64_t k) {
+  if (!block_bytes(type) || m <= 0 || m > 65536 || n <= 0 || k <= 0 || k % QK) return 0;
+  return align_up(act_layout(m, k).bytes, 256) + plan_qgemm(type, m, n, k).ws_bytes;
+}
+
+}  // extern "C"
+
+namespace dllm {
+// The GEMM on plain Q8_K arrays: the operand form is built at the start of ws, the split-K
+// partials follow it.
+static int qgemm_plain(const char* fn, int type, const int8_t* q, const float* d, const int16_t* bsum, int64_t m,
+                       int64_t k, const void* w_packed, int64_t n, float* y, int64_t ldy, int accumulate, void* ws,
+                       size_t ws_bytes, cudaStream_t stream) {
+  if (!y) return fail(DLLM_E_INVAL, "%s: y is NULL", fn);
+  if (m <= 0 || m > 65536 || n <= 0 || n > (1 << 24) || k <= 0 || k % QK || k > (1 << 20))
+    return fail(DLLM_E_SHAPE, "%s: bad shape m=%lld n=%lld k=%lld (k must be a positive multiple of 256)", fn,
+                (long long)m, (long long)n, (long long)k);
+  const size_t need = dllm_qgemm_plain_workspace_bytes(type, m, n, k);
+  if (!ws || ws_bytes < need)
+    return fail(DLLM_E_WORKSPACE, "%s: workspace has %zu bytes, needs %zu (dllm_qgemm_plain_workspace_bytes)", fn,
+                ws ? ws_bytes : (size_t)0, need);
+  if (!aligned(ws, 256)) return fail(DLLM_E_ALIGN, "%s: ws must be 256-byte aligned", fn);
+  const size_t act_b = align_up(act_layout(m, k).bytes, 256);
+  int rc = dllm_pack_act(q, d, bsum, m, k, ws, act_b, (dllm_stream_t)stream);
+  if (rc) return rc;
+  return qgemm_common(fn, type, ws, m, k, w_packed, n, y, ldy, accumulate, static_cast<uint8_t*>(ws) + act_b,
+                      ws_bytes - act_b, nullptr, stream);
+}
+}  // namespace dllm
+
+extern "C" {
+
+DLLM_API int dllm_qgemm_q4k(const int8_t* q, const float* d, const int16_t* bsum, int64_t m, int64_t k,
+                            const void* w_packed, int64_t n, float* y, int64_t ldy, int accumulate, void* ws,
+                            size_t ws_bytes, dllm_stream_t stream) {
+  return qgemm_plain("dllm_qgemm_q4k", DLLM_Q4_K, q, d, bsum, m, k, w_packed, n, y, ldy, accumulate, ws, ws_bytes,
+                     (cudaStream_t)stream);
+}
+
+DLLM_API int dllm_qgemm_q6k(const int8_t* q, const float* d, const int16_t* bsum, int64_t m, int64_t k,
+                            const void* w_packed, int64_t n, float* y, int64_t ldy, int accumulate, void* ws,
+                            size_t ws_bytes, dllm_stream_t stream) {
+  return qgemm_plain("dllm_qgemm_q6k", DLLM_Q6_K, q, d, bsum, m, k, w_packed, n, y, ldy, accumulate, ws, ws_bytes,
+                     (cudaStream_t)stream);
 }
 
 DLLM_API int dllm_qgemm_intsums(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,

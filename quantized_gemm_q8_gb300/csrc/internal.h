@@ -100,6 +100,11 @@ int launch_qgemm_q4k(int nt, const CUtensorMap& map, const QgemmParams& p, int g
 int launch_qgemm_q6k(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s);
 int launch_qgemm_q6k_sample(int nt, const CUtensorMap& map, const QgemmParams& p, int grid, cudaStream_t s);
 
+// y (+)= the sum of `splits` split-K partials P[splits][m][n] (stride elements apart), summed in
+// split order (deterministic); one launch on `stream`. Returns DLLM_OK or a status.
+int launch_reduce_splits(const float* P, int splits, int64_t stride, int64_t m, int64_t n, float* y, int64_t ldy,
+                         int accumulate, cudaStream_t stream);
+
 // Quantize rows of x into the operand form (internal, no validation).
 int quantize_rows(const float* x, int64_t rows, int64_t k, int64_t ldx, const float* norm_w, float eps, void* act,
                   cudaStream_t stream);

@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "internal.h"
 #include "qgemm.cuh"
@@ -561,11 +562,14 @@ struct RowArgs {
   QuantOut o;
 };
 
-// Residual modes (RESID_NORM_QUANT, RESID_ONLY): one CTA of 1024 threads per row (RMSNorm
-// needs the row's sum of squares); each thread's partial loads are issued together.
+// Residual modes (RESID_NORM_QUANT, RESID_ONLY): one CTA per row, warp w holding super-blocks
+// w, w + nwarp, ... (up to RR_J of them) in registers from the residual add through the
+// quantization, lane = 8 consecutive values; RMSNorm needs the row's sum of squares, one block
+// reduction. Each thread's partial loads are issued together.
+constexpr int RR_WARPS = 16, RR_J = 4;  // rows of up to RR_WARPS * RR_J * 256 = 16384 values
 template <int MODE>
-__global__ void __launch_bounds__(1024) row_resid_kernel(RowArgs a) {
-  __shared__ float red[32];
+__global__ void __launch_bounds__(RR_WARPS * 32) row_resid_kernel(RowArgs a) {
+  __shared__ float red[RR_WARPS];
   griddep_wait();
   griddep_launch();
   const int row = blockIdx.x;
@@ -580,35 +584,50 @@ __global__ void __launch_bounds__(1024) row_resid_kernel(RowArgs a) {
   }
   const float* Pr = a.P + (int64_t)row * a.ldp;
   float* xr = a.x + (int64_t)row * a.k;
+  float v[RR_J][8];
   float ss = 0.f;
-  for (int i = threadIdx.x * 4; i < a.k; i += blockDim.x * 4) {
-    float4 v = *reinterpret_cast<float4*>(xr + i);
+#pragma unroll
+  for (int j = 0; j < RR_J; ++j) {
+    const int sb = warp + j * nwarp;
+    if (sb < nsb) {
+      const int base = sb * QK + 8 * lane;
+      float4 x0 = *reinterpret_cast<const float4*>(xr + base);
+      float4 x1 = *reinterpret_cast<const float4*>(xr + base + 4);
 #pragma unroll 4
-    for (int s = 0; s < a.S; ++s) {
-      const float4 pv = *reinterpret_cast<const float4*>(Pr + s * a.pstride + i);
-      v.x += pv.x;
-      v.y += pv.y;
-      v.z += pv.z;
-      v.w += pv.w;
+      for (int sp = 0; sp < a.S; ++sp) {
+        const float4 p0 = *reinterpret_cast<const float4*>(Pr + sp * a.pstride + base);
+        const float4 p1 = *reinterpret_cast<const float4*>(Pr + sp * a.pstride + base + 4);
+        x0.x += p0.x; x0.y += p0.y; x0.z += p0.z; x0.w += p0.w;
+        x1.x += p1.x; x1.y += p1.y; x1.z += p1.z; x1.w += p1.w;
+      }
+      *reinterpret_cast<float4*>(xr + base) = x0;
+      *reinterpret_cast<float4*>(xr + base + 4) = x1;
+      v[j][0] = x0.x; v[j][1] = x0.y; v[j][2] = x0.z; v[j][3] = x0.w;
+      v[j][4] = x1.x; v[j][5] = x1.y; v[j][6] = x1.z; v[j][7] = x1.w;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(v[j][i], v[j][i], ss);
     }
-    *reinterpret_cast<float4*>(xr + i) = v;
-    ss = fmaf(v.x, v.x, ss);
-    ss = fmaf(v.y, v.y, ss);
-    ss = fmaf(v.z, v.z, ss);
-    ss = fmaf(v.w, v.w, ss);
   }
   if (MODE == ROW_RESID_ONLY) return;
-  ss = block_sum(ss, red);  // also orders the x writes above before the reads below
-  const float rstd = 1.0f / sqrtf(ss / (float)a.k + a.eps);
-  for (int sb = warp; sb < nsb; sb += nwarp) {
-    const int base = sb * QK + 8 * lane;
-    const float4 v0 = *reinterpret_cast<const float4*>(xr + base);
-    const float4 v1 = *reinterpret_cast<const float4*>(xr + base + 4);
-    const float4 w0 = *reinterpret_cast<const float4*>(a.norm_w + base);
-    const float4 w1 = *reinterpret_cast<const float4*>(a.norm_w + base + 4);
-    float v[8] = {v0.x * rstd * w0.x, v0.y * rstd * w0.y, v0.z * rstd * w0.z, v0.w * rstd * w0.w,
-                  v1.x * rstd * w1.x, v1.y * rstd * w1.y, v1.z * rstd * w1.z, v1.w * rstd * w1.w};
-    q8k_emit(v, row, a.rows, sb, a.k, a.o);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < nwarp; ++w) tot += red[w];
+  const float rstd = 1.0f / sqrtf(tot / (float)a.k + a.eps);
+#pragma unroll
+  for (int j = 0; j < RR_J; ++j) {
+    const int sb = warp + j * nwarp;
+    if (sb < nsb) {
+      const int base = sb * QK + 8 * lane;
+      const float4 w0 = *reinterpret_cast<const float4*>(a.norm_w + base);
+      const float4 w1 = *reinterpret_cast<const float4*>(a.norm_w + base + 4);
+      const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[j][i] = v[j][i] * rstd * w[i];
+      q8k_emit(v[j], row, a.rows, sb, a.k, a.o);
+    }
   }
 }
 
@@ -648,21 +667,22 @@ __global__ void __launch_bounds__(256) row_sb_kernel(RowArgs a) {
   q8k_emit(v, row, a.rows, sb, a.k, a.o);  // padding rows quantize zeros
 }
 
-static QuantOut quant_out(void* act, int64_t rows, int64_t k) {
+static QuantOut quant_out(void* act, int64_t rows, int64_t k, float* vtap = nullptr) {
   ActLayout L = act_layout(rows, k);
   uint8_t* base = static_cast<uint8_t*>(act);
   return QuantOut{nullptr, nullptr, nullptr, reinterpret_cast<__half*>(base + L.off_a), base + L.off_j,
-                  reinterpret_cast<float*>(base + L.off_d), (int)L.lpad};
+                  reinterpret_cast<float*>(base + L.off_d), (int)L.lpad, vtap};
 }
 
 template <int MODE>
 static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, const float* w, float eps, int rows,
-                   int k, void* act, cudaStream_t s) {
-  RowArgs a{x, P, S, pstride, ldp, w, eps, rows, k, act ? quant_out(act, rows, k) : QuantOut{}};
+                   int k, void* act, cudaStream_t s, float* vtap = nullptr) {
+  RowArgs a{x, P, S, pstride, ldp, w, eps, rows, k, act ? quant_out(act, rows, k, vtap) : QuantOut{}};
   cudaError_t e;
   if (MODE == ROW_RESID_NORM_QUANT || MODE == ROW_RESID_ONLY) {
     const int grid = MODE == ROW_RESID_ONLY ? rows : (int)act_rows_padded(rows);
-    e = launch_pdl(row_resid_kernel<MODE>, dim3(grid), dim3(1024), 0, s, a);
+    const int warps = std::min(RR_WARPS, k / QK);  // k <= RR_WARPS * RR_J * 256: each warp holds <= RR_J
+    e = launch_pdl(row_resid_kernel<MODE>, dim3(grid), dim3(32 * warps), 0, s, a);
   } else {
     const dim3 grid((unsigned)act_rows_padded(rows), (unsigned)((k / QK + 7) / 8));
     e = launch_pdl(row_sb_kernel<MODE>, grid, dim3(256), 0, s, a);
@@ -670,6 +690,30 @@ static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, co
   note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch row kernel");
+}
+
+// Test taps: Q, K, V of a layer as f32 [L][d] each, from the f16 head/tail planes of the
+// tensor-core attention (x = hi + lo) or from the f32 [L][3d] rows of the chunked one.
+__global__ void tap_qkv_kernel(const __half* __restrict__ planes, const float* __restrict__ QKV, int L, int d,
+                               float* __restrict__ q, float* __restrict__ k, float* __restrict__ v) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= (int64_t)L * 3 * d) return;
+  const int which = (int)(i / ((int64_t)L * d));
+  const int64_t r = i % ((int64_t)L * d), p = r / d, c = r % d;
+  float val;
+  if (planes)
+    val = __half2float(planes[(2 * which * (int64_t)L + p) * d + c]) +
+          __half2float(planes[((2 * which + 1) * (int64_t)L + p) * d + c]);
+  else
+    val = QKV[p * 3 * d + which * d + c];
+  float* dst = which == 0 ? q : (which == 1 ? k : v);
+  if (dst) dst[r] = val;
+}
+
+static int tap_copy(void* dst, const void* src, size_t bytes, cudaStream_t s) {
+  if (!dst) return DLLM_OK;
+  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "cudaMemcpyAsync (tap)");
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -717,10 +761,11 @@ static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead
 
 static int check_model(const dllm_model* m, int64_t L, const char* fn) {
   if (!m) return fail(DLLM_E_INVAL, "%s: model is NULL", fn);
-  if (m->n_layers <= 0 || m->d_model <= 0 || m->d_model % QK || m->d_ff <= 0 || m->d_ff % QK ||
+  if (m->n_layers <= 0 || m->d_model <= 0 || m->d_model % QK || m->d_model > RR_WARPS * RR_J * QK || m->d_ff <= 0 ||
+      m->d_ff % QK ||
       m->head_dim != ATT_HD || m->n_heads * m->head_dim != m->d_model || m->vocab <= 0)
     return fail(DLLM_E_SHAPE,
-                "%s: unsupported model shape (d_model %% 256 == 0, d_ff %% 256 == 0, head_dim == 128, "
+                "%s: unsupported model shape (d_model %% 256 == 0 and <= 16384, d_ff %% 256 == 0, head_dim == 128, "
                 "n_heads * head_dim == d_model): d=%d d_ff=%d heads=%d head_dim=%d",
                 fn, m->d_model, m->d_ff, m->n_heads, m->head_dim);
   if (L <= 0 || L > 8192) return fail(DLLM_E_SHAPE, "%s: L=%lld must be in [1, 8192]", fn, (long long)L);
@@ -740,10 +785,57 @@ static int gemm(int type, const void* act, int64_t m, int64_t k, const void* w, 
   return launch_gemm(g, P, s);
 }
 
+// A second stream and two events per device, created on the first forward pass on that device and
+// kept until exit: the V projection runs on the side stream beside the Q|K projection (both read
+// the same activations), so that V's CTAs fill the SMs that Q|K leaves idle. Work on the side
+// stream is forked from and joined back into the caller's stream with the events, so the pair
+// stays stream-ordered and is captured into a CUDA graph like the rest of the step.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static int side_stream(SideStream** out) {
+  static std::mutex mu;
+  static SideStream per_dev[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(DLLM_E_DEVICE, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  SideStream& ss = per_dev[dev];
+  if (!ss.s) {
+    if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess)
+      return cuda_fail(e, "cudaStreamCreateWithFlags (side stream)");
+    if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess)
+      return cuda_fail(e, "cudaEventCreateWithFlags (side stream)");
+  }
+  *out = &ss;
+  return DLLM_OK;
+}
+
+// Q|K on s and V on the side stream, both after the work already on s; s continues after both.
+static int gemm_qk_v(const dllm_layer& Ly, void* actd, int64_t L, int d, float* Pqk, float* Pv, const StepPlan& S,
+                     cudaStream_t s) {
+  SideStream* ss = nullptr;
+  int rc = side_stream(&ss);
+  if (rc) return rc;
+  cudaError_t e = cudaEventRecord(ss->fork, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "fork the side stream");
+  if ((rc = gemm(DLLM_Q6_K, actd, L, d, Ly.wv, d, Pv, S.v, ss->s))) return rc;
+  if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wqk, 2 * d, Pqk, S.qk, s))) return rc;
+  e = cudaEventRecord(ss->join, ss->s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ss->join, 0);
+  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "join the side stream");
+}
+
 // The forward pass over all layers; x is [L][d] (input for the linear stream, output always).
 // kv (optional, full stream only): per layer K (after RoPE) then V of every row, [layers][2][L][d].
+// taps (optional, tests): the intermediates of layer taps->layer are copied out as they appear.
 static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float* x, int flags, uint8_t* ws,
-                   const StepPlan& S, cudaStream_t s, float* kv = nullptr) {
+                   const StepPlan& S, cudaStream_t s, float* kv = nullptr, const dllm_taps* taps = nullptr) {
   const int d = m->d_model, f = m->d_ff, hd = m->head_dim;
   const bool full = flags & DLLM_STREAM_FULL;
   float* Pqk = reinterpret_cast<float*>(ws + S.pqk);
@@ -767,10 +859,13 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
   }
   // layer 0 input: RMSNorm + quantize of x
   if ((rc = quantize_rows(x, L, d, d, m->layers[0].attn_norm, m->eps, actd, s))) return rc;
+  const size_t act_d_bytes = act_layout(L, d).bytes, act_f_bytes = act_layout(L, f).bytes;
   for (int li = 0; li < m->n_layers; ++li) {
     const dllm_layer& Ly = m->layers[li];
-    if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wqk, 2 * d, Pqk, S.qk, s))) return rc;
-    if ((rc = gemm(DLLM_Q6_K, actd, L, d, Ly.wv, d, Pv, S.v, s))) return rc;
+    const dllm_taps* tp = (taps && taps->layer == li) ? taps : nullptr;
+    if (tp && (rc = tap_copy(tp->x_in, x, (size_t)L * d * 4, s))) return rc;
+    if (tp && (rc = tap_copy(tp->act_attn, actd, act_d_bytes, s))) return rc;
+    if ((rc = gemm_qk_v(Ly, actd, L, d, Pqk, Pv, S, s))) return rc;
     if (full) {
       // Q, K, V: f32 rows for the chunked attention, or (short canvases) the f16 head/tail planes
       // of the tensor-core attention, in the same bytes
@@ -785,6 +880,13 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
                                  QKV, planes, 0, kc, kc ? kc + L * d : nullptr);
       note_launch();
       if (e != cudaSuccess) return cuda_fail(e, "launch qkv reduce");
+      if (tp && (tp->q || tp->k || tp->v)) {
+        const int64_t n3 = L * 3 * d;
+        tap_qkv_kernel<<<(unsigned)((n3 + 255) / 256), 256, 0, s>>>(planes, tc_att ? nullptr : QKV, (int)L, d, tp->q,
+                                                                    tp->k, tp->v);
+        note_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch tap_qkv");
+      }
       const AttPart ap{reinterpret_cast<float*>(ws + S.att), reinterpret_cast<float*>(ws + S.attml)};
       int nchunk = 1;
       if (tc_att) {  // whole rows per CTA on the tensor cores
@@ -810,21 +912,27 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
       const dim3 mg((unsigned)act_rows_padded(L), (unsigned)((d / QK + 7) / 8));
       if (e == cudaSuccess)
         e = launch_pdl(attn_merge_quant_kernel, mg, dim3(256), 0, s, ap, nchunk, (int)L, d, m->n_heads,
-                       quant_out(actd, L, d));
+                       quant_out(actd, L, d, tp ? tp->attn : nullptr));
       note_launch();
       if (e == cudaSuccess) e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "launch attention");
     } else {
       // linear stream: the O projection consumes the V projection's output
-      if ((rc = run_row<ROW_SUM_QUANT>(nullptr, Pv, S.v.splits, L * d, d, nullptr, 0.f, (int)L, d, actd, s))) return rc;
+      if ((rc = run_row<ROW_SUM_QUANT>(nullptr, Pv, S.v.splits, L * d, d, nullptr, 0.f, (int)L, d, actd, s,
+                                       tp ? tp->attn : nullptr)))
+        return rc;
     }
+    if (tp && (rc = tap_copy(tp->act_o, actd, act_d_bytes, s))) return rc;
     if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wo, d, Po, S.o, s))) return rc;
     if ((rc = run_row<ROW_RESID_NORM_QUANT>(x, Po, S.o.splits, L * d, d, Ly.ffn_norm, m->eps, (int)L, d, actd, s)))
       return rc;
+    if (tp && (rc = tap_copy(tp->x_mid, x, (size_t)L * d * 4, s))) return rc;
+    if (tp && (rc = tap_copy(tp->act_ffn, actd, act_d_bytes, s))) return rc;
     if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wgu, 2 * f, Pgu, S.gu, s))) return rc;
     if ((rc = run_row<ROW_SWIGLU_QUANT>(nullptr, Pgu, S.gu.splits, L * 2 * f, 2 * f, nullptr, 0.f, (int)L, f, actf,
-                                        s)))
+                                        s, tp ? tp->h : nullptr)))
       return rc;
+    if (tp && (rc = tap_copy(tp->act_down, actf, act_f_bytes, s))) return rc;
     if ((rc = gemm(DLLM_Q6_K, actf, L, f, Ly.wdown, d, Pdn, S.dn, s))) return rc;
     if (li + 1 < m->n_layers) {
       if ((rc = run_row<ROW_RESID_NORM_QUANT>(x, Pdn, S.dn.splits, L * d, d, m->layers[li + 1].attn_norm, m->eps,
@@ -834,6 +942,7 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
       if ((rc = run_row<ROW_RESID_ONLY>(x, Pdn, S.dn.splits, L * d, d, nullptr, 0.f, (int)L, d, nullptr, s)))
         return rc;
     }
+    if (tp && (rc = tap_copy(tp->x_out, x, (size_t)L * d * 4, s))) return rc;
   }
   return DLLM_OK;
 }
@@ -927,6 +1036,11 @@ DLLM_API size_t dllm_step_workspace_bytes(const dllm_model* m, int64_t L, int fl
 
 DLLM_API int dllm_step_linear_stream(const dllm_model* m, const int32_t* canvas, int64_t L, float* x, int flags,
                                      void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  return dllm_step_taps(m, canvas, L, x, flags, nullptr, ws, ws_bytes, stream);
+}
+
+DLLM_API int dllm_step_taps(const dllm_model* m, const int32_t* canvas, int64_t L, float* x, int flags,
+                            const dllm_taps* taps, void* ws, size_t ws_bytes, dllm_stream_t stream) {
   int rc = check_model(m, L, "dllm_step_linear_stream");
   if (rc) return rc;
   if (flags != DLLM_STREAM_LINEAR && flags != DLLM_STREAM_FULL)
@@ -945,7 +1059,21 @@ DLLM_API int dllm_step_linear_stream(const dllm_model* m, const int32_t* canvas,
                 S.bytes);
   if ((reinterpret_cast<uintptr_t>(ws) & 1023) != 0)
     return fail(DLLM_E_ALIGN, "dllm_step_linear_stream: ws must be 1024-byte aligned");
-  return forward(m, canvas, L, x, flags, static_cast<uint8_t*>(ws), S, (cudaStream_t)stream);
+  if (taps) {
+    if (taps->layer < 0 || taps->layer >= m->n_layers)
+      return fail(DLLM_E_INVAL, "dllm_step_taps: taps->layer=%d is not a layer of the model", taps->layer);
+    const void* ps[] = {taps->x_in, taps->act_attn, taps->q, taps->k, taps->v, taps->attn, taps->act_o,
+                        taps->x_mid, taps->act_ffn, taps->h, taps->act_down, taps->x_out};
+    for (const void* p : ps)
+      if (p && !device_ptr(p)) return fail(DLLM_E_INVAL, "dllm_step_taps: a tap pointer is not a device pointer");
+    const float* f4[] = {taps->attn, taps->h};
+    for (const float* p : f4)
+      if (p && (reinterpret_cast<uintptr_t>(p) & 15))
+        return fail(DLLM_E_ALIGN, "dllm_step_taps: the attn and h taps must be 16-byte aligned");
+    if (flags != DLLM_STREAM_FULL && (taps->q || taps->k || taps->v))
+      return fail(DLLM_E_INVAL, "dllm_step_taps: the q, k, v taps need DLLM_STREAM_FULL");
+  }
+  return forward(m, canvas, L, x, flags, static_cast<uint8_t*>(ws), S, (cudaStream_t)stream, nullptr, taps);
 }
 
 DLLM_API size_t dllm_denoise_workspace_bytes(const dllm_model* m, int64_t L, int32_t block_rows) {

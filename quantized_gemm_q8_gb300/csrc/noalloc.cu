@@ -15,7 +15,10 @@
 // before any stream capture. All calls share the array and it keeps the previous call's
 // contents; the GEMM writes every partial it later reads, so nothing needs clearing. Calls
 // that overlap on the GPU (on different streams, or from different host threads without
-// ordering) race on the array and must not be issued that way.
+// ordering) race on the array and must not be issued that way. The cached address belongs to
+// the device's context at the time of the first call: after cudaDeviceReset (or any teardown
+// of that context) it is stale, so a process that resets a device must not call this entry
+// point on that device again.
 #include <mutex>
 
 #include "internal.h"
@@ -45,18 +48,6 @@ int noalloc_scratch(float** out) {
   }
   *out = g_noalloc_ptr[dev];
   return DLLM_OK;
-}
-
-// y (+)= sum over the splits of the partials, in split order.
-__global__ void noalloc_reduce_kernel(const float* __restrict__ P, int splits, int64_t stride, int m, int n,
-                                      float* __restrict__ y, int64_t ldy, int accumulate) {
-  const int64_t total = (int64_t)m * n;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    float s = 0.f;
-    for (int sp = 0; sp < splits; ++sp) s += P[sp * stride + i];
-    float* o = y + (i / n) * ldy + (i % n);
-    *o = accumulate ? *o + s : s;
-  }
 }
 
 }  // namespace
@@ -94,10 +85,5 @@ extern "C" DLLM_API int dllm_qgemm_noalloc(int type, const void* act, int64_t m,
   cudaStream_t s = (cudaStream_t)stream;
   GemmLaunch g{type, act, m, k, w_packed, n, scratch, n, 0, scratch, 0, nullptr, nullptr, nullptr, nullptr};
   if ((rc = launch_gemm(g, P, s))) return rc;
-  const int64_t total = m * n;
-  const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4 * num_sms());
-  noalloc_reduce_kernel<<<blocks, 256, 0, s>>>(scratch, P.splits, m * n, (int)m, (int)n, y, ldy, accumulate);
-  note_launch();
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch noalloc reduce");
+  return launch_reduce_splits(scratch, P.splits, m * n, m, n, y, ldy, accumulate, s);
 }

@@ -17,6 +17,7 @@ enum : int {
   ERR_TIMEOUT_SELFTEST = 1 << 4,
   ERR_TIMEOUT_OTHER = 1 << 5,
   ERR_RANGE = 1 << 6,  // a Q4_K block whose dmin/d ratio cannot be folded (|dmin/d| > 4e6)
+  ERR_BSUM = 1 << 7,   // plain Q8_K input whose 16-sums do not match its codes (dllm_pack_act)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

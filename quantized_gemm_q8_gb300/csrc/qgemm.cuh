@@ -15,21 +15,25 @@
 //
 // Per super-block ONE accumulator part D is produced, in TMEM slot t & 1 (two slots of NT
 // columns: the epilogue drains super-block t while the tensor core fills t + 1):
-//   Q4_K: D = 2^-k * I - sum_g c_g * bsum16_g,   I = sum_k (scale_j * q4_k) * a_k,
-//         c_g = min_{g/2} * (dmin / d) * 2^-k,   y += d_a * (d * 2^k) * D
-//         The 16 MMAs of I read A = scale * q4 * 2^-k from tensor memory (exact f16 values); the
-//         min term is two more K = 16 MMAs from shared memory whose A operands are the f16
-//         head and tail of -c_g (their sum carries c_g to 2^-22 relative) against the exact
-//         f16 activation 16-sums. k >= 0 is the smallest shift keeping 63 * |dmin / d| * 2^-k
-//         below 2^14 (k = 0 for any realistic block). A row with d = 0 uses D = -sum min * bsum
-//         and y += d_a * dmin * D.
+//   Q4_K: D = 2^-k * I' + sum_g c_g * bsum16_g,   I' = sum_k (scale_j * (q4_k - 8)) * a_k,
+//         c_g = (8 * scale_{g/2} - min_{g/2} * (dmin / d)) * 2^-k,   y += d_a * (d * 2^k) * D
+//         so that D = 2^-k (I - (dmin / d) J) with I = sum scale * q4 * a, J = sum min * bsum.
+//         The 16 MMAs of I' read A = scale * (q4 - 8) * 2^-k from tensor memory (exact f16
+//         values); the re-centred quants keep every partial sum of that integer chain within
+//         63 * 8 * 127 * 256 < 2^24, so it is exact for every input. The offset and min term are
+//         two more K = 16 MMAs from shared memory whose A operands are the f16 head and tail of
+//         c_g (their sum carries c_g to 2^-22 relative) against the exact f16 activation
+//         16-sums. k >= 0 is the smallest shift keeping 63 * |dmin / d| * 2^-k below 2^14 (k = 0
+//         for any realistic block). A row with d = 0 uses D = -sum min * bsum and
+//         y += d_a * dmin * D.
 //   Q6_K: the int8 group scale s = 16 * s_hi + s_lo (s_lo in [0,15]); per K-quarter 4 MMAs
-//         with A = 16 * s_hi * (q-32) and 4 with A = s_lo * (q-32) (both exact f16 integers)
-//         accumulate D = sum s (q-32) a;  y += d_a * d * D.
-// Integer sums are exact while every partial sum stays below 2^24 in magnitude (always for
-// Q6_K's separate hi and lo sums, the debug parts below, and random data; an all-extreme
-// block can exceed it and then rounds at 2^-24 relative). A debug mode runs the same kernel
-// with one part isolated (Q4_K: I or J; Q6_K: I_hi or I_lo) and writes the exact integers.
+//         with A = s_hi * (q-32) (exact f16 integers) and 4 with A = s_lo * (q-32) / 16 (exact
+//         f16 multiples of 1/16) accumulate D = sum s (q-32) a / 16;  y += d_a * (16 d) * D.
+// Integer sums are exact while every partial sum stays below 2^24 in magnitude: always for
+// Q4_K's I' chain, Q6_K's separate hi and lo sums and the debug parts below; Q6_K's combined
+// sum stays below it on random data, and an all-extreme Q6_K block can exceed it and then
+// rounds at 2^-24 relative. A debug mode runs the same kernel with one part isolated (Q4_K:
+// I', J or 8 * sum scale * bsum; Q6_K: I_hi or I_lo) and writes the exact integers.
 // The epilogue loads the part into registers in groups, frees the slot once the last group is
 // loaded, and folds y += (f * D) * d_a.
 //
@@ -45,8 +49,8 @@
 // Rings (mbarrier-synchronized, every wait bounded):
 //   W  raw packed super-block of the 128 rows (+ Q4_K d/dmin), smem   weight producer -> decode
 //   E  per-super-block scales for the epilogue, smem: d/dmin, d_a    act. producer -> epilogue
-//   J  Q4_K min operands, smem: activation 16-sums (bulk copy) and     producer, decode -> MMA
-//      -c head and tail rows
+//   J  Q4_K offset/min operands, smem: activation 16-sums (bulk        producer, decode -> MMA
+//      copy) and the c head and tail rows
 //   K  K-stage: activation tile (smem, TMA, 128-byte swizzle) and     producer, decode -> MMA
 //      decoded weights (TMEM), 64 TMEM columns
 //   S  accumulator slots, TMEM                                        MMA -> epilogue
@@ -122,7 +126,7 @@ struct QCfg {
   static constexpr int J_STAGES = Q4 ? 3 : 0;
   static constexpr int J_BJ = 0;
   static constexpr int J_AJ = al128(NT * 32);
-  static constexpr int J_BYTES = J_AJ + 8192;  // -c head, then tail, 128 rows x 16 f16 each
+  static constexpr int J_BYTES = J_AJ + 8192;  // c head, then tail, 128 rows x 16 f16 each
   static constexpr int J_TX = NT * 32;
   static constexpr int B_QUARTER = NT * 128;
   static constexpr int B_STAGE = QPS * B_QUARTER;
@@ -160,7 +164,8 @@ struct QgemmParams {
   long long ldy, split_stride;
   int accumulate;
   int32_t* dbg;   // debug: exact integer sums of one part, [nsb][m][n]
-  int dbg_mode;   // 0 off; 1 part 0 only (Q4_K I, Q6_K I_hi); 2 part 1 only (Q4_K J, Q6_K I_lo)
+  int dbg_mode;   // 0 off; 1 part 0 only (Q4_K I', Q6_K I_hi); 2 part 1 only (Q4_K J, Q6_K I_lo);
+                  // 3 (Q4_K) the offset part 8 * sum scale * bsum, added to dbg (I = I' + it)
   int* err;      // device error word
   // mode 1 (LM head): instead of y, per (weight tile, TMEM lane quadrant, token) softmax
   // partials over the 32 weight rows of the quadrant: max logit, its row (lowest on ties),
@@ -218,30 +223,38 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
 }
 
 // Q4_K, one half of a K-quarter: h = 0 the low nibbles (chunks 0-3), h = 1 the high nibbles
-// (chunks 4-7) of the quarter's 32 quant bytes, as 16 words; (mul, add) as above for the
-// half's sub-block.
+// (chunks 4-7) of the quarter's 32 quant bytes, as 16 words. Each nibble lands in bits 4-7 of
+// an f16 half with the exponent of 1024 (the low nibbles shifted up by 4), i.e. the half holds
+// 1024 + 16 q; (mul, add) = (scale / 16, -72 scale) times the fold's 2^-k turn it into
+// scale * (q - 8) * 2^-k with one exact fused multiply-add (72 * scale has at most 10
+// significant bits, so the addend is an exact f16 value).
 __device__ __forceinline__ void decode_q4k_half(const uint8_t* W, int t, int q, int h, __half2 mul, __half2 add,
                                                 uint32_t (&o)[16]) {
   const uint4 v0 = *reinterpret_cast<const uint4*>(W + (2 * q) * 2048 + t * 16);
   const uint4 v1 = *reinterpret_cast<const uint4*>(W + (2 * q + 1) * 2048 + t * 16);
   const uint32_t x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-  const uint32_t mask = h ? 0x00F000F0u : 0x000F000Fu;
+  constexpr uint32_t mask = 0x00F000F0u;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint32_t w0 = x[2 * c], w1 = x[2 * c + 1];
-    o[4 * c + 0] = hfma2u((w0 & mask) | 0x64006400u, mul, add);
-    o[4 * c + 1] = hfma2u(((w0 >> 8) & mask) | 0x64006400u, mul, add);
-    o[4 * c + 2] = hfma2u((w1 & mask) | 0x64006400u, mul, add);
-    o[4 * c + 3] = hfma2u(((w1 >> 8) & mask) | 0x64006400u, mul, add);
+    // bytes (0, 2) and (1, 3) of each word, their nibble in bits 4-7 of each half
+    const uint32_t a0 = h ? w0 : w0 << 4, b0 = h ? w0 >> 8 : w0 >> 4;
+    const uint32_t a1 = h ? w1 : w1 << 4, b1 = h ? w1 >> 8 : w1 >> 4;
+    o[4 * c + 0] = hfma2u((a0 & mask) | 0x64006400u, mul, add);
+    o[4 * c + 1] = hfma2u((b0 & mask) | 0x64006400u, mul, add);
+    o[4 * c + 2] = hfma2u((a1 & mask) | 0x64006400u, mul, add);
+    o[4 * c + 3] = hfma2u((b1 & mask) | 0x64006400u, mul, add);
   }
 }
 
 // Q6_K: piece ps (0 or 1) of half tt of K-quarter q (half-block hq = q/2, t-slot 2(q%2)+tt) of
 // row t, from one 16-byte load of ql and one of qh: 8 words of the hi operand
-// (hs * s_hi * (q6-32)) and 8 of the lo operand (ls * s_lo * (q6-32)), exact f16 integers (the
-// int8 group scale s = 16 * s_hi + s_lo, s_lo in [0,15]; hs in {0, 1, 16}, ls in {0, 1}).
-// Even quarters take the low ql nibble and the f16 pattern 1024 + q6 (qh bits at 4-5), odd
-// quarters the high nibble and 1024 + 16*q6 (qh bits at 8-9) with the scale divided by 16.
+// (hs * s_hi * (q6-32), exact f16 integers) and 8 of the lo operand (ls * s_lo * (q6-32) / 16,
+// exact f16 multiples of 1/16), where the int8 group scale s = 16 * s_hi + s_lo, s_lo in [0,15],
+// and hs, ls in {0, 1}; so hi + lo = s (q6-32) / 16 and the epilogue applies 16 d. Even
+// quarters take the low ql nibble and the f16 pattern 1024 + q6 (qh bits at 4-5), odd quarters
+// the high nibble and 1024 + 16*q6 (qh bits at 8-9) with the multiplier divided by 16; every
+// operand is one exact fused multiply-add of the pattern.
 __device__ __forceinline__ void decode_q6k_piece(const uint8_t* W, int t, int q, int tt, int ps, const int8_t* sc,
                                                  float hs, float ls, uint32_t (&hi)[8], uint32_t (&lo)[8]) {
   const int hq = q >> 1, odd = q & 1;
@@ -255,10 +268,9 @@ __device__ __forceinline__ void decode_q6k_piece(const uint8_t* W, int t, int q,
   const int tslot = 2 * odd + tt;
   const int shift = tt ? 2 : 4;
   const int s = sc[8 * hq + 2 * tslot + ps];
-  const float s_hi = hs == 0.f ? 0.f : (float)(s >> 4), s_lo = (float)(s & 15) * ls;
+  const float s_hi = hs == 0.f ? 0.f : (float)(s >> 4), s_lo = (float)(s & 15) * ls * 0.0625f;
   const __half2 mH = __float2half2_rn(s_hi * fm), aH = __float2half2_rn(s_hi * fa);
   const __half2 mL = __float2half2_rn(s_lo * fm), aL = __float2half2_rn(s_lo * fa);
-  const __half2 h16 = __float2half2_rn(hs == 16.f ? 16.f : 1.f);
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     const uint32_t X0 = ql[2 * c], X1 = ql[2 * c + 1];
@@ -267,10 +279,10 @@ __device__ __forceinline__ void decode_q6k_piece(const uint8_t* W, int t, int q,
     const uint32_t v1 = ((X0 >> 8) & nmask) | (((H0 >> 8) << shift) & hmask) | 0x64006400u;
     const uint32_t v2 = (X1 & nmask) | ((H1 << shift) & hmask) | 0x64006400u;
     const uint32_t v3 = ((X1 >> 8) & nmask) | (((H1 >> 8) << shift) & hmask) | 0x64006400u;
-    hi[4 * c + 0] = h2u(__hmul2(u2h(hfma2u(v0, mH, aH)), h16));
-    hi[4 * c + 1] = h2u(__hmul2(u2h(hfma2u(v1, mH, aH)), h16));
-    hi[4 * c + 2] = h2u(__hmul2(u2h(hfma2u(v2, mH, aH)), h16));
-    hi[4 * c + 3] = h2u(__hmul2(u2h(hfma2u(v3, mH, aH)), h16));
+    hi[4 * c + 0] = hfma2u(v0, mH, aH);
+    hi[4 * c + 1] = hfma2u(v1, mH, aH);
+    hi[4 * c + 2] = hfma2u(v2, mH, aH);
+    hi[4 * c + 3] = hfma2u(v3, mH, aH);
     lo[4 * c + 0] = hfma2u(v0, mL, aL);
     lo[4 * c + 1] = hfma2u(v1, mL, aL);
     lo[4 * c + 2] = hfma2u(v2, mL, aL);
@@ -508,7 +520,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
               mma_commit(BAR(C::BK_EMPTY + b));
             }
             if (!ok) break;
-            // min term last: head and tail coefficients x activation 16-sums
+            // offset and min term last: head and tail coefficients x activation 16-sums
             const int jx = it % C::J_STAGES;
             if (!(ok = wait_tc(BAR(C::BJ_FULL + jx), (it / C::J_STAGES) & 1))) break;
             const uint32_t js = sbase + C::OFF_J + jx * C::J_BYTES;
@@ -564,7 +576,10 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           // row t's fold of this super-block (see q4k_fold): the A operand carries scale * q * 2^-k
           const __half2 ddv = *reinterpret_cast<const __half2*>(W + C::W_BYTES + t * 4);
           const Q4Fold fo = q4k_fold(__low2float(ddv), __high2float(ddv), &bad);
-          const float ascale = p.dbg_mode == 1 ? 1.f : (p.dbg_mode == 2 ? 0.f : fo.ascale);
+          // A scale, and the J coefficients on 8 * scale and on min (debug modes isolate a part)
+          const float ascale = p.dbg_mode == 0 ? fo.ascale : (p.dbg_mode == 1 ? 1.f : 0.f);
+          const float jsc = p.dbg_mode == 0 ? fo.ascale : (p.dbg_mode == 3 ? 1.f : 0.f);
+          const float jmn = p.dbg_mode == 0 ? fo.cmul : (p.dbg_mode == 2 ? -1.f : 0.f);
           // stage g = quarters 2g, 2g+1 = sub-blocks 4g..4g+3; 6-bit scales: bytes 0-3 of scale
           // word 0 are entries 0..3, entries 4..7 combine word 2's low nibbles and word 0's top bits
           const uint32_t sw0 = *reinterpret_cast<const uint32_t*>(W + 16384 + t * 4);
@@ -576,17 +591,17 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           QTRACE(t == 0, 4, j);
           tc_fence_after();
           const uint32_t ta = tlane + b * C::ASTG;
-          // f16 multipliers (scale * 2^-k, and / 16 for the high nibbles) and addends: exact, from
-          // one integer-to-half conversion per sub-block
+          // f16 multipliers (scale * 2^-k / 16) and addends (-72 scale * 2^-k): exact, from one
+          // integer-to-half conversion per sub-block
           const __half2 asc = __float2half2_rn(ascale);
 #pragma unroll
           for (int qq = 0; qq < 2; ++qq) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              // sub-block 2q + h of quarter q = 2g + qq; value scale * q4 * 2^-k
+              // sub-block 2q + h of quarter q = 2g + qq; value scale * (q4 - 8) * 2^-k
               const __half2 sc = __hmul2(__half2half2(__int2half_rn((s4 >> (16 * qq + 8 * h)) & 0xFF)), asc);
-              const __half2 mul = h ? __hmul2(sc, __float2half2_rn(0.0625f)) : sc;
-              const __half2 add = __hmul2(sc, __float2half2_rn(h ? -64.f : -1024.f));
+              const __half2 mul = __hmul2(sc, __float2half2_rn(0.0625f));
+              const __half2 add = __hmul2(sc, __float2half2_rn(-72.f));
               uint32_t o[16];
               decode_q4k_half(W, t, 2 * g + qq, h, mul, add, o);
               tmem_st16(ta + 32 * qq + 16 * h, o);
@@ -594,11 +609,11 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           }
           {
             // while the stores drain: row t's J operand (K-major 8x16 B core matrices, no
-            // swizzle; K = 16 groups of 16 values, group k pairs with min_{k/2}) holds the f16
-            // head and tail of c = cmul * min; group g writes core matrix g (mins 4g..4g+3)
+            // swizzle; K = 16 groups of 16 values, group k pairs with sub-block k/2) holds the f16
+            // head and tail of c = jsc * 8 * scale + jmn * min; group g writes core matrix g
+            // (sub-blocks 4g..4g+3)
             const int jx = it % C::J_STAGES;
             if (!(ok = warp_wait(BAR(C::BJ_EMPTY + jx), ((it / C::J_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_DEC))) break;
-            const float cmul = p.dbg_mode == 1 ? 0.f : (p.dbg_mode == 2 ? -1.f : fo.cmul);
             const uint32_t w1 = *reinterpret_cast<const uint32_t*>(W + 16384 + 512 + t * 4);
             // 6-bit mins: entries 0..3 are the bytes of word 1, entries 4..7 combine word 2's
             // high nibbles with word 1's top bits
@@ -609,7 +624,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             uint32_t hd[4], tl[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const float c = cmul * (float)((m4 >> (8 * i)) & 0xFF);
+              const float c = fmaf(jmn, (float)((m4 >> (8 * i)) & 0xFF), jsc * (float)(8 * ((s4 >> (8 * i)) & 0xFF)));
               const __half ch = __float2half_rn(c);
               const __half ct = __float2half_rn(c - __half2float(ch));
               hd[i] = h2u(__halves2half2(ch, ch));
@@ -633,7 +648,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         } else {
           const uint4 scv = *reinterpret_cast<const uint4*>(W + 24576 + t * 16);
           const int8_t* sc = reinterpret_cast<const int8_t*>(&scv);
-          const float hs = p.dbg_mode == 2 ? 0.f : (p.dbg_mode == 1 ? 1.f : 16.f);
+          const float hs = p.dbg_mode == 2 ? 0.f : 1.f;
           const float ls = p.dbg_mode == 1 ? 0.f : 1.f;
 #pragma unroll 1
           for (int q = g; q < 4; q += 2) {
@@ -663,7 +678,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
       }
     }
     if (!ok && lane == 0) atomicOr(p.err, ERR_TIMEOUT_DECODE);
-    if (bad && lane == 0) atomicOr(p.err, ERR_RANGE);
+    if (bad) atomicOr(p.err, ERR_RANGE);  // the row's own thread: any lane may hold the bad block
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-15)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(QG_REGS_EPI));
@@ -699,7 +714,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           bool bad = false;
           cp = q4k_fold(__low2float(dd), __high2float(dd), &bad).factor;
         } else {
-          cp = __half2float(*reinterpret_cast<const __half*>(E + C::E_DD + row * 2));
+          cp = 16.f * __half2float(*reinterpret_cast<const __half*>(E + C::E_DD + row * 2));  // D = sum s (q-32) a / 16
         }
         const float4* da4 = reinterpret_cast<const float4*>(E + C::E_DA) + hf * (NC / 4);
         const uint32_t n = s ? sf1++ : sf0++;
@@ -737,13 +752,17 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
               ffma2(acc[b + 2], acc[b + 3], t2, t3, dv.z, dv.w);
             }
             if (p.dbg_mode != 0 && grow < p.n) {
-              // the isolated part's exact integers (Q4_K J is accumulated negated)
-              const float sgn = (C::Q4 && p.dbg_mode == 2) ? -1.f : 1.f;
+              // the isolated part's exact integers (Q4_K J is accumulated negated; the Q4_K offset
+              // part is added to the I' already written, giving I; Q6_K's lo part is held / 16)
+              const float sgn = p.dbg_mode != 2 ? 1.f : (C::Q4 ? -1.f : 16.f);
 #pragma unroll
               for (int jj = 0; jj < 8; ++jj) {
                 const int tok = tokb + ch * 8 + jj;
-                if (tok < p.m)
-                  p.dbg[((size_t)sbp * p.m + tok) * p.n + grow] = (int32_t)(sgn * __uint_as_float(r[c][jj]));
+                if (tok < p.m) {
+                  int32_t* dst = p.dbg + ((size_t)sbp * p.m + tok) * p.n + grow;
+                  const int32_t v = (int32_t)(sgn * __uint_as_float(r[c][jj]));
+                  *dst = p.dbg_mode == 3 ? *dst + v : v;
+                }
               }
             }
           }

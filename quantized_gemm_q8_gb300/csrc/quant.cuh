@@ -18,6 +18,7 @@ struct QuantOut {
   uint8_t* act_j;
   float* act_d;
   int lpad;
+  float* vtap;  // optional: the f32 values being quantized, [rows][k] (row stride k), for tests
 };
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
@@ -32,35 +33,12 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return s;
 }
 
-// Quantize one super-block held as 8 values per lane (lane covers k = 8*lane .. 8*lane+7)
-// and write all requested outputs for (row, sb).
-__device__ __forceinline__ void q8k_emit(float (&v)[8], int row, int rows, int sb, int64_t k, const QuantOut& o) {
+// Write one quantized super-block (lane holds codes k = 8*lane .. 8*lane+7, s16 the sum of
+// its lane pair's 16 codes, dsc the scale) to every requested output of (row, sb).
+__device__ __forceinline__ void q8k_store(const int (&qi)[8], int s16, float dsc, int row, int rows, int sb, int64_t k,
+                                          const QuantOut& o) {
   const int lane = threadIdx.x & 31;
   const int64_t nsb = k / QK;
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  int qi[8];
-  float dsc = 0.f;
-  if (amax == 0.f) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) qi[i] = 0;
-  } else {
-    const float iscale = __fdiv_rn(127.f, amax);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      float r = rintf(__fmul_rn(v[i], iscale));
-      r = fminf(127.f, fmaxf(-127.f, r));
-      qi[i] = (int)r;
-    }
-    dsc = __fdiv_rn(amax, 127.f);
-  }
-  int s8 = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) s8 += qi[i];
-  const int s16 = s8 + __shfl_xor_sync(0xffffffffu, s8, 1);  // group of 16 = lane pair
   const int g = lane >> 1;
   if (row < rows) {
     if (o.q) {
@@ -88,6 +66,41 @@ __device__ __forceinline__ void q8k_emit(float (&v)[8], int row, int rows, int s
     }
     if (lane == 0) o.act_d[(int64_t)sb * o.lpad + row] = dsc;
   }
+}
+
+// Quantize one super-block held as 8 values per lane (lane covers k = 8*lane .. 8*lane+7)
+// and write all requested outputs for (row, sb).
+__device__ __forceinline__ void q8k_emit(float (&v)[8], int row, int rows, int sb, int64_t k, const QuantOut& o) {
+  if (o.vtap && row < rows) {
+    float* t = o.vtap + (int64_t)row * k + (int64_t)sb * QK + 8 * (threadIdx.x & 31);
+    *reinterpret_cast<float4*>(t) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(t + 4) = make_float4(v[4], v[5], v[6], v[7]);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  int qi[8];
+  float dsc = 0.f;
+  if (amax == 0.f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qi[i] = 0;
+  } else {
+    const float iscale = __fdiv_rn(127.f, amax);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float r = rintf(__fmul_rn(v[i], iscale));
+      r = fminf(127.f, fmaxf(-127.f, r));
+      qi[i] = (int)r;
+    }
+    dsc = __fdiv_rn(amax, 127.f);
+  }
+  int s8 = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s8 += qi[i];
+  const int s16 = s8 + __shfl_xor_sync(0xffffffffu, s8, 1);  // group of 16 = lane pair
+  q8k_store(qi, s16, dsc, row, rows, sb, k, o);
 }
 
 }  // namespace dllm

@@ -231,3 +231,85 @@ def test_dual_cache_llada_shapes_two_layers():
     exact = _cached_steps_check(dims, synth.config_seed(4) + 5, 148, 20, 52, 4, n_steps=3)
     print(f"dual cache LLaDA shapes: {exact}/3 steps with commits identical to the oracle's order")
 
+
+
+# ---- config-4 commit parity: level (i), level (ii) on the GPU's own hidden rows, and end to end --
+
+def commit_parity(dims, lws, table, head, canvas, b0, b1, k, label):
+    """One denoising step on the GPU against the oracle, at three levels (Technical Specification,
+    section 19, "Level 2 - diffusion-step parity": mask positions, confidences, selected
+    positions, sampled ids and the updated canvas):
+      (i)   the GPU's commit logic against the oracle's on the GPU's own row confidences and ids:
+            bit-exact;
+      (ii)  the GPU head + commit against the oracle's head + commit on the GPU's own final hidden
+            rows: ids and commits bit-exact (the head's f32 logits agree to ~1e-6 of the oracle's);
+      (iii) the GPU step against the oracle's whole f64 forward: the commits must be identical
+            whenever the oracle's k-th / (k+1)-th confidence gap exceeds twice the largest
+            confidence shift that the measured hidden-state error causes (the oracle head on the
+            GPU's rows against on its own); below that margin the rankings are not decidable
+            in f32 and the step is reported, not failed.
+    Returns a dict with the margin, the bound and whether (iii) was decidable and exact."""
+    L = canvas.size
+    model = dl.DeviceModel(dims, lws, table, head)
+    gcanvas = torch.from_numpy(canvas.copy()).cuda()
+    hid = torch.empty((L, dims["d_model"]), device="cuda")
+    out = dl.denoise_step(model, gcanvas, b0, b1, k, hidden_out=hid)
+    dl.check()
+    gpos, gid = out["pos"].cpu().numpy(), out["id"].cpu().numpy()
+    gh = hid.cpu().numpy()
+    on = head["out_norm"]
+    mask = dims["mask_id"]
+    # (i) the GPU's row confidences and ids through the oracle's commit logic
+    cv = torch.from_numpy(canvas.copy()).cuda()
+    r = dl.lmhead_select(hid, cv, mask, b0, b1, k, torch.from_numpy(on).cuda(), model._keep[-1], dims["vocab"])
+    dl.check()
+    rconf = np.full(L, -np.inf)
+    rid = np.zeros(L, np.int32)
+    rconf[b0:b1] = r["row_conf"].cpu().numpy()
+    rid[b0:b1] = r["row_id"].cpu().numpy()
+    c_i = canvas.copy()
+    pos_i, id_i = orc.commit_topk(c_i, mask, b0, b1, rconf, rid, k)
+    np.testing.assert_array_equal(gpos[:pos_i.size], pos_i, err_msg=f"{label}: level (i) positions")
+    np.testing.assert_array_equal(gid[:pos_i.size], id_i, err_msg=f"{label}: level (i) ids")
+    np.testing.assert_array_equal(gcanvas.cpu().numpy(), c_i, err_msg=f"{label}: level (i) canvas")
+    # (ii) the oracle's head and commit on the GPU's final hidden rows: the GPU head's confidences
+    # agree to ~1e-4 (a row's Q8_K re-quantization can land on a rounding tie), so the commits
+    # must be identical whenever the oracle's k-th / (k+1)-th margin exceeds twice that shift
+    c_ii = canvas.copy()
+    ref_ii = orc.lmhead_commit(np.asarray(gh, np.float64), c_ii, mask, b0, b1, k, on, head["w_out"], dims["eps"])
+    rows = ref_ii["rows"]
+    shift_ii = float(np.max(np.abs(rconf[rows] - ref_ii["conf_rows"]))) if rows.size else 0.0
+    cs = np.sort(ref_ii["conf_rows"])[::-1]
+    margin_ii = float(cs[k - 1] - cs[k]) if cs.size > k else float("inf")
+    n_ii = ref_ii["pos"].size
+    exact_ii = bool(np.array_equal(gpos[:n_ii], ref_ii["pos"]) and np.array_equal(gid[:n_ii], ref_ii["id"]))
+    if margin_ii > 2.0 * shift_ii + 1e-6:
+        assert exact_ii, f"{label}: level (ii) commits differ: GPU {gpos[:n_ii]} {gid[:n_ii]}, oracle {ref_ii['pos']} {ref_ii['id']}"
+        np.testing.assert_array_equal(gcanvas.cpu().numpy(), c_ii, err_msg=f"{label}: level (ii) canvas")
+    ids_ok = rid[rows] == ref_ii["ids_rows"]
+    gap_ii = (ref_ii["top1"] - ref_ii["top2"])[~ids_ok]
+    assert np.all(gap_ii < 1e-2), f"{label}: row ids differ with top-1/top-2 logit gaps {gap_ii}"
+    # (iii) the oracle's own forward
+    x = orc.embed(table, canvas)
+    for lw in lws:
+        x, _ = orc.layer(lw, x, dims, attention_on=True)
+    c_iii = canvas.copy()
+    ref = orc.lmhead_commit(x, c_iii, mask, b0, b1, k, on, head["w_out"], dims["eps"])
+    conf_ref = np.sort(ref["conf_rows"])[::-1]
+    shift = float(np.max(np.abs(ref["conf_rows"] - ref_ii["conf_rows"]))) if ref["rows"].size else 0.0
+    n = ref["pos"].size
+    margin = float(conf_ref[k - 1] - conf_ref[k]) if conf_ref.size > k else float("inf")
+    decidable = margin > 2.0 * shift + 1e-6
+    exact = bool(np.array_equal(gpos[:n], ref["pos"]) and np.array_equal(gid[:n], ref["id"]))
+    errs = _row_errs(gh, x)
+    print(f"\n  {label}: level (ii) margin {margin_ii:.3e} shift {shift_ii:.3e} commits "
+          f"{'identical' if exact_ii else 'differ'}; level (iii): hidden max row error {errs.max():.2e}; oracle "
+          f"k-th/(k+1)-th confidence margin "
+          f"{margin:.3e}, confidence shift from the hidden error {shift:.3e}; "
+          f"{'decidable' if decidable else 'NOT decidable'}; commits {'identical' if exact else 'differ'} "
+          f"(GPU {gpos[:n].tolist()} oracle {ref['pos'].tolist()})")
+    if decidable:
+        assert exact, f"{label}: decidable step with different commits: GPU {gpos[:n]} {gid[:n]}, oracle {ref['pos']} {ref['id']}"
+    return dict(margin=margin, shift=shift, decidable=decidable, exact=exact, max_row_err=float(errs.max()),
+                margin_ii=margin_ii, shift_ii=shift_ii, exact_ii=exact_ii, canvas=gcanvas.cpu().numpy(),
+                oracle_canvas=c_iii)

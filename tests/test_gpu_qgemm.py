@@ -164,6 +164,138 @@ def test_qgemm_adversarial_extremes():
     np.testing.assert_array_equal(16 * s[0] + s[1], U - 32 * J)
 
 
+# ---- plain Q8_K input (the boundary's (q, d, bsum) form) ----------------------------------------
+
+@pytest.mark.parametrize("rows,k", [(37, 768), (148, 4096), (1, 256)])
+def test_pack_act_equals_quantize_operand(rows, k):
+    x = synth.activations(900 + rows, rows, k)
+    x[0, :256] = 0.0
+    nb = dl.act_bytes(rows, k)
+    a1 = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    g = dl.quantize_act(_dev(x), act=a1)
+    a2 = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    dl.pack_act(g["q"], g["d"], g["bsum"], act=a2)
+    dl.check()
+    assert torch.equal(a1, a2)
+
+
+@pytest.mark.parametrize("t", [dl.Q4_K, dl.Q6_K])
+@pytest.mark.parametrize("m,n,k", [(148, 512, 4096), (37, 300, 1024)])
+def test_qgemm_plain_q8k_input(t, m, n, k):
+    w, x = _case(t, m, n, k, 7000 + m + t)
+    q, d, bs = orc.quantize_q8k(x)  # the oracle's Q8_K blocks are the input
+    ref = orc.qgemm(t, w, q, d)
+    pk = _packed(t, w, n, k)
+    y = dl.qgemm_plain(t, _dev(q), _dev(d), _dev(bs), pk, n)
+    g = dl.quantize_act(_dev(x), plain=False)
+    y2 = dl.qgemm(t, g["act"], m, k, pk, n)
+    dl.check()
+    assert torch.equal(y, y2)  # the same operand, the same kernel
+    assert _row_rel_err(y.cpu().numpy(), ref) <= 1e-5
+    acc0 = synth.activations(7001 + m, m, n)
+    ya = _dev(acc0)
+    dl.qgemm_plain(t, _dev(q), _dev(d), _dev(bs), pk, n, y=ya, accumulate=True)
+    dl.check()
+    assert _row_rel_err(ya.cpu().numpy(), ref + acc0) <= 1e-5
+
+
+def test_pack_act_reports_inconsistent_sums():
+    x = synth.activations(950, 8, 512)
+    q, d, bs = orc.quantize_q8k(x)
+    bs[3, 17] += 1
+    dl.pack_act(_dev(q), _dev(d), _dev(bs))
+    with pytest.raises(dl.DllmError) as e:
+        dl.check()
+    assert e.value.code == dl.E_INVAL and "bsum" in str(e.value)
+    dl.check()
+
+
+def _q4k_fields_block(d_bits, dmin_bits, sc, mn, q):
+    from _encoders import encode_q4k
+    return encode_q4k(d_bits, dmin_bits, sc, mn, q)
+
+
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_qgemm_q4k_adversarial_extremes(sign):
+    # scale 63, min 63, quant 15 everywhere and activations of one sign (codes +-127): the
+    # pages' integer sum I = 63 * 15 * 127 * 256 per super-block exceeds 2^24; the kernel's
+    # re-centred chain keeps its partial sums below it, and the sums and outputs stay exact
+    t, m, n, k = dl.Q4_K, 16, 128, 512
+    blk = _q4k_fields_block(0x3C00, 0x3C00, [63] * 8, [63] * 8, [15] * 256)
+    w = np.tile(blk, (n, k // 256, 1))
+    x = np.full((m, k), sign, np.float32)
+    q, d, _ = orc.quantize_q8k(x)
+    assert np.all(q == int(127 * sign))
+    U, J = orc.intsums(t, w, q)
+    assert abs(int(U[0, 0, 0])) == 63 * 15 * 127 * 256 > 2 ** 24
+    pk = _packed(t, w, n, k)
+    g = dl.quantize_act(_dev(x), plain=False)
+    s = dl.qgemm_intsums(t, g["act"], m, k, pk, n).cpu().numpy().astype(np.int64).transpose(0, 2, 3, 1)
+    np.testing.assert_array_equal(s[0], U)
+    np.testing.assert_array_equal(s[1], J)
+    y = dl.qgemm(t, g["act"], m, k, pk, n)
+    dl.check()
+    ref = orc.qgemm(t, w, q, d)
+    assert _row_rel_err(y.cpu().numpy(), ref) <= 1e-6
+
+
+def _fold_case():
+    """Random Q4_K matrix with hand-set super-block scales that take every branch of the
+    kernel's min-term fold: d = 0 (the min term alone), dmin / d = 1024 and 512 and 2^16 (the
+    A operand scaled by 2^-k, k = 2, 1, 8), and an all-zero block."""
+    n, k = 256, 1024
+    w = synth.q4k_blocks(71, n, k)
+
+    def set_dd(row, sb, d_bits, dmin_bits):
+        w[row, sb, 0:2] = np.array([d_bits], np.uint16).view(np.uint8)
+        w[row, sb, 2:4] = np.array([dmin_bits], np.uint16).view(np.uint8)
+
+    for sb in range(k // 256):
+        set_dd(0, sb, 0x0000, 0x3C00)    # d = 0, dmin = 1
+        set_dd(1, sb, 0x1400, 0x3C00)    # d = 2^-10, dmin = 1: k = 2
+        set_dd(2, sb, 0x2400, 0x4800)    # d = 2^-6, dmin = 8: k = 1
+        set_dd(129, sb, 0x0010, 0x2C00)  # d = 2^-20 (subnormal), dmin = 2^-4: k = 8
+    w[3, 1] = 0                          # an all-zero block
+    set_dd(130, 2, 0x0000, 0x0000)       # d = dmin = 0 with non-zero quants
+    return w, n, k
+
+
+def test_qgemm_q4k_fold_branches():
+    w, n, k = _fold_case()
+    m = 24
+    x = synth.activations(72, m, k)
+    q, d, _ = orc.quantize_q8k(x)
+    ref = orc.qgemm(dl.Q4_K, w, q, d)
+    pk = _packed(dl.Q4_K, w, n, k)
+    g = dl.quantize_act(_dev(x), plain=False)
+    y = dl.qgemm(dl.Q4_K, g["act"], m, k, pk, n)
+    dl.check()
+    err = np.abs(y.cpu().numpy() - ref) / np.linalg.norm(ref, axis=1, keepdims=True)
+    assert err.max() <= 1e-5, (err.max(), np.unravel_index(np.argmax(err), err.shape))
+    U, J = orc.intsums(dl.Q4_K, w, q)
+    s = dl.qgemm_intsums(dl.Q4_K, g["act"], m, k, pk, n).cpu().numpy().astype(np.int64).transpose(0, 2, 3, 1)
+    dl.check()
+    np.testing.assert_array_equal(s[0], U)
+    np.testing.assert_array_equal(s[1], J)
+
+
+def test_qgemm_q4k_unfoldable_block_is_reported():
+    # |dmin / d| = 2^24 > 4e6: no f16 shift can carry the min term; the kernel records it in the
+    # device error word (no fault) and dllm_check reports DLLM_E_INVAL; the context stays usable
+    n, k, m = 128, 512, 8
+    w = synth.q4k_blocks(73, n, k)
+    w[5, 1, 0:2] = np.array([0x0001], np.uint16).view(np.uint8)  # d = 2^-24
+    w[5, 1, 2:4] = np.array([0x3C00], np.uint16).view(np.uint8)  # dmin = 1
+    pk = _packed(dl.Q4_K, w, n, k)
+    g = dl.quantize_act(_dev(synth.activations(74, m, k)), plain=False)
+    dl.qgemm(dl.Q4_K, g["act"], m, k, pk, n)
+    with pytest.raises(dl.DllmError) as e:
+        dl.check()
+    assert e.value.code == dl.E_INVAL and "4e6" in str(e.value)
+    dl.check()  # the error word was cleared
+    _gemm_check(dl.Q4_K, 16, 128, 256, 4243)
+
+
 # ---- boundary errors ------------------------------------------------------------------------
 
 def test_errors_are_reported_without_launch():

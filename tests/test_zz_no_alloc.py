@@ -76,3 +76,27 @@ def test_noalloc_accumulate_and_size_limit():
                                      big_n, ctypes.c_void_p(yb.data_ptr()), big_n, 0,
                                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == dl.E_SHAPE and "scratch" in dl.last_error()
+
+
+@pytest.mark.parametrize("accumulate", [0, 1])
+def test_noalloc_single_split_fallback(accumulate):
+    # the workspace plan splits k four ways (partials above the 32 MiB array) while the output
+    # itself fits: the entry point falls back to one split, written straight into the array
+    torch.cuda.set_device(0)
+    t, m, n, k = dl.Q6_K, 148, 40960, 12288
+    limit = 32 << 20
+    assert dl.qgemm_workspace_bytes(t, m, n, k) > limit >= m * n * 4  # the branch under test
+    w = synth.blocks(t, 7005, n, k)
+    x = synth.activations(7006, m, k)
+    pk = dl.pack_weights(t, torch.from_numpy(w.reshape(-1)).cuda(), n, k)
+    act = dl.quantize_act(torch.from_numpy(x).cuda(), plain=False)["act"]
+    y0 = synth.activations(7007, m, n) if accumulate else np.zeros((m, n), np.float32)
+    y = torch.from_numpy(y0).cuda()
+    _noalloc_c(t, act, m, k, pk, n, y, accumulate=accumulate)
+    ref_ws = dl.qgemm(t, act, m, k, pk, n)
+    dl.check()
+    got = y.cpu().numpy().astype(np.float64) - (y0 if accumulate else 0.0)
+    assert _rel(got, ref_ws.cpu().numpy().astype(np.float64)) <= 1e-5
+    rows = np.array([0, 1, 127, 128, 20000, n - 1])  # weight rows checked against the oracle
+    q, d, _ = orc.quantize_q8k(x)
+    assert _rel(got[:, rows], orc.qgemm(t, w, q, d, rows=rows)) <= TOL
