@@ -364,9 +364,11 @@ class DeviceModel:
         self._layers = arr
         te = dev(tok_embd.reshape(-1)).data_ptr() if tok_embd is not None else None
         on = wout = None
+        self.w_out_packed = self.out_norm = None
         if head is not None:
-            on = dev(head["out_norm"]).data_ptr()
-            wout = packed(Q6_K, head["w_out"], dims["vocab"], d).data_ptr()
+            self.out_norm = dev(head["out_norm"])
+            self.w_out_packed = packed(Q6_K, head["w_out"], dims["vocab"], d)
+            on, wout = self.out_norm.data_ptr(), self.w_out_packed.data_ptr()
         self.struct = _Model(n_layers, d, dims["n_heads"], dims["head_dim"], f, dims["vocab"], dims["mask_id"],
                              dims["eps"], dims["rope_theta"], arr, te, on, wout)
         self.ref = C.byref(self.struct)

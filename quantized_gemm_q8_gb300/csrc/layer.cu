@@ -8,7 +8,6 @@
 
 #include <algorithm>
 #include <cmath>
-#include <mutex>
 
 #include "internal.h"
 #include "qgemm.cuh"
@@ -785,52 +784,6 @@ static int gemm(int type, const void* act, int64_t m, int64_t k, const void* w, 
   return launch_gemm(g, P, s);
 }
 
-// A second stream and two events per device, created on the first forward pass on that device and
-// kept until exit: the V projection runs on the side stream beside the Q|K projection (both read
-// the same activations), so that V's CTAs fill the SMs that Q|K leaves idle. Work on the side
-// stream is forked from and joined back into the caller's stream with the events, so the pair
-// stays stream-ordered and is captured into a CUDA graph like the rest of the step.
-struct SideStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-
-static int side_stream(SideStream** out) {
-  static std::mutex mu;
-  static SideStream per_dev[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(DLLM_E_DEVICE, "device index %d out of range", dev);
-  std::lock_guard<std::mutex> lock(mu);
-  SideStream& ss = per_dev[dev];
-  if (!ss.s) {
-    if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess)
-      return cuda_fail(e, "cudaStreamCreateWithFlags (side stream)");
-    if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess ||
-        (e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess)
-      return cuda_fail(e, "cudaEventCreateWithFlags (side stream)");
-  }
-  *out = &ss;
-  return DLLM_OK;
-}
-
-// Q|K on s and V on the side stream, both after the work already on s; s continues after both.
-static int gemm_qk_v(const dllm_layer& Ly, void* actd, int64_t L, int d, float* Pqk, float* Pv, const StepPlan& S,
-                     cudaStream_t s) {
-  SideStream* ss = nullptr;
-  int rc = side_stream(&ss);
-  if (rc) return rc;
-  cudaError_t e = cudaEventRecord(ss->fork, s);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
-  if (e != cudaSuccess) return cuda_fail(e, "fork the side stream");
-  if ((rc = gemm(DLLM_Q6_K, actd, L, d, Ly.wv, d, Pv, S.v, ss->s))) return rc;
-  if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wqk, 2 * d, Pqk, S.qk, s))) return rc;
-  e = cudaEventRecord(ss->join, ss->s);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ss->join, 0);
-  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "join the side stream");
-}
-
 // The forward pass over all layers; x is [L][d] (input for the linear stream, output always).
 // kv (optional, full stream only): per layer K (after RoPE) then V of every row, [layers][2][L][d].
 // taps (optional, tests): the intermediates of layer taps->layer are copied out as they appear.
@@ -865,7 +818,8 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
     const dllm_taps* tp = (taps && taps->layer == li) ? taps : nullptr;
     if (tp && (rc = tap_copy(tp->x_in, x, (size_t)L * d * 4, s))) return rc;
     if (tp && (rc = tap_copy(tp->act_attn, actd, act_d_bytes, s))) return rc;
-    if ((rc = gemm_qk_v(Ly, actd, L, d, Pqk, Pv, S, s))) return rc;
+    if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wqk, 2 * d, Pqk, S.qk, s))) return rc;
+    if ((rc = gemm(DLLM_Q6_K, actd, L, d, Ly.wv, d, Pv, S.v, s))) return rc;
     if (full) {
       // Q, K, V: f32 rows for the chunked attention, or (short canvases) the f16 head/tail planes
       // of the tensor-core attention, in the same bytes

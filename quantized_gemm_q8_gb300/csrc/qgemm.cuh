@@ -79,22 +79,9 @@ constexpr int QG_REGS_EPI = 88, QG_REGS_DEC = 56, QG_REGS_CTL = 40;
 static_assert(512 * QG_REGS_EPI + 256 * QG_REGS_DEC + 128 * QG_REGS_CTL <= QG_THREADS * QG_REGS_LAUNCH,
               "register split");
 constexpr int SMEM_LIMIT = 232448;
-// sleep hints (ns) of the waiting roles (0 = spin); the hint bounds how late a sleeping warp
-// notices that its barrier completed, and a spinning warp takes issue slots from its SMSP
-#ifndef QG_SLEEP_MMA_NS
-#define QG_SLEEP_MMA_NS 0
-#endif
-#ifndef QG_SLEEP_DEC_NS
-#define QG_SLEEP_DEC_NS 32
-#endif
-#ifndef QG_SLEEP_EPI_NS
-#define QG_SLEEP_EPI_NS 128
-#endif
-#ifndef QG_SLEEP_PROD_NS
-#define QG_SLEEP_PROD_NS 64
-#endif
-constexpr uint32_t QG_SLEEP_MMA = QG_SLEEP_MMA_NS, QG_SLEEP_DEC = QG_SLEEP_DEC_NS, QG_SLEEP_EPI = QG_SLEEP_EPI_NS,
-                   QG_SLEEP_PROD = QG_SLEEP_PROD_NS;
+// how each role waits on an mbarrier: the MMA issuer tests back to back (it is one thread and
+// the tensor pipe's feeder); every other role suspends in mbarrier.try_wait (see mbar_wait)
+constexpr bool QG_POLL = true, QG_SUSPEND = false;
 constexpr int TMEM_COLS = 512;
 
 __host__ __device__ constexpr int al128(int x) { return (x + 127) & ~127; }
@@ -417,7 +404,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         const uint8_t* dd = p.wdd + (size_t)tn * p.nsb * C::DD_BYTES;
         for (int sb = sb0; sb < sb1; ++sb, ++it) {
           const int w = it % C::W_STAGES;
-          if (!(ok = mbar_wait(BAR(C::BW_EMPTY + w), ((it / C::W_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_PROD))) break;
+          if (!(ok = mbar_wait(BAR(C::BW_EMPTY + w), ((it / C::W_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
           const uint32_t ws = sbase + C::OFF_W + w * C::W_SLOT;
           mbar_expect_tx(BAR(C::BW_FULL + w), C::W_SLOT);
           bulk_g2s(ws, blob + (size_t)sb * C::W_BYTES, C::W_BYTES, BAR(C::BW_FULL + w));
@@ -446,21 +433,21 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         const int tok0 = tm * NT;
         for (int sb = sb0; sb < sb1; ++sb, ++it) {
           const int e = it % C::E_STAGES;
-          if (!(ok = mbar_wait(BAR(C::BE_EMPTY + e), ((it / C::E_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_PROD))) break;
+          if (!(ok = mbar_wait(BAR(C::BE_EMPTY + e), ((it / C::E_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
           const uint32_t es = sbase + C::OFF_E + e * C::E_BYTES;
           mbar_expect_tx(BAR(C::BE_FULL + e), C::E_TX);
           bulk_g2s(es + C::E_DD, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES, BAR(C::BE_FULL + e));
           bulk_g2s(es + C::E_DA, p.act_d + (size_t)sb * p.lpad + tok0, NT * 4, BAR(C::BE_FULL + e));
           if constexpr (C::Q4) {
             const int jx = it % C::J_STAGES;
-            if (!(ok = mbar_wait(BAR(C::BJ_EMPTY + jx), ((it / C::J_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_PROD))) break;
+            if (!(ok = mbar_wait(BAR(C::BJ_EMPTY + jx), ((it / C::J_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
             mbar_expect_tx(BAR(C::BJ_FULL + jx), C::J_TX);
             bulk_g2s(sbase + C::OFF_J + jx * C::J_BYTES + C::J_BJ, p.act_j + ((size_t)sb * p.lpad + tok0) * 32,
                      NT * 32, BAR(C::BJ_FULL + jx));
           }
           for (int st = 0; st < C::SPS; ++st) {
             const int j = C::SPS * it + st, b = j % C::K_STAGES;
-            if (!(ok = mbar_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_PROD))) break;
+            if (!(ok = mbar_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
             mbar_expect_tx(BAR(C::BK_FULL + b), C::B_STAGE);
 #pragma unroll
             for (int qq = 0; qq < C::QPS; ++qq)
@@ -489,7 +476,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
       uint32_t se0 = 0, se1 = 0;
       bool ok = true;
       auto wait_tc = [&](uint32_t bar, uint32_t parity) -> bool {
-        const bool r = mbar_wait(bar, parity, abort_flag, lim, QG_SLEEP_MMA);
+        const bool r = mbar_wait(bar, parity, abort_flag, lim, QG_POLL);
         tc_fence_after();
         return r;
       };
@@ -569,7 +556,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
       unit_coords(p, u, tn, tm, sp, sb0, sb1);
       for (int sb = sb0; sb < sb1; ++sb, ++it) {
         const int w = it % C::W_STAGES;
-        if (!(ok = warp_wait(BAR(C::BW_FULL + w), (it / C::W_STAGES) & 1, abort_flag, lim, QG_SLEEP_DEC))) break;
+        if (!(ok = warp_wait(BAR(C::BW_FULL + w), (it / C::W_STAGES) & 1, abort_flag, lim, QG_SUSPEND))) break;
         QTRACE(t == 0 && g == 0, 8, it);
         const uint8_t* W = smem + C::OFF_W + w * C::W_SLOT;
         if constexpr (C::Q4) {
@@ -587,7 +574,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
                                    ((sw0 >> 2) & 0x30303030u))
                                 : (sw0 & 0x3F3F3F3Fu);
           const int j = 2 * it + g, b = j % C::K_STAGES;
-          if (!(ok = warp_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_DEC))) break;
+          if (!(ok = warp_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
           QTRACE(t == 0, 4, j);
           tc_fence_after();
           const uint32_t ta = tlane + b * C::ASTG;
@@ -613,7 +600,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             // head and tail of c = jsc * 8 * scale + jmn * min; group g writes core matrix g
             // (sub-blocks 4g..4g+3)
             const int jx = it % C::J_STAGES;
-            if (!(ok = warp_wait(BAR(C::BJ_EMPTY + jx), ((it / C::J_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_DEC))) break;
+            if (!(ok = warp_wait(BAR(C::BJ_EMPTY + jx), ((it / C::J_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
             const uint32_t w1 = *reinterpret_cast<const uint32_t*>(W + 16384 + 512 + t * 4);
             // 6-bit mins: entries 0..3 are the bytes of word 1, entries 4..7 combine word 2's
             // high nibbles with word 1's top bits
@@ -653,7 +640,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
 #pragma unroll 1
           for (int q = g; q < 4; q += 2) {
             const int j = 4 * it + q, b = j % C::K_STAGES;
-            if (!(ok = warp_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SLEEP_DEC))) break;
+            if (!(ok = warp_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
             QTRACE(t == 0, 4, j);
             tc_fence_after();
 #pragma unroll
@@ -706,7 +693,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         const int itp = it0 + i, sbp = sb0 + i;
         const int s = itp & 1;
         const int e = itp % C::E_STAGES;
-        if (!(ok = warp_wait(BAR(C::BE_FULL + e), (itp / C::E_STAGES) & 1, abort_flag, lim, QG_SLEEP_EPI))) break;
+        if (!(ok = warp_wait(BAR(C::BE_FULL + e), (itp / C::E_STAGES) & 1, abort_flag, lim, QG_SUSPEND))) break;
         const uint8_t* E = smem + C::OFF_E + e * C::E_BYTES;
         float cp;
         if constexpr (C::Q4) {
@@ -718,7 +705,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         }
         const float4* da4 = reinterpret_cast<const float4*>(E + C::E_DA) + hf * (NC / 4);
         const uint32_t n = s ? sf1++ : sf0++;
-        if (!(ok = warp_wait(BAR(C::BS_FULL + s), n & 1, abort_flag, lim, QG_SLEEP_EPI))) break;
+        if (!(ok = warp_wait(BAR(C::BS_FULL + s), n & 1, abort_flag, lim, QG_SUSPEND))) break;
         tc_fence_after();
         QTRACE(warp == 0 && lane == 0, 6, itp);
         // drain in groups of up to 2 x 8 columns; the slot is freed as soon as the last group

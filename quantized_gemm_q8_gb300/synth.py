@@ -10,13 +10,15 @@ number generators", OOPSLA 2014), used as a counter-based stream:
 value i of stream s is mix64(s + (i + 1) * GOLDEN). Normals come from the
 Box-Muller transform of two uniforms.
 
-Value ranges (the pages only say "uniform-random"; the plain reading):
+Value ranges (the pages only say "uniform-random"; the plain reading, used by the workloads):
   * every quant bit, every 6-bit Q4_K scale/min and every Q6_K int8 scale is
     uniform over its full range (the raw bytes are uniform);
   * Q4_K d and dmin, and Q6_K d, are f16 values uniform over [2^-14, 2^-13)
     (normal numbers, random 10-bit mantissa, exponent field 1);
   * activations are f32 N(0, 1);
   * the canvas is 20 prompt ids uniform in [0, 126000) followed by the mask id.
+A second Q4_K recipe (q4k_blocks_centered) gives zero-centred weights for the commit-parity
+tests, where a multi-layer model must keep its masked positions apart.
 """
 from __future__ import annotations
 
@@ -115,6 +117,35 @@ def q4k_blocks(seed: int, n: int, k: int) -> np.ndarray:
     return blk.reshape(n, k // QK, Q4K_BYTES)
 
 
+def _f16_bits_in(seed: int, n: int, exp_field: int) -> np.ndarray:
+    """f16 bit patterns uniform over [2^(e-15), 2^(e-14)): exponent field e, random mantissa."""
+    mant = (u64_stream(seed, n) >> np.uint64(54)).astype(np.uint16)
+    return (np.uint16(exp_field << 10) | mant).astype(np.uint16)
+
+
+def q4k_blocks_centered(seed: int, n: int, k: int) -> np.ndarray:
+    """Random GGUF Q4_K matrix whose sub-blocks decode to values centred on zero, like trained
+    weights (the plain random bytes of q4k_blocks give every weight a positive mean, which drives
+    the residual stream of a multi-layer model towards one direction): quant bits uniform, the
+    6-bit scales uniform in [1, 8], each min = round(7.5 * scale) with dmin = d (so a weight is
+    about d * scale * (q - 7.5)), and d uniform in [2^-11, 2^-10) (normal f16)."""
+    assert k % QK == 0
+    nb = n * (k // QK)
+    blk = random_bytes(sub_seed(seed, "q4kc.bytes"), nb * Q4K_BYTES).reshape(nb, Q4K_BYTES)
+    sc = (u64_stream(sub_seed(seed, "q4kc.scales"), nb * 8) % np.uint64(8)).astype(np.int64).reshape(nb, 8) + 1
+    mn = np.floor(7.5 * sc + 0.5).astype(np.int64)
+    s = np.zeros((nb, 12), np.int64)
+    for j in range(4):  # the GGUF 12-byte packing of eight 6-bit scales and eight 6-bit mins
+        s[:, j] = (sc[:, j] & 63) | ((sc[:, j + 4] >> 4) << 6)
+        s[:, j + 4] = (mn[:, j] & 63) | ((mn[:, j + 4] >> 4) << 6)
+        s[:, j + 8] = (sc[:, j + 4] & 15) | ((mn[:, j + 4] & 15) << 4)
+    blk[:, 4:16] = s.astype(np.uint8)
+    d = _f16_bits_in(sub_seed(seed, "q4kc.d"), nb, 4)
+    blk[:, 0:2] = d.view(np.uint8).reshape(nb, 2)
+    blk[:, 2:4] = d.view(np.uint8).reshape(nb, 2)
+    return blk.reshape(n, k // QK, Q4K_BYTES)
+
+
 def q6k_blocks(seed: int, n: int, k: int) -> np.ndarray:
     """Random GGUF Q6_K matrix [n rows, k/256 blocks, 210 B] (row-major AoS)."""
     assert k % QK == 0
@@ -155,12 +186,15 @@ LAYER_MATS = (  # name, type, rows, cols
 )
 
 
-def layer_weights(seed: int, layer: int, dims: dict | None = None) -> dict:
-    """Raw GGUF blocks of one layer's seven projections plus f32 norm weights (= 1)."""
+def layer_weights(seed: int, layer: int, dims: dict | None = None, centered: bool = False) -> dict:
+    """Raw GGUF blocks of one layer's seven projections plus f32 norm weights (= 1). centered:
+    the Q4_K matrices come from q4k_blocks_centered (Q6_K values are centred already)."""
     dims = dict(LLADA if dims is None else dims)
     out = {}
     for name, t, r, c in LAYER_MATS:
-        out[name] = blocks(t, sub_seed(seed, f"L{layer}.{name}"), dims[r], dims[c])
+        sd = sub_seed(seed, f"L{layer}.{name}")
+        out[name] = q4k_blocks_centered(sd, dims[r], dims[c]) if centered and t == GGML_Q4_K else \
+            blocks(t, sd, dims[r], dims[c])
     out["attn_norm"] = np.ones(dims["d_model"], dtype=np.float32)
     out["ffn_norm"] = np.ones(dims["d_model"], dtype=np.float32)
     return out
@@ -174,6 +208,7 @@ def head_weights(seed: int, dims: dict | None = None) -> dict:
     }
 
 
-def embed_weights(seed: int, dims: dict | None = None) -> np.ndarray:
+def embed_weights(seed: int, dims: dict | None = None, centered: bool = False) -> np.ndarray:
     dims = dict(LLADA if dims is None else dims)
-    return q4k_blocks(sub_seed(seed, "token_embd"), dims["vocab"], dims["d_model"])
+    gen = q4k_blocks_centered if centered else q4k_blocks
+    return gen(sub_seed(seed, "token_embd"), dims["vocab"], dims["d_model"])

@@ -235,33 +235,53 @@ def test_dual_cache_llada_shapes_two_layers():
 
 # ---- config-4 commit parity: level (i), level (ii) on the GPU's own hidden rows, and end to end --
 
-def commit_parity(dims, lws, table, head, canvas, b0, b1, k, label):
+def _decided(conf_rows, k, bound):
+    """Whether the top-k SET of positions is decided by these confidences when each may move by
+    `bound`: the k-th and (k+1)-th largest must differ by more than 2 * bound."""
+    c = np.sort(np.asarray(conf_rows, np.float64))[::-1]
+    margin = float(c[k - 1] - c[k]) if c.size > k else float("inf")
+    return margin, margin > 2.0 * bound + 1e-7
+
+
+def _same_commits(gpos, gid, pos, ids):
+    """Same committed positions with the same ids (the canvas update); the selection order of
+    near-equal confidences is not compared."""
+    n = len(pos)
+    a = dict(zip(np.asarray(gpos)[:n].tolist(), np.asarray(gid)[:n].tolist()))
+    return a == dict(zip(np.asarray(pos).tolist(), np.asarray(ids).tolist()))
+
+
+def commit_parity(dims, lws, table, head, canvas, b0, b1, k, label, model=None):
     """One denoising step on the GPU against the oracle, at three levels (Technical Specification,
     section 19, "Level 2 - diffusion-step parity": mask positions, confidences, selected
     positions, sampled ids and the updated canvas):
       (i)   the GPU's commit logic against the oracle's on the GPU's own row confidences and ids:
-            bit-exact;
+            bit-exact, order included;
       (ii)  the GPU head + commit against the oracle's head + commit on the GPU's own final hidden
-            rows: ids and commits bit-exact (the head's f32 logits agree to ~1e-6 of the oracle's);
-      (iii) the GPU step against the oracle's whole f64 forward: the commits must be identical
-            whenever the oracle's k-th / (k+1)-th confidence gap exceeds twice the largest
-            confidence shift that the measured hidden-state error causes (the oracle head on the
-            GPU's rows against on its own); below that margin the rankings are not decidable
-            in f32 and the step is reported, not failed.
-    Returns a dict with the margin, the bound and whether (iii) was decidable and exact."""
+            rows: the committed positions and ids (and so the canvas) must be identical whenever
+            the oracle's k-th / (k+1)-th confidence margin exceeds twice the largest difference
+            between the GPU's and the oracle's row confidences (~1e-6; a row whose Q8_K
+            re-quantization lands on a rounding tie moves by ~1e-4);
+      (iii) the GPU step against the oracle's whole f64 forward: asserted the same way, with the
+            bound the confidence shift that the measured hidden-state error causes (the oracle's
+            head on the GPU's rows against on its own rows); below that margin the step is not
+            decidable in f32 and is reported, not failed.
+    Returns the margins, bounds and outcomes."""
     L = canvas.size
-    model = dl.DeviceModel(dims, lws, table, head)
+    if model is None:
+        model = dl.DeviceModel(dims, lws, table, head)
     gcanvas = torch.from_numpy(canvas.copy()).cuda()
     hid = torch.empty((L, dims["d_model"]), device="cuda")
     out = dl.denoise_step(model, gcanvas, b0, b1, k, hidden_out=hid)
     dl.check()
     gpos, gid = out["pos"].cpu().numpy(), out["id"].cpu().numpy()
+    gcv = gcanvas.cpu().numpy()
     gh = hid.cpu().numpy()
     on = head["out_norm"]
     mask = dims["mask_id"]
     # (i) the GPU's row confidences and ids through the oracle's commit logic
     cv = torch.from_numpy(canvas.copy()).cuda()
-    r = dl.lmhead_select(hid, cv, mask, b0, b1, k, torch.from_numpy(on).cuda(), model._keep[-1], dims["vocab"])
+    r = dl.lmhead_select(hid, cv, mask, b0, b1, k, model.out_norm, model.w_out_packed, dims["vocab"])
     dl.check()
     rconf = np.full(L, -np.inf)
     rid = np.zeros(L, np.int32)
@@ -271,45 +291,74 @@ def commit_parity(dims, lws, table, head, canvas, b0, b1, k, label):
     pos_i, id_i = orc.commit_topk(c_i, mask, b0, b1, rconf, rid, k)
     np.testing.assert_array_equal(gpos[:pos_i.size], pos_i, err_msg=f"{label}: level (i) positions")
     np.testing.assert_array_equal(gid[:pos_i.size], id_i, err_msg=f"{label}: level (i) ids")
-    np.testing.assert_array_equal(gcanvas.cpu().numpy(), c_i, err_msg=f"{label}: level (i) canvas")
-    # (ii) the oracle's head and commit on the GPU's final hidden rows: the GPU head's confidences
-    # agree to ~1e-4 (a row's Q8_K re-quantization can land on a rounding tie), so the commits
-    # must be identical whenever the oracle's k-th / (k+1)-th margin exceeds twice that shift
+    np.testing.assert_array_equal(gcv, c_i, err_msg=f"{label}: level (i) canvas")
+    # (ii) the oracle's head and commit on the GPU's final hidden rows
     c_ii = canvas.copy()
     ref_ii = orc.lmhead_commit(np.asarray(gh, np.float64), c_ii, mask, b0, b1, k, on, head["w_out"], dims["eps"])
     rows = ref_ii["rows"]
     shift_ii = float(np.max(np.abs(rconf[rows] - ref_ii["conf_rows"]))) if rows.size else 0.0
-    cs = np.sort(ref_ii["conf_rows"])[::-1]
-    margin_ii = float(cs[k - 1] - cs[k]) if cs.size > k else float("inf")
-    n_ii = ref_ii["pos"].size
-    exact_ii = bool(np.array_equal(gpos[:n_ii], ref_ii["pos"]) and np.array_equal(gid[:n_ii], ref_ii["id"]))
-    if margin_ii > 2.0 * shift_ii + 1e-6:
-        assert exact_ii, f"{label}: level (ii) commits differ: GPU {gpos[:n_ii]} {gid[:n_ii]}, oracle {ref_ii['pos']} {ref_ii['id']}"
-        np.testing.assert_array_equal(gcanvas.cpu().numpy(), c_ii, err_msg=f"{label}: level (ii) canvas")
-    ids_ok = rid[rows] == ref_ii["ids_rows"]
-    gap_ii = (ref_ii["top1"] - ref_ii["top2"])[~ids_ok]
-    assert np.all(gap_ii < 1e-2), f"{label}: row ids differ with top-1/top-2 logit gaps {gap_ii}"
+    margin_ii, dec_ii = _decided(ref_ii["conf_rows"], k, shift_ii)
+    same_ii = _same_commits(gpos, gid, ref_ii["pos"], ref_ii["id"])
+    if dec_ii:
+        assert same_ii, f"{label}: level (ii) commits differ: GPU {gpos} {gid}, oracle {ref_ii['pos']} {ref_ii['id']}"
+        np.testing.assert_array_equal(gcv, c_ii, err_msg=f"{label}: level (ii) canvas")
     # (iii) the oracle's own forward
     x = orc.embed(table, canvas)
     for lw in lws:
         x, _ = orc.layer(lw, x, dims, attention_on=True)
     c_iii = canvas.copy()
     ref = orc.lmhead_commit(x, c_iii, mask, b0, b1, k, on, head["w_out"], dims["eps"])
-    conf_ref = np.sort(ref["conf_rows"])[::-1]
     shift = float(np.max(np.abs(ref["conf_rows"] - ref_ii["conf_rows"]))) if ref["rows"].size else 0.0
-    n = ref["pos"].size
-    margin = float(conf_ref[k - 1] - conf_ref[k]) if conf_ref.size > k else float("inf")
-    decidable = margin > 2.0 * shift + 1e-6
-    exact = bool(np.array_equal(gpos[:n], ref["pos"]) and np.array_equal(gid[:n], ref["id"]))
+    margin, dec = _decided(ref["conf_rows"], k, shift)
+    same = _same_commits(gpos, gid, ref["pos"], ref["id"])
     errs = _row_errs(gh, x)
-    print(f"\n  {label}: level (ii) margin {margin_ii:.3e} shift {shift_ii:.3e} commits "
-          f"{'identical' if exact_ii else 'differ'}; level (iii): hidden max row error {errs.max():.2e}; oracle "
-          f"k-th/(k+1)-th confidence margin "
-          f"{margin:.3e}, confidence shift from the hidden error {shift:.3e}; "
-          f"{'decidable' if decidable else 'NOT decidable'}; commits {'identical' if exact else 'differ'} "
-          f"(GPU {gpos[:n].tolist()} oracle {ref['pos'].tolist()})")
-    if decidable:
-        assert exact, f"{label}: decidable step with different commits: GPU {gpos[:n]} {gid[:n]}, oracle {ref['pos']} {ref['id']}"
-    return dict(margin=margin, shift=shift, decidable=decidable, exact=exact, max_row_err=float(errs.max()),
-                margin_ii=margin_ii, shift_ii=shift_ii, exact_ii=exact_ii, canvas=gcanvas.cpu().numpy(),
+    print(f"\n  {label}: (ii) margin {margin_ii:.2e} bound {shift_ii:.2e} {'same' if same_ii else 'DIFFERENT'}; "
+          f"(iii) hidden max row error {errs.max():.2e}, margin {margin:.2e} bound {shift:.2e} "
+          f"{'decidable' if dec else 'not decidable'}, {'same' if same else 'different'} commits "
+          f"(GPU {gpos.tolist()} oracle {ref['pos'].tolist()})")
+    if dec:
+        assert same, f"{label}: decidable step with different commits: GPU {gpos} {gid}, oracle {ref['pos']} {ref['id']}"
+    return dict(margin=margin, shift=shift, decidable=dec, same=same, max_row_err=float(errs.max()),
+                margin_ii=margin_ii, shift_ii=shift_ii, decidable_ii=dec_ii, same_ii=same_ii, canvas=gcv,
                 oracle_canvas=c_iii)
+
+
+def _centered_model(dims, seed):
+    """LLaDA-shaped weights with zero-centred Q4_K blocks (synth.q4k_blocks_centered): a model
+    whose masked positions stay apart through the layers, so that the commit rankings are
+    decided well above the head's f32 error (the plain random recipe drives every row towards
+    one direction and leaves the masked rows' confidences equal to 4-6 digits)."""
+    lws = [synth.layer_weights(seed, i, dims, centered=True) for i in range(dims["n_layers"])]
+    table = synth.embed_weights(seed, dims, centered=True)
+    head = synth.head_weights(seed, dims)
+    return lws, table, head
+
+
+def _chain(dims, seed, n_steps, min_decidable_ii):
+    """The protocol's schedule (dllm_schedule(20, 128, 32, 32)) for n_steps steps; each GPU step
+    starts from the oracle's canvas and is checked with commit_parity."""
+    lws, table, head = _centered_model(dims, seed)
+    model = dl.DeviceModel(dims, lws, table, head)
+    sched = dl.schedule(20, 128, 32, 32)[:n_steps]
+    canvas = synth.canvas(seed)
+    results = []
+    for st, (b0, b1, k) in enumerate(sched):
+        r = commit_parity(dims, lws, table, head, canvas, b0, b1, k, f"step {st} block [{b0}, {b1})", model=model)
+        results.append(r)
+        canvas = r["oracle_canvas"]
+    n_ii = sum(r["decidable_ii"] for r in results)
+    n_iii = sum(r["decidable"] for r in results)
+    print(f"\n  level (ii): {n_ii}/{len(results)} steps decidable, all of them identical; level (iii): "
+          f"{n_iii}/{len(results)} decidable, {sum(r['same'] for r in results)}/{len(results)} identical")
+    assert n_ii >= min_decidable_ii, [(r["margin_ii"], r["shift_ii"]) for r in results]
+    return results
+
+
+def test_commit_parity_llada_two_layers_first_block():
+    # LLaDA-8B shapes at two layers, the first block's 8 steps (4 commits each)
+    _chain(dict(synth.LLADA, n_layers=2), synth.config_seed(4) + 21, 8, min_decidable_ii=7)
+
+
+def test_commit_parity_llada_full_depth():
+    # the full 32-layer LLaDA-8B-shaped step, the protocol's first two steps
+    _chain(dict(synth.LLADA), synth.config_seed(4) + 22, 2, min_decidable_ii=2)
