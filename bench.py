@@ -315,6 +315,9 @@ def run_ours(args, rank, local_rank, world):
     bytes_step = dims["n_layers"] * ((4 * d * d + 2 * d * f) // 256 * 144 + (d * d + d * f) // 256 * 210) + \
         dims["vocab"] * d // 256 * 210
     t_roof_ms = max(ops_step / (peak * 1e12), bytes_step / (peaks["hbm_gbs"] * 1e9)) * 1e3
+    # the second roofline: the legacy int8 tensor path's dense rate (mma.sync m16n8k32), measured
+    i8_tops = dl.peak_mma_i8_tops(stream=stream)
+    t_roof_i8_ms = max(ops_step / (i8_tops * 1e12), bytes_step / (peaks["hbm_gbs"] * 1e9)) * 1e3
 
     line = {
         "metric": METRIC, "value": value, "unit": "ms/step", "n_gpus": world, "steps": args.steps,
@@ -329,6 +332,9 @@ def run_ours(args, rank, local_rank, world):
                    "arith": "Q8_K x Q4_K/Q6_K integer sums exact in f16 tcgen05 MMA, f32 accumulate/epilogue"},
         "tok_per_s": (sum(k for _, _, k in sched) / len(sched)) * world / (value * 1e-3),
         "step_roofline_ms": t_roof_ms, "step_roofline_frac": t_roof_ms / ms_per_step,
+        "roofline_int8_mma_sync": {"peak_tops": i8_tops, "source": "measured in this run (dllm_peak_mma_i8)",
+                                   "step_roofline_ms": t_roof_i8_ms, "step_frac": t_roof_i8_ms / ms_per_step,
+                                   "gate_up_frac": achieved / i8_tops},
         "algorithmic_tops": ops_step / (ms_per_step * 1e-3) / 1e12,
         "gpu_launches": int(graphs.launches_per_step[0]) * args.steps,
         "roofline": {"kernel": "qgemm_kernel<Q4_K, NT=160> (gate|up 148x24576x4096)", "bound": "tensor",

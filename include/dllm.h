@@ -374,6 +374,13 @@ DLLM_API size_t dllm_qgemm_partials_bytes(int type, int64_t m, int64_t n, int64_
 DLLM_API int dllm_qgemm_partials(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
                                  float* partials, size_t partials_bytes, int32_t* splits, dllm_stream_t stream);
 
+/* dllm_peak_mma_i8: measures the legacy int8 tensor path's dense rate (mma.sync m16n8k32,
+ *   s8 x s8 -> s32, eight independent chains per warp, four 8-warp CTAs per SM) for the
+ *   benchmark's second roofline: one launch of `iters` iterations; *ops_per_launch (host, may be
+ *   NULL) receives the launch's algorithmic ops (2 * 16 * 8 * 32 per mma). sink: device int32,
+ *   written only in a case that does not happen in practice. Time it with events on `stream`. */
+DLLM_API int dllm_peak_mma_i8(int64_t iters, int32_t* sink, double* ops_per_launch, dllm_stream_t stream);
+
 /* ---- allocation-free GEMM (the pages have no counterpart to this entry point) ----------------
  * For callers that cannot allocate device memory or hand over a workspace at call time (an
  * inference server that reserves all device memory at start-up, a plugin interface that

@@ -68,6 +68,7 @@ _SIGS = {
     "dllm_qgemm_partials": ([INT, P, I64, I64, P, I64, P, SZ, P, P], INT),
     "dllm_qgemm_noalloc": ([INT, P, I64, I64, P, I64, P, I64, INT, P], INT),
     "dllm_step_taps": ([P, P, I64, P, INT, P, P, SZ, P], INT),
+    "dllm_peak_mma_i8": ([I64, P, P, P], INT),
     "dllm_transfer_counts": ([I64, I64, P], INT),
     "dllm_schedule": ([I64, I64, I64, I64, P, P, P], INT),
 }
@@ -238,6 +239,23 @@ def qgemm_partials(type_id: int, act: torch.Tensor, m: int, k: int, w_packed: to
     _ok(lib().dllm_qgemm_partials(type_id, _ptr(act), m, k, _ptr(w_packed), n, _ptr(partials), partials.numel() * 4,
                                   C.byref(sp), _stream(stream)))
     return partials, sp.value
+
+
+def peak_mma_i8_tops(iters: int = 20000, reps: int = 3, stream=None) -> float:
+    """Measured dense rate of mma.sync int8 (m16n8k32) on this GPU, TOPS (best of reps)."""
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops = C.c_double(0.0)
+    s = torch.cuda.current_stream() if stream is None else stream
+    _ok(lib().dllm_peak_mma_i8(100, _ptr(sink), None, _stream(s)))  # warm-up
+    best = 0.0
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        _ok(lib().dllm_peak_mma_i8(iters, _ptr(sink), C.byref(ops), _stream(s)))
+        e1.record(s)
+        s.synchronize()
+        best = max(best, ops.value / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+    return best
 
 
 def selftest_timeout(limit_cycles: int, stream=None):

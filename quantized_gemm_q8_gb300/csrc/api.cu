@@ -35,11 +35,6 @@ static thread_local char g_msg[1024] = "";
 static std::atomic<long long> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
-#ifdef DLLM_TRACE
-// Trace builds only: device buffer of 8 x 256 clock64 stamps written by CTA 0 of each GEMM.
-static unsigned long long* g_trace = nullptr;
-extern "C" DLLM_API void dllm_trace_set(unsigned long long* buf) { g_trace = buf; }
-#endif
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -737,9 +732,6 @@ int launch_gemm(const GemmLaunch& g, const QgemmPlan& P, cudaStream_t stream) {
   prm.timeout = kDefaultTimeoutCycles;
   prm.err = err_word();
   if (!prm.err) return fail(DLLM_E_CUDA, "cannot resolve the device error word");
-#ifdef DLLM_TRACE
-  prm.trace = g_trace;
-#endif
   return g.type == DLLM_Q4_K ? launch_qgemm_q4k(P.nt, map, prm, P.grid, stream)
                              : launch_qgemm_q6k(P.nt, map, prm, P.grid, stream);
 }

@@ -511,7 +511,8 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
 // (blockIdx.y * 8 + w) of row blockIdx.x handles super-block sb (dims 256 sb .. = two heads);
 // lane's 8 dims belong to head 2 sb + lane / 16. O = sum_c e^(m_c - M) a_c / sum_c e^(m_c - M) l_c.
 __global__ void __launch_bounds__(256) attn_merge_quant_kernel(AttPart part, int nchunk, int L, int d, int heads,
-                                                               QuantOut o) {
+                                                               QuantOut o, WPrefetch pf) {
+  if (threadIdx.x == 0 && blockIdx.y == 0) prefetch_weights(pf);
   griddep_wait();
   griddep_launch();
   const int row = blockIdx.x;
@@ -559,6 +560,7 @@ struct RowArgs {
   float eps;
   int rows, k;
   QuantOut o;
+  WPrefetch pf0, pf1;  // the next GEMMs' first weights, prefetched into L2 (optional)
 };
 
 // Residual modes (RESID_NORM_QUANT, RESID_ONLY): one CTA per row, warp w holding super-blocks
@@ -569,6 +571,10 @@ constexpr int RR_WARPS = 16, RR_J = 4;  // rows of up to RR_WARPS * RR_J * 256 =
 template <int MODE>
 __global__ void __launch_bounds__(RR_WARPS * 32) row_resid_kernel(RowArgs a) {
   __shared__ float red[RR_WARPS];
+  if (threadIdx.x == 0) {
+    prefetch_weights(a.pf0);
+    prefetch_weights(a.pf1);
+  }
   griddep_wait();
   griddep_launch();
   const int row = blockIdx.x;
@@ -634,6 +640,10 @@ __global__ void __launch_bounds__(RR_WARPS * 32) row_resid_kernel(RowArgs a) {
 // builds and quantizes one super-block; each lane's partial loads are issued together.
 template <int MODE>
 __global__ void __launch_bounds__(256) row_sb_kernel(RowArgs a) {
+  if (threadIdx.x == 0 && blockIdx.y == 0) {
+    prefetch_weights(a.pf0);
+    prefetch_weights(a.pf1);
+  }
   griddep_wait();
   griddep_launch();
   const int row = blockIdx.x;
@@ -673,10 +683,25 @@ static QuantOut quant_out(void* act, int64_t rows, int64_t k, float* vtap = null
                   reinterpret_cast<float*>(base + L.off_d), (int)L.lpad, vtap};
 }
 
+// The first-wave weights of a GEMM launch with plan P (see WPrefetch): as many super-blocks per
+// unit as the kernel's weight ring holds (3 Q4_K, 6 Q6_K), at most the unit's own.
+static WPrefetch wprefetch(int type, const void* w, const QgemmPlan& P) {
+  WPrefetch f{};
+  f.wblob = static_cast<const uint8_t*>(w);
+  f.tiles_n = P.tiles_n;
+  f.tiles_m = P.tiles_m;
+  f.nsb = P.nsb;
+  f.sbps = P.sbps;
+  f.units = std::min(P.units, P.grid);
+  f.w_bytes = type == DLLM_Q4_K ? Q4K_BLOB : Q6K_BLOB;
+  f.ahead = std::min(P.sbps, type == DLLM_Q4_K ? 3 : 6);
+  return f;
+}
+
 template <int MODE>
 static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, const float* w, float eps, int rows,
-                   int k, void* act, cudaStream_t s, float* vtap = nullptr) {
-  RowArgs a{x, P, S, pstride, ldp, w, eps, rows, k, act ? quant_out(act, rows, k, vtap) : QuantOut{}};
+                   int k, void* act, cudaStream_t s, float* vtap = nullptr, WPrefetch pf0 = {}, WPrefetch pf1 = {}) {
+  RowArgs a{x, P, S, pstride, ldp, w, eps, rows, k, act ? quant_out(act, rows, k, vtap) : QuantOut{}, pf0, pf1};
   cudaError_t e;
   if (MODE == ROW_RESID_NORM_QUANT || MODE == ROW_RESID_ONLY) {
     const int grid = MODE == ROW_RESID_ONLY ? rows : (int)act_rows_padded(rows);
@@ -866,31 +891,34 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
       const dim3 mg((unsigned)act_rows_padded(L), (unsigned)((d / QK + 7) / 8));
       if (e == cudaSuccess)
         e = launch_pdl(attn_merge_quant_kernel, mg, dim3(256), 0, s, ap, nchunk, (int)L, d, m->n_heads,
-                       quant_out(actd, L, d, tp ? tp->attn : nullptr));
+                       quant_out(actd, L, d, tp ? tp->attn : nullptr), wprefetch(DLLM_Q4_K, Ly.wo, S.o));
       note_launch();
       if (e == cudaSuccess) e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "launch attention");
     } else {
       // linear stream: the O projection consumes the V projection's output
       if ((rc = run_row<ROW_SUM_QUANT>(nullptr, Pv, S.v.splits, L * d, d, nullptr, 0.f, (int)L, d, actd, s,
-                                       tp ? tp->attn : nullptr)))
+                                       tp ? tp->attn : nullptr, wprefetch(DLLM_Q4_K, Ly.wo, S.o))))
         return rc;
     }
     if (tp && (rc = tap_copy(tp->act_o, actd, act_d_bytes, s))) return rc;
     if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wo, d, Po, S.o, s))) return rc;
-    if ((rc = run_row<ROW_RESID_NORM_QUANT>(x, Po, S.o.splits, L * d, d, Ly.ffn_norm, m->eps, (int)L, d, actd, s)))
+    if ((rc = run_row<ROW_RESID_NORM_QUANT>(x, Po, S.o.splits, L * d, d, Ly.ffn_norm, m->eps, (int)L, d, actd, s,
+                                            nullptr, wprefetch(DLLM_Q4_K, Ly.wgu, S.gu))))
       return rc;
     if (tp && (rc = tap_copy(tp->x_mid, x, (size_t)L * d * 4, s))) return rc;
     if (tp && (rc = tap_copy(tp->act_ffn, actd, act_d_bytes, s))) return rc;
     if ((rc = gemm(DLLM_Q4_K, actd, L, d, Ly.wgu, 2 * f, Pgu, S.gu, s))) return rc;
     if ((rc = run_row<ROW_SWIGLU_QUANT>(nullptr, Pgu, S.gu.splits, L * 2 * f, 2 * f, nullptr, 0.f, (int)L, f, actf,
-                                        s, tp ? tp->h : nullptr)))
+                                        s, tp ? tp->h : nullptr, wprefetch(DLLM_Q6_K, Ly.wdown, S.dn))))
       return rc;
     if (tp && (rc = tap_copy(tp->act_down, actf, act_f_bytes, s))) return rc;
     if ((rc = gemm(DLLM_Q6_K, actf, L, f, Ly.wdown, d, Pdn, S.dn, s))) return rc;
     if (li + 1 < m->n_layers) {
-      if ((rc = run_row<ROW_RESID_NORM_QUANT>(x, Pdn, S.dn.splits, L * d, d, m->layers[li + 1].attn_norm, m->eps,
-                                              (int)L, d, actd, s)))
+      const dllm_layer& Ln = m->layers[li + 1];
+      if ((rc = run_row<ROW_RESID_NORM_QUANT>(x, Pdn, S.dn.splits, L * d, d, Ln.attn_norm, m->eps, (int)L, d, actd,
+                                              s, nullptr, wprefetch(DLLM_Q4_K, Ln.wqk, S.qk),
+                                              wprefetch(DLLM_Q6_K, Ln.wv, S.v))))
         return rc;
     } else {
       if ((rc = run_row<ROW_RESID_ONLY>(x, Pdn, S.dn.splits, L * d, d, nullptr, 0.f, (int)L, d, nullptr, s)))
@@ -953,7 +981,7 @@ static int forward_block(const dllm_model* m, const int32_t* canvas, int64_t L, 
     const dim3 mg((unsigned)act_rows_padded(R), (unsigned)((d / QK + 7) / 8));
     if (e == cudaSuccess)
       e = launch_pdl(attn_merge_quant_kernel, mg, dim3(256), 0, s, ap, nchunk, (int)R, d, m->n_heads,
-                     quant_out(actd, R, d));
+                     quant_out(actd, R, d), wprefetch(DLLM_Q4_K, Ly.wo, S.o));
     note_launch();
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch attention");

@@ -105,6 +105,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// Asynchronous prefetch of a global range into L2 (a hint: no completion, no data returned);
+// src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 // 16-byte asynchronous copy global -> shared (no register staging; many may be in flight),
 // and the wait for all of this thread's outstanding ones.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {

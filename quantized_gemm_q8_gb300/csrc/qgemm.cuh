@@ -172,22 +172,9 @@ struct QgemmParams {
   float* pscore;
   int* pidx;
   float* plogit;
-#ifdef DLLM_TRACE
-  unsigned long long* trace;  // per-role clock64 stamps of CTA 0 (trace builds only)
-#endif
   long long timeout;
 };
 
-#ifdef DLLM_TRACE
-#define QTRACE(cond, slot, idx)                                                             \
-  do {                                                                                      \
-    if ((cond) && blockIdx.x == 0 && (idx) < 256 && p.trace) p.trace[(slot) * 256 + (idx)] = clock64(); \
-  } while (0)
-#else
-#define QTRACE(cond, slot, idx) \
-  do {                          \
-  } while (0)
-#endif
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
@@ -326,6 +313,25 @@ __device__ __forceinline__ float gumbel_noise(unsigned long long seed, unsigned 
   return -logf(-logf(u));
 }
 
+// The first super-blocks that each CTA of a GEMM launch streams from HBM: the kernel that runs
+// before the GEMM prefetches them into L2 (its data lives in L2, so HBM is otherwise idle then),
+// and the GEMM's first weight copies hit L2 instead of waiting for HBM. wblob = nullptr: none.
+struct WPrefetch {
+  const uint8_t* wblob;
+  int tiles_n, tiles_m, nsb, sbps, units, w_bytes, ahead;
+};
+// One thread per CTA of the prefetching kernel: units blockIdx.x, blockIdx.x + gridDim.x, ...
+// of the GEMM's first wave (units < f.units), `ahead` super-blocks each (contiguous in the
+// tile's blob run).
+__device__ __forceinline__ void prefetch_weights(const WPrefetch& f) {
+  if (f.wblob == nullptr) return;
+  for (int u = blockIdx.x; u < f.units; u += gridDim.x) {
+    const int tn = u % f.tiles_n, sp = (u / f.tiles_n) / f.tiles_m;
+    const int sb0 = sp * f.sbps, n = min(f.ahead, f.nsb - sb0);
+    if (n > 0) bulk_prefetch_l2(f.wblob + ((size_t)tn * f.nsb + sb0) * f.w_bytes, (uint32_t)(n * f.w_bytes));
+  }
+}
+
 __device__ __forceinline__ void unit_coords(const QgemmParams& p, int u, int& tn, int& tm, int& sp, int& sb0,
                                             int& sb1) {
   tn = u % p.tiles_n;
@@ -409,7 +415,6 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           mbar_expect_tx(BAR(C::BW_FULL + w), C::W_SLOT);
           bulk_g2s(ws, blob + (size_t)sb * C::W_BYTES, C::W_BYTES, BAR(C::BW_FULL + w));
           if (C::Q4) bulk_g2s(ws + C::W_BYTES, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES, BAR(C::BW_FULL + w));
-          QTRACE(true, 1, it);
         }
       }
       if (!ok) {
@@ -453,7 +458,6 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             for (int qq = 0; qq < C::QPS; ++qq)
               tma_g2s_3d(sbase + C::OFF_B + b * C::B_STAGE + qq * C::B_QUARTER, &tmap, 0, tok0,
                          sb * 4 + st * C::QPS + qq, BAR(C::BK_FULL + b));
-            QTRACE(true, 0, j);
           }
           if (!ok) break;
         }
@@ -495,7 +499,6 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             for (int st = 0; st < 2; ++st) {
               const int j = 2 * it + st, b = j % C::K_STAGES;
               if (!(ok = wait_tc(BAR(C::BK_FULL + b), (j / C::K_STAGES) & 1))) break;
-              QTRACE(true, 2, j);
               const uint32_t acol = tmem + C::ACOL + b * C::ASTG;
               const uint64_t bdesc = desc_sw128(sbase + C::OFF_B + b * C::B_STAGE);
 #pragma unroll
@@ -515,12 +518,10 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             mma_f16(dslot, desc_noswz(js + C::J_AJ, 128, 256), bj, IDESC, 1);
             mma_f16(dslot, desc_noswz(js + C::J_AJ + 4096, 128, 256), bj, IDESC, 1);
             mma_commit(BAR(C::BJ_EMPTY + jx));
-            QTRACE(true, 3, it);
           } else {
             for (int q = 0; q < 4; ++q) {
               const int j = 4 * it + q, b = j % C::K_STAGES;
               if (!(ok = wait_tc(BAR(C::BK_FULL + b), (j / C::K_STAGES) & 1))) break;
-              QTRACE(true, 2, j);
               const uint32_t acol = tmem + C::ACOL + b * C::ASTG;
               const uint64_t bdesc = desc_sw128(sbase + C::OFF_B + b * C::B_STAGE);
 #pragma unroll
@@ -557,7 +558,6 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
       for (int sb = sb0; sb < sb1; ++sb, ++it) {
         const int w = it % C::W_STAGES;
         if (!(ok = warp_wait(BAR(C::BW_FULL + w), (it / C::W_STAGES) & 1, abort_flag, lim, QG_SUSPEND))) break;
-        QTRACE(t == 0 && g == 0, 8, it);
         const uint8_t* W = smem + C::OFF_W + w * C::W_SLOT;
         if constexpr (C::Q4) {
           // row t's fold of this super-block (see q4k_fold): the A operand carries scale * q * 2^-k
@@ -575,7 +575,6 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
                                 : (sw0 & 0x3F3F3F3Fu);
           const int j = 2 * it + g, b = j % C::K_STAGES;
           if (!(ok = warp_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
-          QTRACE(t == 0, 4, j);
           tc_fence_after();
           const uint32_t ta = tlane + b * C::ASTG;
           // f16 multipliers (scale * 2^-k / 16) and addends (-72 scale * 2^-k): exact, from one
@@ -622,16 +621,13 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             *reinterpret_cast<uint4*>(row + 4096) = make_uint4(tl[0], tl[1], tl[2], tl[3]);
             fence_proxy_async();
           }
-          QTRACE(t == 0, 10, j);
           tmem_st_wait();
-          QTRACE(t == 0, 11, j);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(BAR(C::BK_FULL + b));
             mbar_arrive(BAR(C::BJ_FULL + it % C::J_STAGES));
           }
-          QTRACE(t == 0, 5, j);
         } else {
           const uint4 scv = *reinterpret_cast<const uint4*>(W + 24576 + t * 16);
           const int8_t* sc = reinterpret_cast<const int8_t*>(&scv);
@@ -641,7 +637,6 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           for (int q = g; q < 4; q += 2) {
             const int j = 4 * it + q, b = j % C::K_STAGES;
             if (!(ok = warp_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
-            QTRACE(t == 0, 4, j);
             tc_fence_after();
 #pragma unroll
             for (int h = 0; h < 2; ++h)
@@ -656,7 +651,6 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(C::BK_FULL + b));
-            QTRACE(t == 0, 5, j);
           }
         }
         if (!ok) break;
@@ -707,7 +701,6 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         const uint32_t n = s ? sf1++ : sf0++;
         if (!(ok = warp_wait(BAR(C::BS_FULL + s), n & 1, abort_flag, lim, QG_SUSPEND))) break;
         tc_fence_after();
-        QTRACE(warp == 0 && lane == 0, 6, itp);
         // drain in groups of up to 2 x 8 columns; the slot is freed as soon as the last group
         // is in registers, before its arithmetic
         constexpr int G = 2;
@@ -722,7 +715,6 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(BAR(C::BS_EMPTY + s));
-            QTRACE(warp == 0 && lane == 0, 7, itp);
           }
 #pragma unroll
           for (int c = 0; c < G; ++c) {

@@ -331,3 +331,10 @@ def test_device_timeout_is_reported_and_context_survives():
     assert e.value.code == dl.E_TIMEOUT and "selftest" in str(e.value)
     dl.check()  # the error word was cleared
     _gemm_check(dl.Q4_K, 16, 128, 256, 4242)  # the context still runs kernels
+
+
+def test_peak_mma_i8_runs():
+    # the benchmark's second roofline: a short measurement of mma.sync int8 gives a finite rate
+    tops = dl.peak_mma_i8_tops(iters=2000, reps=1)
+    dl.check()
+    assert 1.0 < tops < 1e5, tops
