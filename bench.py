@@ -110,14 +110,22 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(hi), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def gemm_source_sha1() -> str:
+    """sha1 of the GEMM kernel's sources (the kernel and the PTX wrappers it is built from)."""
+    h = hashlib.sha1()
+    for name in ("qgemm.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "quantized_gemm_q8_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _traffic_for(kernel_file: str):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current source."""
     path = os.path.join(ROOT, "profiles", kernel_file)
     try:
         with open(path) as f:
             rec = json.load(f)
-        src = open(os.path.join(ROOT, "quantized_gemm_q8_gb300", "csrc", "qgemm.cuh"), "rb").read()
-        if rec.get("qgemm_cuh_sha1") == hashlib.sha1(src).hexdigest():
+        if rec.get("gemm_src_sha1") == gemm_source_sha1():
             return rec.get("dram_bytes_per_launch")
     except Exception:
         pass

@@ -594,6 +594,7 @@ DLLM_API size_t dllm_packed_bytes(int type, int64_t n, int64_t k) {
 
 DLLM_API int dllm_pack_weights(int type, const void* blocks, int64_t n, int64_t k, void* packed,
                                size_t packed_bytes, dllm_stream_t stream) {
+  DLLM_RANGE();
   if (!block_bytes(type))
     return fail(DLLM_E_TYPE, "dllm_pack_weights: unsupported block type %d: matrix kernels exist for Q4_K (12) and Q6_K (14)",
                 type);
@@ -636,6 +637,7 @@ DLLM_API size_t dllm_act_bytes(int64_t rows, int64_t k) {
 DLLM_API int dllm_quantize_act(const float* x, int64_t rows, int64_t k, int64_t ldx, const float* norm_w, float eps,
                                int8_t* q, float* d, int16_t* bsum, void* act, size_t act_bytes,
                                dllm_stream_t stream) {
+  DLLM_RANGE();
   if (rows <= 0 || rows > 65536 || k <= 0 || k % QK || k > (1 << 20) || ldx < k)
     return fail(DLLM_E_SHAPE, "dllm_quantize_act: bad shape rows=%lld k=%lld ldx=%lld (k %% 256 == 0, ldx >= k)",
                 (long long)rows, (long long)k, (long long)ldx);
@@ -808,6 +810,7 @@ extern "C" {
 
 DLLM_API int dllm_qgemm(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n, float* y,
                         int64_t ldy, int accumulate, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  DLLM_RANGE();
   if (!y) return fail(DLLM_E_INVAL, "dllm_qgemm: y is NULL");
   return qgemm_common("dllm_qgemm", type, act, m, k, w_packed, n, y, ldy, accumulate, ws, ws_bytes, nullptr,
                       (cudaStream_t)stream);
@@ -815,6 +818,7 @@ DLLM_API int dllm_qgemm(int type, const void* act, int64_t m, int64_t k, const v
 
 DLLM_API int dllm_pack_act(const int8_t* q, const float* d, const int16_t* bsum, int64_t rows, int64_t k, void* act,
                            size_t act_bytes, dllm_stream_t stream) {
+  DLLM_RANGE();
   if (rows <= 0 || rows > 65536 || k <= 0 || k % QK || k > (1 << 20))
     return fail(DLLM_E_SHAPE, "dllm_pack_act: bad shape rows=%lld k=%lld (k must be a positive multiple of 256)",
                 (long long)rows, (long long)k);
@@ -879,6 +883,7 @@ extern "C" {
 DLLM_API int dllm_qgemm_q4k(const int8_t* q, const float* d, const int16_t* bsum, int64_t m, int64_t k,
                             const void* w_packed, int64_t n, float* y, int64_t ldy, int accumulate, void* ws,
                             size_t ws_bytes, dllm_stream_t stream) {
+  DLLM_RANGE();
   return qgemm_plain("dllm_qgemm_q4k", DLLM_Q4_K, q, d, bsum, m, k, w_packed, n, y, ldy, accumulate, ws, ws_bytes,
                      (cudaStream_t)stream);
 }
@@ -886,12 +891,14 @@ DLLM_API int dllm_qgemm_q4k(const int8_t* q, const float* d, const int16_t* bsum
 DLLM_API int dllm_qgemm_q6k(const int8_t* q, const float* d, const int16_t* bsum, int64_t m, int64_t k,
                             const void* w_packed, int64_t n, float* y, int64_t ldy, int accumulate, void* ws,
                             size_t ws_bytes, dllm_stream_t stream) {
+  DLLM_RANGE();
   return qgemm_plain("dllm_qgemm_q6k", DLLM_Q6_K, q, d, bsum, m, k, w_packed, n, y, ldy, accumulate, ws, ws_bytes,
                      (cudaStream_t)stream);
 }
 
 DLLM_API int dllm_qgemm_intsums(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
                                 int32_t* sums, dllm_stream_t stream) {
+  DLLM_RANGE();
   if (!is_device_ptr(sums)) return fail(DLLM_E_INVAL, "dllm_qgemm_intsums: sums is NULL or not a device pointer");
   return qgemm_common("dllm_qgemm_intsums", type, act, m, k, w_packed, n, nullptr, n, 0, nullptr, 0, sums,
                       (cudaStream_t)stream);
@@ -920,6 +927,7 @@ DLLM_API int dllm_lmhead_select(const float* hidden, int64_t L, int64_t d, int64
                                 float temperature, uint64_t seed, uint32_t step, int32_t* out_pos, int32_t* out_id,
                                 float* out_conf, int32_t* row_id, float* row_conf, void* ws, size_t ws_bytes,
                                 dllm_stream_t stream) {
+  DLLM_RANGE();
   const int64_t R = (int64_t)block_end - block_begin;
   if (L <= 0 || d <= 0 || d % QK || d > (1 << 20) || ldh < d || vocab <= 0 || vocab > (1 << 24))
     return fail(DLLM_E_SHAPE, "dllm_lmhead_select: bad shape L=%lld d=%lld ldh=%lld vocab=%lld", (long long)L,
@@ -1016,6 +1024,7 @@ DLLM_API size_t dllm_qgemm_partials_bytes(int type, int64_t m, int64_t n, int64_
 
 DLLM_API int dllm_qgemm_partials(int type, const void* act, int64_t m, int64_t k, const void* w_packed, int64_t n,
                                  float* partials, size_t partials_bytes, int32_t* splits, dllm_stream_t stream) {
+  DLLM_RANGE();
   if (!block_bytes(type))
     return fail(DLLM_E_TYPE, "dllm_qgemm_partials: unsupported block type %d", type);
   if (m <= 0 || m > 65536 || n <= 0 || n > (1 << 24) || k <= 0 || k % QK || k > (1 << 20))

@@ -3,12 +3,24 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstdint>
 #include <string>
 
 #include "dllm.h"
 
 namespace dllm {
+
+// An NVTX range over one C-ABI call, named after the call (NVTX v3 is header-only: with no
+// profiler attached a range costs a few nanoseconds).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define DLLM_RANGE() ::dllm::NvtxRange dllm_nvtx_range_(__func__)
 
 struct QgemmParams;
 

@@ -271,39 +271,43 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
   griddep_launch();
 }
 
-// Tensor-core attention for canvases of up to TA_KEYS tokens. CTA (head, 128 queries), 8 warps;
-// warp w serves TMEM lane quarter w % 4 (query rows 32 (w % 4) ..) and half w / 4 of the columns.
+// Tensor-core attention for canvases of up to TA_KEYS tokens. CTA (head, 128 queries, chunk of
+// TA_KC keys), 8 warps; warp w serves TMEM lane quarter w % 4 (query rows 32 (w % 4) ..) and
+// half w / 4 of the chunk's keys. Splitting the keys in two chunks halves each CTA's work and
+// doubles the CTAs (128 at L = 148); attn_merge_quant_kernel combines the chunks.
 // Operands are f16 head/tail pairs x = hi + lo (qkv_reduce_rope_kernel writes the planes):
 //   Q, K    by TMA (128-byte swizzle, the K-major layout of the GEMM's activation operand),
 //           keys past L read as zeros;
 //   V^T     by a register transpose of the V planes into the no-swizzle K-major layout
 //           (core matrices of 8 rows x 16 bytes, 128 bytes apart along K, 8-row groups SBO apart).
-// One thread issues S = Q K^T (24 MMAs: M 128, N 160, K 16 x 8, terms hi*hi + hi*lo + lo*hi)
-// into TMEM; each row's softmax is exact (the two column halves meet through shared memory);
-// P goes back as head/tail planes over Q and K; O = P V (30 MMAs: M 128, N 128, K 16 x 10) and
-// each row is written unnormalized with (m, l) as the single chunk of attn_merge_quant_kernel.
-// The three-term products carry each product to ~2^-22 relative, far below the f32
-// accumulation's own rounding. Values must stay inside the f16 range.
-constexpr int TA_M = 128, TA_KEYS = 160, TA_HD = 128, TA_THREADS = 256, TA_BOXR = 32;
+// One thread issues S = Q K^T (24 MMAs: M 128, N 80, K 16 x 8, terms hi*hi + hi*lo + lo*hi)
+// into TMEM; each row's softmax over the chunk is exact (the two column halves meet through
+// shared memory); P goes back as head/tail planes over Q and K; O = P V (15 MMAs: M 128, N 128,
+// K 16 x 5) and each row is written unnormalized with its chunk's (m, l). The three-term
+// products carry each product to ~2^-22 relative, far below the f32 accumulation's own
+// rounding. Values must stay inside the f16 range.
+constexpr int TA_M = 128, TA_KC = 80, TA_KEYS = 2 * TA_KC, TA_HD = 128, TA_THREADS = 256, TA_BOXR = 16;
 constexpr int TA_ATOM_Q = TA_M * 128;                 // one 64-dim swizzled atom column of Q rows
-constexpr int TA_ATOM_K = TA_KEYS * 128;              // ... of K rows
-constexpr int TA_SBO_P = (TA_KEYS / 8) * 128;         // 8-row group stride of P (K = keys)
-constexpr int TA_SBO_V = (TA_KEYS / 8) * 128 + 16;    // ... of V^T, padded: spreads the staging stores
+constexpr int TA_ATOM_K = TA_KC * 128;                // ... of K rows
+constexpr int TA_SBO_P = (TA_KC / 8) * 128;           // 8-row group stride of P (K = keys)
+constexpr int TA_SBO_V = (TA_KC / 8) * 128 + 16;      // ... of V^T, padded: spreads the staging stores
 constexpr int TA_VPL = (TA_HD / 8) * TA_SBO_V;        // one V^T plane
 constexpr int TA_PPL = (TA_M / 8) * TA_SBO_P;         // one P plane
 // Q[hl][atom] at (2 hl + atom) TA_ATOM_Q; K[hl][atom] after them; V^T hi, lo last
 constexpr int TA_OFF_Q = 0, TA_OFF_K = 4 * TA_ATOM_Q, TA_OFF_VH = TA_OFF_K + 4 * TA_ATOM_K;
 constexpr int TA_OFF_VL = TA_OFF_VH + TA_VPL;
 constexpr int TA_OFF_PH = 0, TA_OFF_PL = TA_PPL;      // P overwrites Q and K once S is complete
-constexpr int TA_OFF_RED = TA_OFF_PL + TA_PPL;        // row max / sum exchange, also over K
+constexpr int TA_OFF_RED = TA_OFF_VL + TA_VPL;        // row max / sum exchange, after V^T: the O
+                                                      // staging below overwrites Q, K and P
 constexpr int TA_OP = TA_HD + 4;                      // padded O row (floats) for the write-back
-constexpr int TA_SMEM = TA_OFF_VL + TA_VPL + 1024;    // + slack to align the base to 1024
-constexpr uint32_t TA_TX = (4 * TA_M + 4 * TA_KEYS) * 128;  // TMA bytes of Q and K
-static_assert(TA_OFF_RED + 2 * 2 * TA_M * 4 <= TA_OFF_VH, "P and the exchange fit over Q and K");
-static_assert(TA_M * TA_OP * 4 <= TA_OFF_RED, "O staging fits over the P planes");
+constexpr int TA_SMEM = TA_OFF_RED + 2 * 2 * TA_M * 4 + 1024;  // + slack to align the base to 1024
+constexpr uint32_t TA_TX = (4 * TA_M + 4 * TA_KC) * 128;  // TMA bytes of Q and K
+static_assert(2 * TA_PPL <= TA_OFF_VH, "P fits over Q and K");
+static_assert(TA_M * TA_OP * 4 <= TA_OFF_VH, "O staging fits over Q, K and P");
 static_assert(TA_ATOM_Q % 1024 == 0 && TA_ATOM_K % 1024 == 0, "swizzle atoms 1024-byte aligned");
 static_assert(TA_SMEM + 64 <= 232448, "shared memory budget");
-constexpr int TA_COLS = 512;                          // S at columns [0, 160), O at [160, 288)
+static_assert(TA_KC % 16 == 0 && TA_KC % TA_BOXR == 0 && (TA_KC / 2) % 8 == 0, "chunk shape");
+constexpr int TA_COLS = 256;                          // S at columns [0, 80), O at [80, 208)
 
 __global__ void __launch_bounds__(TA_THREADS, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap qk_map, const __half* __restrict__ planes, AttPart part,
@@ -314,7 +318,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
   // 1024-byte aligned base (the swizzled operands), by offset from the shared array
   uint8_t* ta_smem = ta_raw + ((1024u - (smem_u32(ta_raw) & 1023u)) & 1023u);
   float(*ta_red)[2][TA_M] = reinterpret_cast<float(*)[2][TA_M]>(ta_smem + TA_OFF_RED);  // [max|sum][half][row]
-  const int h = blockIdx.x, q0 = blockIdx.y * TA_M;
+  const int h = blockIdx.x, q0 = blockIdx.y * TA_M, kb = blockIdx.z * TA_KC;  // keys [kb, kb + TA_KC)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qd = warp & 3, ch = warp >> 2, row = 32 * qd + lane;
   const uint32_t sbase = smem_u32(ta_smem);
@@ -335,7 +339,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
   tc_fence_after();
   griddep_wait();  // the planes are the preceding kernel's output
   if (threadIdx.x == 0) {
-    // Q (planes 0, 1) rows q0.., K (planes 2, 3) rows 0..: boxes of 64 dims x 32 rows
+    // Q (planes 0, 1) rows q0.., K (planes 2, 3) rows kb..: boxes of 64 dims x TA_BOXR rows
     mbar_expect_tx(bar_in, TA_TX);
 #pragma unroll 1
     for (int hl = 0; hl < 2; ++hl)
@@ -344,17 +348,17 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         for (int b = 0; b < TA_M / TA_BOXR; ++b)
           tma_g2s_3d(sbase + TA_OFF_Q + (2 * hl + a) * TA_ATOM_Q + b * TA_BOXR * 128, &qk_map, h * TA_HD + 64 * a,
                      q0 + b * TA_BOXR, hl, bar_in);
-        for (int b = 0; b < TA_KEYS / TA_BOXR; ++b)
+        for (int b = 0; b < TA_KC / TA_BOXR; ++b)
           tma_g2s_3d(sbase + TA_OFF_K + (2 * hl + a) * TA_ATOM_K + b * TA_BOXR * 128, &qk_map, h * TA_HD + 64 * a,
-                     b * TA_BOXR, 2 + hl, bar_in);
+                     kb + b * TA_BOXR, 2 + hl, bar_in);
       }
   }
-  // V^T (rows = dims, K = keys) by a register transpose of the V planes: item = (key pair, block
-  // of 8 dims), all of a thread's loads in flight, then (key, key + 1) pairs per 4-byte store
+  // V^T (rows = dims, K = the chunk's keys) by a register transpose of the V planes: item = (key
+  // pair, block of 8 dims), all of a thread's loads in flight, then (key, key + 1) pairs per
+  // 4-byte store
   {
     const int64_t pl = (int64_t)L * d;
-    constexpr int NIT = (TA_KEYS / 2) * (TA_HD / 8), PER = NIT / TA_THREADS;
-    static_assert(NIT % TA_THREADS == 0, "V^T staging split");
+    constexpr int NIT = (TA_KC / 2) * (TA_HD / 8), PER = (NIT + TA_THREADS - 1) / TA_THREADS;
     uint4 vh[PER][2], vl[PER][2];
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
@@ -363,8 +367,8 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         vh[u][e] = vl[u][e] = make_uint4(0u, 0u, 0u, 0u);
-        if (k0 + e < L) {
-          const __half* src = planes + (int64_t)(k0 + e) * d + h * TA_HD + 8 * nb;
+        if (i < NIT && kb + k0 + e < L) {
+          const __half* src = planes + (int64_t)(kb + k0 + e) * d + h * TA_HD + 8 * nb;
           vh[u][e] = *reinterpret_cast<const uint4*>(src + 4 * pl);
           vl[u][e] = *reinterpret_cast<const uint4*>(src + 5 * pl);
         }
@@ -373,6 +377,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
       const int i = threadIdx.x + u * TA_THREADS;
+      if (i >= NIT) break;
       const int k0 = 2 * (i / (TA_HD / 8)), nb = i % (TA_HD / 8);
       const uint32_t* h0 = reinterpret_cast<const uint32_t*>(&vh[u][0]);
       const uint32_t* h1 = reinterpret_cast<const uint32_t*>(&vh[u][1]);
@@ -398,7 +403,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
   if (threadIdx.x == 0) {
     ok = mbar_wait(bar_in, 0, &never, kDefaultTimeoutCycles);
     tc_fence_after();
-    constexpr uint32_t IDS = idesc_f16(TA_M, TA_KEYS);
+    constexpr uint32_t IDS = idesc_f16(TA_M, TA_KC);
 #pragma unroll 1
     for (int kk = 0; kk < TA_HD / 16 && ok; ++kk) {
       const int a = kk >> 2;
@@ -413,23 +418,23 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
     }
     mma_commit(bar_s);  // arrives even when the inputs timed out, so the waits below end
   }
-  // this thread's row, its column half of S: keys [80 ch, 80 ch + 80)
+  // this thread's row, its half of the chunk's columns of S: keys kb + [HK ch, HK ch + HK)
   ok = __all_sync(0xffffffffu, mbar_wait(bar_s, 0, &never, kDefaultTimeoutCycles));
   tc_fence_after();
   const uint32_t trow = tmem + ((uint32_t)(32 * qd) << 16);
-  constexpr int HK = TA_KEYS / 2;
+  constexpr int HK = TA_KC / 2;
   float m = -INFINITY, l = 0.f;
   {
     uint32_t sv[HK];
 #pragma unroll
-    for (int c = 0; c < HK / 16; ++c) tmem_ld16(trow + HK * ch + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(sv + 16 * c));
+    for (int c = 0; c < HK / 8; ++c) tmem_ld8(trow + HK * ch + 8 * c, *reinterpret_cast<uint32_t(*)[8]>(sv + 8 * c));
     tmem_ld_wait();
 #pragma unroll
     for (int k = 0; k < HK; ++k)
-      if (HK * ch + k < L) m = fmaxf(m, __uint_as_float(sv[k]));
+      if (kb + HK * ch + k < L) m = fmaxf(m, __uint_as_float(sv[k]));
     ta_red[0][ch][row] = m;
     __syncthreads();
-    m = fmaxf(ta_red[0][0][row], ta_red[0][1][row]);  // key 0 is real, so m is finite
+    m = fmaxf(ta_red[0][0][row], ta_red[0][1][row]);  // the chunk's first key is real, so m is finite
     // p = e^(s - m) as 2^((s - m) log2 e) (exp2f: 2 ulp)
     constexpr float LOG2E = 1.4426950408889634f;
     const float ml2 = m * LOG2E;
@@ -439,7 +444,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int k = HK * ch + 8 * c + e;
-        pv[e] = k < L ? exp2f(fmaf(__uint_as_float(sv[8 * c + e]), LOG2E, -ml2)) : 0.f;
+        pv[e] = kb + k < L ? exp2f(fmaf(__uint_as_float(sv[8 * c + e]), LOG2E, -ml2)) : 0.f;
         l += pv[e];
       }
       uint32_t hi[4], lo[4];
@@ -459,37 +464,40 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
   if (threadIdx.x == 0) {
     constexpr uint32_t IDO = idesc_f16(TA_M, TA_HD);
 #pragma unroll 1
-    for (int kk = 0; kk < TA_KEYS / 16 && ok; ++kk) {
+    for (int kk = 0; kk < TA_KC / 16 && ok; ++kk) {
       const uint32_t ko = (uint32_t)kk * 256;
       const uint64_t ph = desc_noswz(sbase + TA_OFF_PH + ko, 128, TA_SBO_P);
       const uint64_t pl = desc_noswz(sbase + TA_OFF_PL + ko, 128, TA_SBO_P);
       const uint64_t vh = desc_noswz(sbase + TA_OFF_VH + ko, 128, TA_SBO_V);
       const uint64_t vl = desc_noswz(sbase + TA_OFF_VL + ko, 128, TA_SBO_V);
-      mma_f16(tmem + TA_KEYS, ph, vh, IDO, kk > 0);
-      mma_f16(tmem + TA_KEYS, ph, vl, IDO, 1);
-      mma_f16(tmem + TA_KEYS, pl, vh, IDO, 1);
+      mma_f16(tmem + TA_KC, ph, vh, IDO, kk > 0);
+      mma_f16(tmem + TA_KC, ph, vl, IDO, 1);
+      mma_f16(tmem + TA_KC, pl, vh, IDO, 1);
     }
     mma_commit(bar_o);
   }
   ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_o, 0, &never, kDefaultTimeoutCycles));
   tc_fence_after();
-  // O through shared memory (rows padded to TA_OP floats, over the finished P planes), then out
-  // row-contiguously: this thread's row, its half of the dims; all lanes load from TMEM
+  // O through shared memory (rows padded to TA_OP floats, over the finished Q, K and P), then out
+  // row-contiguously into chunk blockIdx.z: this thread's row, its half of the dims; all lanes
+  // load from TMEM
   const int q = q0 + row;
+  const int64_t cofs = (int64_t)blockIdx.z * L;  // the chunk's first row in the partial arrays
   {
     float* os = reinterpret_cast<float*>(ta_smem);
     uint32_t ov[TA_HD / 2];
 #pragma unroll
     for (int c = 0; c < TA_HD / 32; ++c)
-      tmem_ld16(trow + TA_KEYS + (TA_HD / 2) * ch + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(ov + 16 * c));
+      tmem_ld16(trow + TA_KC + (TA_HD / 2) * ch + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(ov + 16 * c));
     tmem_ld_wait();
 #pragma unroll
     for (int e = 0; e < TA_HD / 2; e += 4)
       *reinterpret_cast<uint4*>(os + row * TA_OP + (TA_HD / 2) * ch + e) = make_uint4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
-    if (ok && ch == 0 && q < L) *reinterpret_cast<float2*>(part.ml + ((int64_t)q * heads + h) * 2) = make_float2(m, l);
+    if (ok && ch == 0 && q < L)
+      *reinterpret_cast<float2*>(part.ml + ((cofs + q) * heads + h) * 2) = make_float2(m, l);
     __syncthreads();
     if (ok) {
-      float* dst = part.acc + (int64_t)q0 * d + h * TA_HD;
+      float* dst = part.acc + (cofs + q0) * d + h * TA_HD;
 #pragma unroll 4
       for (int i = threadIdx.x; i < TA_M * (TA_HD / 4); i += TA_THREADS) {
         const int r = i / (TA_HD / 4), c4 = i % (TA_HD / 4);
@@ -875,7 +883,8 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
         if ((rc = make_planes_tmap(&qk_map, planes, 6, L, d, TA_BOXR))) return rc;
         e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TA_SMEM);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
-        const dim3 ag(m->n_heads, (unsigned)((L + TA_M - 1) / TA_M));
+        nchunk = (int)((L + TA_KC - 1) / TA_KC);
+        const dim3 ag(m->n_heads, (unsigned)((L + TA_M - 1) / TA_M), (unsigned)nchunk);
         e = launch_pdl(attention_tc_kernel, ag, dim3(TA_THREADS), TA_SMEM, s, qk_map, (const __half*)planes, ap,
                        (int)L, d, m->n_heads, err);
       } else {  // longer canvases: chunks of 32 keys, merged below
@@ -1023,6 +1032,7 @@ DLLM_API int dllm_step_linear_stream(const dllm_model* m, const int32_t* canvas,
 
 DLLM_API int dllm_step_taps(const dllm_model* m, const int32_t* canvas, int64_t L, float* x, int flags,
                             const dllm_taps* taps, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  DLLM_RANGE();
   int rc = check_model(m, L, "dllm_step_linear_stream");
   if (rc) return rc;
   if (flags != DLLM_STREAM_LINEAR && flags != DLLM_STREAM_FULL)
@@ -1067,6 +1077,7 @@ DLLM_API size_t dllm_denoise_workspace_bytes(const dllm_model* m, int64_t L, int
 DLLM_API int dllm_denoise_step(const dllm_model* m, int32_t* canvas, int64_t L, int32_t block_begin, int32_t block_end,
                                int32_t k_commit, int32_t* out_pos, int32_t* out_id, float* out_conf,
                                float* hidden_out, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  DLLM_RANGE();
   int rc = check_model(m, L, "dllm_denoise_step");
   if (rc) return rc;
   if ((rc = check_device())) return rc;
@@ -1109,6 +1120,7 @@ DLLM_API int dllm_denoise_step_cached(const dllm_model* m, int32_t* canvas, int6
                                       int32_t block_end, int32_t k_commit, int32_t refresh, float* kv_cache,
                                       size_t kv_bytes, int32_t* out_pos, int32_t* out_id, float* out_conf,
                                       float* hidden_out, void* ws, size_t ws_bytes, dllm_stream_t stream) {
+  DLLM_RANGE();
   int rc = check_model(m, L, "dllm_denoise_step_cached");
   if (rc) return rc;
   if ((rc = check_device())) return rc;

@@ -57,6 +57,7 @@ using namespace dllm;
 
 extern "C" DLLM_API int dllm_qgemm_noalloc(int type, const void* act, int64_t m, int64_t k, const void* w_packed,
                                            int64_t n, float* y, int64_t ldy, int accumulate, dllm_stream_t stream) {
+  DLLM_RANGE();
   if (type != DLLM_Q4_K && type != DLLM_Q6_K)
     return fail(DLLM_E_TYPE, "dllm_qgemm_noalloc: unsupported block type %d: matrix kernels exist for Q4_K (12) and Q6_K (14)",
                 type);

@@ -229,7 +229,7 @@ __device__ __forceinline__ void decode_q4k_half(const uint8_t* W, int t, int q, 
 // quarters take the low ql nibble and the f16 pattern 1024 + q6 (qh bits at 4-5), odd quarters
 // the high nibble and 1024 + 16*q6 (qh bits at 8-9) with the multiplier divided by 16; every
 // operand is one exact fused multiply-add of the pattern.
-__device__ __forceinline__ void decode_q6k_piece(const uint8_t* W, int t, int q, int tt, int ps, const int8_t* sc,
+__device__ __forceinline__ void decode_q6k_piece(const uint8_t* W, int t, int q, int tt, int ps, uint32_t sw,
                                                  float hs, float ls, uint32_t (&hi)[8], uint32_t (&lo)[8]) {
   const int hq = q >> 1, odd = q & 1;
   const uint4 v = *reinterpret_cast<const uint4*>(W + (4 * hq + 2 * tt + ps) * 2048 + t * 16);
@@ -241,7 +241,9 @@ __device__ __forceinline__ void decode_q6k_piece(const uint8_t* W, int t, int q,
   const float fa = odd ? -96.0f : -1056.0f;
   const int tslot = 2 * odd + tt;
   const int shift = tt ? 2 : 4;
-  const int s = sc[8 * hq + 2 * tslot + ps];
+  // the row's int8 group scale: scale byte 8 hq + 2 tslot + ps = byte 2 tt + ps of the quarter's
+  // scale word sw (its bytes 4q .. 4q + 3)
+  const int s = (int)(int8_t)(sw >> (8 * (2 * tt + ps)));
   const float s_hi = hs == 0.f ? 0.f : (float)(s >> 4), s_lo = (float)(s & 15) * ls * 0.0625f;
   const __half2 mH = __float2half2_rn(s_hi * fm), aH = __float2half2_rn(s_hi * fa);
   const __half2 mL = __float2half2_rn(s_lo * fm), aL = __float2half2_rn(s_lo * fa);
@@ -629,8 +631,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             mbar_arrive(BAR(C::BJ_FULL + it % C::J_STAGES));
           }
         } else {
-          const uint4 scv = *reinterpret_cast<const uint4*>(W + 24576 + t * 16);
-          const int8_t* sc = reinterpret_cast<const int8_t*>(&scv);
+
           const float hs = p.dbg_mode == 2 ? 0.f : 1.f;
           const float ls = p.dbg_mode == 1 ? 0.f : 1.f;
 #pragma unroll 1
@@ -638,12 +639,13 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             const int j = 4 * it + q, b = j % C::K_STAGES;
             if (!(ok = warp_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
             tc_fence_after();
+            const uint32_t sw = *reinterpret_cast<const uint32_t*>(W + 24576 + t * 16 + 4 * q);  // quarter q's scales
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
               for (int ps = 0; ps < 2; ++ps) {
                 uint32_t hi[8], lo[8];
-                decode_q6k_piece(W, t, q, h, ps, sc, hs, ls, hi, lo);
+                decode_q6k_piece(W, t, q, h, ps, sw, hs, ls, hi, lo);
                 tmem_st8(tlane + b * C::ASTG + 16 * h + 8 * ps, hi);
                 tmem_st8(tlane + b * C::ASTG + 32 + 16 * h + 8 * ps, lo);
               }
