@@ -50,7 +50,10 @@
 //   W  raw packed super-block of the 128 rows (+ Q4_K d/dmin), smem   weight producer -> decode
 //   E  per-super-block scales for the epilogue, smem: d/dmin, d_a    act. producer -> epilogue
 //   J  Q4_K offset/min operands, smem: activation 16-sums (bulk        producer, decode -> MMA
-//      copy) and the c head and tail rows
+//      copy) and the c head and tail rows; only an "empty" barrier:
+//      the copy completes on the super-block's last K-stage barrier
+//      and each decode group writes its rows before arriving on its
+//      own K-stage, so the MMA's K-stage waits cover the J operands
 //   K  K-stage: activation tile (smem, TMA, 128-byte swizzle) and     producer, decode -> MMA
 //      decoded weights (TMEM), 64 TMEM columns
 //   S  accumulator slots, TMEM                                        MMA -> epilogue
@@ -103,14 +106,17 @@ struct QCfg {
   static constexpr int NSLOT = 2;
   static constexpr int ACOL = NSLOT * NT;
   static constexpr int ASTG = 64;
-  static constexpr int K_STAGES = cmin(6, (TMEM_COLS - ACOL) / ASTG);
+  // Q4_K keeps an odd stage count: its J operands live in the slot of the super-block's last
+  // stage, (2 it + 1) % K_STAGES, which then walks through every slot (see the J ring below)
+  static constexpr int K_FIT = cmin(6, (TMEM_COLS - ACOL) / ASTG);
+  static constexpr int K_STAGES = Q4 ? K_FIT - (K_FIT % 2 == 0 ? 1 : 0) : K_FIT;
   // shared memory: E ring (epilogue scales), J ring (Q4_K min operands)
   static constexpr int E_STAGES = 6;
   static constexpr int E_DD = 0;
   static constexpr int E_DA = al128(DD_BYTES);
   static constexpr int E_BYTES = al128(E_DA + NT * 4);
   static constexpr int E_TX = DD_BYTES + NT * 4;
-  static constexpr int J_STAGES = Q4 ? 3 : 0;
+  static constexpr int J_STAGES = Q4 ? K_STAGES : 0;
   static constexpr int J_BJ = 0;
   static constexpr int J_AJ = al128(NT * 32);
   static constexpr int J_BYTES = J_AJ + 8192;  // c head, then tail, 128 rows x 16 f16 each
@@ -128,8 +134,7 @@ struct QCfg {
   static constexpr int BK_FULL = 0, BK_EMPTY = BK_FULL + K_STAGES;
   static constexpr int BW_FULL = BK_EMPTY + K_STAGES, BW_EMPTY = BW_FULL + W_STAGES;
   static constexpr int BE_FULL = BW_EMPTY + W_STAGES, BE_EMPTY = BE_FULL + E_STAGES;
-  static constexpr int BJ_FULL = BE_EMPTY + E_STAGES, BJ_EMPTY = BJ_FULL + J_STAGES;
-  static constexpr int BS_FULL = BJ_EMPTY + J_STAGES, BS_EMPTY = BS_FULL + NSLOT;
+  static constexpr int BS_FULL = BE_EMPTY + E_STAGES, BS_EMPTY = BS_FULL + NSLOT;
   static constexpr int B_DONE = BS_EMPTY + NSLOT;
   static constexpr int NBAR = B_DONE + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -373,10 +378,6 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
       mbar_init(BAR(C::BE_FULL + i), 1);
       mbar_init(BAR(C::BE_EMPTY + i), QG_EPI_WARPS);
     }
-    for (int i = 0; i < C::J_STAGES; ++i) {
-      mbar_init(BAR(C::BJ_FULL + i), 1 + QG_DEC_WARPS);  // producer (activation sums, tx) + decode
-      mbar_init(BAR(C::BJ_EMPTY + i), 1);                // MMA commit
-    }
     for (int i = 0; i < C::NSLOT; ++i) {
       mbar_init(BAR(C::BS_FULL + i), 1);
       mbar_init(BAR(C::BS_EMPTY + i), QG_EPI_WARPS);
@@ -445,21 +446,23 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           mbar_expect_tx(BAR(C::BE_FULL + e), C::E_TX);
           bulk_g2s(es + C::E_DD, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES, BAR(C::BE_FULL + e));
           bulk_g2s(es + C::E_DA, p.act_d + (size_t)sb * p.lpad + tok0, NT * 4, BAR(C::BE_FULL + e));
-          if constexpr (C::Q4) {
-            const int jx = it % C::J_STAGES;
-            if (!(ok = mbar_wait(BAR(C::BJ_EMPTY + jx), ((it / C::J_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
-            mbar_expect_tx(BAR(C::BJ_FULL + jx), C::J_TX);
-            bulk_g2s(sbase + C::OFF_J + jx * C::J_BYTES + C::J_BJ, p.act_j + ((size_t)sb * p.lpad + tok0) * 32,
-                     NT * 32, BAR(C::BJ_FULL + jx));
-          }
           for (int st = 0; st < C::SPS; ++st) {
             const int j = C::SPS * it + st, b = j % C::K_STAGES;
             if (!(ok = mbar_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
-            mbar_expect_tx(BAR(C::BK_FULL + b), C::B_STAGE);
+            // Q4_K: the super-block's activation 16-sums go to J slot b of its last stage and ride
+            // on that stage's barrier, so the MMA issuer's wait for the stage also covers the
+            // offset/min operands (the decode groups write their coefficient rows before they
+            // arrive on their own stages); the BK_EMPTY wait above also frees the J slot (below)
+            const bool jcopy = C::Q4 && st == C::SPS - 1;
+            const int jx = b;
+            mbar_expect_tx(BAR(C::BK_FULL + b), C::B_STAGE + (jcopy ? C::J_TX : 0));
 #pragma unroll
             for (int qq = 0; qq < C::QPS; ++qq)
               tma_g2s_3d(sbase + C::OFF_B + b * C::B_STAGE + qq * C::B_QUARTER, &tmap, 0, tok0,
                          sb * 4 + st * C::QPS + qq, BAR(C::BK_FULL + b));
+            if (jcopy)
+              bulk_g2s(sbase + C::OFF_J + jx * C::J_BYTES + C::J_BJ, p.act_j + ((size_t)sb * p.lpad + tok0) * 32,
+                       NT * 32, BAR(C::BK_FULL + b));
           }
           if (!ok) break;
         }
@@ -509,17 +512,18 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
                 for (int kk = 0; kk < 4; ++kk)
                   mma_f16_ts(dslot, acol + qq * 32 + kk * 8, bdesc + (uint64_t)((qq * C::B_QUARTER + kk * 32) >> 4),
                                   IDESC, (st | qq | kk) != 0);
+              if (st == 1) {
+                // offset and min term: head and tail coefficients x activation 16-sums, in J slot
+                // b (ready with this stage: see the activation producer); the stage's commit
+                // below then also releases the J slot
+                const uint32_t js = sbase + C::OFF_J + b * C::J_BYTES;
+                const uint64_t bj = desc_noswz(js + C::J_BJ, 128, 256);
+                mma_f16(dslot, desc_noswz(js + C::J_AJ, 128, 256), bj, IDESC, 1);
+                mma_f16(dslot, desc_noswz(js + C::J_AJ + 4096, 128, 256), bj, IDESC, 1);
+              }
               mma_commit(BAR(C::BK_EMPTY + b));
             }
             if (!ok) break;
-            // offset and min term last: head and tail coefficients x activation 16-sums
-            const int jx = it % C::J_STAGES;
-            if (!(ok = wait_tc(BAR(C::BJ_FULL + jx), (it / C::J_STAGES) & 1))) break;
-            const uint32_t js = sbase + C::OFF_J + jx * C::J_BYTES;
-            const uint64_t bj = desc_noswz(js + C::J_BJ, 128, 256);
-            mma_f16(dslot, desc_noswz(js + C::J_AJ, 128, 256), bj, IDESC, 1);
-            mma_f16(dslot, desc_noswz(js + C::J_AJ + 4096, 128, 256), bj, IDESC, 1);
-            mma_commit(BAR(C::BJ_EMPTY + jx));
           } else {
             for (int q = 0; q < 4; ++q) {
               const int j = 4 * it + q, b = j % C::K_STAGES;
@@ -600,8 +604,11 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             // swizzle; K = 16 groups of 16 values, group k pairs with sub-block k/2) holds the f16
             // head and tail of c = jsc * 8 * scale + jmn * min; group g writes core matrix g
             // (sub-blocks 4g..4g+3)
-            const int jx = it % C::J_STAGES;
-            if (!(ok = warp_wait(BAR(C::BJ_EMPTY + jx), ((it / C::J_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
+            // J slot of the super-block's last stage. Its previous user is super-block it - K_STAGES
+            // (2 it + 1 walks every slot mod an odd K_STAGES), whose J MMAs were issued before the
+            // stage this group waited on above (2 it + g - K_STAGES > 2 (it - K_STAGES) + 1), and
+            // MMAs complete in issue order: the slot is free
+            const int jx = (2 * it + 1) % C::K_STAGES;
             const uint32_t w1 = *reinterpret_cast<const uint32_t*>(W + 16384 + 512 + t * 4);
             // 6-bit mins: entries 0..3 are the bytes of word 1, entries 4..7 combine word 2's
             // high nibbles with word 1's top bits
@@ -626,10 +633,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(BAR(C::BK_FULL + b));
-            mbar_arrive(BAR(C::BJ_FULL + it % C::J_STAGES));
-          }
+          if (lane == 0) mbar_arrive(BAR(C::BK_FULL + b));
         } else {
 
           const float hs = p.dbg_mode == 2 ? 0.f : 1.f;
