@@ -540,7 +540,9 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             }
             if (!ok) break;
           }
-          mma_commit(BAR(C::BS_FULL + s));
+          // Q4_K: the last stage's commit (its K-stage barrier) already tells the epilogue that
+          // the super-block's part is complete (see the epilogue's wait)
+          if constexpr (!C::Q4) mma_commit(BAR(C::BS_FULL + s));
         }
       }
       if (!ok) atomicOr(p.err, ERR_TIMEOUT_MMA);
@@ -705,7 +707,18 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
         }
         const float4* da4 = reinterpret_cast<const float4*>(E + C::E_DA) + hf * (NC / 4);
         const uint32_t n = s ? sf1++ : sf0++;
-        if (!(ok = warp_wait(BAR(C::BS_FULL + s), n & 1, abort_flag, lim, QG_SUSPEND))) break;
+        if constexpr (C::Q4) {
+          // the commit after the super-block's last stage, j = 2 itp + 1, covers all its MMAs. That
+          // K-stage barrier cannot complete another phase before this wait is satisfied: its next
+          // use, stage j + K_STAGES (odd), belongs to super-block itp + 2 or later, whose MMAs wait
+          // for this epilogue to free slot s. So its parity identifies the phase.
+          const int j = 2 * itp + 1;
+          if (!(ok = warp_wait(BAR(C::BK_EMPTY + j % C::K_STAGES), (j / C::K_STAGES) & 1, abort_flag, lim,
+                               QG_SUSPEND)))
+            break;
+        } else {
+          if (!(ok = warp_wait(BAR(C::BS_FULL + s), n & 1, abort_flag, lim, QG_SUSPEND))) break;
+        }
         tc_fence_after();
         // drain in groups of up to 2 x 8 columns; the slot is freed as soon as the last group
         // is in registers, before its arithmetic
