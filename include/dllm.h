@@ -64,7 +64,9 @@ enum {
   DLLM_E_WORKSPACE = 5,   /* workspace smaller than the matching *_workspace_bytes()       */
   DLLM_E_CUDA = 6,        /* a CUDA runtime call failed (message names it)                 */
   DLLM_E_TIMEOUT = 7,     /* a device-side bounded wait ran out (reported by dllm_check)   */
-  DLLM_E_DEVICE = 8       /* current device is not sm_103 / lacks a feature               */
+  DLLM_E_DEVICE = 8,      /* current device is not sm_103 / lacks a feature               */
+  DLLM_E_BOUNDS = 9       /* bounds-checked build only: a kernel access fell outside its
+                             buffer and was skipped (reported by dllm_check with its site) */
 };
 
 /* GGML block type ids of the two matrix formats with kernels ([DP-CO]). */
@@ -77,8 +79,10 @@ DLLM_API const char* dllm_last_error(void);
 DLLM_API int dllm_version(void);
 
 /* Synchronize `stream`, then read and clear the device error word. Returns DLLM_OK,
- * DLLM_E_TIMEOUT (a kernel's bounded wait ran out; the message names the kernel role) or
- * DLLM_E_CUDA (a launch or execution error, message from the runtime). */
+ * DLLM_E_TIMEOUT (a kernel's bounded wait ran out; the message names the kernel role),
+ * DLLM_E_INVAL (an input a kernel found invalid: an unfoldable Q4_K block, inconsistent plain
+ * Q8_K sums), DLLM_E_BOUNDS (bounds-checked build only, see below) or DLLM_E_CUDA (a launch or
+ * execution error, message from the runtime). */
 DLLM_API int dllm_check(dllm_stream_t stream);
 
 /* ---- weight packing ------------------------------------------------------------------------
@@ -401,6 +405,26 @@ DLLM_API int dllm_qgemm_noalloc(int type, const void* act, int64_t m, int64_t k,
  * complete, bounded by `limit_cycles` SM clock cycles; the kernel then records a timeout
  * in the device error word and returns. dllm_check() afterwards reports DLLM_E_TIMEOUT. */
 DLLM_API int dllm_selftest_timeout(int64_t limit_cycles, dllm_stream_t stream);
+
+/* ---- bounds-checked build --------------------------------------------------------------------
+ * The same sources also build libdllm_checked.so (compiled with DLLM_BOUNDS_CHECK), a debug
+ * library with the same entry points in which every global-memory access of every kernel is
+ * first checked against the extent of the buffer it targets. The extents are computed on the
+ * host from each call's shapes (the buffer sizes documented above); tensor-map copies are
+ * checked by the hardware against their maps. An access outside its buffer is skipped instead
+ * of performed, and dllm_check then returns DLLM_E_BOUNDS naming the source file and line of the
+ * first such access (a skipped copy also makes the waits on it run out, so a GEMM launch may
+ * report a timeout with it). Outputs of a launch that reported DLLM_E_BOUNDS are not valid. The
+ * checked library is slower and is meant for tests and debugging, not for measurement.
+ *
+ * dllm_bounds_checked: 1 in the bounds-checked build, 0 in the regular one.
+ * dllm_selftest_bounds: test hook; writes buf[i] = i for 0 <= i < n_write, each store checked
+ *   against a span of the first n_declared floats of buf. The regular build performs every
+ *   store; the checked build skips those with i >= n_declared and records DLLM_E_BOUNDS. `buf`
+ *   must hold n_write floats, so no store ever leaves the real buffer. Errors: DLLM_E_INVAL
+ *   (0 < n_write <= 2^20 and 0 <= n_declared <= n_write required). */
+DLLM_API int dllm_bounds_checked(void);
+DLLM_API int dllm_selftest_bounds(float* buf, int32_t n_write, int32_t n_declared, dllm_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -14,13 +14,16 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libdllm.so")
+# DLLM_CHECKED=1 loads the bounds-checked build (every kernel access checked against its
+# buffer; slower, for tests and debugging) in place of the regular library.
+CHECKED = os.environ.get("DLLM_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(_HERE, "libdllm_checked.so" if CHECKED else "libdllm.so")
 
 Q4_K = 12
 Q6_K = 14
 QK = 256
 
-OK, E_INVAL, E_SHAPE, E_ALIGN, E_TYPE, E_WORKSPACE, E_CUDA, E_TIMEOUT, E_DEVICE = range(9)
+OK, E_INVAL, E_SHAPE, E_ALIGN, E_TYPE, E_WORKSPACE, E_CUDA, E_TIMEOUT, E_DEVICE, E_BOUNDS = range(10)
 
 
 class DllmError(RuntimeError):
@@ -51,6 +54,8 @@ _SIGS = {
     "dllm_qgemm_q6k": ([P, P, P, I64, I64, P, I64, P, I64, INT, P, SZ, P], INT),
     "dllm_qgemm_intsums": ([INT, P, I64, I64, P, I64, P, P], INT),
     "dllm_selftest_timeout": ([I64, P], INT),
+    "dllm_bounds_checked": ([], INT),
+    "dllm_selftest_bounds": ([P, I32, I32, P], INT),
     "dllm_lmhead_workspace_bytes": ([I64, I64, I64], SZ),
     "dllm_lmhead_masked_select": ([P, I64, I64, I64, P, F32, P, I64, P, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P],
                                   INT),
@@ -260,6 +265,17 @@ def peak_mma_i8_tops(iters: int = 20000, reps: int = 3, stream=None) -> float:
 
 def selftest_timeout(limit_cycles: int, stream=None):
     _ok(lib().dllm_selftest_timeout(limit_cycles, _stream(stream)))
+
+
+def bounds_checked() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(lib().dllm_bounds_checked())
+
+
+def selftest_bounds(buf: torch.Tensor, n_write: int, n_declared: int, stream=None):
+    """buf[i] = i for i < n_write, each store checked against the first n_declared floats."""
+    assert buf.dtype == torch.float32 and buf.is_cuda and buf.numel() >= n_write
+    _ok(lib().dllm_selftest_bounds(_ptr(buf), n_write, n_declared, _stream(stream)))
 
 
 # --- transfer schedule (host only) -----------------------------------------------------------

@@ -15,9 +15,12 @@
 #include "qgemm.cuh"
 #include "quant.cuh"
 
+#define DLLM_FILE 1  // bounds-check sites of this file
+
 namespace dllm {
 
 __device__ int g_err_word = 0;
+__device__ int g_bounds_site = 0;  // checked build: DLLM_SITE_AT of the first failing check
 
 int* err_word() {
   static int* cache[64] = {nullptr};
@@ -29,6 +32,48 @@ int* err_word() {
     cache[dev] = static_cast<int*>(p);
   }
   return cache[dev];
+}
+
+int* site_word() {
+  static int* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bounds_site) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+void set_quant_bounds(QuantOut& o, int64_t rows, int64_t k) {
+  const int64_t nsb = k / QK, lp = o.lpad;
+  o.bd = make_bounds({{o.q, (size_t)(rows * k)},
+                      {o.d, (size_t)(rows * nsb * 4)},
+                      {o.bsum, (size_t)(rows * (k / 16) * 2)},
+                      {o.act_a, (size_t)(lp * k * 2)},
+                      {o.act_j, (size_t)(nsb * lp * 32)},
+                      {o.act_d, (size_t)(nsb * lp * 4)},
+                      {o.vtap, (size_t)(rows * k * 4)}});
+}
+
+Bounds make_bounds(std::initializer_list<Span> spans) {
+  Bounds b{};
+#ifdef DLLM_BOUNDS_CHECK
+  int i = 0;
+  for (const Span& s : spans) {
+    if (i < kMaxSpans) {
+      b.lo[i] = reinterpret_cast<unsigned long long>(s.p);
+      b.hi[i] = b.lo[i] + (s.p ? s.bytes : 0);
+    }
+    ++i;
+  }
+  b.err = err_word();
+  b.site = site_word();
+#else
+  (void)spans;
+#endif
+  return b;
 }
 
 static thread_local char g_msg[1024] = "";
@@ -174,40 +219,44 @@ int make_planes_tmap(CUtensorMap* map, const void* base, int64_t planes, int64_t
 // ---------------------------------------------------------------------------------------------
 static int block_bytes(int type) { return type == DLLM_Q4_K ? 144 : type == DLLM_Q6_K ? 210 : 0; }
 
+// Spans (bounds-checked build): 0 the source blocks, 1 the blob, 2 the scale plane.
 __global__ void pack_q4k_kernel(const uint8_t* __restrict__ src, int n, int nsb, uint8_t* __restrict__ blob,
-                                uint8_t* __restrict__ dd) {
+                                uint8_t* __restrict__ dd, Bounds bd) {
   const int ts = blockIdx.x;  // tile * nsb + sb
   const int tile = ts / nsb, sb = ts % nsb, r = threadIdx.x;
   const int64_t grow = (int64_t)tile * BM + r;
   const bool valid = grow < n;
   const uint8_t* b = src + (grow * nsb + sb) * 144;
   uint8_t* o = blob + (size_t)ts * Q4K_BLOB;
+  const uint4 z4 = make_uint4(0, 0, 0, 0);
 #pragma unroll
   for (int h = 0; h < 8; ++h)
-    *reinterpret_cast<uint4*>(o + h * 2048 + r * 16) =
-        valid ? *reinterpret_cast<const uint4*>(b + 16 + 16 * h) : make_uint4(0, 0, 0, 0);
+    STB(bd, 1, reinterpret_cast<uint4*>(o + h * 2048 + r * 16),
+        valid ? LDB(bd, 0, reinterpret_cast<const uint4*>(b + 16 + 16 * h), z4) : z4);
 #pragma unroll
   for (int w = 0; w < 3; ++w)
-    *reinterpret_cast<uint32_t*>(o + 16384 + w * 512 + r * 4) =
-        valid ? *reinterpret_cast<const uint32_t*>(b + 4 + 4 * w) : 0u;
-  *reinterpret_cast<uint32_t*>(dd + (size_t)ts * Q4K_DD + r * 4) =
-      valid ? *reinterpret_cast<const uint32_t*>(b) : 0u;
+    STB(bd, 1, reinterpret_cast<uint32_t*>(o + 16384 + w * 512 + r * 4),
+        valid ? LDB(bd, 0, reinterpret_cast<const uint32_t*>(b + 4 + 4 * w), 0u) : 0u);
+  STB(bd, 2, reinterpret_cast<uint32_t*>(dd + (size_t)ts * Q4K_DD + r * 4),
+      valid ? LDB(bd, 0, reinterpret_cast<const uint32_t*>(b), 0u) : 0u);
 }
 
 __global__ void pack_q6k_kernel(const uint8_t* __restrict__ src, int n, int nsb, uint8_t* __restrict__ blob,
-                                uint8_t* __restrict__ dd) {
+                                uint8_t* __restrict__ dd, Bounds bd) {
   const int ts = blockIdx.x;
   const int tile = ts / nsb, sb = ts % nsb, r = threadIdx.x;
   const int64_t grow = (int64_t)tile * BM + r;
   const bool valid = grow < n;
   const uint8_t* b = src + (grow * nsb + sb) * 210;
   uint8_t* o = blob + (size_t)ts * Q6K_BLOB;
-  for (int i = 0; i < 128; ++i) o[(i >> 4) * 2048 + r * 16 + (i & 15)] = valid ? b[i] : 0;
-  for (int i = 0; i < 64; ++i) o[16384 + (i >> 4) * 2048 + r * 16 + (i & 15)] = valid ? b[128 + i] : 0;
-  for (int i = 0; i < 16; ++i) o[24576 + r * 16 + i] = valid ? b[192 + i] : 0;
+  const uint8_t z = 0;
+  for (int i = 0; i < 128; ++i) STB(bd, 1, o + (i >> 4) * 2048 + r * 16 + (i & 15), valid ? LDB(bd, 0, b + i, z) : z);
+  for (int i = 0; i < 64; ++i)
+    STB(bd, 1, o + 16384 + (i >> 4) * 2048 + r * 16 + (i & 15), valid ? LDB(bd, 0, b + 128 + i, z) : z);
+  for (int i = 0; i < 16; ++i) STB(bd, 1, o + 24576 + r * 16 + i, valid ? LDB(bd, 0, b + 192 + i, z) : z);
   uint8_t* d = dd + (size_t)ts * Q6K_DD + r * 2;
-  d[0] = valid ? b[208] : 0;
-  d[1] = valid ? b[209] : 0;
+  STB(bd, 2, d, valid ? LDB(bd, 0, b + 208, z) : z);
+  STB(bd, 2, d + 1, valid ? LDB(bd, 0, b + 209, z) : z);
 }
 
 struct Packed {
@@ -227,9 +276,10 @@ static Packed packed_sizes(int type, int64_t n, int64_t k) {
 // Q8_K activation quantization (+ optional RMSNorm), writing the plain arrays and/or the
 // tensor-core operand planes.
 // ---------------------------------------------------------------------------------------------
+// Spans (bounds-checked build): 0 x, 1 norm_w; the outputs carry their own (QuantOut::bd).
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restrict__ x, int rows, int64_t k,
                                                            int64_t ldx, const float* __restrict__ norm_w, float eps,
-                                                           QuantOut o) {
+                                                           QuantOut o, Bounds bd) {
   __shared__ float red[8];
   griddep_wait();
   const int row = blockIdx.x;
@@ -247,8 +297,9 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
   float rstd = 1.f;
   if (norm_w) {
     float ss = 0.f;
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int64_t i = threadIdx.x * 4; i < k; i += blockDim.x * 4) {
-      const float4 v = *reinterpret_cast<const float4*>(xr + i);
+      const float4 v = LDB(bd, 0, reinterpret_cast<const float4*>(xr + i), z4);
       ss = fmaf(v.x, v.x, ss);
       ss = fmaf(v.y, v.y, ss);
       ss = fmaf(v.z, v.z, ss);
@@ -259,12 +310,13 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
   }
   for (int sb = sbw; sb < nsb; sb += sbstep) {
     const int64_t base = (int64_t)sb * QK + 8 * lane;
-    const float4 a = *reinterpret_cast<const float4*>(xr + base);
-    const float4 b = *reinterpret_cast<const float4*>(xr + base + 4);
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 a = LDB(bd, 0, reinterpret_cast<const float4*>(xr + base), z4);
+    const float4 b = LDB(bd, 0, reinterpret_cast<const float4*>(xr + base + 4), z4);
     float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     if (norm_w) {
-      const float4 wa = *reinterpret_cast<const float4*>(norm_w + base);
-      const float4 wb = *reinterpret_cast<const float4*>(norm_w + base + 4);
+      const float4 wa = LDB(bd, 1, reinterpret_cast<const float4*>(norm_w + base), z4);
+      const float4 wb = LDB(bd, 1, reinterpret_cast<const float4*>(norm_w + base + 4), z4);
       const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = (v[i] * rstd) * w[i];
@@ -277,9 +329,10 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float* __restri
 // Plain Q8_K arrays -> the operand form: warp (blockIdx.y * 8 + w) of row blockIdx.x copies
 // super-block sb (lane = codes 8*lane .. 8*lane+7); padding rows are written as zeros. Each lane
 // pair checks that its group's 16-sum matches the codes and records ERR_BSUM if not.
+// Spans (bounds-checked build): 0 q, 1 d, 2 bsum.
 __global__ void __launch_bounds__(256) pack_act_kernel(const int8_t* __restrict__ q, const float* __restrict__ d,
                                                        const int16_t* __restrict__ bsum, int rows, int64_t k,
-                                                       QuantOut o, int* err) {
+                                                       QuantOut o, int* err, Bounds bd) {
   griddep_wait();
   griddep_launch();
   const int row = blockIdx.x;
@@ -290,14 +343,15 @@ __global__ void __launch_bounds__(256) pack_act_kernel(const int8_t* __restrict_
   int s16 = 0;
   float dsc = 0.f;
   if (row < rows) {
-    const uint2 w = *reinterpret_cast<const uint2*>(q + (int64_t)row * k + (int64_t)sb * QK + 8 * lane);
+    const uint2 w = LDB(bd, 0, reinterpret_cast<const uint2*>(q + (int64_t)row * k + (int64_t)sb * QK + 8 * lane),
+                        make_uint2(0u, 0u));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       qi[i] = (int)(int8_t)(w.x >> (8 * i));
       qi[4 + i] = (int)(int8_t)(w.y >> (8 * i));
     }
-    s16 = bsum[(int64_t)row * (k / 16) + (int64_t)sb * 16 + (lane >> 1)];
-    dsc = d[(int64_t)row * nsb + sb];
+    s16 = LDB(bd, 2, bsum + (int64_t)row * (k / 16) + (int64_t)sb * 16 + (lane >> 1), (int16_t)0);
+    dsc = LDB(bd, 1, d + (int64_t)row * nsb + sb, 0.f);
     int s8 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) s8 += qi[i];
@@ -311,15 +365,16 @@ __global__ void __launch_bounds__(256) pack_act_kernel(const int8_t* __restrict_
 }
 
 // y (+)= sum of split partials, fixed order.
+// Spans (bounds-checked build): 0 P, 1 y.
 __global__ void reduce_splits_kernel(const float* __restrict__ P, int splits, int64_t stride, int m, int n,
-                                     float* __restrict__ y, int64_t ldy, int accumulate) {
+                                     float* __restrict__ y, int64_t ldy, int accumulate, Bounds bd) {
   const int64_t total = (int64_t)m * n;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / n, c = i % n;
     float s = 0.f;
-    for (int sp = 0; sp < splits; ++sp) s += P[sp * stride + i];
+    for (int sp = 0; sp < splits; ++sp) s += LDB(bd, 0, P + sp * stride + i, 0.f);
     float* o = y + r * ldy + c;
-    *o = accumulate ? *o + s : s;
+    STB(bd, 1, o, accumulate ? LDB(bd, 1, (const float*)o, 0.f) + s : s);
   }
 }
 
@@ -338,6 +393,12 @@ __global__ void selftest_timeout_kernel(long long limit) {
     if (!mbar_wait(b, 0, &abort_flag, limit)) atomicOr(&g_err_word, ERR_TIMEOUT_SELFTEST);
     mbar_arrive(b);  // complete the phase so the barrier is left consistent
   }
+}
+
+// buf[i] = i for i < n, each store checked against span 0 (dllm_selftest_bounds).
+__global__ void selftest_bounds_kernel(float* buf, int n, Bounds bd) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) STB(bd, 0, buf + i, (float)i);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -385,12 +446,15 @@ __device__ __forceinline__ SampPart samp_merge(SampPart x, SampPart y) {
 // (pent holds the t partials; unused for kind 0). With sampling (pscore non-null) the row's
 // token is the Gumbel-max draw instead of the argmax, and kind 0 is its probability
 // exp(l_draw - l_max) / s.
+// Spans (bounds-checked build), in LmSpan order.
+enum LmSpan : int { LS_PMAX = 0, LS_PARG, LS_PSUM, LS_PENT, LS_PSCORE, LS_PIDX, LS_PLOGIT, LS_CANVAS, LS_OPOS, LS_OID,
+                    LS_OCONF, LS_RID, LS_RCONF, LS_CONF, LS_ID, LS_DONE };
 __global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
     const float* __restrict__ pmax, const int* __restrict__ parg, const float* __restrict__ psum,
     const float* __restrict__ pent, const float* __restrict__ pscore, const int* __restrict__ pidx,
     const float* __restrict__ plogit, int kind, int P, int R, int32_t* canvas, int32_t mask_id, int b0, int k,
     int32_t* out_pos, int32_t* out_id, float* out_conf, int32_t* row_id, float* row_conf, float* conf_ws, int* id_ws,
-    unsigned int* done) {
+    unsigned int* done, Bounds bd) {
   __shared__ SoftPart red[8];
   __shared__ SampPart sred[8];
   __shared__ bool last;
@@ -402,8 +466,12 @@ __global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
   const bool sample = pscore != nullptr;
   const size_t base = (size_t)r * P;
   for (int i = threadIdx.x; i < P; i += blockDim.x) {
-    acc = soft_merge(acc, SoftPart{pmax[base + i], parg[base + i], psum[base + i], kind ? pent[base + i] : 0.f});
-    if (sample) sacc = samp_merge(sacc, SampPart{pscore[base + i], pidx[base + i], plogit[base + i]});
+    acc = soft_merge(acc, SoftPart{LDB(bd, LS_PMAX, pmax + base + i, -INFINITY), LDB(bd, LS_PARG, parg + base + i, 0),
+                                   LDB(bd, LS_PSUM, psum + base + i, 0.f),
+                                   kind ? LDB(bd, LS_PENT, pent + base + i, 0.f) : 0.f});
+    if (sample)
+      sacc = samp_merge(sacc, SampPart{LDB(bd, LS_PSCORE, pscore + base + i, -INFINITY),
+                                       LDB(bd, LS_PIDX, pidx + base + i, 0), LDB(bd, LS_PLOGIT, plogit + base + i, 0.f)});
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -426,12 +494,12 @@ __global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
     }
     if (sample) acc.a = sacc.a;  // the committed token is the draw
     const float c = kind ? acc.t / acc.s - logf(acc.s) : (sample ? expf(sacc.l - acc.m) : 1.0f) / acc.s;
-    conf_ws[r] = c;
-    id_ws[r] = acc.a;
-    if (row_id) row_id[r] = acc.a;
-    if (row_conf) row_conf[r] = c;
+    STB(bd, LS_CONF, conf_ws + r, c);
+    STB(bd, LS_ID, id_ws + r, acc.a);
+    if (row_id) STB(bd, LS_RID, row_id + r, acc.a);
+    if (row_conf) STB(bd, LS_RCONF, row_conf + r, c);
     __threadfence();
-    last = atomicAdd(done, 1u) == (unsigned)(R - 1);
+    last = BOK(bd, LS_DONE, done, 4) && atomicAdd(done, 1u) == (unsigned)(R - 1);
   }
   __syncthreads();
   if (!last || warp != 0) return;
@@ -441,10 +509,11 @@ __global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
     int bp = 0x7fffffff;
     for (int q = lane; q < R; q += 32) {
       const volatile float* cv = conf_ws;
-      const float cq = cv[q];
-      if (canvas[b0 + q] == mask_id && (cq > best || (cq == best && q < bp))) {
+      const float cq = BOK(bd, LS_CONF, cv + q, 4) ? cv[q] : -INFINITY;
+      if (LDB(bd, LS_CANVAS, (const int32_t*)canvas + b0 + q, ~mask_id) == mask_id &&
+          (cq > best || (cq == best && q < bp))) {
         bool taken = false;
-        for (int s2 = 0; s2 < step; ++s2) taken |= out_pos[s2] == b0 + q;
+        for (int s2 = 0; s2 < step; ++s2) taken |= LDB(bd, LS_OPOS, (const int32_t*)out_pos + s2, -1) == b0 + q;
         if (!taken) {
           best = cq;
           bp = q;
@@ -463,21 +532,23 @@ __global__ void __launch_bounds__(256) lmhead_merge_commit_kernel(
     if (lane == 0) {
       const volatile int* iv = id_ws;
       if (bp != 0x7fffffff) {
-        out_pos[step] = b0 + bp;
-        out_id[step] = iv[bp];
-        if (out_conf) out_conf[step] = best;
+        STB(bd, LS_OPOS, out_pos + step, b0 + bp);
+        STB(bd, LS_OID, out_id + step, BOK(bd, LS_ID, iv + bp, 4) ? iv[bp] : -1);
+        if (out_conf) STB(bd, LS_OCONF, out_conf + step, best);
       } else {
-        out_pos[step] = -1;
-        out_id[step] = -1;
-        if (out_conf) out_conf[step] = 0.f;
+        STB(bd, LS_OPOS, out_pos + step, -1);
+        STB(bd, LS_OID, out_id + step, -1);
+        if (out_conf) STB(bd, LS_OCONF, out_conf + step, 0.f);
       }
     }
     __syncwarp();
     __threadfence_block();
   }
   if (lane == 0) {
-    for (int step = 0; step < k; ++step)
-      if (out_pos[step] >= 0) canvas[out_pos[step]] = out_id[step];
+    for (int step = 0; step < k; ++step) {
+      const int32_t pos = LDB(bd, LS_OPOS, (const int32_t*)out_pos + step, -1);
+      if (pos >= 0) STB(bd, LS_CANVAS, canvas + pos, LDB(bd, LS_OID, (const int32_t*)out_id + step, 0));
+    }
   }
 }
 
@@ -545,8 +616,10 @@ int quantize_rows(const float* x, int64_t rows, int64_t k, int64_t ldx, const fl
   uint8_t* base = static_cast<uint8_t*>(act);
   QuantOut o{nullptr, nullptr, nullptr, reinterpret_cast<__half*>(base + L.off_a), base + L.off_j,
              reinterpret_cast<float*>(base + L.off_d), (int)L.lpad};
+  set_quant_bounds(o, rows, k);
   const dim3 grid((unsigned)L.lpad, norm_w ? 1u : (unsigned)((k / QK + 7) / 8));
-  cudaError_t e = launch_pdl(quantize_act_kernel, grid, dim3(256), 0, stream, x, (int)rows, k, ldx, norm_w, eps, o);
+  cudaError_t e = launch_pdl(quantize_act_kernel, grid, dim3(256), 0, stream, x, (int)rows, k, ldx, norm_w, eps, o,
+                             make_bounds({{x, strided_bytes(rows, k, ldx, 4)}, {norm_w, (size_t)k * 4}}));
   note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch quantize_act");
@@ -570,6 +643,19 @@ DLLM_API int dllm_check(dllm_stream_t stream) {
   if (w) {
     int z = 0;
     cudaMemcpyToSymbol(g_err_word, &z, sizeof(int));
+    if (w & ERR_BOUNDS) {
+      int site = 0;
+      cudaMemcpyFromSymbol(&site, g_bounds_site, sizeof(int));
+      cudaMemcpyToSymbol(g_bounds_site, &z, sizeof(int));
+      static const char* const files[] = {"?", "api.cu", "layer.cu", "noalloc.cu", "peak.cu", "?", "?", "?", "?",
+                                          "qgemm.cuh", "quant.cuh"};
+      const int f = site / 100000;
+      return fail(DLLM_E_BOUNDS,
+                  "bounds-checked build: a kernel access outside its buffer was skipped (first at %s:%d); the "
+                  "outputs of that launch are not valid%s",
+                  f >= 0 && f <= 10 ? files[f] : "?", site % 100000,
+                  (w & ~ERR_BOUNDS) ? " (other error bits were set too; a skipped copy can make waits run out)" : "");
+    }
     if ((w & ~(ERR_RANGE | ERR_BSUM)) == 0)
       return fail(DLLM_E_INVAL, "%s%s",
                   (w & ERR_RANGE) ? "a Q4_K super-block has |dmin / d| above 4e6: its min term cannot be folded into "
@@ -618,10 +704,11 @@ DLLM_API int dllm_pack_weights(int type, const void* blocks, int64_t n, int64_t 
   uint8_t* blob = static_cast<uint8_t*>(packed);
   uint8_t* dd = blob + ps.blob_bytes;
   const uint8_t* src = static_cast<const uint8_t*>(blocks);
+  const Bounds bd = make_bounds({{src, (size_t)n * nsb * block_bytes(type)}, {blob, ps.blob_bytes}, {dd, ps.dd_bytes}});
   if (type == DLLM_Q4_K)
-    pack_q4k_kernel<<<tiles * nsb, BM, 0, (cudaStream_t)stream>>>(src, (int)n, nsb, blob, dd);
+    pack_q4k_kernel<<<tiles * nsb, BM, 0, (cudaStream_t)stream>>>(src, (int)n, nsb, blob, dd, bd);
   else
-    pack_q6k_kernel<<<tiles * nsb, BM, 0, (cudaStream_t)stream>>>(src, (int)n, nsb, blob, dd);
+    pack_q6k_kernel<<<tiles * nsb, BM, 0, (cudaStream_t)stream>>>(src, (int)n, nsb, blob, dd, bd);
   note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch pack kernel");
@@ -670,7 +757,9 @@ DLLM_API int dllm_quantize_act(const float* x, int64_t rows, int64_t k, int64_t 
     o.lpad = (int)L.lpad;
     grid = (int)L.lpad;
   }
-  quantize_act_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(x, (int)rows, k, ldx, norm_w, eps, o);
+  set_quant_bounds(o, rows, k);
+  quantize_act_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
+      x, (int)rows, k, ldx, norm_w, eps, o, make_bounds({{x, strided_bytes(rows, k, ldx, 4)}, {norm_w, (size_t)k * 4}}));
   note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch quantize_act");
@@ -734,6 +823,23 @@ int launch_gemm(const GemmLaunch& g, const QgemmPlan& P, cudaStream_t stream) {
   prm.timeout = kDefaultTimeoutCycles;
   prm.err = err_word();
   if (!prm.err) return fail(DLLM_E_CUDA, "cannot resolve the device error word");
+  {
+    const size_t ys = P.splits > 1 ? (size_t)P.splits * g.m * g.n * 4 : strided_bytes(g.m, g.n, g.ldy, 4);
+    const size_t pb = (size_t)g.m * P.tiles_n * 4 * 4;  // LM-head partials: [m][tiles_n * 4]
+    prm.bd = make_bounds({{prm.wblob, ps.blob_bytes},
+                          {prm.wdd, ps.dd_bytes},
+                          {prm.act_j, (size_t)P.nsb * L.lpad * 32},
+                          {prm.act_d, (size_t)P.nsb * L.lpad * 4},
+                          {prm.y, ys},
+                          {g.dbg, (size_t)P.nsb * g.m * g.n * 4},
+                          {g.pmax, pb},
+                          {g.parg, pb},
+                          {g.psum, pb},
+                          {g.pent, pb},
+                          {g.pscore, pb},
+                          {g.pidx, pb},
+                          {g.plogit, pb}});
+  }
   return g.type == DLLM_Q4_K ? launch_qgemm_q4k(P.nt, map, prm, P.grid, stream)
                              : launch_qgemm_q6k(P.nt, map, prm, P.grid, stream);
 }
@@ -798,7 +904,9 @@ int launch_reduce_splits(const float* P, int splits, int64_t stride, int64_t m, 
                          int accumulate, cudaStream_t stream) {
   const int64_t total = m * n;
   const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4 * num_sms());
-  reduce_splits_kernel<<<blocks, 256, 0, stream>>>(P, splits, stride, (int)m, (int)n, y, ldy, accumulate);
+  reduce_splits_kernel<<<blocks, 256, 0, stream>>>(
+      P, splits, stride, (int)m, (int)n, y, ldy, accumulate,
+      make_bounds({{P, (size_t)splits * stride * 4}, {y, strided_bytes(m, n, ldy, 4)}}));
   note_launch();
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch reduce_splits");
@@ -840,9 +948,13 @@ DLLM_API int dllm_pack_act(const int8_t* q, const float* d, const int16_t* bsum,
   uint8_t* base = static_cast<uint8_t*>(act);
   QuantOut o{nullptr, nullptr, nullptr, reinterpret_cast<__half*>(base + L.off_a), base + L.off_j,
              reinterpret_cast<float*>(base + L.off_d), (int)L.lpad};
+  set_quant_bounds(o, rows, k);
   const dim3 grid((unsigned)L.lpad, (unsigned)((k / QK + 7) / 8));
   cudaError_t e = launch_pdl(pack_act_kernel, grid, dim3(256), 0, (cudaStream_t)stream, q, d, bsum, (int)rows, k, o,
-                             err);
+                             err,
+                             make_bounds({{q, (size_t)(rows * k)},
+                                          {d, (size_t)(rows * (k / QK) * 4)},
+                                          {bsum, (size_t)(rows * (k / 16) * 2)}}));
   note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch pack_act");
@@ -902,6 +1014,27 @@ DLLM_API int dllm_qgemm_intsums(int type, const void* act, int64_t m, int64_t k,
   if (!is_device_ptr(sums)) return fail(DLLM_E_INVAL, "dllm_qgemm_intsums: sums is NULL or not a device pointer");
   return qgemm_common("dllm_qgemm_intsums", type, act, m, k, w_packed, n, nullptr, n, 0, nullptr, 0, sums,
                       (cudaStream_t)stream);
+}
+
+DLLM_API int dllm_bounds_checked(void) {
+#ifdef DLLM_BOUNDS_CHECK
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+DLLM_API int dllm_selftest_bounds(float* buf, int32_t n_write, int32_t n_declared, dllm_stream_t stream) {
+  if (n_write <= 0 || n_write > (1 << 20) || n_declared < 0 || n_declared > n_write)
+    return fail(DLLM_E_INVAL, "dllm_selftest_bounds: need 0 < n_write <= 2^20 and 0 <= n_declared <= n_write");
+  int rc = check_device();
+  if (rc) return rc;
+  CHECK_DEV(buf, "buf");
+  selftest_bounds_kernel<<<(n_write + 255) / 256, 256, 0, (cudaStream_t)stream>>>(
+      buf, n_write, make_bounds({{buf, (size_t)n_declared * 4}}));
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch selftest_bounds");
 }
 
 DLLM_API int dllm_selftest_timeout(int64_t limit_cycles, dllm_stream_t stream) {
@@ -996,7 +1129,23 @@ DLLM_API int dllm_lmhead_select(const float* hidden, int64_t L, int64_t d, int64
                  reinterpret_cast<const float*>(base + W.psum), reinterpret_cast<const float*>(base + W.pent),
                  g.pscore, g.pidx, g.plogit, (int)conf_kind, W.P, (int)R, canvas, mask_id, (int)block_begin,
                  (int)k_commit, out_pos, out_id, out_conf, row_id, row_conf, reinterpret_cast<float*>(base + W.conf),
-                 reinterpret_cast<int*>(base + W.id), done);
+                 reinterpret_cast<int*>(base + W.id), done,
+                 make_bounds({{base + W.pmax, (size_t)W.P * R * 4},
+                              {base + W.parg, (size_t)W.P * R * 4},
+                              {base + W.psum, (size_t)W.P * R * 4},
+                              {base + W.pent, (size_t)W.P * R * 4},
+                              {g.pscore, (size_t)W.P * R * 4},
+                              {g.pidx, (size_t)W.P * R * 4},
+                              {g.plogit, (size_t)W.P * R * 4},
+                              {canvas, (size_t)L * 4},
+                              {out_pos, (size_t)k_commit * 4},
+                              {out_id, (size_t)k_commit * 4},
+                              {out_conf, (size_t)k_commit * 4},
+                              {row_id, (size_t)R * 4},
+                              {row_conf, (size_t)R * 4},
+                              {base + W.conf, (size_t)R * 4},
+                              {base + W.id, (size_t)R * 4},
+                              {done, 4}}));
   note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? DLLM_OK : cuda_fail(e, "launch lmhead_merge_commit");

@@ -6,8 +6,10 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include <cstdint>
+#include <initializer_list>
 #include <string>
 
+#include "bounds.cuh"
 #include "dllm.h"
 
 namespace dllm {
@@ -32,6 +34,21 @@ int cuda_fail(cudaError_t e, const char* what);
 int num_sms();
 int check_device();  // DLLM_OK if the current device is sm_103
 int* err_word();     // device address of the current device's error word (nullptr on failure)
+int* site_word();    // device address of the first failing bounds-check site (checked build)
+
+// One buffer of a launch for the bounds-checked build: `bytes` bytes from p (a null p is an
+// empty span). make_bounds lays the spans out in order (span i = the i-th); in the regular
+// build it returns the empty Bounds and the spans are not used.
+struct Span {
+  const void* p;
+  size_t bytes;
+};
+Bounds make_bounds(std::initializer_list<Span> spans);
+// Bytes covered by `rows` rows of `cols` elements of `esize` bytes with a row stride of `ld`
+// elements: the extent of a strided matrix (0 when empty).
+inline size_t strided_bytes(int64_t rows, int64_t cols, int64_t ld, size_t esize) {
+  return rows <= 0 || cols <= 0 ? 0 : ((size_t)(rows - 1) * (size_t)ld + (size_t)cols) * esize;
+}
 
 // Activation operand layout ("act" buffer of dllm_quantize_act).
 struct ActLayout {

@@ -13,12 +13,15 @@
 #include "qgemm.cuh"
 #include "quant.cuh"
 
+#define DLLM_FILE 2  // bounds-check sites of this file
+
 namespace dllm {
 
 // ---------------------------------------------------------------------------------------------
 // RoPE table: cs[p][i] = (cos, sin) of p * theta^(-2i/hd), computed in f64 once per step.
 // ---------------------------------------------------------------------------------------------
-__global__ void rope_table_kernel(float2* cs, int L, int half, double theta, int hd) {
+// Span (bounds-checked build): 0 cs.
+__global__ void rope_table_kernel(float2* cs, int L, int half, double theta, int hd, Bounds bd) {
   griddep_wait();
   griddep_launch();
   const int p = blockIdx.x, i = threadIdx.x;
@@ -26,20 +29,22 @@ __global__ void rope_table_kernel(float2* cs, int L, int half, double theta, int
     const double ang = (double)p * pow(theta, -2.0 * (double)i / (double)hd);
     double s, c;
     sincos(ang, &s, &c);
-    cs[p * half + i] = make_float2((float)c, (float)s);
+    STB(bd, 0, cs + p * half + i, make_float2((float)c, (float)s));
   }
 }
 
 // Token embedding: x[p] = decoded Q4_K row ids[p] of the GGUF table (AoS blocks), f32.
 // w = d * scale * q - dmin * min is formed with one fused multiply-add.
+// Spans (bounds-checked build): 0 the table, 1 ids, 2 x.
 __global__ void embed_q4k_kernel(const uint8_t* __restrict__ table, int nsb, const int32_t* __restrict__ ids,
-                                 float* __restrict__ x, int d) {
+                                 float* __restrict__ x, int d, Bounds bd) {
   griddep_wait();
   griddep_launch();
   const int p = blockIdx.x;
-  const int64_t row = ids[p];
+  const int64_t row = LDB(bd, 1, ids + p, 0);
   for (int k = threadIdx.x; k < d; k += blockDim.x) {
     const uint8_t* blk = table + (row * nsb + k / QK) * 144;
+    if (!BOK(bd, 0, blk, 144)) continue;
     const int i = k % QK, j = i / 32;
     const uint8_t* sc = blk + 4;
     int scale, mn;
@@ -54,7 +59,7 @@ __global__ void embed_q4k_kernel(const uint8_t* __restrict__ table, int nsb, con
     const int q = ((i % 64) < 32) ? (b & 15) : (b >> 4);
     const float dd = __half2float(*reinterpret_cast<const __half*>(blk));
     const float dm = __half2float(*reinterpret_cast<const __half*>(blk + 2));
-    x[(int64_t)p * d + k] = fmaf(dd, (float)(scale * q), -dm * (float)mn);
+    STB(bd, 2, x + (int64_t)p * d + k, fmaf(dd, (float)(scale * q), -dm * (float)mn));
   }
 }
 
@@ -77,7 +82,8 @@ __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __res
                                                               const float2* __restrict__ cs, int L, int d, int hd,
                                                               float qscale, float* __restrict__ QKV,
                                                               __half* __restrict__ planes, int pos0,
-                                                              float* __restrict__ kcache, float* __restrict__ vcache) {
+                                                              float* __restrict__ kcache, float* __restrict__ vcache,
+                                                              Bounds bd) {
   griddep_wait();
   griddep_launch();
   // one thread per 4 consecutive columns (two RoPE pairs): 16-byte partial loads
@@ -91,14 +97,14 @@ __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __res
     const int64_t st = (int64_t)L * 2 * d;
 #pragma unroll 4
     for (int sp = 0; sp < Sqk; ++sp) {
-      const float4 v = *reinterpret_cast<const float4*>(src + sp * st);
+      const float4 v = LDB(bd, 0, reinterpret_cast<const float4*>(src + sp * st), make_float4(0.f, 0.f, 0.f, 0.f));
       a.x += v.x;
       a.y += v.y;
       a.z += v.z;
       a.w += v.w;
     }
     const int64_t rp = (int64_t)(pos0 + p) * (hd / 2) + (c % hd) / 2;
-    const float2 r0 = cs[rp], r1 = cs[rp + 1];
+    const float2 r0 = LDB(bd, 2, cs + rp, make_float2(1.f, 0.f)), r1 = LDB(bd, 2, cs + rp + 1, make_float2(1.f, 0.f));
     const float sc = c < d ? qscale : 1.f;
     a = make_float4((a.x * r0.x - a.y * r0.y) * sc, (a.x * r0.y + a.y * r0.x) * sc, (a.z * r1.x - a.w * r1.y) * sc,
                     (a.z * r1.y + a.w * r1.x) * sc);
@@ -107,7 +113,7 @@ __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __res
     const int64_t st = (int64_t)L * d;
 #pragma unroll 4
     for (int sp = 0; sp < Sv; ++sp) {
-      const float4 v = *reinterpret_cast<const float4*>(src + sp * st);
+      const float4 v = LDB(bd, 1, reinterpret_cast<const float4*>(src + sp * st), make_float4(0.f, 0.f, 0.f, 0.f));
       a.x += v.x;
       a.y += v.y;
       a.z += v.z;
@@ -116,17 +122,17 @@ __global__ void __launch_bounds__(256) qkv_reduce_rope_kernel(const float* __res
   }
   if (kcache && c >= d) {
     float* dst = (c < 2 * d ? kcache : vcache) + (int64_t)(pos0 + p) * d + (c % d);
-    *reinterpret_cast<float4*>(dst) = a;
+    STB(bd, c < 2 * d ? 4 : 5, reinterpret_cast<float4*>(dst), a);
   }
   if (planes) {
     const int which = c / d, col = c % d;
     uint32_t h0, l0, h1, l1;
     split2(a.x, a.y, h0, l0);
     split2(a.z, a.w, h1, l1);
-    *reinterpret_cast<uint2*>(planes + ((int64_t)(2 * which) * L + p) * d + col) = make_uint2(h0, h1);
-    *reinterpret_cast<uint2*>(planes + ((int64_t)(2 * which + 1) * L + p) * d + col) = make_uint2(l0, l1);
+    STB(bd, 3, reinterpret_cast<uint2*>(planes + ((int64_t)(2 * which) * L + p) * d + col), make_uint2(h0, h1));
+    STB(bd, 3, reinterpret_cast<uint2*>(planes + ((int64_t)(2 * which + 1) * L + p) * d + col), make_uint2(l0, l1));
   } else {
-    *reinterpret_cast<float4*>(QKV + (int64_t)p * 3 * d + c) = a;
+    STB(bd, 3, reinterpret_cast<float4*>(QKV + (int64_t)p * 3 * d + c), a);
   }
 }
 
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
                                                                        const float* __restrict__ Km,
                                                                        const float* __restrict__ Vm, int64_t ldkv,
                                                                        AttPart part, int Lq, int Lk, int d,
-                                                                       int heads) {
+                                                                       int heads, Bounds bd) {
   extern __shared__ float4 att_smem4[];
   float* Ks = reinterpret_cast<float*>(att_smem4);  // [KC][KP]
   float* Vs = Ks + ATT_KC * ATT_KP;                 // [KC][HD]
@@ -175,15 +181,16 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
 #pragma unroll
     for (int r = 0; r < RQ; ++r) {
       const int i = threadIdx.x + ATT_THREADS * r, p = q0 + i / HV;
-      qv[r] = p < Lq ? *reinterpret_cast<const float4*>(Qm + p * ldq + h * ATT_HD + 4 * (i % HV))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      qv[r] = p < Lq ? LDB(bd, 0, reinterpret_cast<const float4*>(Qm + p * ldq + h * ATT_HD + 4 * (i % HV)), z4) : z4;
     }
 #pragma unroll
     for (int r = 0; r < RK; ++r) {
       const int i = threadIdx.x + ATT_THREADS * r, p = k0 + i / HV;
       const int64_t off = p * ldkv + h * ATT_HD + 4 * (i % HV);
-      kv[r] = p < Lk ? *reinterpret_cast<const float4*>(Km + off) : make_float4(0.f, 0.f, 0.f, 0.f);
-      vv[r] = p < Lk ? *reinterpret_cast<const float4*>(Vm + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      kv[r] = p < Lk ? LDB(bd, 1, reinterpret_cast<const float4*>(Km + off), z4) : z4;
+      vv[r] = p < Lk ? LDB(bd, 2, reinterpret_cast<const float4*>(Vm + off), z4) : z4;
     }
 #pragma unroll
     for (int r = 0; r < RQ; ++r) {
@@ -262,10 +269,11 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
   for (int qq = 0; qq < 4; ++qq) {
     const int qi = q0 + warp * 4 + qq;
     if (qi < Lq) {
-      *reinterpret_cast<float4*>(part.acc + ((int64_t)c * Lq + qi) * d + h * ATT_HD + lane * 4) =
-          make_float4(acc[qq][0], acc[qq][1], acc[qq][2], acc[qq][3]);
+      STB(bd, 3, reinterpret_cast<float4*>(part.acc + ((int64_t)c * Lq + qi) * d + h * ATT_HD + lane * 4),
+          make_float4(acc[qq][0], acc[qq][1], acc[qq][2], acc[qq][3]));
       if (lane == 0)
-        *reinterpret_cast<float2*>(part.ml + (((int64_t)c * Lq + qi) * heads + h) * 2) = make_float2(mq[qq], lq[qq]);
+        STB(bd, 4, reinterpret_cast<float2*>(part.ml + (((int64_t)c * Lq + qi) * heads + h) * 2),
+            make_float2(mq[qq], lq[qq]));
     }
   }
   griddep_launch();
@@ -311,7 +319,7 @@ constexpr int TA_COLS = 256;                          // S at columns [0, 80), O
 
 __global__ void __launch_bounds__(TA_THREADS, 1)
     attention_tc_kernel(const __grid_constant__ CUtensorMap qk_map, const __half* __restrict__ planes, AttPart part,
-                        int L, int d, int heads, int* err) {
+                        int L, int d, int heads, int* err, Bounds bd) {
   extern __shared__ uint8_t ta_raw[];
   __shared__ uint64_t ta_bar[3];
   __shared__ uint32_t ta_tmem;
@@ -369,8 +377,8 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         vh[u][e] = vl[u][e] = make_uint4(0u, 0u, 0u, 0u);
         if (i < NIT && kb + k0 + e < L) {
           const __half* src = planes + (int64_t)(kb + k0 + e) * d + h * TA_HD + 8 * nb;
-          vh[u][e] = *reinterpret_cast<const uint4*>(src + 4 * pl);
-          vl[u][e] = *reinterpret_cast<const uint4*>(src + 5 * pl);
+          vh[u][e] = LDB(bd, 0, reinterpret_cast<const uint4*>(src + 4 * pl), vh[u][e]);
+          vl[u][e] = LDB(bd, 0, reinterpret_cast<const uint4*>(src + 5 * pl), vl[u][e]);
         }
       }
     }
@@ -494,7 +502,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
     for (int e = 0; e < TA_HD / 2; e += 4)
       *reinterpret_cast<uint4*>(os + row * TA_OP + (TA_HD / 2) * ch + e) = make_uint4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
     if (ok && ch == 0 && q < L)
-      *reinterpret_cast<float2*>(part.ml + ((cofs + q) * heads + h) * 2) = make_float2(m, l);
+      STB(bd, 2, reinterpret_cast<float2*>(part.ml + ((cofs + q) * heads + h) * 2), make_float2(m, l));
     __syncthreads();
     if (ok) {
       float* dst = part.acc + (cofs + q0) * d + h * TA_HD;
@@ -502,7 +510,8 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
       for (int i = threadIdx.x; i < TA_M * (TA_HD / 4); i += TA_THREADS) {
         const int r = i / (TA_HD / 4), c4 = i % (TA_HD / 4);
         if (q0 + r < L)
-          *reinterpret_cast<float4*>(dst + (int64_t)r * d + 4 * c4) = *reinterpret_cast<const float4*>(os + r * TA_OP + 4 * c4);
+          STB(bd, 1, reinterpret_cast<float4*>(dst + (int64_t)r * d + 4 * c4),
+              *reinterpret_cast<const float4*>(os + r * TA_OP + 4 * c4));
       }
     }
   }
@@ -518,8 +527,9 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
 // Merge the key chunks of the attention and quantize the output to Q8_K in one pass: warp
 // (blockIdx.y * 8 + w) of row blockIdx.x handles super-block sb (dims 256 sb .. = two heads);
 // lane's 8 dims belong to head 2 sb + lane / 16. O = sum_c e^(m_c - M) a_c / sum_c e^(m_c - M) l_c.
+// Spans (bounds-checked build): 0 part.acc, 1 part.ml; the output carries its own.
 __global__ void __launch_bounds__(256) attn_merge_quant_kernel(AttPart part, int nchunk, int L, int d, int heads,
-                                                               QuantOut o, WPrefetch pf) {
+                                                               QuantOut o, WPrefetch pf, Bounds bd) {
   if (threadIdx.x == 0 && blockIdx.y == 0) prefetch_weights(pf);
   griddep_wait();
   griddep_launch();
@@ -531,15 +541,18 @@ __global__ void __launch_bounds__(256) attn_merge_quant_kernel(AttPart part, int
   if (row < L) {
     const int dim = sb * QK + 8 * lane, h = dim / ATT_HD;
     float M = -INFINITY;
-    for (int c = 0; c < nchunk; ++c) M = fmaxf(M, part.ml[(((int64_t)c * L + row) * heads + h) * 2]);
+    for (int c = 0; c < nchunk; ++c)
+      M = fmaxf(M, LDB(bd, 1, (const float*)part.ml + (((int64_t)c * L + row) * heads + h) * 2, -INFINITY));
     float den = 0.f;
     for (int c = 0; c < nchunk; ++c) {
-      const float2 ml = *reinterpret_cast<const float2*>(part.ml + (((int64_t)c * L + row) * heads + h) * 2);
+      const float2 ml = LDB(bd, 1, reinterpret_cast<const float2*>(part.ml + (((int64_t)c * L + row) * heads + h) * 2),
+                            make_float2(-INFINITY, 0.f));
       const float w = expf(ml.x - M);
       den = fmaf(w, ml.y, den);
       const float* ac = part.acc + ((int64_t)c * L + row) * d + dim;
-      const float4 a0 = *reinterpret_cast<const float4*>(ac);
-      const float4 a1 = *reinterpret_cast<const float4*>(ac + 4);
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 a0 = LDB(bd, 0, reinterpret_cast<const float4*>(ac), z4);
+      const float4 a1 = LDB(bd, 0, reinterpret_cast<const float4*>(ac + 4), z4);
       v[0] = fmaf(w, a0.x, v[0]); v[1] = fmaf(w, a0.y, v[1]); v[2] = fmaf(w, a0.z, v[2]); v[3] = fmaf(w, a0.w, v[3]);
       v[4] = fmaf(w, a1.x, v[4]); v[5] = fmaf(w, a1.y, v[5]); v[6] = fmaf(w, a1.z, v[6]); v[7] = fmaf(w, a1.w, v[7]);
     }
@@ -569,6 +582,7 @@ struct RowArgs {
   int rows, k;
   QuantOut o;
   WPrefetch pf0, pf1;  // the next GEMMs' first weights, prefetched into L2 (optional)
+  Bounds bd;           // bounds-checked build: spans 0 x, 1 P, 2 norm_w
 };
 
 // Residual modes (RESID_NORM_QUANT, RESID_ONLY): one CTA per row, warp w holding super-blocks
@@ -604,17 +618,18 @@ __global__ void __launch_bounds__(RR_WARPS * 32) row_resid_kernel(RowArgs a) {
     const int sb = warp + j * nwarp;
     if (sb < nsb) {
       const int base = sb * QK + 8 * lane;
-      float4 x0 = *reinterpret_cast<const float4*>(xr + base);
-      float4 x1 = *reinterpret_cast<const float4*>(xr + base + 4);
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 x0 = LDB(a.bd, 0, reinterpret_cast<const float4*>(xr + base), z4);
+      float4 x1 = LDB(a.bd, 0, reinterpret_cast<const float4*>(xr + base + 4), z4);
 #pragma unroll 4
       for (int sp = 0; sp < a.S; ++sp) {
-        const float4 p0 = *reinterpret_cast<const float4*>(Pr + sp * a.pstride + base);
-        const float4 p1 = *reinterpret_cast<const float4*>(Pr + sp * a.pstride + base + 4);
+        const float4 p0 = LDB(a.bd, 1, reinterpret_cast<const float4*>(Pr + sp * a.pstride + base), z4);
+        const float4 p1 = LDB(a.bd, 1, reinterpret_cast<const float4*>(Pr + sp * a.pstride + base + 4), z4);
         x0.x += p0.x; x0.y += p0.y; x0.z += p0.z; x0.w += p0.w;
         x1.x += p1.x; x1.y += p1.y; x1.z += p1.z; x1.w += p1.w;
       }
-      *reinterpret_cast<float4*>(xr + base) = x0;
-      *reinterpret_cast<float4*>(xr + base + 4) = x1;
+      STB(a.bd, 0, reinterpret_cast<float4*>(xr + base), x0);
+      STB(a.bd, 0, reinterpret_cast<float4*>(xr + base + 4), x1);
       v[j][0] = x0.x; v[j][1] = x0.y; v[j][2] = x0.z; v[j][3] = x0.w;
       v[j][4] = x1.x; v[j][5] = x1.y; v[j][6] = x1.z; v[j][7] = x1.w;
 #pragma unroll
@@ -634,8 +649,9 @@ __global__ void __launch_bounds__(RR_WARPS * 32) row_resid_kernel(RowArgs a) {
     const int sb = warp + j * nwarp;
     if (sb < nsb) {
       const int base = sb * QK + 8 * lane;
-      const float4 w0 = *reinterpret_cast<const float4*>(a.norm_w + base);
-      const float4 w1 = *reinterpret_cast<const float4*>(a.norm_w + base + 4);
+      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 w0 = LDB(a.bd, 2, reinterpret_cast<const float4*>(a.norm_w + base), z4);
+      const float4 w1 = LDB(a.bd, 2, reinterpret_cast<const float4*>(a.norm_w + base + 4), z4);
       const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[j][i] = v[j][i] * rstd * w[i];
@@ -664,14 +680,15 @@ __global__ void __launch_bounds__(256) row_sb_kernel(RowArgs a) {
     const float* ps = a.P + (int64_t)row * a.ldp + base;
     float u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll 4
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < a.S; ++s, ps += a.pstride) {
-      const float4 p0 = *reinterpret_cast<const float4*>(ps);
-      const float4 p1 = *reinterpret_cast<const float4*>(ps + 4);
+      const float4 p0 = LDB(a.bd, 1, reinterpret_cast<const float4*>(ps), z4);
+      const float4 p1 = LDB(a.bd, 1, reinterpret_cast<const float4*>(ps + 4), z4);
       v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
       v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
       if (MODE == ROW_SWIGLU_QUANT) {
-        const float4 q0 = *reinterpret_cast<const float4*>(ps + a.k);
-        const float4 q1 = *reinterpret_cast<const float4*>(ps + a.k + 4);
+        const float4 q0 = LDB(a.bd, 1, reinterpret_cast<const float4*>(ps + a.k), z4);
+        const float4 q1 = LDB(a.bd, 1, reinterpret_cast<const float4*>(ps + a.k + 4), z4);
         u[0] += q0.x; u[1] += q0.y; u[2] += q0.z; u[3] += q0.w;
         u[4] += q1.x; u[5] += q1.y; u[6] += q1.z; u[7] += q1.w;
       }
@@ -687,8 +704,10 @@ __global__ void __launch_bounds__(256) row_sb_kernel(RowArgs a) {
 static QuantOut quant_out(void* act, int64_t rows, int64_t k, float* vtap = nullptr) {
   ActLayout L = act_layout(rows, k);
   uint8_t* base = static_cast<uint8_t*>(act);
-  return QuantOut{nullptr, nullptr, nullptr, reinterpret_cast<__half*>(base + L.off_a), base + L.off_j,
-                  reinterpret_cast<float*>(base + L.off_d), (int)L.lpad, vtap};
+  QuantOut o{nullptr, nullptr, nullptr, reinterpret_cast<__half*>(base + L.off_a), base + L.off_j,
+             reinterpret_cast<float*>(base + L.off_d), (int)L.lpad, vtap};
+  set_quant_bounds(o, rows, k);
+  return o;
 }
 
 // The first-wave weights of a GEMM launch with plan P (see WPrefetch): as many super-blocks per
@@ -703,13 +722,15 @@ static WPrefetch wprefetch(int type, const void* w, const QgemmPlan& P) {
   f.units = std::min(P.units, P.grid);
   f.w_bytes = type == DLLM_Q4_K ? Q4K_BLOB : Q6K_BLOB;
   f.ahead = std::min(P.sbps, type == DLLM_Q4_K ? 3 : 6);
+  f.bd = make_bounds({{w, (size_t)P.tiles_n * P.nsb * f.w_bytes}});
   return f;
 }
 
 template <int MODE>
 static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, const float* w, float eps, int rows,
                    int k, void* act, cudaStream_t s, float* vtap = nullptr, WPrefetch pf0 = {}, WPrefetch pf1 = {}) {
-  RowArgs a{x, P, S, pstride, ldp, w, eps, rows, k, act ? quant_out(act, rows, k, vtap) : QuantOut{}, pf0, pf1};
+  RowArgs a{x, P, S, pstride, ldp, w, eps, rows, k, act ? quant_out(act, rows, k, vtap) : QuantOut{}, pf0, pf1,
+            make_bounds({{x, (size_t)rows * k * 4}, {P, (size_t)S * pstride * 4}, {w, (size_t)k * 4}})};
   cudaError_t e;
   if (MODE == ROW_RESID_NORM_QUANT || MODE == ROW_RESID_ONLY) {
     const int grid = MODE == ROW_RESID_ONLY ? rows : (int)act_rows_padded(rows);
@@ -726,20 +747,22 @@ static int run_row(float* x, const float* P, int S, int64_t pstride, int ldp, co
 
 // Test taps: Q, K, V of a layer as f32 [L][d] each, from the f16 head/tail planes of the
 // tensor-core attention (x = hi + lo) or from the f32 [L][3d] rows of the chunked one.
+// Spans (bounds-checked build): 0 planes, 1 QKV, 2 q, 3 k, 4 v.
 __global__ void tap_qkv_kernel(const __half* __restrict__ planes, const float* __restrict__ QKV, int L, int d,
-                               float* __restrict__ q, float* __restrict__ k, float* __restrict__ v) {
+                               float* __restrict__ q, float* __restrict__ k, float* __restrict__ v, Bounds bd) {
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (i >= (int64_t)L * 3 * d) return;
   const int which = (int)(i / ((int64_t)L * d));
   const int64_t r = i % ((int64_t)L * d), p = r / d, c = r % d;
   float val;
+  const __half hz = __float2half(0.f);
   if (planes)
-    val = __half2float(planes[(2 * which * (int64_t)L + p) * d + c]) +
-          __half2float(planes[((2 * which + 1) * (int64_t)L + p) * d + c]);
+    val = __half2float(LDB(bd, 0, planes + (2 * which * (int64_t)L + p) * d + c, hz)) +
+          __half2float(LDB(bd, 0, planes + ((2 * which + 1) * (int64_t)L + p) * d + c, hz));
   else
-    val = QKV[p * 3 * d + which * d + c];
+    val = LDB(bd, 1, QKV + p * 3 * d + which * d + c, 0.f);
   float* dst = which == 0 ? q : (which == 1 ? k : v);
-  if (dst) dst[r] = val;
+  if (dst) STB(bd, 2 + which, dst + r, val);
 }
 
 static int tap_copy(void* dst, const void* src, size_t bytes, cudaStream_t s) {
@@ -832,13 +855,16 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
   void* actd = ws + S.act_d;
   void* actf = ws + S.act_ff;
   int rc;
+  const size_t rope_bytes = (size_t)L * (hd / 2) * 8, table_bytes = (size_t)m->vocab * (d / QK) * 144;
   if (full) {
     cudaError_t e = launch_pdl(rope_table_kernel, dim3((unsigned)L), dim3(hd / 2), 0, s,
-                               reinterpret_cast<float2*>(ws + S.rope), (int)L, hd / 2, (double)m->rope_theta, hd);
+                               reinterpret_cast<float2*>(ws + S.rope), (int)L, hd / 2, (double)m->rope_theta, hd,
+                               make_bounds({{ws + S.rope, rope_bytes}}));
     note_launch();
     if (e == cudaSuccess)
       e = launch_pdl(embed_q4k_kernel, dim3((unsigned)L), dim3(256), 0, s, static_cast<const uint8_t*>(m->tok_embd),
-                     d / QK, canvas, x, d);
+                     d / QK, canvas, x, d,
+                     make_bounds({{m->tok_embd, table_bytes}, {canvas, (size_t)L * 4}, {x, (size_t)L * d * 4}}));
     note_launch();
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch embedding");
@@ -864,17 +890,26 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
       cudaError_t e = launch_pdl(qkv_reduce_rope_kernel, dim3((unsigned)((nquad + 255) / 256)), dim3(256), 0, s,
                                  (const float*)Pqk, S.qk.splits, (const float*)Pv, S.v.splits,
                                  reinterpret_cast<const float2*>(ws + S.rope), (int)L, d, hd, 1.0f / sqrtf((float)hd),
-                                 QKV, planes, 0, kc, kc ? kc + L * d : nullptr);
+                                 QKV, planes, 0, kc, kc ? kc + L * d : nullptr,
+                                 make_bounds({{Pqk, (size_t)S.qk.splits * L * 2 * d * 4},
+                                              {Pv, (size_t)S.v.splits * L * d * 4},
+                                              {ws + S.rope, rope_bytes},
+                                              {ws + S.qkv, (size_t)L * 3 * d * 4},
+                                              {kc, (size_t)L * d * 4},
+                                              {kc ? kc + L * d : nullptr, (size_t)L * d * 4}}));
       note_launch();
       if (e != cudaSuccess) return cuda_fail(e, "launch qkv reduce");
       if (tp && (tp->q || tp->k || tp->v)) {
         const int64_t n3 = L * 3 * d;
-        tap_qkv_kernel<<<(unsigned)((n3 + 255) / 256), 256, 0, s>>>(planes, tc_att ? nullptr : QKV, (int)L, d, tp->q,
-                                                                    tp->k, tp->v);
+        tap_qkv_kernel<<<(unsigned)((n3 + 255) / 256), 256, 0, s>>>(
+            planes, tc_att ? nullptr : QKV, (int)L, d, tp->q, tp->k, tp->v,
+            make_bounds({{planes, (size_t)L * 3 * d * 4}, {QKV, (size_t)L * 3 * d * 4}, {tp->q, (size_t)L * d * 4},
+                         {tp->k, (size_t)L * d * 4}, {tp->v, (size_t)L * d * 4}}));
         note_launch();
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch tap_qkv");
       }
       const AttPart ap{reinterpret_cast<float*>(ws + S.att), reinterpret_cast<float*>(ws + S.attml)};
+      const size_t att_bytes = (size_t)((L + 31) / 32) * L * d * 4, ml_bytes = (size_t)((L + 31) / 32) * L * m->n_heads * 8;
       int nchunk = 1;
       if (tc_att) {  // whole rows per CTA on the tensor cores
         int* err = err_word();
@@ -886,21 +921,25 @@ static int forward(const dllm_model* m, const int32_t* canvas, int64_t L, float*
         nchunk = (int)((L + TA_KC - 1) / TA_KC);
         const dim3 ag(m->n_heads, (unsigned)((L + TA_M - 1) / TA_M), (unsigned)nchunk);
         e = launch_pdl(attention_tc_kernel, ag, dim3(TA_THREADS), TA_SMEM, s, qk_map, (const __half*)planes, ap,
-                       (int)L, d, m->n_heads, err);
+                       (int)L, d, m->n_heads, err,
+                       make_bounds({{planes, (size_t)L * 3 * d * 4}, {ap.acc, att_bytes}, {ap.ml, ml_bytes}}));
       } else {  // longer canvases: chunks of 32 keys, merged below
         nchunk = (int)((L + ATT_KC - 1) / ATT_KC);
         e = cudaFuncSetAttribute(attention_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attention)");
         const dim3 ag(m->n_heads, (unsigned)((L + ATT_QB - 1) / ATT_QB), (unsigned)nchunk);
+        const Span qkv{QKV, (size_t)L * 3 * d * 4};
         e = launch_pdl(attention_partial_kernel, ag, dim3(ATT_THREADS), ATT_SMEM, s, (const float*)QKV,
                        (int64_t)3 * d, (const float*)(QKV + d), (const float*)(QKV + 2 * d), (int64_t)3 * d, ap,
-                       (int)L, (int)L, d, m->n_heads);
+                       (int)L, (int)L, d, m->n_heads,
+                       make_bounds({qkv, qkv, qkv, {ap.acc, att_bytes}, {ap.ml, ml_bytes}}));
       }
       note_launch();
       const dim3 mg((unsigned)act_rows_padded(L), (unsigned)((d / QK + 7) / 8));
       if (e == cudaSuccess)
         e = launch_pdl(attn_merge_quant_kernel, mg, dim3(256), 0, s, ap, nchunk, (int)L, d, m->n_heads,
-                       quant_out(actd, L, d, tp ? tp->attn : nullptr), wprefetch(DLLM_Q4_K, Ly.wo, S.o));
+                       quant_out(actd, L, d, tp ? tp->attn : nullptr), wprefetch(DLLM_Q4_K, Ly.wo, S.o),
+                       make_bounds({{ap.acc, att_bytes}, {ap.ml, ml_bytes}}));
       note_launch();
       if (e == cudaSuccess) e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "launch attention");
@@ -956,12 +995,15 @@ static int forward_block(const dllm_model* m, const int32_t* canvas, int64_t L, 
   void* actf = ws + S.act_ff;
   float* xb = x + b0 * d;
   int rc;
+  const size_t rope_bytes = (size_t)L * (hd / 2) * 8, table_bytes = (size_t)m->vocab * (d / QK) * 144;
   cudaError_t e = launch_pdl(rope_table_kernel, dim3((unsigned)L), dim3(hd / 2), 0, s,
-                             reinterpret_cast<float2*>(ws + S.rope), (int)L, hd / 2, (double)m->rope_theta, hd);
+                             reinterpret_cast<float2*>(ws + S.rope), (int)L, hd / 2, (double)m->rope_theta, hd,
+                             make_bounds({{ws + S.rope, rope_bytes}}));
   note_launch();
   if (e == cudaSuccess)
     e = launch_pdl(embed_q4k_kernel, dim3((unsigned)R), dim3(256), 0, s, static_cast<const uint8_t*>(m->tok_embd),
-                   d / QK, canvas + b0, xb, d);
+                   d / QK, canvas + b0, xb, d,
+                   make_bounds({{m->tok_embd, table_bytes}, {canvas + b0, (size_t)R * 4}, {xb, (size_t)R * d * 4}}));
   note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch embedding");
@@ -979,18 +1021,31 @@ static int forward_block(const dllm_model* m, const int32_t* canvas, int64_t L, 
     const int64_t nquad = R * (3 * d / 4);
     e = launch_pdl(qkv_reduce_rope_kernel, dim3((unsigned)((nquad + 255) / 256)), dim3(256), 0, s, (const float*)Pqk,
                    S.qk.splits, (const float*)Pv, S.v.splits, reinterpret_cast<const float2*>(ws + S.rope), (int)R, d,
-                   hd, 1.0f / sqrtf((float)hd), QKV, (__half*)nullptr, (int)b0, kc, vc);
+                   hd, 1.0f / sqrtf((float)hd), QKV, (__half*)nullptr, (int)b0, kc, vc,
+                   make_bounds({{Pqk, (size_t)S.qk.splits * R * 2 * d * 4},
+                                {Pv, (size_t)S.v.splits * R * d * 4},
+                                {ws + S.rope, rope_bytes},
+                                {QKV, (size_t)R * 3 * d * 4},
+                                {kc, (size_t)L * d * 4},
+                                {vc, (size_t)L * d * 4}}));
     note_launch();
     if (e != cudaSuccess) return cuda_fail(e, "launch qkv reduce");
     const AttPart ap{reinterpret_cast<float*>(ws + S.att), reinterpret_cast<float*>(ws + S.attml)};
+    const size_t att_bytes = (size_t)nchunk * R * d * 4, ml_bytes = (size_t)nchunk * R * m->n_heads * 8;
     const dim3 ag(m->n_heads, (unsigned)((R + ATT_QB - 1) / ATT_QB), (unsigned)nchunk);
     e = launch_pdl(attention_partial_kernel, ag, dim3(ATT_THREADS), ATT_SMEM, s, (const float*)QKV, (int64_t)3 * d,
-                   (const float*)kc, (const float*)vc, (int64_t)d, ap, (int)R, (int)L, d, m->n_heads);
+                   (const float*)kc, (const float*)vc, (int64_t)d, ap, (int)R, (int)L, d, m->n_heads,
+                   make_bounds({{QKV, (size_t)R * 3 * d * 4},
+                                {kc, (size_t)L * d * 4},
+                                {vc, (size_t)L * d * 4},
+                                {ap.acc, att_bytes},
+                                {ap.ml, ml_bytes}}));
     note_launch();
     const dim3 mg((unsigned)act_rows_padded(R), (unsigned)((d / QK + 7) / 8));
     if (e == cudaSuccess)
       e = launch_pdl(attn_merge_quant_kernel, mg, dim3(256), 0, s, ap, nchunk, (int)R, d, m->n_heads,
-                     quant_out(actd, R, d), wprefetch(DLLM_Q4_K, Ly.wo, S.o));
+                     quant_out(actd, R, d), wprefetch(DLLM_Q4_K, Ly.wo, S.o),
+                     make_bounds({{ap.acc, att_bytes}, {ap.ml, ml_bytes}}));
     note_launch();
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch attention");

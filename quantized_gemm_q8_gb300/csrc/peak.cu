@@ -5,12 +5,14 @@
 // four CTAs per SM. Work per launch: grid * 8 warps * iters * 8 mma * 2 * 16 * 8 * 32 ops.
 #include "internal.h"
 
+#define DLLM_FILE 4  // bounds-check sites of this file
+
 namespace dllm {
 namespace {
 
 constexpr int PK_WARPS = 8, PK_CHAINS = 8;
 
-__global__ void __launch_bounds__(PK_WARPS * 32) mma_i8_peak_kernel(long long iters, int* sink) {
+__global__ void __launch_bounds__(PK_WARPS * 32) mma_i8_peak_kernel(long long iters, int* sink, Bounds bd) {
   const uint32_t t = threadIdx.x * 2654435761u + blockIdx.x;
   const uint32_t a0 = t, a1 = t ^ 0x5A5A5A5Au, a2 = t * 3u, a3 = ~t, b0 = t >> 3, b1 = t * 7u;
   int acc[PK_CHAINS][4];
@@ -28,7 +30,7 @@ __global__ void __launch_bounds__(PK_WARPS * 32) mma_i8_peak_kernel(long long it
   int s = 0;
 #pragma unroll
   for (int c = 0; c < PK_CHAINS; ++c) s += acc[c][0] + acc[c][1] + acc[c][2] + acc[c][3];
-  if (s == 0x7fffffff) *sink = s;  // keeps the chains live; practically never true
+  if (s == 0x7fffffff) STB(bd, 0, sink, s);  // keeps the chains live; practically never true
 }
 
 }  // namespace
@@ -43,7 +45,8 @@ extern "C" DLLM_API int dllm_peak_mma_i8(int64_t iters, int32_t* sink, double* o
   if (rc) return rc;
   if (!device_ptr(sink)) return fail(DLLM_E_INVAL, "dllm_peak_mma_i8: sink is NULL or not a device pointer");
   const int grid = 4 * num_sms();
-  mma_i8_peak_kernel<<<grid, PK_WARPS * 32, 0, (cudaStream_t)stream>>>((long long)iters, sink);
+  mma_i8_peak_kernel<<<grid, PK_WARPS * 32, 0, (cudaStream_t)stream>>>((long long)iters, sink,
+                                                                       make_bounds({{sink, sizeof(int)}}));
   note_launch();
   if (ops_per_launch) *ops_per_launch = (double)grid * PK_WARPS * (double)iters * PK_CHAINS * 2.0 * 16 * 8 * 32;
   cudaError_t e = cudaGetLastError();

@@ -18,6 +18,7 @@ enum : int {
   ERR_TIMEOUT_OTHER = 1 << 5,
   ERR_RANGE = 1 << 6,  // a Q4_K block whose dmin/d ratio cannot be folded (|dmin/d| > 4e6)
   ERR_BSUM = 1 << 7,   // plain Q8_K input whose 16-sums do not match its codes (dllm_pack_act)
+  ERR_BOUNDS = 1 << 8, // bounds-checked build: an access outside its buffer was skipped
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

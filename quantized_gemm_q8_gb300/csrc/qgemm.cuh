@@ -62,9 +62,12 @@
 #pragma once
 #include <cuda_fp16.h>
 
+#include "bounds.cuh"
 #include "ptx.cuh"
 
 namespace dllm {
+
+#define QG_FILE 9  // bounds-check sites of this file
 
 constexpr int QK = 256;
 constexpr int BM = 128;
@@ -178,7 +181,10 @@ struct QgemmParams {
   int* pidx;
   float* plogit;
   long long timeout;
+  Bounds bd;  // bounds-checked build: one span per buffer, indexed by QgSpan
 };
+enum QgSpan : int { QS_W = 0, QS_DD, QS_AJ, QS_AD, QS_Y, QS_DBG, QS_PMAX, QS_PARG, QS_PSUM, QS_PENT, QS_PSCORE,
+                    QS_PIDX, QS_PLOGIT };
 
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
@@ -326,6 +332,7 @@ __device__ __forceinline__ float gumbel_noise(unsigned long long seed, unsigned 
 struct WPrefetch {
   const uint8_t* wblob;
   int tiles_n, tiles_m, nsb, sbps, units, w_bytes, ahead;
+  Bounds bd;  // span 0: the blob
 };
 // One thread per CTA of the prefetching kernel: units blockIdx.x, blockIdx.x + gridDim.x, ...
 // of the GEMM's first wave (units < f.units), `ahead` super-blocks each (contiguous in the
@@ -335,7 +342,8 @@ __device__ __forceinline__ void prefetch_weights(const WPrefetch& f) {
   for (int u = blockIdx.x; u < f.units; u += gridDim.x) {
     const int tn = u % f.tiles_n, sp = (u / f.tiles_n) / f.tiles_m;
     const int sb0 = sp * f.sbps, n = min(f.ahead, f.nsb - sb0);
-    if (n > 0) bulk_prefetch_l2(f.wblob + ((size_t)tn * f.nsb + sb0) * f.w_bytes, (uint32_t)(n * f.w_bytes));
+    const uint8_t* src = f.wblob + ((size_t)tn * f.nsb + sb0) * f.w_bytes;
+    if (n > 0 && BOK_AT(QG_FILE, f.bd, 0, src, (size_t)n * f.w_bytes)) bulk_prefetch_l2(src, (uint32_t)(n * f.w_bytes));
   }
 }
 
@@ -416,8 +424,12 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           if (!(ok = mbar_wait(BAR(C::BW_EMPTY + w), ((it / C::W_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
           const uint32_t ws = sbase + C::OFF_W + w * C::W_SLOT;
           mbar_expect_tx(BAR(C::BW_FULL + w), C::W_SLOT);
-          bulk_g2s(ws, blob + (size_t)sb * C::W_BYTES, C::W_BYTES, BAR(C::BW_FULL + w));
-          if (C::Q4) bulk_g2s(ws + C::W_BYTES, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES, BAR(C::BW_FULL + w));
+          // a copy outside its buffer (bounds-checked build) is not issued: its stage never
+          // fills and the waits on it run out, so the launch ends with both errors set
+          if (BOK_AT(QG_FILE, p.bd, QS_W, blob + (size_t)sb * C::W_BYTES, C::W_BYTES))
+            bulk_g2s(ws, blob + (size_t)sb * C::W_BYTES, C::W_BYTES, BAR(C::BW_FULL + w));
+          if (C::Q4 && BOK_AT(QG_FILE, p.bd, QS_DD, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES))
+            bulk_g2s(ws + C::W_BYTES, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES, BAR(C::BW_FULL + w));
         }
       }
       if (!ok) {
@@ -444,8 +456,10 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           if (!(ok = mbar_wait(BAR(C::BE_EMPTY + e), ((it / C::E_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
           const uint32_t es = sbase + C::OFF_E + e * C::E_BYTES;
           mbar_expect_tx(BAR(C::BE_FULL + e), C::E_TX);
-          bulk_g2s(es + C::E_DD, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES, BAR(C::BE_FULL + e));
-          bulk_g2s(es + C::E_DA, p.act_d + (size_t)sb * p.lpad + tok0, NT * 4, BAR(C::BE_FULL + e));
+          if (BOK_AT(QG_FILE, p.bd, QS_DD, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES))
+            bulk_g2s(es + C::E_DD, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES, BAR(C::BE_FULL + e));
+          if (BOK_AT(QG_FILE, p.bd, QS_AD, p.act_d + (size_t)sb * p.lpad + tok0, NT * 4))
+            bulk_g2s(es + C::E_DA, p.act_d + (size_t)sb * p.lpad + tok0, NT * 4, BAR(C::BE_FULL + e));
           for (int st = 0; st < C::SPS; ++st) {
             const int j = C::SPS * it + st, b = j % C::K_STAGES;
             if (!(ok = mbar_wait(BAR(C::BK_EMPTY + b), ((j / C::K_STAGES) & 1) ^ 1, abort_flag, lim, QG_SUSPEND))) break;
@@ -460,7 +474,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             for (int qq = 0; qq < C::QPS; ++qq)
               tma_g2s_3d(sbase + C::OFF_B + b * C::B_STAGE + qq * C::B_QUARTER, &tmap, 0, tok0,
                          sb * 4 + st * C::QPS + qq, BAR(C::BK_FULL + b));
-            if (jcopy)
+            if (jcopy && BOK_AT(QG_FILE, p.bd, QS_AJ, p.act_j + ((size_t)sb * p.lpad + tok0) * 32, NT * 32))
               bulk_g2s(sbase + C::OFF_J + jx * C::J_BYTES + C::J_BJ, p.act_j + ((size_t)sb * p.lpad + tok0) * 32,
                        NT * 32, BAR(C::BK_FULL + b));
           }
@@ -759,7 +773,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
                 if (tok < p.m) {
                   int32_t* dst = p.dbg + ((size_t)sbp * p.m + tok) * p.n + grow;
                   const int32_t v = (int32_t)(sgn * __uint_as_float(r[c][jj]));
-                  *dst = p.dbg_mode == 3 ? *dst + v : v;
+                  if (BOK_AT(QG_FILE, p.bd, QS_DBG, dst, 4)) *dst = p.dbg_mode == 3 ? *dst + v : v;
                 }
               }
             }
@@ -817,17 +831,17 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
             }
             if (lane == 0 && tok < p.m) {
               const size_t o = (size_t)tok * (p.tiles_n * 4) + tn * 4 + qd;
-              p.pscore[o] = sc;
-              p.pidx[o] = si;
-              p.plogit[o] = sl;
+              STB_AT(QG_FILE, p.bd, QS_PSCORE, p.pscore + o, sc);
+              STB_AT(QG_FILE, p.bd, QS_PIDX, p.pidx + o, si);
+              STB_AT(QG_FILE, p.bd, QS_PLOGIT, p.plogit + o, sl);
             }
           }
           if (lane == 0 && tok < p.m) {
             const size_t o = (size_t)tok * (p.tiles_n * 4) + tn * 4 + qd;
-            p.pmax[o] = v;
-            p.parg[o] = idx;
-            p.psum[o] = ex;
-            if (p.pent != nullptr) p.pent[o] = tx;
+            STB_AT(QG_FILE, p.bd, QS_PMAX, p.pmax + o, v);
+            STB_AT(QG_FILE, p.bd, QS_PARG, p.parg + o, idx);
+            STB_AT(QG_FILE, p.bd, QS_PSUM, p.psum + o, ex);
+            if (p.pent != nullptr) STB_AT(QG_FILE, p.bd, QS_PENT, p.pent + o, tx);
           }
         }
       } else if (p.y != nullptr && grow < p.n) {
@@ -837,13 +851,13 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
 #pragma unroll
           for (int j = 0; j < NC; ++j) {
             const int tok = tokb + j;
-            if (tok < p.m) dst[(size_t)tok * p.ldy] += acc[j];
+            if (tok < p.m && BOK_AT(QG_FILE, p.bd, QS_Y, dst + (size_t)tok * p.ldy, 4)) dst[(size_t)tok * p.ldy] += acc[j];
           }
         } else {
 #pragma unroll
           for (int j = 0; j < NC; ++j) {
             const int tok = tokb + j;
-            if (tok < p.m) dst[(size_t)tok * p.ldy] = acc[j];
+            if (tok < p.m) STB_AT(QG_FILE, p.bd, QS_Y, dst + (size_t)tok * p.ldy, acc[j]);
           }
         }
       }

@@ -28,6 +28,19 @@ def test_library_exports_every_declared_symbol():
     assert not missing, missing
 
 
+def test_checked_library_exports_every_declared_symbol_and_says_so():
+    # the bounds-checked twin is built by the same build() and has the same ABI
+    dlbuild.build()
+    names = _declared()
+    chk = ctypes.CDLL(dlbuild.LIB_CHECKED)
+    missing = [n for n in names if not hasattr(chk, n)]
+    assert not missing, missing
+    chk.dllm_bounds_checked.restype = ctypes.c_int
+    reg = ctypes.CDLL(dlbuild.LIB)
+    reg.dllm_bounds_checked.restype = ctypes.c_int
+    assert chk.dllm_bounds_checked() == 1 and reg.dllm_bounds_checked() == 0
+
+
 def test_binding_covers_declared_symbols():
     names = set(_declared())
     assert names <= set(dl._SIGS), sorted(names - set(dl._SIGS))
