@@ -369,6 +369,12 @@ def test_commit_parity_llada_two_layers_first_block():
     _chain(dict(synth.LLADA, n_layers=2), synth.config_seed(4) + 21, 8, min_decidable_ii=7)
 
 
+def test_commit_parity_llada_two_layers_whole_protocol():
+    # the protocol's whole 32-step chain (four blocks of 8 steps, 4 commits each) at LLaDA-8B
+    # shapes and two layers; every step is decidable at level (ii) on this seed and must match
+    _chain(dict(synth.LLADA, n_layers=2), synth.config_seed(4) + 32, 32, min_decidable_ii=30)
+
+
 def test_commit_parity_llada_full_depth():
     # the full 32-layer LLaDA-8B-shaped step, the protocol's first two steps
     _chain(dict(synth.LLADA), synth.config_seed(4) + 22, 2, min_decidable_ii=2)
