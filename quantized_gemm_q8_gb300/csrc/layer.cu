@@ -800,11 +800,17 @@ static StepPlan step_plan(const dllm_model* m, int64_t L, int flags, bool lmhead
   S.x = take(lmhead ? (size_t)Lk * d * 4 : 0);
   S.act_d = take(act_layout(L, d).bytes);
   S.act_ff = take(act_layout(L, f).bytes);
-  S.pqk = take((size_t)S.qk.splits * L * 2 * d * 4);
+  // The split-K partials of Q|K, O, gate|up and down share one region: each is read by the row
+  // kernel right after its GEMM and is dead before the next of them is written (each kernel
+  // waits for its predecessor before it writes), so the GEMMs keep storing into lines that are
+  // already in L2 instead of allocating fresh ones. V's partials are read together with Q|K's.
+  {
+    const size_t r1 = std::max(std::max((size_t)S.qk.splits * L * 2 * d * 4, (size_t)S.o.splits * L * d * 4),
+                               std::max((size_t)S.gu.splits * L * 2 * f * 4, (size_t)S.dn.splits * L * d * 4));
+    S.pqk = take(r1);
+    S.po = S.pgu = S.pdn = S.pqk;
+  }
   S.pv = take((size_t)S.v.splits * L * d * 4);
-  S.po = take((size_t)S.o.splits * L * d * 4);
-  S.pgu = take((size_t)S.gu.splits * L * 2 * f * 4);
-  S.pdn = take((size_t)S.dn.splits * L * d * 4);
   S.qkv = take(full ? (size_t)L * 3 * d * 4 : 0);
   S.att = take(full ? (size_t)((Lk + 31) / 32) * L * d * 4 : 0);
   S.attml = take(full ? (size_t)((Lk + 31) / 32) * L * m->n_heads * 8 : 0);

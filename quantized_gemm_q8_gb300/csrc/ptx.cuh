@@ -106,6 +106,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// The same with an L2 evict-first policy, for data read once per step (the weights): their
+// lines are the first to go, so the activations, partials and K/V the step reuses stay in L2.
+__device__ __forceinline__ void bulk_g2s_once(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "{\n .reg .b64 pol;\n createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n"
+      " cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], pol;\n}\n"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 // Asynchronous prefetch of a global range into L2 (a hint: no completion, no data returned);
 // src 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {

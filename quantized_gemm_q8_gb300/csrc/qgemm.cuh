@@ -411,7 +411,8 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
     if (warp == QG_WPROD_WARP && lane == 0) {
       // ---------------------------------------------------------- weight producer (one thread):
       // raw packed super-blocks as far ahead as the W ring allows (HBM latency is hidden only
-      // by depth, so this runs independently of the activation stages)
+      // by depth, so this runs independently of the activation stages); each blob is read once
+      // per step, so it is copied with an L2 evict-first policy
       int it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
@@ -427,7 +428,7 @@ __global__ void __launch_bounds__(QG_THREADS, 1)
           // a copy outside its buffer (bounds-checked build) is not issued: its stage never
           // fills and the waits on it run out, so the launch ends with both errors set
           if (BOK_AT(QG_FILE, p.bd, QS_W, blob + (size_t)sb * C::W_BYTES, C::W_BYTES))
-            bulk_g2s(ws, blob + (size_t)sb * C::W_BYTES, C::W_BYTES, BAR(C::BW_FULL + w));
+            bulk_g2s_once(ws, blob + (size_t)sb * C::W_BYTES, C::W_BYTES, BAR(C::BW_FULL + w));
           if (C::Q4 && BOK_AT(QG_FILE, p.bd, QS_DD, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES))
             bulk_g2s(ws + C::W_BYTES, dd + (size_t)sb * C::DD_BYTES, C::DD_BYTES, BAR(C::BW_FULL + w));
         }
