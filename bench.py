@@ -253,19 +253,24 @@ def run_ours(args, rank, local_rank, world):
     ms_max, ms_per_step, value = job_timing(ev0.elapsed_time(ev1), args.steps, world, dist, "cuda")
 
     # ---- end-to-end through the public call with host buffers (H2D canvas, D2H commits) ----
+    # one dllm_step_graph_host call per step: the pinned host canvas in, the step's graph, the
+    # commits out and applied to the host canvas (torch builds without a raw graph handle fall
+    # back to the same copies issued from Python)
     canvas_h = torch.from_numpy(synth.canvas(seed)).pin_memory()
     kmax = max(k for _, _, k in kinds)
     out_h = torch.empty(2 * kmax, dtype=torch.int32).pin_memory()
-    out_dev = torch.cat([graphs.out["pos"], graphs.out["id"]])
     e2e_steps = min(args.steps, 32)
+    via_c = hasattr(torch.cuda.CUDAGraph, "raw_cuda_graph_exec")
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for s in range(e2e_steps):
+        if via_c:
+            graphs.step_host(block_of(s), canvas_h, out_h)
+            continue
         with torch.cuda.stream(stream):
             canvas.copy_(canvas_h, non_blocking=True)
             graphs.replay(block_of(s))
-            torch.cat([graphs.out["pos"], graphs.out["id"]], out=out_dev)
-            out_h.copy_(out_dev, non_blocking=True)
+            out_h.copy_(graphs.pos_id, non_blocking=True)
         stream.synchronize()
         k = sched[s % len(sched)][2]
         pos, ids = out_h[:k].numpy(), out_h[kmax:kmax + k].numpy()
@@ -354,7 +359,8 @@ def run_ours(args, rank, local_rank, world):
         "layer_gemm_ms": layer_gemm_ms,
         "clocks": clk.summary(),
         "e2e": {"value": e2e_ms, "unit": "ms/step", "h2d_bytes_per_step": int(canvas_h.numel() * 4),
-                "d2h_bytes_per_step": int(out_h.numel() * 4), "steps": e2e_steps, "committed_after": committed},
+                "d2h_bytes_per_step": int(2 * max(k for _, _, k in sched) * 4), "steps": e2e_steps,
+                "committed_after": committed, "path": "dllm_step_graph_host" if via_c else "python copies"},
         "context": {"pages_rtx3050_ms_per_step": 221, "pages_i5_13420h_ms_per_step": 3005},
     }
     if rank == 0 and not args.no_cpu_baseline:

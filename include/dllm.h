@@ -406,6 +406,24 @@ DLLM_API int dllm_qgemm_noalloc(int type, const void* act, int64_t m, int64_t k,
  * in the device error word and returns. dllm_check() afterwards reports DLLM_E_TIMEOUT. */
 DLLM_API int dllm_selftest_timeout(int64_t limit_cycles, dllm_stream_t stream);
 
+/* ---- one step from host buffers ------------------------------------------------------------
+ * The host side of one denoising step around a step the caller captured once into a CUDA graph
+ * (e.g. dllm_denoise_step on `canvas` between cudaStreamBeginCapture and cudaStreamEndCapture,
+ * instantiated): one call copies the host canvas in, runs the graph and reads the commits out
+ * (README "How it works": each step commits k tokens into the canvas, which the next step
+ * reads). `graph_exec` is the cudaGraphExec_t; `canvas_host` the host canvas (L int32, pinned
+ * host memory for asynchronous copies), `canvas` the device canvas the graph was captured on;
+ * `out` the device positions (int32 [k_commit] at out[0]) and ids (at out[out_stride]) the
+ * graph's commit writes. The call copies the host canvas to `canvas`, launches the graph on
+ * `stream`, copies the positions then the ids to out_host (host int32 [2 * k_commit]), waits
+ * for the stream and writes each committed id into canvas_host (positions < 0, meaning no
+ * commit, are skipped). It is synchronous (it returns after the step). Errors: DLLM_E_INVAL
+ * (null host pointers or graph, k_commit > out_stride, L out of range, canvas / out not device
+ * pointers), DLLM_E_CUDA. */
+DLLM_API int dllm_step_graph_host(void* graph_exec, int32_t* canvas_host, int32_t* canvas, int64_t L,
+                                  const int32_t* out, int32_t out_stride, int32_t k_commit, int32_t* out_host,
+                                  dllm_stream_t stream);
+
 /* ---- bounds-checked build --------------------------------------------------------------------
  * The same sources also build libdllm_checked.so (compiled with DLLM_BOUNDS_CHECK), a debug
  * library with the same entry points in which every global-memory access of every kernel is

@@ -54,6 +54,7 @@ _SIGS = {
     "dllm_qgemm_q6k": ([P, P, P, I64, I64, P, I64, P, I64, INT, P, SZ, P], INT),
     "dllm_qgemm_intsums": ([INT, P, I64, I64, P, I64, P, P], INT),
     "dllm_selftest_timeout": ([I64, P], INT),
+    "dllm_step_graph_host": ([P, P, P, I64, P, I32, I32, P, P], INT),
     "dllm_bounds_checked": ([], INT),
     "dllm_selftest_bounds": ([P, I32, I32, P], INT),
     "dllm_lmhead_workspace_bytes": ([I64, I64, I64], SZ),
@@ -534,8 +535,9 @@ class StepGraphs:
         kmax = max(max(k for _, _, k in self.kinds), 1)
         nb = denoise_workspace_bytes(model, L, rows)
         self.ws = torch.empty(nb + 1024, dtype=torch.uint8, device=dev)
-        self.out = {"pos": torch.empty(kmax, dtype=torch.int32, device=dev),
-                    "id": torch.empty(kmax, dtype=torch.int32, device=dev),
+        self.kmax = kmax
+        self.pos_id = torch.empty(2 * kmax, dtype=torch.int32, device=dev)  # positions, then ids
+        self.out = {"pos": self.pos_id[:kmax], "id": self.pos_id[kmax:],
                     "conf": torch.empty(kmax, dtype=torch.float32, device=dev)}
         self.stream = torch.cuda.Stream(device=dev)
         self.graphs = []
@@ -560,6 +562,15 @@ class StepGraphs:
         """Replay on self.stream (a graph replays on the caller's current stream)."""
         with torch.cuda.stream(self.stream):
             self.graphs[kind_index].replay()
+
+    def step_host(self, kind_index: int, canvas_host: torch.Tensor, out_host: torch.Tensor):
+        """One step from host buffers through dllm_step_graph_host: the host canvas (pinned int32
+        [L]) goes in, graph kind_index runs, its commits come back into out_host (pinned int32
+        [2 * kmax]: positions, then ids) and are applied to canvas_host."""
+        k = self.kinds[kind_index][2]
+        exec_ = self.graphs[kind_index].raw_cuda_graph_exec()
+        _ok(lib().dllm_step_graph_host(C.c_void_p(exec_), _ptr(canvas_host), _ptr(self.canvas), self.canvas.shape[0],
+                                       _ptr(self.pos_id), self.kmax, k, _ptr(out_host), _stream(self.stream)))
 
 
 class CachedStepGraphs:

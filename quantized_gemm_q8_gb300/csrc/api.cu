@@ -1016,6 +1016,33 @@ DLLM_API int dllm_qgemm_intsums(int type, const void* act, int64_t m, int64_t k,
                       (cudaStream_t)stream);
 }
 
+DLLM_API int dllm_step_graph_host(void* graph_exec, int32_t* canvas_host, int32_t* canvas, int64_t L,
+                                  const int32_t* out, int32_t out_stride, int32_t k_commit, int32_t* out_host,
+                                  dllm_stream_t stream) {
+  DLLM_RANGE();
+  if (!graph_exec || !canvas_host || !out_host || L <= 0 || L > (1 << 24) || k_commit < 0 || out_stride < k_commit)
+    return fail(DLLM_E_INVAL,
+                "dllm_step_graph_host: graph_exec, canvas_host and out_host must be set, L in [1, 2^24], "
+                "0 <= k_commit <= out_stride");
+  CHECK_DEV(canvas, "canvas");
+  CHECK_DEV(out, "out");
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(canvas, canvas_host, (size_t)L * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaGraphLaunch(static_cast<cudaGraphExec_t>(graph_exec), s);
+  if (e == cudaSuccess && k_commit > 0) {
+    e = cudaMemcpyAsync(out_host, out, (size_t)k_commit * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(out_host + k_commit, out + out_stride, (size_t)k_commit * 4, cudaMemcpyDeviceToHost, s);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "dllm_step_graph_host");
+  for (int32_t i = 0; i < k_commit; ++i) {
+    const int32_t pos = out_host[i];
+    if (pos >= 0 && pos < L) canvas_host[pos] = out_host[k_commit + i];
+  }
+  return DLLM_OK;
+}
+
 DLLM_API int dllm_bounds_checked(void) {
 #ifdef DLLM_BOUNDS_CHECK
   return 1;

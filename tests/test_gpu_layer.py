@@ -176,6 +176,34 @@ def test_denoise_step_small_canvas_edges(L):
     print(f"denoise small L={L}: {exact}/1 steps with commits identical to the oracle's order")
 
 
+def test_step_graph_host_matches_device_replay():
+    # dllm_step_graph_host (host canvas in, captured step, commits out and applied on the host)
+    # must leave the host canvas exactly where plain replays leave the device canvas
+    dims = SMALL
+    seed = 47
+    model = dl.model_from_seed(dims, seed)
+    canvas0 = synth.canvas(seed, prompt_len=8, gen_len=32, mask_id=dims["mask_id"], prompt_max=990)
+    sched = dl.schedule(8, 32, 16, 8)  # two blocks of 16, 4 steps each
+    kinds = sorted(set(sched))
+    kind_of = [kinds.index(x) for x in sched]
+    canvas = torch.from_numpy(canvas0.copy()).cuda()
+    graphs = dl.StepGraphs(model, canvas, kinds)
+    for s in range(len(sched)):
+        graphs.replay(kind_of[s])
+    torch.cuda.synchronize()
+    dl.check(graphs.stream)
+    want = canvas.cpu().numpy().copy()
+    assert (want[8:] != dims["mask_id"]).all()  # the 8 steps committed all 32 positions
+    canvas.copy_(torch.from_numpy(canvas0.copy()))
+    canvas_h = torch.from_numpy(canvas0.copy()).pin_memory()
+    out_h = torch.empty(2 * graphs.kmax, dtype=torch.int32).pin_memory()
+    for s in range(len(sched)):
+        graphs.step_host(kind_of[s], canvas_h, out_h)
+    dl.check(graphs.stream)
+    np.testing.assert_array_equal(canvas_h.numpy(), want)
+    np.testing.assert_array_equal(canvas.cpu().numpy(), want)
+
+
 def test_denoise_step_llada_shapes_two_layers():
     dims = dict(synth.LLADA, n_layers=2)
     exact = _full_step_check(dims, synth.config_seed(4), 148, 20, 52, 4, n_steps=2)
