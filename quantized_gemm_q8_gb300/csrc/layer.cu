@@ -636,26 +636,27 @@ __global__ void __launch_bounds__(RR_WARPS * 32) row_resid_kernel(RowArgs a) {
       for (int i = 0; i < 8; ++i) ss = fmaf(v[j][i], v[j][i], ss);
     }
   }
-  if (MODE == ROW_RESID_ONLY) return;
+  if constexpr (MODE != ROW_RESID_ONLY) {  // RMSNorm + Q8_K of the updated row
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) red[warp] = ss;
-  __syncthreads();
-  float tot = 0.f;
-  for (int w = 0; w < nwarp; ++w) tot += red[w];
-  const float rstd = 1.0f / sqrtf(tot / (float)a.k + a.eps);
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < nwarp; ++w) tot += red[w];
+    const float rstd = 1.0f / sqrtf(tot / (float)a.k + a.eps);
 #pragma unroll
-  for (int j = 0; j < RR_J; ++j) {
-    const int sb = warp + j * nwarp;
-    if (sb < nsb) {
-      const int base = sb * QK + 8 * lane;
-      const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 w0 = LDB(a.bd, 2, reinterpret_cast<const float4*>(a.norm_w + base), z4);
-      const float4 w1 = LDB(a.bd, 2, reinterpret_cast<const float4*>(a.norm_w + base + 4), z4);
-      const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    for (int j = 0; j < RR_J; ++j) {
+      const int sb = warp + j * nwarp;
+      if (sb < nsb) {
+        const int base = sb * QK + 8 * lane;
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 w0 = LDB(a.bd, 2, reinterpret_cast<const float4*>(a.norm_w + base), z4);
+        const float4 w1 = LDB(a.bd, 2, reinterpret_cast<const float4*>(a.norm_w + base + 4), z4);
+        const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[j][i] = v[j][i] * rstd * w[i];
-      q8k_emit(v[j], row, a.rows, sb, a.k, a.o);
+        for (int i = 0; i < 8; ++i) v[j][i] = v[j][i] * rstd * w[i];
+        q8k_emit(v[j], row, a.rows, sb, a.k, a.o);
+      }
     }
   }
 }
@@ -679,8 +680,8 @@ __global__ void __launch_bounds__(256) row_sb_kernel(RowArgs a) {
     const int base = sb * QK + 8 * lane;
     const float* ps = a.P + (int64_t)row * a.ldp + base;
     float u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll 4
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
     for (int s = 0; s < a.S; ++s, ps += a.pstride) {
       const float4 p0 = LDB(a.bd, 1, reinterpret_cast<const float4*>(ps), z4);
       const float4 p1 = LDB(a.bd, 1, reinterpret_cast<const float4*>(ps + 4), z4);

@@ -250,10 +250,9 @@ __device__ __forceinline__ void decode_q6k_piece(const uint8_t* W, int t, int q,
   const uint32_t hmask = odd ? 0x03000300u : 0x00300030u;
   const float fm = odd ? 0.0625f : 1.0f;
   const float fa = odd ? -96.0f : -1056.0f;
-  const int tslot = 2 * odd + tt;
   const int shift = tt ? 2 : 4;
-  // the row's int8 group scale: scale byte 8 hq + 2 tslot + ps = byte 2 tt + ps of the quarter's
-  // scale word sw (its bytes 4q .. 4q + 3)
+  // the row's int8 group scale: scale byte 8 hq + 2 (2 odd + tt) + ps = byte 2 tt + ps of the
+  // quarter's scale word sw (its bytes 4q .. 4q + 3)
   const int s = (int)(int8_t)(sw >> (8 * (2 * tt + ps)));
   const float s_hi = hs == 0.f ? 0.f : (float)(s >> 4), s_lo = (float)(s & 15) * ls * 0.0625f;
   const __half2 mH = __float2half2_rn(s_hi * fm), aH = __float2half2_rn(s_hi * fa);
