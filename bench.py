@@ -405,6 +405,49 @@ def run_only_layer(args):
                       "note": "one-layer model, embedding + layer; a profiling target"}))
 
 
+def run_only_lmhead(args):
+    """Config 3's masked-rows LM head alone (126464 x 4096 Q6_K on the 32 rows of block 0, softmax
+    confidence, top-4 commit): the profiling target of the narrow-tile GEMM (--steps calls)."""
+    import torch
+
+    import quantized_gemm_q8_gb300 as dl
+    from quantized_gemm_q8_gb300 import synth
+
+    torch.cuda.set_device(0)
+    dims = dict(synth.LLADA)
+    seed = synth.config_seed(3)
+    d, vocab = dims["d_model"], dims["vocab"]
+    head = synth.head_weights(seed, dims)
+    w_out = dl.pack_weights(dl.Q6_K, torch.from_numpy(head["w_out"].reshape(-1)).cuda(), vocab, d)
+    out_norm = torch.from_numpy(head["out_norm"]).cuda()
+    canvas0 = torch.from_numpy(synth.canvas(seed)).cuda()
+    canvas = canvas0.clone()
+    hidden = torch.from_numpy(synth.activations(seed, L_CANVAS, d)).cuda()
+    b0, b1, k_commit = _schedule()[0][0]
+    ws = torch.empty(max(dl.lmhead_workspace_bytes(b1 - b0, vocab, d), 1), dtype=torch.uint8, device="cuda")
+
+    def run():
+        canvas.copy_(canvas0)
+        dl.lmhead_masked_select(hidden, canvas, dims["mask_id"], b0, b1, k_commit, out_norm, w_out, vocab,
+                                dims["eps"], ws=ws)
+
+    for _ in range(args.warmup):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    dl.check()
+    ms = e0.elapsed_time(e1) / max(args.steps, 1)
+    wbytes = vocab * d // 256 * 210
+    print(json.dumps({"kernel": "lm_head", "rows": b1 - b0, "vocab": vocab, "d": d, "ms_per_call": ms,
+                      "weight_gbs": wbytes / (ms * 1e-3) / 1e9,
+                      "note": "weights (425 MB) exceed L2: read from HBM every call; a profiling target"}))
+
+
 def run_only_kernel(args):
     """Time one GEMM of the step alone (the profiling target): --steps launches after --warmup."""
     import torch
@@ -414,6 +457,8 @@ def run_only_kernel(args):
 
     if args.only_kernel == "layer_full":
         return run_only_layer(args)
+    if args.only_kernel == "lm_head":
+        return run_only_lmhead(args)
 
     ty_name, n, k = ONLY_KERNELS[args.only_kernel]
     ty = dl.Q4_K if ty_name == "q4k" else dl.Q6_K
@@ -687,7 +732,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only-kernel", choices=sorted(ONLY_KERNELS) + ["layer_full"], default=None,
+    ap.add_argument("--only-kernel", choices=sorted(ONLY_KERNELS) + ["layer_full", "lm_head"], default=None,
                     help="time one GEMM of the step alone (profiling target) instead of the step")
     ap.add_argument("--configs", action="store_true",
                     help="one JSON line per other configuration (1, 2, 3, 5) instead of the step")
