@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -111,11 +112,14 @@ class ClockSampler:
 
 
 def gemm_source_sha1() -> str:
-    """sha1 of the GEMM kernel's sources (the kernel and the PTX wrappers it is built from)."""
+    """sha1 of the GEMM kernel's code (the kernel and the PTX wrappers it is built from), with
+    comments, indentation and blank lines left out, so that a comment edit keeps the record."""
     h = hashlib.sha1()
     for name in ("qgemm.cuh", "ptx.cuh"):
-        with open(os.path.join(ROOT, "quantized_gemm_q8_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "quantized_gemm_q8_gb300", "csrc", name), encoding="utf-8") as f:
+            src = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        lines = (re.sub(r"//.*$", "", ln).strip() for ln in src.splitlines())
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()
 
 

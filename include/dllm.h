@@ -5,21 +5,23 @@
  * top-k token commit, and the per-layer linear stream.
  *
  * Sources (mojo-dllm pages; cited by page title and section):
- *   [TS10]  Technical Specification, section 10 "Quantized Compute" (linear_q4k(x, weight,
- *           out): Q4_K_M matmul directly on quantized weights, block decode, dot, f32 acc.)
+ *   [TS10]  Technical Specification, section 10 "Quantized Compute" (the entry point
+ *           linear_q4k(x, weight, out): the product is formed from the packed blocks, each
+ *           block expanded as it is used, with f32 accumulation; no dense weight copy)
  *   [TS9]   Technical Specification, section 9.2 (unknown types fail explicitly, no silent
  *           fallback) and section 27 (actionable errors).
  *   [TS28]  Technical Specification, section 28 (preallocated, reusable runtime buffers).
  *   [TS11]  Technical Specification, section 11 (LLaDA layer order) and 11.1 (bidirectional).
  *   [TS12]  Technical Specification, sections 12-14 (diffusion loop, scheduler select/update,
  *           softmax / argmax / top-k / scatter).
- *   [DP-CD] Development plan, "Compute design" (Q8_K activations: int8, one f32 scale per
- *           256 values, int sums per 16; weights decoded to unsigned bytes + per-16 scale +
- *           per-16 offset; LM head only on the masked rows of the current block).
+ *   [DP-CD] Development plan, "Compute design" (each token's activations become 8-bit codes
+ *           with a float scale for every 256 of them and integer sums of every 16; each weight
+ *           block expands to small unsigned integers with a scale and an offset for every 16;
+ *           the output head runs only for the still-masked rows of the active block).
  *   [DP-MF] Development plan, "Model facts" (d 4096, 32 x 128 MHA, FFN 12288 SwiGLU,
  *           RMSNorm eps 1e-5, NORM RoPE theta 500000, vocab 126464, mask 126336).
  *   [DP-CO] Development plan, "Corrections to the spec" (Q4_K / Q6_K matrices, F32 norms).
- *   [RM-HW] README, "How it works" (logits only where the sampler looks; LLaDA low-confidence
+ *   [RM-HW] README, "How it works" (logits for the positions the sampler reads, no others; LLaDA low-confidence
  *           remasking).
  *
  * Conventions for every call:
@@ -145,8 +147,8 @@ DLLM_API int dllm_qgemm(int type, const void* act, int64_t m, int64_t k, const v
                         int64_t n, float* y, int64_t ldy, int accumulate, void* ws, size_t ws_bytes,
                         dllm_stream_t stream);
 
-/* The same GEMM on plain Q8_K activations, the form the pages' Q8_K blocks take ([DP-CD]: int8
- * codes, one f32 scale per 256 values, int sums per 16):
+/* The same GEMM on plain Q8_K activations, the form the pages' Q8_K blocks take ([DP-CD]: 8-bit
+ * codes, an f32 scale for every 256 of them, int16 sums of every 16):
  *   q int8 [m][k], d f32 [m][k/256], bsum int16 [m][k/16] (e.g. dllm_quantize_act's q, d, bsum).
  * dllm_pack_act builds the operand form `act` (layout as in dllm_quantize_act, act_bytes >=
  *   dllm_act_bytes(rows, k), 256-byte aligned) from them; codes, scales and sums are copied

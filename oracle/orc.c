@@ -16,10 +16,11 @@
  * Sources (mojo-dllm pages):
  *   - Development plan, "Corrections to the spec": a Q4_K_M GGUF of LLaDA-8B
  *     holds Q4_K and Q6_K matrices and F32 norms.
- *   - Development plan, "Compute design": per-token Q8_K activations (int8,
- *     one f32 scale per 256 values, int sums per 16); weights decoded into
- *     unsigned bytes, a per-16 integer scale and a per-16 f32 offset; the
- *     integer inner product runs to the end of the row before scales apply.
+ *   - Development plan, "Compute design": every token's activations are
+ *     quantized as Q8_K (8-bit codes, an f32 scale for each 256 of them, the
+ *     integer sum of each 16); every weight block expands to small unsigned
+ *     integers with an integer scale and an f32 offset for each 16; the
+ *     integer products are summed over the whole row before any scale.
  *   - Development plan, "Model facts": RMSNorm eps 1e-5, RoPE theta 500000
  *     (adjacent-pair / NORM form), 32 x 128 MHA, non-causal, SwiGLU FFN.
  *   - Technical specification, section 12 (diffusion loop) and section 14

@@ -1,9 +1,9 @@
 // Quantized GEMM y = A(Q8_K activations) x W(Q4_K | Q6_K)^T on the sm_103a tensor cores.
 //
-// Method (mojo-dllm "Development plan", "Compute design"): activations are Q8_K (int8 codes,
-// one f32 scale per 256, int sums per 16); each weight super-block is decoded to small
-// integers plus a per-16 scale and per-16 offset; the integer inner product of a
-// super-block runs to its end before the f32 scales apply. Here every such integer sum is
+// Method (mojo-dllm "Development plan", "Compute design"): the activations are Q8_K (8-bit
+// codes, an f32 scale for every 256 and the integer sum of every 16); every weight
+// super-block expands to small integers with a scale and an offset for each 16; within a
+// super-block the integer products are summed completely before the f32 scales apply. Here every such integer sum is
 // computed EXACTLY by tcgen05.mma kind::f16: the small integers are carried in f16 operands
 // (exactly representable) and accumulated in f32 tensor memory (exact below 2^24).
 //

@@ -1,6 +1,7 @@
 // Q8_K quantization of one super-block held in registers (shared by the activation
 // quantizer and the fused layer kernels). Rule (mojo-dllm "Development plan", "Compute
-// design": int8, one f32 scale per 256, int sums per 16): amax = max|x|, d = amax / 127,
+// design": 8-bit codes, an f32 scale for every 256, the integer sum of every 16):
+// amax = max|x|, d = amax / 127,
 // q = clamp(rint(x * (127 / amax)), -127, 127) with an f32 multiply and IEEE division;
 // amax == 0 gives d = 0 and q = 0.
 #pragma once
