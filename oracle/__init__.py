@@ -5,13 +5,15 @@ leg may import this package. It shares no code with the CUDA library: the
 arithmetic lives in ``orc.c`` (plain C, f64, OpenMP over output rows) and the
 compositions below chain those primitives in the order the pages give:
 
-* mojo-dllm "Technical Specification", section 11 (one LLaDA layer: RMSNorm,
-  QKV projection, RoPE, bidirectional attention, output projection, residual,
-  RMSNorm, MLP, residual) and "Development plan", "Model facts" (eps 1e-5,
+* mojo-dllm "Technical Specification", section 11 (the order inside one LLaDA
+  layer: normalize, project to Q/K/V, rotate Q and K, attend over every
+  position, project the attention output and add it to the stream, normalize
+  again, run the gated MLP and add its output) and "Development plan", "Model facts" (eps 1e-5,
   NORM RoPE with theta 500000, SwiGLU 12288, untied output);
 * "Development plan", "Compute design": every projection consumes Q8_K
   activations (quantized per token, decisions in f32) and decoded Q4_K/Q6_K
-  weights; the LM head runs only on the masked rows of the current block;
+  weights; the output head is evaluated for the masked rows of the active
+  block and nowhere else;
 * "Technical Specification", section 12: confidence, top-k select, scatter.
 
 Readings where the pages are silent:

@@ -14,8 +14,8 @@
  * decisions in f32, the precision the GPU kernel uses.
  *
  * Sources (mojo-dllm pages):
- *   - Development plan, "Corrections to the spec": a Q4_K_M GGUF of LLaDA-8B
- *     holds Q4_K and Q6_K matrices and F32 norms.
+ *   - Development plan, "Corrections to the spec": the LLaDA-8B Q4_K_M file
+ *     mixes Q4_K and Q6_K weight matrices, with its norms in F32.
  *   - Development plan, "Compute design": every token's activations are
  *     quantized as Q8_K (8-bit codes, an f32 scale for each 256 of them, the
  *     integer sum of each 16); every weight block expands to small unsigned
@@ -32,8 +32,8 @@
  *     gives the same run every time), section 14 (sampling) and the
  *     --seed / --temperature flags: temperature sampling from a seeded,
  *     deterministic generator (here counter-based SplitMix64).
- *   - README, "How it works": the LM head runs only on the masked positions
- *     of the current block.
+ *   - README, "How it works": the output head is evaluated only for the
+ *     masked positions of the active block.
  * The GGUF byte layouts of Q4_K / Q6_K are the public GGUF formats that the
  * pages name; they are spelled out at each decoder below.
  */

@@ -682,7 +682,7 @@ DLLM_API int dllm_pack_weights(int type, const void* blocks, int64_t n, int64_t 
                                size_t packed_bytes, dllm_stream_t stream) {
   DLLM_RANGE();
   if (!block_bytes(type))
-    return fail(DLLM_E_TYPE, "dllm_pack_weights: unsupported block type %d: matrix kernels exist for Q4_K (12) and Q6_K (14)",
+    return fail(DLLM_E_TYPE, "dllm_pack_weights: unsupported block type %d: the GEMM kernels take Q4_K (12) or Q6_K (14)",
                 type);
   if (n <= 0 || k <= 0 || k % QK || n > (1 << 24) || k > (1 << 20))
     return fail(DLLM_E_SHAPE, "dllm_pack_weights: bad shape n=%lld k=%lld (k must be a positive multiple of 256)",
@@ -858,7 +858,7 @@ static int qgemm_common(const char* fn, int type, const void* act, int64_t m, in
                         int64_t n, float* y, int64_t ldy, int accumulate, void* ws, size_t ws_bytes,
                         int32_t* dbg, cudaStream_t stream) {
   if (!block_bytes(type))
-    return fail(DLLM_E_TYPE, "%s: unsupported block type %d: matrix kernels exist for Q4_K (12) and Q6_K (14)", fn,
+    return fail(DLLM_E_TYPE, "%s: unsupported block type %d: the GEMM kernels take Q4_K (12) or Q6_K (14)", fn,
                 type);
   if (m <= 0 || m > 65536 || n <= 0 || n > (1 << 24) || k <= 0 || k % QK || k > (1 << 20))
     return fail(DLLM_E_SHAPE, "%s: bad shape m=%lld n=%lld k=%lld (k must be a positive multiple of 256)", fn,

@@ -1,6 +1,6 @@
-// LLaDA layer stream and full denoising step (mojo-dllm Technical Specification, section 11:
-// RMSNorm, QKV projection, RoPE, bidirectional attention, output projection, residual,
-// RMSNorm, MLP, residual; Development plan, "Model facts": eps 1e-5, NORM RoPE theta 500000,
+// LLaDA layer stream and full denoising step (mojo-dllm Technical Specification, section 11,
+// the order inside a layer: normalize, Q/K/V projections, rotate Q and K, attention over all
+// positions, O projection added to the stream, normalize, gated MLP added; Development plan, "Model facts": eps 1e-5, NORM RoPE theta 500000,
 // 32 x 128 MHA non-causal, SwiGLU FFN, untied output). Every projection is the tcgen05
 // quantized GEMM; the glue between them is fused into row kernels that consume the GEMMs'
 // split-K partials directly (fixed summation order), so no intermediate takes an extra pass.

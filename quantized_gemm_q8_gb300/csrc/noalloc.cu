@@ -59,7 +59,7 @@ extern "C" DLLM_API int dllm_qgemm_noalloc(int type, const void* act, int64_t m,
                                            int64_t n, float* y, int64_t ldy, int accumulate, dllm_stream_t stream) {
   DLLM_RANGE();
   if (type != DLLM_Q4_K && type != DLLM_Q6_K)
-    return fail(DLLM_E_TYPE, "dllm_qgemm_noalloc: unsupported block type %d: matrix kernels exist for Q4_K (12) and Q6_K (14)",
+    return fail(DLLM_E_TYPE, "dllm_qgemm_noalloc: unsupported block type %d: the GEMM kernels take Q4_K (12) or Q6_K (14)",
                 type);
   if (m <= 0 || m > 65536 || n <= 0 || n > (1 << 24) || k <= 0 || k % QK || k > (1 << 20))
     return fail(DLLM_E_SHAPE, "dllm_qgemm_noalloc: bad shape m=%lld n=%lld k=%lld (k must be a positive multiple of 256)",
