@@ -120,14 +120,6 @@ __device__ __forceinline__ void bulk_g2s_once(uint32_t dst, const void* src, uin
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
-// 16-byte asynchronous copy global -> shared (no register staging; many may be in flight),
-// and the wait for all of this thread's outstanding ones.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-}
 // 3-D tiled tensor copy global -> shared through a tensor map (swizzle from the map).
 __device__ __forceinline__ void tma_g2s_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                            uint32_t bar) {
@@ -176,30 +168,6 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Warp-wide forms: every lane of the warp executes them with identical (warp-uniform) operands
-// and one elected lane issues, which keeps the operands in uniform registers.
-__device__ __forceinline__ void mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                                uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.b32 q, %4, 0;\n elect.sync _|p, 0xffffffff;\n"
-      " @p tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, q;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_f16_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.b32 q, %4, 0;\n elect.sync _|p, 0xffffffff;\n"
-      " @p tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
-  asm volatile(
-      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n"
-      " @p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
       : "memory");
 }
 // Arrive once on `bar` when all previously issued tcgen05 operations of this thread complete.
