@@ -288,8 +288,8 @@ __global__ void __launch_bounds__(ATT_THREADS) attention_partial_kernel(const fl
 //           keys past L read as zeros;
 //   V^T     by a register transpose of the V planes into the no-swizzle K-major layout
 //           (core matrices of 8 rows x 16 bytes, 128 bytes apart along K, 8-row groups SBO apart).
-// One thread issues S = Q K^T (24 MMAs: M 128, N 80, K 16 x 8, terms hi*hi + hi*lo + lo*hi)
-// into TMEM; each row's softmax over the chunk is exact (the two column halves meet through
+// One thread of warp 0 issues S = Q K^T (24 MMAs: M 128, N 80, K 16 x 8, terms hi*hi + hi*lo +
+// lo*hi) into TMEM as soon as Q and K land, while warps 1-7 stage V^T; each row's softmax over the chunk is exact (the two column halves meet through
 // shared memory); P goes back as head/tail planes over Q and K; O = P V (15 MMAs: M 128, N 128,
 // K 16 x 5) and each row is written unnormalized with its chunk's (m, l). The three-term
 // products carry each product to ~2^-22 relative, far below the f32 accumulation's own
@@ -361,16 +361,41 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
                      kb + b * TA_BOXR, 2 + hl, bar_in);
       }
   }
-  // V^T (rows = dims, K = the chunk's keys) by a register transpose of the V planes: item = (key
-  // pair, block of 8 dims), all of a thread's loads in flight, then (key, key + 1) pairs per
-  // 4-byte store
-  {
+  const uint32_t tmem = ta_tmem;
+  volatile int never = 0;
+  bool ok = true;
+  if (warp == 0) {
+    // S = Q K^T as soon as Q and K have landed, while warps 1-7 stage V^T
+    if (lane == 0) {
+      ok = mbar_wait(bar_in, 0, &never, kDefaultTimeoutCycles);
+      tc_fence_after();
+      constexpr uint32_t IDS = idesc_f16(TA_M, TA_KC);
+#pragma unroll 1
+      for (int kk = 0; kk < TA_HD / 16 && ok; ++kk) {
+        const int a = kk >> 2;
+        const uint32_t ko = (uint32_t)(kk & 3) * 32;  // K advance inside the 128-byte swizzled row
+        const uint64_t qh = desc_sw128(sbase + TA_OFF_Q + (0 + a) * TA_ATOM_Q + ko);
+        const uint64_t ql = desc_sw128(sbase + TA_OFF_Q + (2 + a) * TA_ATOM_Q + ko);
+        const uint64_t kh = desc_sw128(sbase + TA_OFF_K + (0 + a) * TA_ATOM_K + ko);
+        const uint64_t kl = desc_sw128(sbase + TA_OFF_K + (2 + a) * TA_ATOM_K + ko);
+        mma_f16(tmem, qh, kh, IDS, kk > 0);
+        mma_f16(tmem, qh, kl, IDS, 1);
+        mma_f16(tmem, ql, kh, IDS, 1);
+      }
+      mma_commit(bar_s);  // arrives even when the inputs timed out, so the waits below end
+    }
+  } else {
+    // V^T (rows = dims, K = the chunk's keys) by a register transpose of the V planes: item =
+    // (key pair, block of 8 dims), all of a thread's loads in flight, then (key, key + 1) pairs
+    // per 4-byte store; warps 1-7
+    constexpr int NST = TA_THREADS - 32;
+    const int tid = threadIdx.x - 32;
     const int64_t pl = (int64_t)L * d;
-    constexpr int NIT = (TA_KC / 2) * (TA_HD / 8), PER = (NIT + TA_THREADS - 1) / TA_THREADS;
+    constexpr int NIT = (TA_KC / 2) * (TA_HD / 8), PER = (NIT + NST - 1) / NST;
     uint4 vh[PER][2], vl[PER][2];
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
-      const int i = threadIdx.x + u * TA_THREADS;
+      const int i = tid + u * NST;
       const int k0 = 2 * (i / (TA_HD / 8)), nb = i % (TA_HD / 8);
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -384,7 +409,7 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
     }
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
-      const int i = threadIdx.x + u * TA_THREADS;
+      const int i = tid + u * NST;
       if (i >= NIT) break;
       const int k0 = 2 * (i / (TA_HD / 8)), nb = i % (TA_HD / 8);
       const uint32_t* h0 = reinterpret_cast<const uint32_t*>(&vh[u][0]);
@@ -401,31 +426,10 @@ __global__ void __launch_bounds__(TA_THREADS, 1)
         *reinterpret_cast<uint32_t*>(ta_smem + TA_OFF_VL + o) = lw;
       }
     }
+    fence_proxy_async();  // V^T is read by the tensor core
   }
-  fence_proxy_async();  // V^T is read by the tensor core
   __syncthreads();
   griddep_launch();
-  const uint32_t tmem = ta_tmem;
-  volatile int never = 0;
-  bool ok = true;
-  if (threadIdx.x == 0) {
-    ok = mbar_wait(bar_in, 0, &never, kDefaultTimeoutCycles);
-    tc_fence_after();
-    constexpr uint32_t IDS = idesc_f16(TA_M, TA_KC);
-#pragma unroll 1
-    for (int kk = 0; kk < TA_HD / 16 && ok; ++kk) {
-      const int a = kk >> 2;
-      const uint32_t ko = (uint32_t)(kk & 3) * 32;  // K advance inside the 128-byte swizzled row
-      const uint64_t qh = desc_sw128(sbase + TA_OFF_Q + (0 + a) * TA_ATOM_Q + ko);
-      const uint64_t ql = desc_sw128(sbase + TA_OFF_Q + (2 + a) * TA_ATOM_Q + ko);
-      const uint64_t kh = desc_sw128(sbase + TA_OFF_K + (0 + a) * TA_ATOM_K + ko);
-      const uint64_t kl = desc_sw128(sbase + TA_OFF_K + (2 + a) * TA_ATOM_K + ko);
-      mma_f16(tmem, qh, kh, IDS, kk > 0);
-      mma_f16(tmem, qh, kl, IDS, 1);
-      mma_f16(tmem, ql, kh, IDS, 1);
-    }
-    mma_commit(bar_s);  // arrives even when the inputs timed out, so the waits below end
-  }
   // this thread's row, its half of the chunk's columns of S: keys kb + [HK ch, HK ch + HK)
   ok = __all_sync(0xffffffffu, mbar_wait(bar_s, 0, &never, kDefaultTimeoutCycles));
   tc_fence_after();
