@@ -37,6 +37,11 @@
  *   - Device-side failures (a bounded wait that ran out) are recorded in a device error
  *     word; dllm_check(stream) synchronizes the stream and reports them.
  *   - Shapes: k (reduction length) must be a multiple of 256 (one super-block).
+ *   - Host threads: calls may be made from several host threads at once, each with its own
+ *     stream and buffers (the library's per-device caches are atomic, its error message is
+ *     per thread). dllm_qgemm_noalloc is the exception: its calls share one device array. The
+ *     device error word is one per device, so a device-side failure is reported by the next
+ *     dllm_check on that device, whichever thread or stream makes it.
  */
 #ifndef DLLM_H
 #define DLLM_H

@@ -22,28 +22,30 @@ namespace dllm {
 __device__ int g_err_word = 0;
 __device__ int g_bounds_site = 0;  // checked build: DLLM_SITE_AT of the first failing check
 
-int* err_word() {
-  static int* cache[64] = {nullptr};
+// Per-device caches of symbol addresses and attributes: atomic, so that host threads calling
+// the library concurrently may fill them at the same time (each writes the same value).
+template <typename Sym>
+static int* symbol_address(const Sym& sym, std::atomic<int*>* cache) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!cache[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<int*>(p);
+  int* p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, sym) != cudaSuccess) return nullptr;
+    p = static_cast<int*>(a);
+    cache[dev].store(p, std::memory_order_release);
   }
-  return cache[dev];
+  return p;
+}
+
+int* err_word() {
+  static std::atomic<int*> cache[64];
+  return symbol_address(g_err_word, cache);
 }
 
 int* site_word() {
-  static int* cache[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!cache[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bounds_site) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<int*>(p);
-  }
-  return cache[dev];
+  static std::atomic<int*> cache[64];
+  return symbol_address(g_bounds_site, cache);
 }
 
 void set_quant_bounds(QuantOut& o, int64_t rows, int64_t k) {
@@ -93,24 +95,24 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(DLLM_E_CUDA, "%s failed: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-static int cached_attr(cudaDeviceAttr attr, int* cache, int dflt) {
+static int cached_attr(cudaDeviceAttr attr, std::atomic<int>* cache, int dflt) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return dflt;
-  if (cache[dev] == 0) {
-    int v = 0;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     if (cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess || v <= 0) return dflt;
-    cache[dev] = v;
+    cache[dev].store(v, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return v;
 }
 
 int num_sms() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];
   return cached_attr(cudaDevAttrMultiProcessorCount, cache, 152);
 }
 
 int check_device() {
-  static int major_c[64] = {0}, minor_c[64] = {0};
+  static std::atomic<int> major_c[64], minor_c[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");

@@ -338,3 +338,43 @@ def test_peak_mma_i8_runs():
     tops = dl.peak_mma_i8_tops(iters=2000, reps=1)
     dl.check()
     assert 1.0 < tops < 1e5, tops
+
+
+def test_concurrent_host_threads_match_sequential_results():
+    # four host threads, each with its own stream and buffers, quantize and multiply at the same
+    # time (ctypes releases the interpreter lock during each call, so the library's host code runs
+    # concurrently); every result is bit-identical to the same call made alone
+    import threading
+    cases = [(dl.Q4_K, 148, 512, 1024), (dl.Q6_K, 37, 768, 2048), (dl.Q4_K, 16, 1024, 512), (dl.Q6_K, 160, 256, 4096)]
+    prep, ref = [], []
+    for i, (t, m, n, k) in enumerate(cases):
+        w, x = _case(t, m, n, k, 7100 + i)
+        pk, xd = _packed(t, w, n, k), _dev(x)
+        prep.append((t, m, n, k, pk, xd))
+        ref.append(dl.qgemm(t, dl.quantize_act(xd, plain=False)["act"], m, k, pk, n))
+    torch.cuda.synchronize()
+    dl.check()
+    out, errs = [None] * len(cases), []
+
+    def work(i):
+        try:
+            torch.cuda.set_device(0)
+            t, m, n, k, pk, xd = prep[i]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(10):
+                    y = dl.qgemm(t, dl.quantize_act(xd, plain=False, stream=s)["act"], m, k, pk, n, stream=s)
+            s.synchronize()
+            out[i] = y
+        except Exception as e:  # reported by the main thread
+            errs.append(repr(e))
+
+    ths = [threading.Thread(target=work, args=(i,)) for i in range(len(cases))]
+    for th in ths:
+        th.start()
+    for th in ths:
+        th.join()
+    assert not errs, errs
+    dl.check()
+    for i in range(len(cases)):
+        assert torch.equal(out[i], ref[i]), cases[i]
